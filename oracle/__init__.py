@@ -1,0 +1,424 @@
+"""CPU oracle for block-scaled FP4 (NVFP4 / MXFP4) linear layers and the
+NVFP4 fused-MoE layer.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py``'s CPU-baseline / reference leg may import this package.  It shares
+no code with the CUDA library and never imports it; it takes plain numpy
+arrays (bf16 values as uint16 bit patterns) and returns numpy arrays.
+
+Bit-level codecs and the quantisers are plain C (``fp4_oracle.c``, fp32
+arithmetic in the written order); the GEMMs are "dequantise, then fp64
+matmul"; routing, permutation and the MoE composition are numpy, following
+the stages named on "vLLM on DGX Spark: technical report", section 7.1
+"The modular fused-MoE architecture" (router -> quantise/dispatch ->
+permute/experts/unpermute -> combine) and section 4.3 (two expert GEMMs with a
+SwiGLU activation between them and a top-k weighted reduction).
+
+Parity pins for every function here live in ``tests/test_oracle_pins.py``;
+the one part without a pin is the GPU's own fp32 accumulation order (covered
+by the tolerance only).
+"""
+import ctypes
+
+import numpy as np
+
+from .build import build_oracle
+
+NVFP4 = 0
+MXFP4 = 1
+BLOCK = {NVFP4: 16, MXFP4: 32}
+DYNAMIC = 0
+STATIC = 1
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        L = ctypes.CDLL(build_oracle())
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        f32p = ctypes.POINTER(ctypes.c_float)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        i64 = ctypes.c_int64
+        L.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
+        L.orc_bf16_to_f32.restype = ctypes.c_float
+        L.orc_f32_to_bf16.argtypes = [ctypes.c_float]
+        L.orc_f32_to_bf16.restype = ctypes.c_uint16
+        L.orc_e2m1_decode.argtypes = [ctypes.c_uint8]
+        L.orc_e2m1_decode.restype = ctypes.c_float
+        L.orc_e2m1_encode.argtypes = [ctypes.c_float]
+        L.orc_e2m1_encode.restype = ctypes.c_uint8
+        L.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+        L.orc_e4m3_decode.restype = ctypes.c_float
+        L.orc_e4m3_encode.argtypes = [ctypes.c_float]
+        L.orc_e4m3_encode.restype = ctypes.c_uint8
+        L.orc_e8m0_decode.argtypes = [ctypes.c_uint8]
+        L.orc_e8m0_decode.restype = ctypes.c_float
+        L.orc_scale_cols_padded.argtypes = [i64, i64]
+        L.orc_scale_cols_padded.restype = i64
+        L.orc_scale_mma_bytes.argtypes = [i64, i64, i64]
+        L.orc_scale_mma_bytes.restype = i64
+        L.orc_scale_mma_index.argtypes = [i64, i64, i64]
+        L.orc_scale_mma_index.restype = i64
+        L.orc_scales_to_mma.argtypes = [u8p, i64, i64, i64, u8p]
+        L.orc_scales_from_mma.argtypes = [u8p, i64, i64, i64, u8p]
+        L.orc_amax_bf16.argtypes = [u16p, i64]
+        L.orc_amax_bf16.restype = ctypes.c_float
+        L.orc_nvfp4_global_scale.argtypes = [ctypes.c_float]
+        L.orc_nvfp4_global_scale.restype = ctypes.c_float
+        L.orc_quantize_nvfp4_given_scale.argtypes = [u16p, i64, i64, ctypes.c_float, u8p, u8p]
+        L.orc_quantize_nvfp4.argtypes = [u16p, i64, i64, ctypes.c_int, ctypes.c_float, u8p, u8p, f32p]
+        L.orc_quantize_mxfp4.argtypes = [u16p, i64, i64, u8p, u8p]
+        L.orc_dequantize.argtypes = [ctypes.c_int, u8p, u8p, ctypes.c_float, ctypes.c_int, i64, i64, f64p]
+        L.orc_gemm_nvfp4_exact.argtypes = [u8p, u8p, u8p, u8p, i64, i64, i64, ctypes.POINTER(ctypes.c_int64)]
+        _lib = L
+    return _lib
+
+
+def _p(a, ct):
+    return a.ctypes.data_as(ctypes.POINTER(ct))
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ------------------------------------------------------------------ codecs
+
+def e2m1_decode(code):
+    return lib().orc_e2m1_decode(int(code))
+
+
+def e2m1_encode(v):
+    return lib().orc_e2m1_encode(float(v))
+
+
+def e4m3_decode(b):
+    return lib().orc_e4m3_decode(int(b))
+
+
+def e4m3_encode(v):
+    return lib().orc_e4m3_encode(float(v))
+
+
+def e8m0_decode(b):
+    return lib().orc_e8m0_decode(int(b))
+
+
+def f32_to_bf16(a):
+    """fp32 array -> bf16 bit patterns (uint16), round to nearest even."""
+    a = _c(a, np.float32).ravel()
+    L = lib()
+    return np.array([L.orc_f32_to_bf16(float(v)) for v in a], dtype=np.uint16)
+
+
+def bf16_to_f32(u16):
+    u = _c(u16, np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32)
+
+
+def e2m1_table():
+    """Value of each of the 16 E2M1 codes (float64)."""
+    return np.array([e2m1_decode(c) for c in range(16)], dtype=np.float64)
+
+
+def e4m3_table():
+    return np.array([e4m3_decode(b) for b in range(256)], dtype=np.float64)
+
+
+def e8m0_table():
+    return np.array([e8m0_decode(b) for b in range(256)], dtype=np.float64)
+
+
+# ------------------------------------------------------------ scale layout
+
+def scale_cols_padded(k, fmt):
+    return lib().orc_scale_cols_padded(k, BLOCK[fmt])
+
+
+def scale_mma_bytes(rows, k, fmt):
+    return lib().orc_scale_mma_bytes(rows, k, BLOCK[fmt])
+
+
+def scale_mma_index(row, j, ksf_pad):
+    return lib().orc_scale_mma_index(row, j, ksf_pad)
+
+
+def scales_to_mma(canon, rows, k, fmt):
+    canon = _c(canon, np.uint8)
+    out = np.zeros(scale_mma_bytes(rows, k, fmt), dtype=np.uint8)
+    lib().orc_scales_to_mma(_p(canon, ctypes.c_uint8), rows, k, BLOCK[fmt], _p(out, ctypes.c_uint8))
+    return out
+
+
+def scales_from_mma(mma, rows, k, fmt):
+    mma = _c(mma, np.uint8)
+    out = np.zeros((rows, k // BLOCK[fmt]), dtype=np.uint8)
+    lib().orc_scales_from_mma(_p(mma, ctypes.c_uint8), rows, k, BLOCK[fmt], _p(out, ctypes.c_uint8))
+    return out
+
+
+# -------------------------------------------------------------- quantisers
+
+def amax_bf16(x_u16):
+    x = _c(x_u16, np.uint16)
+    return lib().orc_amax_bf16(_p(x, ctypes.c_uint16), x.size)
+
+
+def nvfp4_global_scale(amax):
+    return lib().orc_nvfp4_global_scale(float(amax))
+
+
+def quantize_nvfp4(x_u16, mode=DYNAMIC, static_scale=0.0):
+    """x: [rows, k] bf16 bits -> (codes [rows, k/2] u8, scales [rows, k/16] u8, s_g float)."""
+    x = _c(x_u16, np.uint16)
+    rows, k = x.shape
+    codes = np.zeros((rows, k // 2), dtype=np.uint8)
+    scales = np.zeros((rows, k // 16), dtype=np.uint8)
+    sg = ctypes.c_float(0.0)
+    lib().orc_quantize_nvfp4(_p(x, ctypes.c_uint16), rows, k, mode, float(static_scale), _p(codes, ctypes.c_uint8),
+                             _p(scales, ctypes.c_uint8), ctypes.byref(sg))
+    return codes, scales, sg.value
+
+
+def quantize_nvfp4_given_scale(x_u16, s_g):
+    x = _c(x_u16, np.uint16)
+    rows, k = x.shape
+    codes = np.zeros((rows, k // 2), dtype=np.uint8)
+    scales = np.zeros((rows, k // 16), dtype=np.uint8)
+    lib().orc_quantize_nvfp4_given_scale(_p(x, ctypes.c_uint16), rows, k, float(s_g), _p(codes, ctypes.c_uint8),
+                                         _p(scales, ctypes.c_uint8))
+    return codes, scales
+
+
+def quantize_mxfp4(x_u16):
+    """x: [rows, k] bf16 bits -> (codes [rows, k/2] u8, scales [rows, k/32] u8 E8M0)."""
+    x = _c(x_u16, np.uint16)
+    rows, k = x.shape
+    codes = np.zeros((rows, k // 2), dtype=np.uint8)
+    scales = np.zeros((rows, k // 32), dtype=np.uint8)
+    lib().orc_quantize_mxfp4(_p(x, ctypes.c_uint16), rows, k, _p(codes, ctypes.c_uint8), _p(scales, ctypes.c_uint8))
+    return codes, scales
+
+
+def quantize(fmt, x_u16, mode=DYNAMIC, static_scale=0.0):
+    """Uniform interface: returns (codes, canonical scales, s_g); MXFP4 has s_g = 1."""
+    if fmt == NVFP4:
+        return quantize_nvfp4(x_u16, mode, static_scale)
+    c, s = quantize_mxfp4(x_u16)
+    return c, s, 1.0
+
+
+def dequantize(fmt, codes, scales, s_g=1.0, apply_global=True):
+    """[rows, k] float64 values of quantised data (E2M1 x block scale [x s_g])."""
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    rows = codes.shape[0]
+    k = codes.shape[1] * 2
+    out = np.zeros((rows, k), dtype=np.float64)
+    lib().orc_dequantize(fmt, _p(codes, ctypes.c_uint8), _p(scales, ctypes.c_uint8), float(s_g),
+                         1 if apply_global else 0, rows, k, _p(out, ctypes.c_double))
+    return out
+
+
+# ------------------------------------------------------------------- GEMMs
+
+def alpha_of(fmt, sg_a, sg_w):
+    """GEMM dequantisation factor: the product of the two per-tensor global
+    scales, formed in fp32 (NVFP4); 1 for MXFP4, which has no global scale."""
+    if fmt == MXFP4:
+        return 1.0
+    return float(np.float32(sg_a) * np.float32(sg_w))
+
+
+def gemm(fmt, ca, sa, sga, cb, sb, sgb):
+    """out[m, n] = alpha * sum_k deqA[m, k] * deqB[n, k] in fp64, plus the
+    magnitude sum alpha * sum_k |deqA * deqB| that sizes the fp32
+    accumulation error.  A and B are both K-major (B is the weight [N, K])."""
+    da = dequantize(fmt, ca, sa, apply_global=False)
+    db = dequantize(fmt, cb, sb, apply_global=False)
+    alpha = alpha_of(fmt, sga, sgb)
+    return alpha * (da @ db.T), alpha * (np.abs(da) @ np.abs(db).T)
+
+
+def gemm_rows(fmt, ca, sa, sga, cb, sb, sgb, rows_a, rows_b):
+    """gemm() restricted to the output block rows_a x rows_b (index arrays)."""
+    return gemm(fmt, ca[rows_a], sa[rows_a], sga, cb[rows_b], sb[rows_b], sgb)
+
+
+def gemm_nvfp4_exact(ca, sa, cb, sb):
+    """Exact S * 2^20 (int64) of the unscaled NVFP4 product, see fp4_oracle.c."""
+    ca, sa, cb, sb = (_c(a, np.uint8) for a in (ca, sa, cb, sb))
+    M, N, K = ca.shape[0], cb.shape[0], ca.shape[1] * 2
+    out = np.zeros((M, N), dtype=np.int64)
+    lib().orc_gemm_nvfp4_exact(_p(ca, ctypes.c_uint8), _p(sa, ctypes.c_uint8), _p(cb, ctypes.c_uint8),
+                               _p(sb, ctypes.c_uint8), M, N, K, _p(out, ctypes.c_int64))
+    return out
+
+
+def linear(fmt, x_u16, w_u16, mode=DYNAMIC, static_scale=0.0):
+    """The whole W4A4 linear layer: quantise activations (per call) and
+    weights, then the block-scaled GEMM.  Returns (out fp64, magnitude sum,
+    quantised A, quantised W)."""
+    qa = quantize(fmt, x_u16, mode, static_scale)
+    qw = quantize(fmt, w_u16, DYNAMIC)
+    out, mag = gemm(fmt, qa[0], qa[1], qa[2], qw[0], qw[1], qw[2])
+    return out, mag, qa, qw
+
+
+def bf16_round(x64):
+    """fp64 -> nearest bf16 value (round half to even), as float64.  bf16 keeps
+    8 significant bits; its spacing at |x| in [2^(e-1), 2^e) is 2^(e-8), and
+    never below the subnormal quantum 2^-133."""
+    x = np.asarray(x64, dtype=np.float64)
+    _, e = np.frexp(x)
+    q = np.maximum(e - 8, -133)
+    return np.ldexp(np.rint(np.ldexp(x, -q)), q)
+
+
+def f32_to_bf16_trunc(u32f):
+    return (np.ascontiguousarray(u32f, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+# ---------------------------------------------------------- router/permute
+
+def router_topk(logits, top_k):
+    """Softmax over experts, top-k, renormalise.  Selection is on the raw
+    logits (softmax is monotone), ties to the lower expert index.  Weights are
+    exp(l_j - l_max) / sum over the selected experts, in fp64, which equals the
+    renormalised softmax probabilities.  Returns ids [T, k] int32 (by
+    descending weight) and weights [T, k] float64."""
+    logits = np.asarray(logits, dtype=np.float32)
+    order = np.argsort(-logits.astype(np.float64), axis=1, kind="stable")
+    ids = order[:, :top_k].astype(np.int32)
+    sel = np.take_along_axis(logits, ids, axis=1).astype(np.float64)
+    ex = np.exp(sel - sel.max(axis=1, keepdims=True))
+    return ids, ex / ex.sum(axis=1, keepdims=True)
+
+
+def permute(ids, n_experts):
+    """Counting sort of the T*k assignments by expert, stable in (token, j).
+    Returns counts [E], offsets [E+1] (exclusive prefix sum) and order
+    [T*k]: order[p] = t*k + j of the assignment at sorted position p."""
+    flat = np.asarray(ids, dtype=np.int64).ravel()
+    order = np.argsort(flat, kind="stable").astype(np.int64)
+    counts = np.bincount(flat, minlength=n_experts).astype(np.int64)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    return counts, offsets, order
+
+
+# ---------------------------------------------------------------------- MoE
+
+def silu(g):
+    """SiLU(g) = g / (1 + exp(-g)), fp64."""
+    g = np.asarray(g, dtype=np.float64)
+    return g / (1.0 + np.exp(-g))
+
+
+def quantize_experts(w_u16):
+    """Per-expert dynamic NVFP4 quantisation of stacked weights [E, rows, k]."""
+    E = w_u16.shape[0]
+    out = [quantize_nvfp4(w_u16[e], DYNAMIC) for e in range(E)]
+    codes = np.stack([o[0] for o in out])
+    scales = np.stack([o[1] for o in out])
+    sg = np.array([o[2] for o in out], dtype=np.float32)
+    return codes, scales, sg
+
+
+def moe(hidden_u16, logits, w13_u16=None, w2_u16=None, top_k=8, q13=None, q2=None, mode=DYNAMIC,
+        static13=None, static2=None, h_override=None):
+    """NVFP4 fused MoE, stage by stage.
+
+    hidden [T, H] bf16 bits; logits [T, E] fp32; w13 [E, 2I, H] bf16 bits with
+    gate rows 0..I-1 and up rows I..2I-1 (reading where the pages are silent);
+    w2 [E, H, I].  q13 / q2 may carry already-quantised expert weights
+    (codes, scales, s_g) to skip re-quantising them.
+
+    Stages (each returned for staged parity):
+      1. router: ids, weights                       (router_topk)
+      2. permute: counts, offsets, order           (permute)
+      3. hidden quantised once, per-tensor dynamic scale s_gA (static mode:
+         per-expert scale static13[e] applied to that expert's rows)
+      4. GEMM1 per expert: G = alpha1_e * A_q[rows_e] . W13_e^T,
+         alpha1_e = s_gA * s_gW13[e]; h = SiLU(G[:, :I]) * G[:, I:] stored as
+         bf16 (reading: bf16 storage of h)
+      5. requantise h with the per-expert dynamic scale s_gH[e] =
+         amax(h over e's rows) / 2688 (static mode: static2[e])
+      6. GEMM2: D = alpha2_e * H_q . W2_e^T, alpha2_e = s_gH[e] * s_gW2[e]
+      7. combine: y[t] = sum_j w[t, j] * D[pos(t, j)], fp64, then bf16.
+    h_override (bf16 bits [T*k, I] in sorted order) replaces stage 4's h so
+    that stages 5-7 can be checked from a given h.
+    """
+    T, H = hidden_u16.shape
+    E = logits.shape[1]
+    ids, w = router_topk(logits, top_k)
+    counts, offsets, order = permute(ids, E)
+    if q13 is None:
+        q13 = quantize_experts(w13_u16)
+    if q2 is None:
+        q2 = quantize_experts(w2_u16)
+    c13, s13, sg13 = q13
+    c2, s2, sg2 = q2
+    I = c13.shape[1] // 2
+    tok = order // top_k
+    if mode == DYNAMIC:
+        ca, sa, sga = quantize_nvfp4(hidden_u16, DYNAMIC)
+        ca_rows, sa_rows = ca[tok], sa[tok]
+        sga_rows = np.full(len(order), sga, dtype=np.float32)
+    else:
+        ca_rows = np.zeros((len(order), H // 2), dtype=np.uint8)
+        sa_rows = np.zeros((len(order), H // 16), dtype=np.uint8)
+        sga_rows = np.zeros(len(order), dtype=np.float32)
+        for e in range(E):
+            lo, hi = offsets[e], offsets[e + 1]
+            if hi > lo:
+                c, s = quantize_nvfp4_given_scale(hidden_u16[tok[lo:hi]], static13[e])
+                ca_rows[lo:hi], sa_rows[lo:hi], sga_rows[lo:hi] = c, s, static13[e]
+        sga = None
+    G = np.zeros((len(order), 2 * I))
+    Gmag = np.zeros((len(order), 2 * I))
+    for e in range(E):
+        lo, hi = offsets[e], offsets[e + 1]
+        if hi > lo:
+            G[lo:hi], Gmag[lo:hi] = gemm(NVFP4, ca_rows[lo:hi], sa_rows[lo:hi], sga_rows[lo], c13[e], s13[e], sg13[e])
+    gate, up = G[:, :I], G[:, I:]
+    h64 = silu(gate) * up
+    h_bf16 = f32_to_bf16_exact(h64)
+    h_used = h_bf16 if h_override is None else np.asarray(h_override, dtype=np.uint16)
+    sgH = np.zeros(E, dtype=np.float32)
+    ch = np.zeros((len(order), I // 2), dtype=np.uint8)
+    sh = np.zeros((len(order), I // 16), dtype=np.uint8)
+    for e in range(E):
+        lo, hi = offsets[e], offsets[e + 1]
+        if hi > lo:
+            if mode == DYNAMIC:
+                sgH[e] = nvfp4_global_scale(amax_bf16(h_used[lo:hi]))
+            else:
+                sgH[e] = static2[e]
+            ch[lo:hi], sh[lo:hi] = quantize_nvfp4_given_scale(h_used[lo:hi], sgH[e])
+    D = np.zeros((len(order), H))
+    Dmag = np.zeros((len(order), H))
+    for e in range(E):
+        lo, hi = offsets[e], offsets[e + 1]
+        if hi > lo:
+            D[lo:hi], Dmag[lo:hi] = gemm(NVFP4, ch[lo:hi], sh[lo:hi], sgH[e], c2[e], s2[e], sg2[e])
+    pos = np.empty(len(order), dtype=np.int64)
+    pos[order] = np.arange(len(order))
+    wf = w.ravel()
+    y = np.zeros((T, H))
+    ymag = np.zeros((T, H))
+    for j in range(top_k):
+        p = pos[np.arange(T) * top_k + j]
+        y += wf[np.arange(T) * top_k + j][:, None] * D[p]
+        ymag += np.abs(wf[np.arange(T) * top_k + j])[:, None] * Dmag[p]
+    return dict(ids=ids, weights=w, counts=counts, offsets=offsets, order=order, sgA=sga, a_codes=ca_rows,
+                a_scales=sa_rows, G=G, Gmag=Gmag, h64=h64, h_bf16=h_bf16, sgH=sgH, h_codes=ch, h_scales=sh, D=D,
+                Dmag=Dmag, y=y, ymag=ymag, q13=q13, q2=q2)
+
+
+def f32_to_bf16_exact(x64):
+    """fp64 values -> bf16 bit patterns, rounded to nearest even from the fp64
+    value itself (no intermediate fp32 rounding)."""
+    return f32_to_bf16_trunc(np.asarray(bf16_round(x64), dtype=np.float32))
