@@ -1,0 +1,183 @@
+// gemm.cu -- launchers of the block-scaled GEMM (dense linear and decode
+// variants), the split-K reduction and the instantiation table.
+#include <cudaTypedefs.h>
+#include <stdio.h>
+
+#include <mutex>
+
+#include "gemm_kernel.cuh"
+
+namespace fp4 {
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D map over packed codes [rows][k/2] bytes; box = 128 bytes x box_rows,
+// 128-byte swizzle (matches the MMA's K-major SWIZZLE_128B operand layout).
+static bool make_codes_map(CUtensorMap* m, const void* base, int64_t rows, int64_t k, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)(k / 2), (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(k / 2)};
+    cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1u, 1u};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int64_t gemm_k_blocks(int64_t k) { return (k + 255) / 256; }
+
+template <int BN, bool MX, int EPI>
+static cudaError_t launch_one(const GemmLaunch& g, cudaStream_t s) {
+    using C = GemmCfg<BN, MX>;
+    auto kern = gemm_kernel<BN, MX, EPI>;
+    static bool attr_set = false;  // per instantiation; the attribute is per device function
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    CUtensorMap tmP, tmQ;
+    if (!make_codes_map(&tmP, g.p_codes, g.p_rows, g.k, 128) || !make_codes_map(&tmQ, g.q_codes, g.q_rows, g.k, BN)) {
+        set_error("cuTensorMapEncodeTiled failed (rows %lld/%lld, k %lld)", (long long)g.p_rows, (long long)g.q_rows,
+                  (long long)g.k);
+        return cudaErrorInvalidValue;
+    }
+    const DeviceInfo* d = current_device();
+    if (!d) return cudaErrorNoDevice;
+    int64_t units;
+    if (g.grouped) {
+        // upper bound: every padded 128-row tile of the capacity
+        units = ((g.p_rows + 127) / 128) * ((g.q_rows_valid + BN - 1) / BN) * g.splits;
+    } else {
+        units = ((g.p_rows_valid + 127) / 128) * ((g.q_rows_valid + BN - 1) / BN) * g.splits;
+    }
+    int64_t grid = d->sm_count;
+    if (g.max_ctas > 0 && g.max_ctas < grid) grid = g.max_ctas;
+    if (units < grid) grid = units;
+    if (grid < 1) return cudaSuccess;
+    WaitCfg wc;
+    wc.limit_ns = wait_limit_ns();
+    wc.err = d->err_word;
+    GemmLaunch gg = g;
+    void* args[] = {(void*)&tmP, (void*)&tmQ, (void*)&gg, (void*)&wc};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (g.pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelExC(&cfg, (const void*)kern, args);
+}
+
+cudaError_t launch_gemm_moe(const GemmLaunch& g, cudaStream_t s);  // moe.cu
+
+cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
+    const bool mx = g.fmt == FP4_MXFP4;
+    switch (g.epi) {
+        case EPI_BF16:
+            if (g.bn == 256) return mx ? launch_one<256, true, EPI_BF16>(g, s) : launch_one<256, false, EPI_BF16>(g, s);
+            if (g.bn == 128) return mx ? launch_one<128, true, EPI_BF16>(g, s) : launch_one<128, false, EPI_BF16>(g, s);
+            break;
+        case EPI_BF16_T:
+            if (g.bn == 32) return mx ? launch_one<32, true, EPI_BF16_T>(g, s) : launch_one<32, false, EPI_BF16_T>(g, s);
+            if (g.bn == 64) return mx ? launch_one<64, true, EPI_BF16_T>(g, s) : launch_one<64, false, EPI_BF16_T>(g, s);
+            break;
+        case EPI_PARTIAL_T:
+            if (g.bn == 32)
+                return mx ? launch_one<32, true, EPI_PARTIAL_T>(g, s) : launch_one<32, false, EPI_PARTIAL_T>(g, s);
+            if (g.bn == 64)
+                return mx ? launch_one<64, true, EPI_PARTIAL_T>(g, s) : launch_one<64, false, EPI_PARTIAL_T>(g, s);
+            break;
+        case EPI_SWIGLU:
+        case EPI_COMBINE:
+            return launch_gemm_moe(g, s);
+    }
+    set_error("no GEMM instantiation for epilogue %d, BN %d", g.epi, g.bn);
+    return cudaErrorInvalidValue;
+}
+
+// Instantiations for the grouped MoE GEMMs live here too (one TU keeps the
+// template's code in one place; moe.cu only builds the launch records).
+cudaError_t launch_gemm_moe(const GemmLaunch& g, cudaStream_t s) {
+    if (g.fmt != FP4_NVFP4) return cudaErrorInvalidValue;
+    if (g.epi == EPI_SWIGLU) {
+        if (g.bn == 256) return launch_one<256, false, EPI_SWIGLU>(g, s);
+        if (g.bn == 128) return launch_one<128, false, EPI_SWIGLU>(g, s);
+        if (g.bn == 64) return launch_one<64, false, EPI_SWIGLU>(g, s);
+    } else {
+        if (g.bn == 256) return launch_one<256, false, EPI_COMBINE>(g, s);
+        if (g.bn == 128) return launch_one<128, false, EPI_COMBINE>(g, s);
+        if (g.bn == 64) return launch_one<64, false, EPI_COMBINE>(g, s);
+    }
+    set_error("no MoE GEMM instantiation for BN %d", g.bn);
+    return cudaErrorInvalidValue;
+}
+
+// out[t][f] = bf16(alpha * sum_s part[s][t][f]) in split order (deterministic).
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4* __restrict__ part, int splits, int64_t mn4,
+                                                            const float* ga, const float* gw, int mx,
+                                                            uint2* __restrict__ out) {
+    pdl_wait();
+    const float alpha = mx ? 1.0f : __fmul_rn(gw[0], ga[0]);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < mn4; i += (int64_t)gridDim.x * blockDim.x) {
+        float4 a = part[i];
+        for (int s = 1; s < splits; ++s) {
+            const float4 b = part[(int64_t)s * mn4 + i];
+            a.x = __fadd_rn(a.x, b.x);
+            a.y = __fadd_rn(a.y, b.y);
+            a.z = __fadd_rn(a.z, b.z);
+            a.w = __fadd_rn(a.w, b.w);
+        }
+        out[i] = make_uint2(pack_bf16x2(__fmul_rn(alpha, a.x), __fmul_rn(alpha, a.y)),
+                            pack_bf16x2(__fmul_rn(alpha, a.z), __fmul_rn(alpha, a.w)));
+    }
+    pdl_launch_dependents();
+}
+
+cudaError_t launch_splitk_reduce(const float* part, int splits, int64_t m, int64_t n, const float* ga,
+                                 const float* gw, bool mx, uint16_t* out, bool pdl, cudaStream_t s) {
+    const DeviceInfo* d = current_device();
+    if (!d) return cudaErrorNoDevice;
+    int64_t mn4 = m * n / 4;
+    int64_t blocks = (mn4 + 255) / 256;
+    if (blocks > (int64_t)d->sm_count * 8) blocks = (int64_t)d->sm_count * 8;
+    if (blocks < 1) blocks = 1;
+    const float4* p4 = reinterpret_cast<const float4*>(part);
+    uint2* o2 = reinterpret_cast<uint2*>(out);
+    int mxi = mx ? 1 : 0;
+    void* args[] = {(void*)&p4, (void*)&splits, (void*)&mn4, (void*)&ga, (void*)&gw, (void*)&mxi, (void*)&o2};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelExC(&cfg, (const void*)splitk_reduce_kernel, args);
+}
+
+}  // namespace fp4

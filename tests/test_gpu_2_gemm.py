@@ -1,0 +1,144 @@
+"""GPU block-scaled GEMM vs the CPU oracle's dequantise-then-fp64 GEMM.
+
+The oracle quantises the same bf16 inputs itself (its codes are checked bit
+for bit against the GPU quantiser elsewhere) and computes the reference and
+the magnitude sum that sizes the fp32 accumulation floor; see tests/util.py
+for the tolerance."""
+import numpy as np
+import pytest
+import torch
+
+from mxfp4_block_scaled_gb300 import inputs as I
+from util import bf16_to_np, check_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def F():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    import __graft_entry__ as ge
+    ge.build()
+    from mxfp4_block_scaled_gb300 import fp4
+    return fp4
+
+
+def run_gemm(F, a, w, fmt, mode=0, st=0.0):
+    wq = F.prepack_weight(w.cuda(), fmt)
+    out = F.gemm(a.cuda(), wq, mode, st)
+    torch.cuda.synchronize()
+    F.device_status()
+    return bf16_to_np(out)
+
+
+def check_linear(F, O, a, w, fmt, mode=0, st=0.0):
+    got = run_gemm(F, a, w, fmt, mode, st)
+    ref, mag, _, _ = O.linear(fmt, I.u16(a), I.u16(w), mode, st)
+    check_close(got, ref, mag)
+
+
+def test_single_linear_workload(F, O):
+    """A [16, 512] ~ N(0,1) seed 0, W [256, 512] ~ N(0, 0.02), NVFP4 dynamic."""
+    check_linear(F, O, I.randn_bf16((16, 512), 0), I.weights_bf16(256, 512, 100), 0)
+
+
+# (m, n, k): several tiles, ragged M / N / K tails, both the prefill (m > 64)
+# and the weight-streaming decode (m <= 64, split-K) paths.
+SHAPES = [(1, 256, 512), (3, 1024, 768), (8, 520, 1024), (32, 1024, 4096), (33, 264, 512), (64, 384, 256),
+          (65, 264, 800), (128, 256, 256), (130, 520, 1056), (300, 1280, 2048), (512, 2048, 512)]
+
+
+@pytest.mark.parametrize("m,n,k", SHAPES)
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_shapes(F, O, m, n, k, fmt):
+    check_linear(F, O, I.randn_bf16((m, k), m + n), I.weights_bf16(n, k, k + 3), fmt)
+
+
+def test_static_scale(F, O):
+    a = I.randn_bf16((96, 512), 9)
+    w = I.weights_bf16(256, 512, 10)
+    check_linear(F, O, a, w, 0, mode=1, st=3.5 / 2688)   # clips the largest activations
+    check_linear(F, O, a[:8], w, 0, mode=1, st=0.02)
+
+
+def test_prequant_with_oracle_operands(F, O):
+    """The GEMM alone, on operands quantised by the oracle and uploaded."""
+    for fmt, (m, n, k) in [(0, (200, 512, 1024)), (1, (200, 512, 1024)), (0, (5, 640, 2048))]:
+        a = I.randn_bf16((m, k), 1)
+        w = I.weights_bf16(n, k, 2)
+        ca, sa, ga = O.quantize(fmt, I.u16(a))
+        cw, sw, gw = O.quantize(fmt, I.u16(w))
+        ref, mag = O.gemm(fmt, ca, sa, ga, cw, sw, gw)
+
+        def up(c, s, g, rows):
+            q = F.empty_qtensor(fmt, rows, k, "cuda")
+            q.codes.copy_(torch.from_numpy(c))
+            q.scales.copy_(torch.from_numpy(O.scales_to_mma(s, rows, k, fmt)))
+            q.gscale.fill_(float(g))
+            return q
+
+        out = F.gemm_prequant(up(ca, sa, ga, m), up(cw, sw, gw, n))
+        torch.cuda.synchronize()
+        check_close(bf16_to_np(out), ref, mag)
+
+
+def test_zero_m_is_noop(F):
+    w = I.weights_bf16(256, 512, 1).cuda()
+    wq = F.prepack_weight(w)
+    out = F.gemm(torch.empty((0, 512), dtype=torch.bfloat16, device="cuda"), wq)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 256)
+
+
+def test_zero_activations_give_zero(F):
+    w = I.weights_bf16(256, 512, 1).cuda()
+    out = F.gemm(torch.zeros((40, 512), dtype=torch.bfloat16, device="cuda"), F.prepack_weight(w))
+    torch.cuda.synchronize()
+    assert not out.float().abs().sum().item()
+
+
+# ------------------------------------------------------------ full sizes
+
+@pytest.fixture(scope="module")
+def decode_weights(O):
+    w = I.weights_bf16(14336, 4096, 101)
+    return w, O.quantize_nvfp4(I.u16(w))
+
+
+@pytest.mark.parametrize("m", [1, 8, 32])
+def test_decode_full_size(F, O, decode_weights, m):
+    """Decode-shaped NVFP4 GEMM: K=4096, N=14336, activations with 0.1%
+    outliers x50; every output element checked."""
+    w, qw = decode_weights
+    a = I.activations_with_outliers(m, 4096, 1)
+    got = run_gemm(F, a, w, 0)
+    qa = O.quantize_nvfp4(I.u16(a))
+    ref, mag = O.gemm(0, qa[0], qa[1], qa[2], *qw)
+    check_close(got, ref, mag)
+
+
+@pytest.mark.parametrize("n", [4096, 14336])
+def test_prefill_full_size_sampled(F, O, n):
+    """Prefill-shaped NVFP4 GEMM M=8192, K=4096: all columns of 48 sampled
+    rows and all rows of 24 sampled columns (rows/cols span every tile)."""
+    m, k = 8192, 4096
+    a = I.randn_bf16((m, k), 2)
+    w = I.weights_bf16(n, k, 102)
+    got = run_gemm(F, a, w, 0)
+    qa = O.quantize_nvfp4(I.u16(a))
+    qw = O.quantize_nvfp4(I.u16(w))
+    rng = np.random.default_rng(n)
+    rows = np.unique(np.concatenate([rng.choice(m, 40, replace=False), [0, 127, 128, m - 1]]))
+    cols = np.unique(np.concatenate([rng.choice(n, 20, replace=False), [0, 255, 256, n - 1]]))
+    ref, mag = O.gemm_rows(0, qa[0], qa[1], qa[2], qw[0], qw[1], qw[2], rows, np.arange(n))
+    check_close(got[rows], ref, mag, what="sampled rows")
+    ref, mag = O.gemm_rows(0, qa[0], qa[1], qa[2], qw[0], qw[1], qw[2], np.arange(m), cols)
+    check_close(got[:, cols], ref, mag, what="sampled columns")
+
+
+def test_mxfp4_full_size(F, O):
+    """MXFP4 W4A4 M=2048, K=7168, N=2048: every output element."""
+    a = I.randn_bf16((2048, 7168), 4)
+    w = I.weights_bf16(2048, 7168, 104)
+    check_linear(F, O, a, w, 1)
