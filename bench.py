@@ -1,0 +1,469 @@
+"""Benchmark of the block-scaled FP4 linear layer on one GB300.
+
+Headline workload: the prefill-shaped NVFP4 W4A4 linear layer, M=8192,
+K=4096, N=14336: bf16 activations quantised on the device per call (dynamic
+per-tensor scale: amax pass + quantise pass), pre-quantised NVFP4 weights,
+tcgen05 block-scaled GEMM with the alpha / bf16 epilogue.  One step = one
+such layer call.  value = 2*M*N*K / step time (TFLOP/s).
+
+Also reported on the same line: the GEMM kernel's roofline (tensor-bound,
+against the dense-FP4 peak = measured bf16 peak x 6), the oracle timed on the
+host cores on a bounded row sample, the end-to-end rate through the public
+API with host buffers (H2D of the activations and D2H of the output inside
+the timed region), SM clocks sampled during the timed region, and secondary
+workloads (decode-shaped NVFP4, MXFP4, fused MoE) as extra keys.
+
+--impl reference times the CPU oracle (the reference arm of this build) on
+the same workload, one bounded row sample per step.
+Multi-GPU: replicas only (the path has no exchange step); value = sum over
+ranks of the units each processed / max time over ranks.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 GEMM TFLOPS (prefill) & GB/s (decode/MoE) on 1 GB300, % of FP4/HBM roofline"
+M, K, N = 8192, 4096, 14336
+WORKLOAD = "prefill NVFP4 W4A4 linear M=8192 K=4096 N=14336, activations quantised per call"
+FP4_PER_BF16 = 13.5 / 2.25  # nominal dense FP4 : bf16 tensor-core throughput
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=40)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-secondary", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--profile", action="store_true",
+                   help="only the layer calls (warmup + steps), for ncu captures; prints kernel timings")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo", rank=rank, world_size=ws)
+    return rank, local, ws
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(v, ws):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t[0])
+
+
+def reduce_sum(v, ws):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t[0])
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- peaks
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16": p["bf16_tflops"], "bf16_sustained": p["bf16_tflops_sustained"],
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+def profile_traffic(name, kernel_sources):
+    """Per-launch DRAM bytes from a committed ncu summary, if the kernel
+    sources still hash to the value recorded there (else None)."""
+    path = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(path):
+        return None
+    h = hashlib.sha256()
+    for s in kernel_sources:
+        with open(os.path.join(ROOT, s), "rb") as f:
+            h.update(f.read())
+    digest = h.hexdigest()[:16]
+    rec = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                rec[k.strip()] = v.strip().strip("`")
+    if rec.get("kernel_sources_sha256_16") != digest:
+        return None
+    try:
+        return float(rec["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+GEMM_SOURCES = ["mxfp4_block_scaled_gb300/csrc/gemm_kernel.cuh", "mxfp4_block_scaled_gb300/csrc/common.cuh"]
+
+
+# ------------------------------------------------------------ timing
+
+def time_steps(torch, steps, warmup, step_fn, flush=None, marks=0):
+    """Per-step CUDA events on the current stream (the one the library
+    launches on); an L2 flush runs between steps outside the events.
+    step_fn(evs) may record `marks` extra events inside a step.  Returns the
+    list of per-step durations (ms) and per-step mark durations."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        if flush is not None:
+            flush()
+        step_fn(None)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 + marks)] for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush()
+        e = evs[i]
+        e[0].record(stream)
+        step_fn(e[1:1 + marks])
+        e[-1].record(stream)
+    torch.cuda.synchronize()
+    tot = [e[0].elapsed_time(e[-1]) for e in evs]
+    parts = [[e[j].elapsed_time(e[j + 1]) for j in range(1 + marks)] for e in evs]
+    return tot, parts
+
+
+# ------------------------------------------------------------ our arm
+
+def run_ours(args, rank, local, ws):
+    import numpy as np
+    import torch
+
+    import __graft_entry__ as ge
+    ge.build_library()
+    from mxfp4_block_scaled_gb300 import fp4
+    from mxfp4_block_scaled_gb300 import inputs as I
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    L = fp4.lib()
+    peaks = load_peaks()
+
+    a_cpu = I.randn_bf16((M, K), 2)
+    w_cpu = I.weights_bf16(N, K, 102)
+    a = a_cpu.to(dev)
+    wq = fp4.prepack_weight(w_cpu.to(dev))
+    aq = fp4.empty_qtensor(fp4.NVFP4, M, K, dev)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    qws = torch.empty(max(L.fp4_quantize_workspace_size(0, M, K), 256), dtype=torch.uint8, device=dev)
+    gws_n = L.fp4_gemm_prequant_workspace_size(0, M, N, K)
+    gws = torch.empty(max(gws_n, 256), dtype=torch.uint8, device=dev)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = fp4._stream()
+    p = fp4._ptr
+
+    def step(marks):
+        # one layer call = quantise (amax + quantise launches) + GEMM launch,
+        # with an event between them to time the GEMM kernel on its own
+        fp4._check(L.fp4_quantize_act(0, p(a), M, K, 0, 0.0, p(aq.codes), p(aq.scales), p(aq.gscale), p(qws),
+                                      qws.numel(), stream))
+        if marks:
+            marks[0].record()
+        fp4._check(L.fp4_gemm_prequant(0, p(aq.codes), p(aq.scales), p(aq.gscale), M, p(wq.codes), p(wq.scales),
+                                       p(wq.gscale), N, K, p(out), p(gws), gws.numel(), stream))
+
+    def flush():
+        flush_buf.zero_()
+
+    if args.profile:
+        for _ in range(args.warmup + args.steps):
+            step(None)
+        torch.cuda.synchronize()
+        fp4.device_status()
+        return {"profile": True, "steps": args.steps, "warmup": args.warmup, "workload": WORKLOAD}
+
+    clocks = ClockSampler(local)
+    barrier(ws)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0 = time.perf_counter()
+    tot, parts = time_steps(torch, args.steps, args.warmup, step, flush=flush, marks=1)
+    barrier(ws)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    ck = clocks.stop()
+    fp4.device_status()
+
+    ms = statistics.mean(tot)
+    ms_max = reduce_max(ms, ws)
+    flops = 2.0 * M * N * K
+    value = reduce_sum(flops * args.steps, ws) / (ms_max * 1e-3 * args.steps) / 1e12
+    gemm_ms = statistics.mean(pp[1] for pp in parts)
+    quant_ms = statistics.mean(pp[0] for pp in parts)
+    peak_fp4 = peaks["bf16_sustained"] * FP4_PER_BF16
+    achieved = flops / (gemm_ms * 1e-3) / 1e12
+    traffic = profile_traffic("gemm_nvfp4_prefill_m8192_n14336_k4096.md", GEMM_SOURCES)
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(torch, fp4, L, a_cpu, wq, dev, max(3, args.steps // 4))
+
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp4 (e2m1) x fp4 -> fp32 acc, bf16 out", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "m": M, "k": K, "n": N, "format": "NVFP4", "activation_scale": "dynamic",
+                   "l2": "flushed between steps (512 MiB write, outside the timed events)",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "kernel": "gemm_kernel<256, NVFP4, bf16 epilogue>",
+                     "achieved": round(achieved, 1), "peak": round(peak_fp4, 1), "unit": "TFLOP/s",
+                     "frac": round(achieved / peak_fp4, 4), "traffic": traffic,
+                     "peak_source": "%s bf16 sustained %.1f TF/s x %.0f (nominal FP4:bf16)" % (
+                         peaks["source"], peaks["bf16_sustained"], FP4_PER_BF16),
+                     "kernel_ms": round(gemm_ms, 5)},
+        "quantiser": {"ms": round(quant_ms, 5),
+                      "gbs": round((M * K * 2 + M * K / 2 + M * K / 16) / (quant_ms * 1e-3) / 1e9, 1),
+                      "note": "algorithmic bytes: bf16 read once + codes + scales written"},
+        "e2e": e2e,
+        "clocks": ck,
+        "gpu_launches": 3 * (args.steps + args.warmup),
+        "wall_s": round(wall, 3),
+    }
+    if not args.no_secondary:
+        res["secondary"] = run_secondary(torch, fp4, L, I, dev, peaks)
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline()
+    return res
+
+
+def run_e2e(torch, fp4, L, a_cpu, wq, dev, steps):
+    """fp4_gemm with the activations copied from pinned host memory and the
+    output copied back, every step, inside the timed region."""
+    a_host = a_cpu.pin_memory()
+    out_host = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    a_dev = torch.empty_like(a_cpu, device=dev)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(L.fp4_gemm_workspace_size(0, M, N, K), dtype=torch.uint8, device=dev)
+
+    def step(_):
+        a_dev.copy_(a_host, non_blocking=True)
+        fp4.gemm(a_dev, wq, out=out, workspace=ws)
+        out_host.copy_(out, non_blocking=True)
+
+    tot, _ = time_steps(torch, steps, 2, step)
+    ms = statistics.mean(tot)
+    return {"value": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 2}
+
+
+def graph_time(torch, fn_list, iters=20):
+    """Capture the calls in fn_list once into a CUDA graph (each call one
+    step, e.g. over rotating weight copies); returns ms per step."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for fn in fn_list:
+            fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for fn in fn_list:
+            fn()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (iters * len(fn_list))
+
+
+def run_secondary(torch, fp4, L, I, dev, peaks):
+    out = {}
+    hbm = peaks["hbm_gbs"]
+    # decode: K=4096, N=14336, M in {1, 8, 32}; weights rotated over copies
+    # whose total exceeds 2x L2 so every step streams them from HBM
+    nk = 4096
+    w = I.weights_bf16(14336, nk, 101).to(dev)
+    copies = [fp4.prepack_weight(w) for _ in range(8)]
+    wbytes = 14336 * nk // 2 + L.fp4_scales_bytes(0, 14336, nk)
+    for m in (1, 8, 32):
+        a = I.activations_with_outliers(m, nk, 1).to(dev)
+        o = torch.empty((m, 14336), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(L.fp4_gemm_workspace_size(0, m, 14336, nk), dtype=torch.uint8, device=dev)
+        fns = [(lambda wq=wq: fp4.gemm(a, wq, out=o, workspace=ws)) for wq in copies]
+        ms = graph_time(torch, fns)
+        byt = wbytes + m * nk * 2 + m * 14336 * 2
+        out["decode_m%d" % m] = {"us": round(ms * 1e3, 2), "GB/s": round(byt / (ms * 1e-3) / 1e9, 1),
+                                 "frac_hbm": round(byt / (ms * 1e-3) / 1e9 / hbm, 4),
+                                 "note": "quantise + split-K GEMM + reduce, CUDA graph, 8 rotating weight copies"}
+    del copies
+    # MXFP4 M=2048 K=7168 N=2048
+    a = I.randn_bf16((2048, 7168), 4).to(dev)
+    wq = fp4.prepack_weight(I.weights_bf16(2048, 7168, 104).to(dev), fp4.MXFP4)
+    o = torch.empty((2048, 2048), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(L.fp4_gemm_workspace_size(1, 2048, 2048, 7168), dtype=torch.uint8, device=dev)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    tot, _ = time_steps(torch, 20, 3, lambda _: fp4.gemm(a, wq, out=o, workspace=ws), flush=flush_buf.zero_)
+    ms = statistics.mean(tot)
+    fl = 2.0 * 2048 * 2048 * 7168
+    out["mxfp4_m2048_k7168_n2048"] = {"us": round(ms * 1e3, 2), "TFLOP/s": round(fl / (ms * 1e-3) / 1e12, 1),
+                                      "frac_fp4_peak": round(fl / (ms * 1e-3) / 1e12 /
+                                                             (peaks["bf16"] * FP4_PER_BF16), 4),
+                                      "note": "quantise (one pass) + GEMM, L2 flushed between steps"}
+    return out
+
+
+# ------------------------------------------------------- oracle (CPU) arm
+
+def oracle_sample(rows, a_cpu=None, qw=None):
+    """The CPU oracle as it stands on `rows` rows of the workload: quantise
+    the activation rows, then its dequantise + fp64 GEMM against the
+    pre-quantised weights.  Returns seconds."""
+    import oracle as O
+    from mxfp4_block_scaled_gb300 import inputs as I
+    if a_cpu is None:
+        a_cpu = I.randn_bf16((rows, K), 2)
+    t0 = time.perf_counter()
+    qa = O.quantize_nvfp4(I.u16(a_cpu[:rows]))
+    O.gemm(O.NVFP4, qa[0], qa[1], qa[2], *qw)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(target_s=10.0):
+    import oracle as O
+    from mxfp4_block_scaled_gb300 import inputs as I
+    w_cpu = I.weights_bf16(N, K, 102)
+    qw = O.quantize_nvfp4(I.u16(w_cpu))  # weights are pre-quantised in the workload (untimed)
+    a_cpu = I.randn_bf16((1024, K), 2)
+    t = oracle_sample(16, a_cpu, qw)
+    rows = int(min(1024, max(16, 16 * target_s / max(t, 1e-3))))
+    t = oracle_sample(rows, a_cpu, qw)
+    return {"value": round(2.0 * rows * N * K / t / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle", "seconds": round(t, 2),
+            "sample": "%d of %d activation rows (quantise + dequantise-and-fp64 GEMM vs pre-quantised W "
+                      "[14336, 4096]); numpy BLAS threads = cores" % (rows, M)}
+
+
+def run_reference(args, rank, ws):
+    if rank != 0:
+        return None
+    import oracle as O
+    from mxfp4_block_scaled_gb300 import inputs as I
+    w_cpu = I.weights_bf16(N, K, 102)
+    qw = O.quantize_nvfp4(I.u16(w_cpu))
+    a_cpu = I.randn_bf16((64, K), 2)
+    rows = 16
+    for _ in range(args.warmup):
+        oracle_sample(rows, a_cpu, qw)
+    times = [oracle_sample(rows, a_cpu, qw) for _ in range(args.steps)]
+    s = statistics.mean(times)
+    v = 2.0 * rows * N * K / s / 1e12
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (dequantised fp4)", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "m": M, "k": K, "n": N, "format": "NVFP4"},
+            "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": "%d activation rows per step" % rows},
+            "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, local, ws = dist_setup(args)
+    if args.impl == "reference":
+        res = run_reference(args, rank, ws)
+    else:
+        res = run_ours(args, rank, local, ws)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
