@@ -130,6 +130,26 @@ fp4_status fp4_quantize_act(int fmt, const void* x_bf16, int64_t rows, int64_t k
                             void* codes, void* scales, float* global_scale, void* workspace, size_t workspace_bytes,
                             void* stream);
 
+/* fp4_quantize_act without a workspace, for callers that cannot allocate
+ * device memory: code that runs under another component's memory plan (a
+ * framework that forbids allocation on its hot path, a pre-built CUDA graph
+ * with fixed buffers, a real-time loop) or a C caller with no device
+ * allocator.  The paper has no counterpart to this entry point.
+ * Same arguments, results and errors as fp4_quantize_act, minus the
+ * workspace: the dynamic NVFP4 amax partials go to a static device array of
+ * 1024 floats (4 KiB) that every GPU loading the library keeps until the
+ * process exits; a launch that would need more partial slots is rejected with
+ * FP4_ERR_WORKSPACE.  No cudaMalloc / cudaFree or allocating library call is
+ * made.  The first call on each device looks the array's device address up
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the array, so calls that
+ * overlap on the GPU (other streams, other host threads) race; the array keeps
+ * the last call's contents, and every slot a call reads is written earlier
+ * in that same call. */
+fp4_status fp4_quantize_act_noalloc(int fmt, const void* x_bf16, int64_t rows, int64_t k, int mode,
+                                    float static_scale, void* codes, void* scales, float* global_scale,
+                                    void* stream);
+
 /* Weight preparation (done once at load time, not on the hot path): the same
  * quantiser with a dynamic per-tensor scale, w [n, k] -> codes, MMA-layout
  * scales and *global_scale.  The scale layout conversion to the MMA layout

@@ -47,6 +47,7 @@ _SIGNATURES = {
     "fp4_debug_timeout_probe": (_INT, [_I64, _P]),
     "fp4_quantize_workspace_size": (_SZ, [_INT, _I64, _I64]),
     "fp4_quantize_act": (_INT, [_INT, _P, _I64, _I64, _INT, _F, _P, _P, _P, _P, _SZ, _P]),
+    "fp4_quantize_act_noalloc": (_INT, [_INT, _P, _I64, _I64, _INT, _F, _P, _P, _P, _P]),
     "fp4_prepack_weight": (_INT, [_INT, _P, _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
     "fp4_gemm_workspace_size": (_SZ, [_INT, _I64, _I64, _I64]),
     "fp4_gemm": (_INT, [_INT, _P, _I64, _INT, _F, _P, _P, _P, _I64, _I64, _P, _P, _SZ, _P]),
