@@ -46,6 +46,7 @@ struct QuantLaunch {
     int64_t rows_pad = 0;         // destination rows whose scales are written (>= rows, multiple of 128)
     int64_t k = 0;
     const int32_t* row_map = nullptr;  // dest row -> source row (-1: zero row); nullptr = identity
+    bool row_map_is_mask = false;      // row_map[r] >= 0 only marks row r as real (source row = r)
     uint8_t* codes = nullptr;
     uint8_t* scales = nullptr;
     int sg_mode = SG_STATIC;

@@ -1,27 +1,748 @@
-// moe.cu -- fused-MoE pipeline (entry points stubbed until the kernels land).
+// moe.cu -- NVFP4 fused-MoE layer: routing, permutation, grouped expert GEMMs
+// with the SwiGLU and combine epilogues, per-expert requantisation.
+//
+// The stages follow "vLLM on DGX Spark: technical report", section 7.1 (router
+// -> quantise/dispatch -> permute, experts, unpermute -> combine) and the
+// expert computation of section 4.3 (two GEMMs, SwiGLU, top-k weighted
+// reduction).  Launch chain on one stream, no host synchronisation:
+//   1 route     top-k per token (warp per token), renormalised weights, expert
+//               bitmap; zeroes the fp32 output accumulator and the h amax
+//   2 scan      (one CTA) expert counts, padded offsets (128-row tiles per
+//               expert), tile -> expert map, row -> (token, slot) map
+//   3 amax      hidden amax partials (dynamic scale)
+//   4 quantise  hidden rows straight into expert-sorted padded order
+//   5 GEMM1     grouped tcgen05 GEMM against the interleaved W13, epilogue
+//               h = bf16(SiLU(gate) * up) and the per-expert amax of h
+//   6 requant   h -> NVFP4 with s_gH[e] = amax_e / 2688
+//   7 GEMM2     grouped tcgen05 GEMM against W2, epilogue
+//               y[token] += weight * alpha2 * D (fp32 reductions)
+//   8 finalise  y -> bf16
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
+namespace fp4 {
+
+static constexpr int kMaxExperts = 1024;
+static constexpr int kMaxTopK = 32;
+static constexpr int kMaxStaticExperts = 256;
+
+// ---------------------------------------------------------------- layout
+
+enum MoeSlot : int {
+    MS_IDS = 0,
+    MS_WEIGHTS,
+    MS_OFFSETS,
+    MS_PADDED,
+    MS_ROW_SRC,
+    MS_A_CODES,
+    MS_A_SCALES,
+    MS_SG_A,
+    MS_H,
+    MS_AMAX_H,
+    MS_SG_H,
+    MS_H_CODES,
+    MS_H_SCALES,
+    MS_Y,
+    MS_PUBLIC_END,  // entry 14 of the public layout is R (the padded row capacity)
+    // internal
+    MS_BITMAP = MS_PUBLIC_END,
+    MS_WPREFIX,
+    MS_TILE_EXPERT,
+    MS_NPTILES,
+    MS_ROW_VALID_END,
+    MS_ROW_TOK,
+    MS_PARTIALS,
+    MS_STATIC13,
+    MS_STATIC2,
+    MS_COUNT
+};
+
+struct MoeLayout {
+    int64_t off[MS_COUNT];
+    int64_t total;
+    int64_t R;  // padded row capacity (multiple of 128)
+    int64_t W;  // bitmap words per expert
+};
+
+static int64_t a256(int64_t x) { return (x + 255) & ~(int64_t)255; }
+
+static MoeLayout moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
+    MoeLayout L;
+    const int64_t slots = T * k;
+    const int64_t active = slots < E ? slots : E;
+    L.R = round_up(slots + active * 127, 128);
+    if (L.R < 128) L.R = 128;
+    L.W = (T + 31) / 32;
+    int64_t sz[MS_COUNT];
+    sz[MS_IDS] = slots * 4;
+    sz[MS_WEIGHTS] = slots * 4;
+    sz[MS_OFFSETS] = (E + 1) * 4;
+    sz[MS_PADDED] = (E + 1) * 4;
+    sz[MS_ROW_SRC] = L.R * 4;
+    sz[MS_A_CODES] = L.R * H / 2;
+    sz[MS_A_SCALES] = L.R * sf_cols_padded(H, 16);
+    sz[MS_SG_A] = E * 4;
+    sz[MS_H] = L.R * I * 2;
+    sz[MS_AMAX_H] = E * 4;
+    sz[MS_SG_H] = E * 4;
+    sz[MS_H_CODES] = L.R * I / 2;
+    sz[MS_H_SCALES] = L.R * sf_cols_padded(I, 16);
+    sz[MS_Y] = T * H * 4;
+    sz[MS_BITMAP] = E * L.W * 4;
+    sz[MS_WPREFIX] = E * L.W * 4;
+    sz[MS_TILE_EXPERT] = (L.R / 128) * 4;
+    sz[MS_NPTILES] = 16;
+    sz[MS_ROW_VALID_END] = (L.R / 128) * 4;
+    sz[MS_ROW_TOK] = L.R * 4;
+    sz[MS_PARTIALS] = 4096;
+    sz[MS_STATIC13] = E * 4;
+    sz[MS_STATIC2] = E * 4;
+    int64_t o = 0;
+    for (int i = 0; i < MS_COUNT; ++i) {
+        L.off[i] = o;
+        o += a256(sz[i] > 0 ? sz[i] : 16);
+    }
+    L.total = o;
+    return L;
+}
+
+// ------------------------------------------------------------ kernels
+
+struct StaticScales {
+    float s13[kMaxStaticExperts];
+    float s2[kMaxStaticExperts];
+};
+
+struct RouteArgs {
+    const float* logits;
+    int64_t T;
+    int E, k;
+    int32_t* ids;
+    float* weights;
+    uint32_t* bitmap;  // [E][W]
+    int64_t W;
+    float* y;          // zeroed: [T*H] fp32
+    int64_t y_elems;
+    float* amax_h;     // zeroed: [E]
+    int route_blocks;
+    int has_static;
+    float* static13_out;
+    float* static2_out;
+    int zero_outputs;  // 0: route only (staged runs zero in their own stage)
+};
+
+// Warp-cooperative top-k over one token's logits; ties go to the lower
+// expert index.  Lane j < k returns the j-th selection and its weight
+// exp(l_j - l_max) / sum over the selection.
+template <int PER_LANE>
+__device__ __forceinline__ void topk_token(const float* row, int E, int k, int lane, int& my_e, float& my_w) {
+    float v[PER_LANE];
+#pragma unroll
+    for (int q = 0; q < PER_LANE; ++q) {
+        const int e = q * 32 + lane;
+        v[q] = e < E ? row[e] : -INFINITY;
+    }
+    uint32_t taken = 0;
+    float v0 = 0.0f, sum = 0.0f, mine = 0.0f;
+    my_e = 0;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int be = 0x7FFFFFFF;
+#pragma unroll
+        for (int q = 0; q < PER_LANE; ++q) {
+            const int e = q * 32 + lane;
+            if (e < E && !((taken >> q) & 1u) && (v[q] > bv || be == 0x7FFFFFFF)) {
+                bv = v[q];
+                be = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+            const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
+            if (ov > bv || (ov == bv && oe < be)) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        if (j == 0) v0 = bv;
+        const float ex = expf(bv - v0);
+        sum += ex;
+        if (lane == j) {
+            my_e = be;
+            mine = ex;
+        }
+    }
+    my_w = __fdiv_rn(mine, sum);
+}
+
+template <int PER_LANE>
+__global__ void __launch_bounds__(256) moe_route_kernel(const RouteArgs a, const StaticScales st) {
+    extern __shared__ uint32_t sbm[];  // [E][8] bitmap words of this block's 256 tokens
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (blockIdx.x == 0) {
+        if (a.zero_outputs)
+            for (int e = threadIdx.x; e < a.E; e += 256) a.amax_h[e] = 0.0f;
+        if (a.has_static)
+            for (int e = threadIdx.x; e < a.E; e += 256) {
+                a.static13_out[e] = st.s13[e];
+                a.static2_out[e] = st.s2[e];
+            }
+    }
+    if ((int)blockIdx.x < a.route_blocks) {
+        for (int i = threadIdx.x; i < a.E * 8; i += 256) sbm[i] = 0u;
+        __syncthreads();
+        for (int i = 0; i < 32; ++i) {
+            const int64_t t = (int64_t)blockIdx.x * 256 + warp * 32 + i;
+            if (t >= a.T) break;
+            int e;
+            float w;
+            topk_token<PER_LANE>(a.logits + t * a.E, a.E, a.k, lane, e, w);
+            if (lane < a.k) {
+                a.ids[t * a.k + lane] = e;
+                a.weights[t * a.k + lane] = w;
+                atomicOr(&sbm[e * 8 + warp], 1u << i);
+            }
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < a.E * 8; i += 256) {
+            const int e = i >> 3, w = i & 7;
+            const int64_t word = (int64_t)blockIdx.x * 8 + w;
+            if (word < a.W) a.bitmap[e * a.W + word] = sbm[i];
+        }
+    } else if (a.zero_outputs) {
+        const int64_t nb = (int64_t)gridDim.x - a.route_blocks;
+        float4* y4 = reinterpret_cast<float4*>(a.y);
+        const int64_t n4 = a.y_elems / 4;
+        for (int64_t i = ((int64_t)blockIdx.x - a.route_blocks) * 256 + threadIdx.x; i < n4; i += nb * 256)
+            y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    pdl_launch_dependents();
+}
+
+struct ScanArgs {
+    const uint32_t* bitmap;  // [E][W]
+    int32_t* wprefix;        // [E][W]
+    const int32_t* ids;      // [T*k]
+    int64_t T, W;
+    int E, k;
+    int32_t* offsets;        // [E+1]
+    int32_t* padded;         // [E+1]
+    int32_t* n_ptiles;
+    int32_t* tile_expert;    // [R/128]
+    int32_t* row_valid_end;  // [R/128]
+    int32_t* row_src;        // [R]
+    int32_t* row_tok;        // [R]
+};
+
+// One CTA: counts and word-level prefix counts per expert from the bitmap,
+// exclusive scans over experts (plain and padded to 128 rows), the tile map,
+// then every assignment's row = padded[e] + (tokens before it routed to e).
+__global__ void __launch_bounds__(1024) moe_scan_kernel(const ScanArgs a) {
+    __shared__ int32_t cnt[kMaxExperts];
+    __shared__ int32_t pad[kMaxExperts + 1];
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int e = warp; e < a.E; e += 32) {
+        int32_t base = 0;
+        for (int64_t w0 = 0; w0 < a.W; w0 += 32) {
+            const int64_t w = w0 + lane;
+            const int32_t c = w < a.W ? __popc(a.bitmap[e * a.W + w]) : 0;
+            int32_t incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            if (w < a.W) a.wprefix[e * a.W + w] = base + incl - c;
+            base += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (lane == 0) cnt[e] = base;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int32_t o = 0, p = 0;
+        for (int e = 0; e < a.E; ++e) {
+            a.offsets[e] = o;
+            pad[e] = p;
+            a.padded[e] = p;
+            o += cnt[e];
+            p += (cnt[e] + 127) / 128 * 128;
+        }
+        a.offsets[a.E] = o;
+        a.padded[a.E] = p;
+        pad[a.E] = p;
+        *a.n_ptiles = p / 128;
+    }
+    __syncthreads();
+    for (int e = warp; e < a.E; e += 32) {
+        const int32_t t0 = pad[e] / 128, t1 = pad[e + 1] / 128;
+        for (int32_t t = t0 + lane; t < t1; t += 32) {
+            a.tile_expert[t] = e;
+            a.row_valid_end[t] = pad[e] + cnt[e];
+        }
+        for (int32_t r = pad[e] + cnt[e] + lane; r < pad[e + 1]; r += 32) {
+            a.row_src[r] = -1;
+            a.row_tok[r] = -1;
+        }
+    }
+    const int64_t slots = a.T * a.k;
+    for (int64_t s = threadIdx.x; s < slots; s += blockDim.x) {
+        const int64_t t = s / a.k;
+        const int e = a.ids[s];
+        const int64_t w = t >> 5;
+        const uint32_t below = a.bitmap[e * a.W + w] & ((1u << (t & 31)) - 1u);
+        const int64_t row = pad[e] + a.wprefix[e * a.W + w] + __popc(below);
+        a.row_src[row] = (int32_t)s;
+        a.row_tok[row] = (int32_t)t;
+    }
+    pdl_launch_dependents();
+}
+
+// fp32 accumulator -> bf16 output
+__global__ void __launch_bounds__(256) moe_finalize_kernel(const float4* __restrict__ y, uint2* __restrict__ out,
+                                                           int64_t n4) {
+    pdl_wait();
+    for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n4; i += (int64_t)gridDim.x * 256) {
+        const float4 v = y[i];
+        __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+        out[i] = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+    }
+    pdl_launch_dependents();
+}
+
+// zero n floats (staged runs)
+__global__ void __launch_bounds__(256) zero_kernel(float4* __restrict__ p, int64_t n4) {
+    pdl_wait();
+    for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n4; i += (int64_t)gridDim.x * 256)
+        p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    pdl_launch_dependents();
+}
+
+// W13 row interleave for the prepack: destination row r of an expert's
+// [2I, H] block <- source row (gate rows 0..I-1, up rows I..2I-1), groups of 32.
+__global__ void w13_interleave_map_kernel(int32_t* map, int64_t I) {
+    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < 2 * I; r += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t b = r / 64, w = r % 64;
+        map[r] = (int32_t)(w < 32 ? b * 32 + w : I + b * 32 + (w - 32));
+    }
+}
+
+static cudaError_t launch_k(const void* fn, dim3 grid, dim3 block, size_t smem, bool pdl, cudaStream_t s,
+                            void** args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+}  // namespace fp4
+
 using namespace fp4;
 
-extern "C" size_t fp4_moe_prepack_workspace_size(int64_t, int64_t, int64_t) { return 4096; }
-extern "C" fp4_status fp4_moe_prepack_weights(const void*, const void*, int64_t, int64_t, int64_t, void*, void*, float*,
-                                              void*, void*, float*, void*, size_t, void*) {
-    set_error("MoE not built yet");
-    return FP4_ERR_INVALID_ARG;
+#define MOE_CHECK(cond, status, ...) \
+    do {                             \
+        if (!(cond)) {               \
+            set_error(__VA_ARGS__);  \
+            return (status);         \
+        }                            \
+    } while (0)
+
+#define MOE_CUDA(call, what)                                                   \
+    do {                                                                       \
+        cudaError_t _e = (call);                                               \
+        if (_e != cudaSuccess) {                                               \
+            cudaGetLastError();                                                \
+            set_error("%s: %s", what, cudaGetErrorString(_e));                 \
+            return FP4_ERR_CUDA;                                               \
+        }                                                                      \
+    } while (0)
+
+static bool al16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+// ------------------------------------------------------------ prepack
+
+extern "C" size_t fp4_moe_prepack_workspace_size(int64_t E, int64_t H, int64_t I) {
+    (void)E;
+    (void)H;
+    if (I <= 0) return 4096;
+    return 4096 + (size_t)a256(2 * I * 4);
 }
-extern "C" size_t fp4_moe_workspace_size(int64_t, int64_t, int64_t, int64_t, int64_t) { return 0; }
-extern "C" int fp4_moe_workspace_layout(int64_t, int64_t, int64_t, int64_t, int64_t, int64_t*, int) { return 0; }
-extern "C" fp4_status fp4_moe_grouped(const void*, const float*, int64_t, int64_t, int64_t, int64_t, int64_t, int,
-                                      const float*, const float*, const void*, const void*, const float*,
-                                      const void*, const void*, const float*, void*, void*, size_t, void*) {
-    set_error("MoE not built yet");
-    return FP4_ERR_INVALID_ARG;
+
+extern "C" fp4_status fp4_moe_prepack_weights(const void* w13, const void* w2, int64_t E, int64_t H, int64_t I,
+                                              void* w13_codes, void* w13_scales, float* w13_global, void* w2_codes,
+                                              void* w2_scales, float* w2_global, void* ws, size_t wsb,
+                                              void* stream) {
+    MOE_CHECK(E > 0 && E <= kMaxExperts, FP4_ERR_SHAPE, "n_experts = %lld must be in [1, %d]", (long long)E,
+              kMaxExperts);
+    MOE_CHECK(H > 0 && H % 128 == 0 && I > 0 && I % 64 == 0, FP4_ERR_SHAPE,
+              "hidden must be a positive multiple of 128 and inter of 64 (hidden %lld, inter %lld)", (long long)H,
+              (long long)I);
+    MOE_CHECK(w13 && w2 && w13_codes && w13_scales && w13_global && w2_codes && w2_scales && w2_global,
+              FP4_ERR_INVALID_ARG, "null pointer argument");
+    MOE_CHECK(al16(w13) && al16(w2) && al16(w13_codes) && al16(w13_scales) && al16(w2_codes) && al16(w2_scales) &&
+                  ((uintptr_t)w13_global & 3) == 0 && ((uintptr_t)w2_global & 3) == 0,
+              FP4_ERR_ALIGNMENT, "pointers must be 16-byte aligned (global scales 4-byte)");
+    const size_t need = fp4_moe_prepack_workspace_size(E, H, I);
+    MOE_CHECK(ws && wsb >= need && al16(ws), FP4_ERR_WORKSPACE, "workspace %zu bytes, need %zu", wsb, need);
+    fp4_status st = check_arch();
+    if (st != FP4_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    float* partials = static_cast<float*>(ws);
+    int32_t* map = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + 4096);
+    w13_interleave_map_kernel<<<(unsigned)((2 * I + 255) / 256), 256, 0, s>>>(map, I);
+    MOE_CUDA(cudaGetLastError(), "interleave map launch");
+    const size_t sc13 = (size_t)round_up(2 * I, 128) * sf_cols_padded(H, 16);
+    const size_t sc2 = (size_t)round_up(H, 128) * sf_cols_padded(I, 16);
+    for (int64_t e = 0; e < E; ++e) {
+        for (int which = 0; which < 2; ++which) {
+            QuantLaunch q;
+            q.fmt = FP4_NVFP4;
+            if (which == 0) {
+                q.x = static_cast<const uint16_t*>(w13) + e * 2 * I * H;
+                q.x_ld = H;
+                q.rows = 2 * I;
+                q.k = H;
+                q.row_map = map;
+                q.codes = static_cast<uint8_t*>(w13_codes) + e * 2 * I * (H / 2);
+                q.scales = static_cast<uint8_t*>(w13_scales) + e * sc13;
+                q.global_out = w13_global + e;
+            } else {
+                q.x = static_cast<const uint16_t*>(w2) + e * H * I;
+                q.x_ld = I;
+                q.rows = H;
+                q.k = I;
+                q.codes = static_cast<uint8_t*>(w2_codes) + e * H * (I / 2);
+                q.scales = static_cast<uint8_t*>(w2_scales) + e * sc2;
+                q.global_out = w2_global + e;
+            }
+            q.rows_pad = round_up(q.rows, 128);
+            const int np = amax_partials_count(q.rows * q.k);
+            MOE_CUDA(launch_amax_partials(q.x, q.rows * q.k, partials, np, false, s), "amax launch");
+            q.sg_mode = SG_PARTIALS;
+            q.partials = partials;
+            q.n_partials = np;
+            MOE_CUDA(launch_quant(q, s), "quantise launch");
+        }
+    }
+    return FP4_OK;
 }
-extern "C" fp4_status fp4_moe_grouped_stages(const void*, const float*, int64_t, int64_t, int64_t, int64_t, int64_t,
-                                             int, const float*, const float*, const void*, const void*,
-                                             const float*, const void*, const void*, const float*, void*, void*,
-                                             size_t, unsigned, void*) {
-    set_error("MoE not built yet");
-    return FP4_ERR_INVALID_ARG;
+
+// ------------------------------------------------------------ forward
+
+extern "C" size_t fp4_moe_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
+    if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return 0;
+    return (size_t)moe_layout(T, H, I, E, k).total;
+}
+
+extern "C" int fp4_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, int64_t* offsets,
+                                        int max_entries) {
+    if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || !offsets) return 0;
+    MoeLayout L = moe_layout(T, H, I, E, k);
+    int n = 0;
+    for (int i = 0; i < MS_PUBLIC_END && n < max_entries; ++i) offsets[n++] = L.off[i];
+    if (n < max_entries) offsets[n++] = L.R;
+    return n;
+}
+
+enum : unsigned { ST_ROUTE = 1u, ST_QUANT = 2u, ST_GEMM1 = 4u, ST_REQUANT = 8u, ST_GEMM2 = 16u, ST_ALL = 31u };
+
+static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, int64_t H, int64_t I, int64_t E,
+                          int64_t k, int mode, const float* s13, const float* s2, const void* w13c,
+                          const void* w13s, const float* w13g, const void* w2c, const void* w2s, const float* w2g,
+                          void* out, void* ws, size_t wsb, unsigned mask, void* stream) {
+    MOE_CHECK(T >= 0 && T < (1ll << 26), FP4_ERR_SHAPE, "tokens = %lld out of range", (long long)T);
+    MOE_CHECK(E > 0 && E <= kMaxExperts, FP4_ERR_SHAPE, "n_experts = %lld must be in [1, %d]", (long long)E,
+              kMaxExperts);
+    MOE_CHECK(k > 0 && k <= E && k <= kMaxTopK, FP4_ERR_INVALID_ARG, "top_k = %lld must be in [1, min(E, %d)]",
+              (long long)k, kMaxTopK);
+    MOE_CHECK(H > 0 && H % 128 == 0 && I > 0 && I % 64 == 0, FP4_ERR_SHAPE,
+              "hidden must be a positive multiple of 128 and inter of 64");
+    MOE_CHECK(mode == FP4_SCALE_DYNAMIC || mode == FP4_SCALE_STATIC, FP4_ERR_INVALID_ARG, "unknown scale mode %d",
+              mode);
+    if (mode == FP4_SCALE_STATIC) {
+        MOE_CHECK(s13 != nullptr && s2 != nullptr, FP4_ERR_MISSING_SCALE,
+                  "static scale mode without per-expert activation scales (a weight-only checkpoint must use "
+                  "FP4_SCALE_DYNAMIC)");
+        MOE_CHECK(E <= kMaxStaticExperts, FP4_ERR_SHAPE, "static scale mode supports at most %d experts",
+                  kMaxStaticExperts);
+        for (int64_t e = 0; e < E; ++e)
+            MOE_CHECK(isfinite(s13[e]) && s13[e] > 0.0f && isfinite(s2[e]) && s2[e] > 0.0f, FP4_ERR_INVALID_SCALE,
+                      "static activation scale of expert %lld is not finite and > 0 (%g, %g)", (long long)e,
+                      (double)s13[e], (double)s2[e]);
+    }
+    if (T == 0) return check_arch();
+    MOE_CHECK(hidden && logits && w13c && w13s && w13g && w2c && w2s && w2g && out, FP4_ERR_INVALID_ARG,
+              "null pointer argument");
+    MOE_CHECK(al16(hidden) && al16(logits) && al16(w13c) && al16(w13s) && al16(w2c) && al16(w2s) && al16(out) &&
+                  ((uintptr_t)w13g & 3) == 0 && ((uintptr_t)w2g & 3) == 0,
+              FP4_ERR_ALIGNMENT, "pointers must be 16-byte aligned (global scales 4-byte)");
+    const MoeLayout L = moe_layout(T, H, I, E, k);
+    MOE_CHECK(ws && wsb >= (size_t)L.total && ((uintptr_t)ws & 255) == 0, FP4_ERR_WORKSPACE,
+              "workspace %zu bytes, need %lld (256-byte aligned)", wsb, (long long)L.total);
+    fp4_status st = check_arch();
+    if (st != FP4_OK) return st;
+    const DeviceInfo* d = current_device();
+    cudaStream_t s = (cudaStream_t)stream;
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    auto at = [&](int slot) { return b + L.off[slot]; };
+    int32_t* ids = (int32_t*)at(MS_IDS);
+    float* wts = (float*)at(MS_WEIGHTS);
+    int32_t* offsets = (int32_t*)at(MS_OFFSETS);
+    int32_t* padded = (int32_t*)at(MS_PADDED);
+    int32_t* row_src = (int32_t*)at(MS_ROW_SRC);
+    uint8_t* a_codes = at(MS_A_CODES);
+    uint8_t* a_scales = at(MS_A_SCALES);
+    float* sg_a = (float*)at(MS_SG_A);
+    uint16_t* h = (uint16_t*)at(MS_H);
+    float* amax_h = (float*)at(MS_AMAX_H);
+    float* sg_h = (float*)at(MS_SG_H);
+    uint8_t* h_codes = at(MS_H_CODES);
+    uint8_t* h_scales = at(MS_H_SCALES);
+    float* y = (float*)at(MS_Y);
+    uint32_t* bitmap = (uint32_t*)at(MS_BITMAP);
+    int32_t* wprefix = (int32_t*)at(MS_WPREFIX);
+    int32_t* tile_expert = (int32_t*)at(MS_TILE_EXPERT);
+    int32_t* n_ptiles = (int32_t*)at(MS_NPTILES);
+    int32_t* row_valid_end = (int32_t*)at(MS_ROW_VALID_END);
+    int32_t* row_tok = (int32_t*)at(MS_ROW_TOK);
+    float* partials = (float*)at(MS_PARTIALS);
+    float* st13 = (float*)at(MS_STATIC13);
+    float* st2 = (float*)at(MS_STATIC2);
+    const bool is_static = mode == FP4_SCALE_STATIC;
+    const bool full = (mask & ST_ALL) == ST_ALL;
+    bool pdl = false;  // first launch of the call waits for everything before it
+
+    // 1. route (+ zeroing of y and amax_h when the whole pipeline runs)
+    if (mask & ST_ROUTE) {
+        RouteArgs ra;
+        ra.logits = logits;
+        ra.T = T;
+        ra.E = (int)E;
+        ra.k = (int)k;
+        ra.ids = ids;
+        ra.weights = wts;
+        ra.bitmap = bitmap;
+        ra.W = L.W;
+        ra.y = y;
+        ra.y_elems = T * H;
+        ra.amax_h = amax_h;
+        ra.route_blocks = (int)((T + 255) / 256);
+        ra.has_static = is_static ? 1 : 0;
+        ra.static13_out = st13;
+        ra.static2_out = st2;
+        ra.zero_outputs = full ? 1 : 0;
+        StaticScales sc;
+        memset(&sc, 0, sizeof(sc));
+        if (is_static)
+            for (int64_t e = 0; e < E; ++e) sc.s13[e] = s13[e], sc.s2[e] = s2[e];
+        int zero_blocks = full ? (int)std::min<int64_t>((T * H / 4 + 255) / 256, (int64_t)d->sm_count * 4) : 0;
+        void* args[] = {(void*)&ra, (void*)&sc};
+        const int per_lane = (int)((E + 31) / 32);
+        const void* fn = per_lane <= 4 ? (const void*)moe_route_kernel<4>
+                         : per_lane <= 8 ? (const void*)moe_route_kernel<8>
+                         : per_lane <= 16 ? (const void*)moe_route_kernel<16>
+                                          : (const void*)moe_route_kernel<32>;
+        MOE_CUDA(launch_k(fn, dim3(ra.route_blocks + zero_blocks), dim3(256), (size_t)E * 8 * 4, pdl, s, args),
+                 "route launch");
+        pdl = true;
+        ScanArgs sa;
+        sa.bitmap = bitmap;
+        sa.wprefix = wprefix;
+        sa.ids = ids;
+        sa.T = T;
+        sa.W = L.W;
+        sa.E = (int)E;
+        sa.k = (int)k;
+        sa.offsets = offsets;
+        sa.padded = padded;
+        sa.n_ptiles = n_ptiles;
+        sa.tile_expert = tile_expert;
+        sa.row_valid_end = row_valid_end;
+        sa.row_src = row_src;
+        sa.row_tok = row_tok;
+        void* sargs[] = {(void*)&sa};
+        MOE_CUDA(launch_k((const void*)moe_scan_kernel, dim3(1), dim3(1024), 0, pdl, s, sargs), "scan launch");
+    }
+    // 2-3. hidden amax (dynamic) and quantise into expert-sorted padded rows
+    if (mask & ST_QUANT) {
+        QuantLaunch q;
+        q.fmt = FP4_NVFP4;
+        q.x = static_cast<const uint16_t*>(hidden);
+        q.x_ld = H;
+        q.rows = L.R;
+        q.rows_pad = L.R;
+        q.k = H;
+        q.row_map = row_tok;
+        q.codes = a_codes;
+        q.scales = a_scales;
+        q.rows_dev = nullptr;
+        q.pdl = pdl;
+        q.tile_expert = tile_expert;
+        q.n_experts = (int)E;
+        if (!is_static) {
+            const int np = amax_partials_count(T * H);
+            MOE_CUDA(launch_amax_partials(q.x, T * H, partials, np, pdl, s), "amax launch");
+            pdl = true;
+            q.pdl = true;
+            q.sg_mode = SG_PARTIALS;
+            q.partials = partials;
+            q.n_partials = np;
+            q.global_out = sg_a;
+        } else {
+            q.sg_mode = SG_EXPERT_TABLE;
+            q.table = st13;
+        }
+        // rows beyond the padded total are skipped: their count is on the device
+        q.rows_dev = padded + E;
+        MOE_CUDA(launch_quant(q, s), "quantise launch");
+        pdl = true;
+    }
+    // 4. GEMM1 + SiLU * up + per-expert amax of h
+    if (mask & ST_GEMM1) {
+        if (!full) {
+            float4* z = reinterpret_cast<float4*>(amax_h);
+            int64_t n4 = (E + 3) / 4;
+            void* zargs[] = {(void*)&z, (void*)&n4};
+            MOE_CUDA(launch_k((const void*)zero_kernel, dim3(1), dim3(256), 0, pdl, s, zargs), "zero launch");
+            pdl = true;
+        }
+        GemmLaunch g;
+        g.fmt = FP4_NVFP4;
+        g.epi = EPI_SWIGLU;
+        // the tile width must divide the expert's 2I rows (tiles never straddle experts)
+        g.bn = (T * k >= 4 * E * 64 && (2 * I) % 256 == 0) ? 256 : 64;
+        g.p_codes = a_codes;
+        g.p_scales = a_scales;
+        g.p_rows = L.R;
+        g.q_codes = static_cast<const uint8_t*>(w13c);
+        g.q_scales = static_cast<const uint8_t*>(w13s);
+        g.q_rows = E * 2 * I;
+        g.q_rows_valid = 2 * I;
+        g.k = H;
+        g.p_global = is_static ? st13 : sg_a;
+        g.p_global_per_expert = is_static;
+        g.q_global = w13g;
+        g.out = h;
+        g.ldo = I;
+        g.grouped = true;
+        g.n_experts = (int)E;
+        g.tile_expert = tile_expert;
+        g.n_ptiles_dev = n_ptiles;
+        g.row_valid_end = row_valid_end;
+        g.amax_out = amax_h;
+        g.pdl = pdl;
+        MOE_CUDA(launch_gemm(g, s), "GEMM1 launch");
+        pdl = true;
+    }
+    // 5. requantise h per expert
+    if (mask & ST_REQUANT) {
+        QuantLaunch q;
+        q.fmt = FP4_NVFP4;
+        q.x = h;
+        q.x_ld = I;
+        q.rows = L.R;
+        q.rows_pad = L.R;
+        q.k = I;
+        q.row_map = row_tok;
+        q.row_map_is_mask = true;
+        q.codes = h_codes;
+        q.scales = h_scales;
+        q.tile_expert = tile_expert;
+        q.n_experts = (int)E;
+        q.rows_dev = padded + E;
+        q.pdl = pdl;
+        if (!is_static) {
+            q.sg_mode = SG_EXPERT_AMAX;
+            q.table = amax_h;
+            q.expert_sg_out = sg_h;
+        } else {
+            q.sg_mode = SG_EXPERT_TABLE;
+            q.table = st2;
+        }
+        MOE_CUDA(launch_quant(q, s), "requantise launch");
+        pdl = true;
+    }
+    // 6. GEMM2 + weighted combine into y, then y -> bf16
+    if (mask & ST_GEMM2) {
+        if (!full) {
+            float4* z = reinterpret_cast<float4*>(y);
+            int64_t n4 = T * H / 4;
+            void* zargs[] = {(void*)&z, (void*)&n4};
+            int64_t zb = std::min<int64_t>((n4 + 255) / 256, (int64_t)d->sm_count * 4);
+            MOE_CUDA(launch_k((const void*)zero_kernel, dim3((unsigned)zb), dim3(256), 0, pdl, s, zargs),
+                     "zero launch");
+            pdl = true;
+        }
+        GemmLaunch g;
+        g.fmt = FP4_NVFP4;
+        g.epi = EPI_COMBINE;
+        // the tile width must divide H (output columns of one token row)
+        g.bn = (T * k >= 4 * E * 64 && H % 256 == 0) ? 256 : 64;
+        g.p_codes = h_codes;
+        g.p_scales = h_scales;
+        g.p_rows = L.R;
+        g.q_codes = static_cast<const uint8_t*>(w2c);
+        g.q_scales = static_cast<const uint8_t*>(w2s);
+        g.q_rows = E * H;
+        g.q_rows_valid = H;
+        g.k = I;
+        g.p_global = is_static ? st2 : sg_h;
+        g.p_global_per_expert = true;
+        g.q_global = w2g;
+        g.out = y;
+        g.ldo = H;
+        g.grouped = true;
+        g.n_experts = (int)E;
+        g.tile_expert = tile_expert;
+        g.n_ptiles_dev = n_ptiles;
+        g.row_valid_end = row_valid_end;
+        g.row_src = row_src;
+        g.slot_weight = wts;
+        g.top_k = (int)k;
+        g.pdl = pdl;
+        MOE_CUDA(launch_gemm(g, s), "GEMM2 launch");
+        const float4* y4 = reinterpret_cast<const float4*>(y);
+        uint2* o2 = reinterpret_cast<uint2*>(out);
+        int64_t n4 = T * H / 4;
+        void* fargs[] = {(void*)&y4, (void*)&o2, (void*)&n4};
+        int64_t fb = std::min<int64_t>((n4 + 255) / 256, (int64_t)d->sm_count * 4);
+        MOE_CUDA(launch_k((const void*)moe_finalize_kernel, dim3((unsigned)fb), dim3(256), 0, true, s, fargs),
+                 "finalise launch");
+    }
+    return FP4_OK;
+}
+
+extern "C" fp4_status fp4_moe_grouped(const void* hidden, const float* logits, int64_t T, int64_t H, int64_t I,
+                                      int64_t E, int64_t k, int mode, const float* s13, const float* s2,
+                                      const void* w13c, const void* w13s, const float* w13g, const void* w2c,
+                                      const void* w2s, const float* w2g, void* out, void* ws, size_t wsb,
+                                      void* stream) {
+    return moe_run(hidden, logits, T, H, I, E, k, mode, s13, s2, w13c, w13s, w13g, w2c, w2s, w2g, out, ws, wsb,
+                   ST_ALL, stream);
+}
+
+extern "C" fp4_status fp4_moe_grouped_stages(const void* hidden, const float* logits, int64_t T, int64_t H,
+                                             int64_t I, int64_t E, int64_t k, int mode, const float* s13,
+                                             const float* s2, const void* w13c, const void* w13s, const float* w13g,
+                                             const void* w2c, const void* w2s, const float* w2g, void* out, void* ws,
+                                             size_t wsb, unsigned mask, void* stream) {
+    return moe_run(hidden, logits, T, H, I, E, k, mode, s13, s2, w13c, w13s, w13g, w2c, w2s, w2g, out, ws, wsb,
+                   mask & ST_ALL, stream);
 }

@@ -148,7 +148,13 @@ __global__ void __launch_bounds__(QT) quant_kernel(const QuantLaunch q) {
         if (r >= row_limit) continue;  // warp-uniform
         const int64_t col = c * 256 + lane * 8;
         int64_t src = -1;
-        if (r < q.rows) src = q.row_map ? (int64_t)q.row_map[r] : r;
+        if (r < q.rows) {
+            src = r;
+            if (q.row_map) {
+                const int64_t m = q.row_map[r];
+                src = q.row_map_is_mask ? (m >= 0 ? r : -1) : m;
+            }
+        }
         const bool in = (src >= 0) && (col < q.k);
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (in) v = __ldg(reinterpret_cast<const uint4*>(q.x + src * q.x_ld + col));

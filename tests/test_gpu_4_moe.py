@@ -1,0 +1,251 @@
+"""Fused MoE on the GPU against the CPU oracle, stage by stage.
+
+One requantisation code flip moves an element by a whole E2M1 step, so the
+chain is checked per stage with the oracle's own values injected into the
+workspace where a stage starts (oracle -> GPU only):
+  1 route + permute    ids, expert offsets, row order: exact; weights 2e-6 rel
+  2 dispatch-quantise  permuted hidden codes / scales / s_gA: bit-exact
+  3 GEMM1 + SiLU*up    h within the bf16-rounding tolerance of the oracle's h
+  4 requantise         (oracle h and amax injected) codes / scales / s_gH bit-exact
+  5 GEMM2 + combine    (oracle requantised h injected) y within tolerance
+  6 end to end         norm-wise error and the fraction of flipped requant codes
+"""
+import numpy as np
+import pytest
+import torch
+
+from mxfp4_block_scaled_gb300 import inputs as I
+from util import bf16_to_np, check_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def F():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    import __graft_entry__ as ge
+    ge.build()
+    from mxfp4_block_scaled_gb300 import fp4
+    return fp4
+
+
+class Case:
+    def __init__(self, F, O, T, E, k, H, Inter, seed, std=0.02):
+        self.T, self.E, self.k, self.H, self.I = T, E, k, H, Inter
+        self.hidden = I.randn_bf16((T, H), seed + 1)
+        self.logits = I.router_logits(T, E, seed + 2)
+        self.w13 = I.expert_weights_bf16(E, 2 * Inter, H, seed + 3, std)
+        self.w2 = I.expert_weights_bf16(E, H, Inter, seed + 4, std)
+        self.mw = F.moe_prepack(self.w13.cuda(), self.w2.cuda())
+        self.q13 = O.quantize_experts(I.u16(self.w13))
+        self.q2 = O.quantize_experts(I.u16(self.w2))
+        self.ref = O.moe(I.u16(self.hidden), self.logits.numpy(), top_k=k, q13=self.q13, q2=self.q2)
+        self.hid_d = self.hidden.cuda()
+        self.log_d = self.logits.cuda()
+        L = F.lib()
+        self.ws = torch.zeros(L.fp4_moe_workspace_size(T, H, Inter, E, k), dtype=torch.uint8, device="cuda")
+        self.off = F.moe_workspace_layout(T, H, Inter, E, k)
+        self.R = self.off[14]
+        counts = self.ref["counts"]
+        self.padded = np.concatenate([[0], np.cumsum((counts + 127) // 128 * 128)]).astype(np.int64)
+
+    def view(self, slot, dtype, shape):
+        nbytes = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+        return self.ws[self.off[slot]:self.off[slot] + nbytes].view(dtype).view(shape)
+
+    def run(self, F, mask=None):
+        out = F.moe(self.hid_d, self.log_d, self.mw, self.k, workspace=self.ws, stage_mask=mask)
+        torch.cuda.synchronize()
+        F.device_status()
+        return out
+
+    def gpu_rows(self):
+        """GPU padded row index of each oracle sorted position."""
+        c, offs = self.ref["counts"], self.ref["offsets"]
+        rows = np.empty(offs[-1], dtype=np.int64)
+        for e in range(self.E):
+            rows[offs[e]:offs[e + 1]] = self.padded[e] + np.arange(c[e])
+        return rows
+
+
+def _stage_checks(F, O, c):
+    T, E, k, H, Inter = c.T, c.E, c.k, c.H, c.I
+    r = c.ref
+    # 1. route + permute
+    c.run(F, mask=1)
+    ids = c.view(0, torch.int32, (T, k)).cpu().numpy()
+    wts = c.view(1, torch.float32, (T, k)).cpu().numpy()
+    assert np.array_equal(ids, r["ids"])
+    assert np.allclose(wts, r["weights"], rtol=2e-6, atol=0)
+    assert np.array_equal(c.view(2, torch.int32, (E + 1,)).cpu().numpy(), r["offsets"])
+    assert np.array_equal(c.view(3, torch.int32, (E + 1,)).cpu().numpy(), c.padded)
+    rows = c.gpu_rows()
+    row_src = c.view(4, torch.int32, (c.R,)).cpu().numpy()
+    assert np.array_equal(row_src[rows], r["order"])
+    pad_rows = np.setdiff1d(np.arange(c.padded[-1]), rows)
+    assert np.all(row_src[pad_rows] == -1)
+    # 2. dispatch-quantise
+    c.run(F, mask=2)
+    codes = c.view(5, torch.uint8, (c.R, H // 2)).cpu().numpy()
+    assert np.array_equal(codes[rows], r["a_codes"])
+    scales = c.view(6, torch.uint8, (c.R * (O.scale_cols_padded(H, 0)),)).cpu().numpy()
+    canon = O.scales_from_mma(scales, c.R, H, 0)
+    assert np.array_equal(canon[rows], r["a_scales"])
+    assert np.all(canon[pad_rows] == 0)
+    assert np.float32(c.view(7, torch.float32, (E,))[0].item()) == np.float32(r["sgA"])
+    # 3. GEMM1 + SiLU * up
+    c.run(F, mask=4)
+    h = bf16_to_np(c.view(8, torch.bfloat16, (c.R, Inter)))[rows]
+    G, Gm = r["G"], r["Gmag"]
+    tau_g = 2.0 ** -18 * Gm + 2.0 ** -22 * np.abs(G)
+    g, u = G[:, :Inter], G[:, Inter:]
+    sg = O.silu(g)
+    tau_h = 1.1 * np.abs(u) * tau_g[:, :Inter] + np.abs(sg) * tau_g[:, Inter:] + 2.0 ** -20 * np.abs(sg * u)
+    check_close(h, r["h64"], np.zeros_like(h), floor=0.0, extra_tau=tau_h, what="h")
+    amax_gpu = c.view(9, torch.float32, (E,)).cpu().numpy()
+    for e in range(E):
+        lo, hi = r["offsets"][e], r["offsets"][e + 1]
+        if hi > lo:
+            assert amax_gpu[e] == np.abs(h[lo:hi]).max()
+    # 4. requantise, from the oracle's h and its per-expert amax
+    hbuf = c.view(8, torch.int16, (c.R, Inter))
+    hb = torch.zeros((c.R, Inter), dtype=torch.int16)
+    hb[torch.from_numpy(rows)] = torch.from_numpy(r["h_bf16"].view(np.int16))
+    hbuf.copy_(hb)
+    amax_o = np.zeros(E, dtype=np.float32)
+    for e in range(E):
+        lo, hi = r["offsets"][e], r["offsets"][e + 1]
+        if hi > lo:
+            amax_o[e] = O.amax_bf16(r["h_bf16"][lo:hi])
+    c.view(9, torch.float32, (E,)).copy_(torch.from_numpy(amax_o))
+    c.run(F, mask=8)
+    hc = c.view(11, torch.uint8, (c.R, Inter // 2)).cpu().numpy()
+    assert np.array_equal(hc[rows], r["h_codes"])
+    hs = O.scales_from_mma(c.view(12, torch.uint8, (c.R * O.scale_cols_padded(Inter, 0),)).cpu().numpy(), c.R,
+                           Inter, 0)
+    assert np.array_equal(hs[rows], r["h_scales"])
+    assert np.all(hs[pad_rows] == 0)
+    sgh = c.view(10, torch.float32, (E,)).cpu().numpy()
+    used = r["counts"] > 0
+    assert np.array_equal(sgh[used], r["sgH"][used])
+    # 5. GEMM2 + combine from the oracle's requantised h
+    hcb = np.zeros((c.R, Inter // 2), dtype=np.uint8)
+    hcb[rows] = r["h_codes"]
+    c.view(11, torch.uint8, (c.R, Inter // 2)).copy_(torch.from_numpy(hcb))
+    hsb = np.zeros((c.R, Inter // 16), dtype=np.uint8)
+    hsb[rows] = r["h_scales"]
+    c.view(12, torch.uint8, (c.R * O.scale_cols_padded(Inter, 0),)).copy_(
+        torch.from_numpy(O.scales_to_mma(hsb, c.R, Inter, 0)))
+    c.view(10, torch.float32, (E,)).copy_(torch.from_numpy(r["sgH"]))
+    out = c.run(F, mask=16)
+    y = bf16_to_np(out)
+    # fp32 combine of k terms in any order: k * 2^-24 of the magnitude on top
+    check_close(y, r["y"], r["ymag"], what="y", extra_tau=k * 2.0 ** -23 * r["ymag"])
+
+
+def _end_to_end(F, O, c, max_norm_err=2e-2):
+    out = c.run(F)
+    y = bf16_to_np(out)
+    assert np.isfinite(y).all()
+    ny = np.linalg.norm(c.ref["y"])
+    err = np.linalg.norm(y - c.ref["y"]) / ny
+    assert err <= max_norm_err, err
+    # requantised codes of the full run vs the oracle's: they differ only where h
+    # sits at a rounding boundary (or an expert's amax differs by one bf16 ulp)
+    rows = c.gpu_rows()
+    hc = c.view(11, torch.uint8, (c.R, c.I // 2)).cpu().numpy()[rows]
+    flips = np.mean(hc != c.ref["h_codes"])
+    assert flips <= 1e-2, flips
+    return err, flips
+
+
+@pytest.mark.parametrize("T,E,k,H,Inter", [(1, 8, 2, 256, 128), (5, 8, 2, 256, 128), (40, 16, 4, 512, 192),
+                                           (300, 8, 2, 256, 128), (257, 32, 8, 384, 256)])
+def test_moe_staged_small(F, O, T, E, k, H, Inter):
+    c = Case(F, O, T, E, k, H, Inter, seed=3 + T, std=0.1)
+    _stage_checks(F, O, c)
+    _end_to_end(F, O, c)
+
+
+def test_moe_all_tokens_one_expert(F, O):
+    """Degenerate routing: logits make expert 3 win for every token."""
+    c = Case(F, O, 200, 8, 1, 256, 128, seed=9, std=0.1)
+    c.logits[:, 3] += 100.0
+    c.log_d = c.logits.cuda()
+    c.ref = O.moe(I.u16(c.hidden), c.logits.numpy(), top_k=1, q13=c.q13, q2=c.q2)
+    c.padded = np.concatenate([[0], np.cumsum((c.ref["counts"] + 127) // 128 * 128)]).astype(np.int64)
+    _stage_checks(F, O, c)
+
+
+def test_moe_static_scales_and_errors(F, O):
+    T, E, k, H, Inter = 24, 8, 2, 256, 128
+    c = Case(F, O, T, E, k, H, Inter, seed=21, std=0.1)
+    st13 = np.full(E, 4.0 / 2688, dtype=np.float32)
+    st2 = np.full(E, 0.5 / 2688, dtype=np.float32)
+    out = F.moe(c.hid_d, c.log_d, c.mw, k, mode=1, static13=st13, static2=st2, workspace=c.ws)
+    torch.cuda.synchronize()
+    ref = O.moe(I.u16(c.hidden), c.logits.numpy(), top_k=k, q13=c.q13, q2=c.q2, mode=1, static13=st13,
+                static2=st2)
+    y = bf16_to_np(out)
+    assert np.linalg.norm(y - ref["y"]) / np.linalg.norm(ref["y"]) < 1e-2
+    # the zeroed-alpha failure mode is refused: no scales, or a zero scale
+    with pytest.raises(F.FP4Error) as e1:
+        F.moe(c.hid_d, c.log_d, c.mw, k, mode=1, static13=None, static2=st2, workspace=c.ws)
+    assert e1.value.name == "FP4_ERR_MISSING_SCALE"
+    bad = st13.copy()
+    bad[3] = 0.0
+    with pytest.raises(F.FP4Error) as e2:
+        F.moe(c.hid_d, c.log_d, c.mw, k, mode=1, static13=bad, static2=st2, workspace=c.ws)
+    assert e2.value.name == "FP4_ERR_INVALID_SCALE"
+
+
+def test_moe_prepack_bit_exact(F, O):
+    E, H, Inter = 4, 256, 128
+    w13 = I.expert_weights_bf16(E, 2 * Inter, H, 5)
+    w2 = I.expert_weights_bf16(E, H, Inter, 6)
+    mw = F.moe_prepack(w13.cuda(), w2.cuda())
+    torch.cuda.synchronize()
+    c13, s13, g13 = O.quantize_experts(I.u16(w13))
+    # the library stores W13 rows interleaved in groups of 32 (gate, up, ...)
+    perm = np.array([(r // 64) * 32 + (r % 64 if r % 64 < 32 else Inter + r % 64 - 32) for r in range(2 * Inter)])
+    got_c = mw.w13.codes.cpu().numpy().reshape(E, 2 * Inter, H // 2)
+    got_s = mw.w13.scales.cpu().numpy().reshape(E, -1)
+    for e in range(E):
+        assert np.array_equal(got_c[e], c13[e][perm])
+        assert np.array_equal(O.scales_from_mma(got_s[e], 2 * Inter, H, 0), s13[e][perm])
+    assert np.array_equal(mw.w13.gscale.cpu().numpy(), g13)
+    c2, s2, g2 = O.quantize_experts(I.u16(w2))
+    assert np.array_equal(mw.w2.codes.cpu().numpy().reshape(E, H, Inter // 2), c2)
+    assert np.array_equal(mw.w2.gscale.cpu().numpy(), g2)
+
+
+# ------------------------------------------------------------ full size
+
+@pytest.fixture(scope="module")
+def full_weights(F, O):
+    E, H, Inter = 128, 2048, 768
+    w13 = I.expert_weights_bf16(E, 2 * Inter, H, 103)
+    w2 = I.expert_weights_bf16(E, H, Inter, 104)
+    mw = F.moe_prepack(w13.cuda(), w2.cuda())
+    return w13, w2, mw, O.quantize_experts(I.u16(w13)), O.quantize_experts(I.u16(w2))
+
+
+@pytest.mark.parametrize("T", [1, 64, 4096])
+def test_moe_full_size(F, O, full_weights, T):
+    """128 experts, top-8, hidden 2048, expert intermediate 768."""
+    w13, w2, mw, q13, q2 = full_weights
+    c = Case.__new__(Case)
+    c.T, c.E, c.k, c.H, c.I = T, 128, 8, 2048, 768
+    c.hidden = I.randn_bf16((T, 2048), 3)
+    c.logits = I.router_logits(T, 128, 203)
+    c.mw, c.q13, c.q2 = mw, q13, q2
+    c.ref = O.moe(I.u16(c.hidden), c.logits.numpy(), top_k=8, q13=q13, q2=q2)
+    c.hid_d, c.log_d = c.hidden.cuda(), c.logits.cuda()
+    L = F.lib()
+    c.ws = torch.zeros(L.fp4_moe_workspace_size(T, 2048, 768, 128, 8), dtype=torch.uint8, device="cuda")
+    c.off = F.moe_workspace_layout(T, 2048, 768, 128, 8)
+    c.R = c.off[14]
+    c.padded = np.concatenate([[0], np.cumsum((c.ref["counts"] + 127) // 128 * 128)]).astype(np.int64)
+    _stage_checks(F, O, c)
+    _end_to_end(F, O, c)
