@@ -47,7 +47,10 @@ def parse():
     p.add_argument("--no-secondary", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--profile", action="store_true",
-                   help="only the layer calls (warmup + steps), for ncu captures; prints kernel timings")
+                   help="only the layer calls (warmup + steps), for ncu captures")
+    p.add_argument("--workload", default="prefill",
+                   choices=["prefill", "decode1", "decode8", "decode32", "mxfp4", "moe1", "moe64", "moe4096"],
+                   help="workload run by --profile")
     return p.parse_args()
 
 
@@ -255,6 +258,8 @@ def run_ours(args, rank, local, ws):
         flush_buf.zero_()
 
     if args.profile:
+        if args.workload != "prefill":
+            return run_profile_other(args, torch, fp4, L, I, dev)
         for _ in range(args.warmup + args.steps):
             step(None)
         torch.cuda.synchronize()
@@ -313,6 +318,32 @@ def run_ours(args, rank, local, ws):
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline()
     return res
+
+
+def run_profile_other(args, torch, fp4, L, I, dev):
+    """--profile for the secondary workloads: plain calls, no timing."""
+    wl = args.workload
+    if wl.startswith("decode"):
+        m = int(wl[6:])
+        wq = fp4.prepack_weight(I.weights_bf16(14336, 4096, 101).to(dev))
+        a = I.activations_with_outliers(m, 4096, 1).to(dev)
+        fn = lambda: fp4.gemm(a, wq)
+    elif wl == "mxfp4":
+        wq = fp4.prepack_weight(I.weights_bf16(2048, 7168, 104).to(dev), fp4.MXFP4)
+        a = I.randn_bf16((2048, 7168), 4).to(dev)
+        fn = lambda: fp4.gemm(a, wq)
+    else:
+        T = int(wl[3:])
+        mw = fp4.moe_prepack(I.expert_weights_bf16(MOE_E, 2 * MOE_I, MOE_H, 103).to(dev),
+                             I.expert_weights_bf16(MOE_E, MOE_H, MOE_I, 104).to(dev))
+        hidden = I.randn_bf16((T, MOE_H), 3).to(dev)
+        logits = I.router_logits(T, MOE_E, 203).to(dev)
+        fn = lambda: fp4.moe(hidden, logits, mw, MOE_K)
+    for _ in range(args.warmup + args.steps):
+        fn()
+    torch.cuda.synchronize()
+    fp4.device_status()
+    return {"profile": True, "steps": args.steps, "warmup": args.warmup, "workload": wl}
 
 
 def run_e2e(torch, fp4, L, a_cpu, wq, dev, steps):
@@ -394,6 +425,49 @@ def run_secondary(torch, fp4, L, I, dev, peaks):
                                       "frac_fp4_peak": round(fl / (ms * 1e-3) / 1e12 /
                                                              (peaks["bf16"] * FP4_PER_BF16), 4),
                                       "note": "quantise (one pass) + GEMM, L2 flushed between steps"}
+    out.update(run_moe(torch, fp4, L, I, dev, peaks))
+    return out
+
+
+MOE_E, MOE_K, MOE_H, MOE_I = 128, 8, 2048, 768
+MOE_EXPERT_BYTES = (2 * MOE_I * MOE_H // 2 + 2 * MOE_I * MOE_H // 16) + (MOE_H * MOE_I // 2 + MOE_H * MOE_I // 16)
+
+
+def run_moe(torch, fp4, L, I, dev, peaks):
+    """Fused MoE, 128 experts, top-8, hidden 2048, intermediate 768.
+    GB/s counts the weights of the experts the batch touches plus hidden in,
+    router logits in and the output; timed as a CUDA graph of the C-ABI call
+    (T=1 cycles through 8 weight copies so the touched experts come from HBM)."""
+    out = {}
+    w13 = I.expert_weights_bf16(MOE_E, 2 * MOE_I, MOE_H, 103).to(dev)
+    w2 = I.expert_weights_bf16(MOE_E, MOE_H, MOE_I, 104).to(dev)
+    mw = fp4.moe_prepack(w13, w2)
+    del w13, w2
+    for T in (1, 64, 4096):
+        hidden = I.randn_bf16((T, MOE_H), 3).to(dev)
+        logits = I.router_logits(T, MOE_E, 203).to(dev)
+        touched = int(torch.unique(torch.topk(logits, MOE_K, dim=1).indices).numel())
+        copies = [mw]
+        if T == 1:
+            for _ in range(7):
+                c = fp4.MoEWeights(mw.E, mw.H, mw.I, None, None)
+                c.w13 = fp4.QTensor(0, mw.w13.rows, mw.w13.k, mw.w13.codes.clone(), mw.w13.scales.clone(),
+                                    mw.w13.gscale.clone())
+                c.w2 = fp4.QTensor(0, mw.w2.rows, mw.w2.k, mw.w2.codes.clone(), mw.w2.scales.clone(),
+                                   mw.w2.gscale.clone())
+                copies.append(c)
+        o = torch.empty((T, MOE_H), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(L.fp4_moe_workspace_size(T, MOE_H, MOE_I, MOE_E, MOE_K), dtype=torch.uint8, device=dev)
+        fns = [(lambda c=c: fp4.moe(hidden, logits, c, MOE_K, out=o, workspace=ws)) for c in copies]
+        ms = graph_time(torch, fns, iters=10 if T == 4096 else 20)
+        byt = touched * MOE_EXPERT_BYTES + T * MOE_H * 2 * 2 + T * MOE_E * 4
+        fl = 2.0 * T * MOE_K * (2 * MOE_I * MOE_H + MOE_H * MOE_I)
+        out["moe_T%d" % T] = {"us": round(ms * 1e3, 2), "GB/s": round(byt / (ms * 1e-3) / 1e9, 1),
+                              "frac_hbm": round(byt / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                              "TFLOP/s": round(fl / (ms * 1e-3) / 1e12, 1), "experts_touched": touched,
+                              "note": "route + permute + quantise + GEMM1/SwiGLU + requant + GEMM2/combine, "
+                                      "CUDA graph"}
+        del copies
     return out
 
 

@@ -295,11 +295,14 @@ static GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int sms) {
     GemmPlan p;
     const int64_t kbt = gemm_k_blocks(k);
     if (m <= kDecodeMaxM) {
+        // decode: one 128-row activation tile (rows beyond m are zero-filled by
+        // the TMA, not read), 256-wide weight tiles, split-K so that about
+        // three units land on every SM; deterministic reduction afterwards
         p.decode = true;
-        p.bn = m <= 32 ? 32 : 64;
-        const int64_t ptiles = (n + 127) / 128;
-        int64_t s = (2 * (int64_t)sms + ptiles - 1) / ptiles;
-        if (s > kbt) s = kbt;
+        p.bn = 256;
+        const int64_t qtiles = (n + 255) / 256;
+        int64_t s = (3 * (int64_t)sms + qtiles - 1) / qtiles;
+        if (s > kbt / 2) s = kbt / 2;
         if (s > 16) s = 16;
         if (s < 1) s = 1;
         // make every split non-empty
@@ -375,17 +378,17 @@ static fp4_status enqueue_gemm(int fmt, const uint8_t* ac, const uint8_t* as, co
         g.ldo = n;
         return cuda_status(launch_gemm(g, s), "GEMM launch");
     }
-    // decode: weights on the MMA M side (swap-AB), tokens on N
-    g.p_codes = wc, g.p_scales = wsc, g.p_rows = n, g.p_rows_valid = n, g.p_global = wg;
-    g.q_codes = ac, g.q_scales = as, g.q_rows = m, g.q_rows_valid = m, g.q_global = ag;
+    // decode: activations on the MMA M side, weights on N, split-K partials
+    g.p_codes = ac, g.p_scales = as, g.p_rows = m, g.p_rows_valid = m, g.p_global = ag;
+    g.q_codes = wc, g.q_scales = wsc, g.q_rows = n, g.q_rows_valid = n, g.q_global = wg;
     g.splits = p.splits;
     if (p.splits == 1) {
-        g.epi = EPI_BF16_T;
+        g.epi = EPI_BF16;
         g.out = out;
         g.ldo = n;
         return cuda_status(launch_gemm(g, s), "GEMM launch");
     }
-    g.epi = EPI_PARTIAL_T;
+    g.epi = EPI_PARTIAL;
     g.out = part;
     g.ldo = n;
     TRY(cuda_status(launch_gemm(g, s), "GEMM launch"));

@@ -76,7 +76,7 @@ static cudaError_t launch_one(const GemmLaunch& g, cudaStream_t s) {
     void* args[] = {(void*)&tmP, (void*)&tmQ, (void*)&gg, (void*)&wc};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(192);
+    cfg.blockDim = dim3(512);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -102,6 +102,10 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
             if (g.bn == 32) return mx ? launch_one<32, true, EPI_BF16_T>(g, s) : launch_one<32, false, EPI_BF16_T>(g, s);
             if (g.bn == 64) return mx ? launch_one<64, true, EPI_BF16_T>(g, s) : launch_one<64, false, EPI_BF16_T>(g, s);
             break;
+        case EPI_PARTIAL:
+            if (g.bn == 256) return mx ? launch_one<256, true, EPI_PARTIAL>(g, s) : launch_one<256, false, EPI_PARTIAL>(g, s);
+            if (g.bn == 128) return mx ? launch_one<128, true, EPI_PARTIAL>(g, s) : launch_one<128, false, EPI_PARTIAL>(g, s);
+            break;
         case EPI_PARTIAL_T:
             if (g.bn == 32)
                 return mx ? launch_one<32, true, EPI_PARTIAL_T>(g, s) : launch_one<32, false, EPI_PARTIAL_T>(g, s);
@@ -125,7 +129,6 @@ cudaError_t launch_gemm_moe(const GemmLaunch& g, cudaStream_t s) {
         if (g.bn == 128) return launch_one<128, false, EPI_SWIGLU>(g, s);
         if (g.bn == 64) return launch_one<64, false, EPI_SWIGLU>(g, s);
     } else {
-        if (g.bn == 256) return launch_one<256, false, EPI_COMBINE>(g, s);
         if (g.bn == 128) return launch_one<128, false, EPI_COMBINE>(g, s);
         if (g.bn == 64) return launch_one<64, false, EPI_COMBINE>(g, s);
     }

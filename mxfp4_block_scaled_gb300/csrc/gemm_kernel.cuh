@@ -5,17 +5,22 @@
 // of "vLLM on DGX Spark: technical report", section 6.1 (value = element x
 // block scale x global scale; the global scales leave as one alpha factor).
 //
-// One CTA per SM, 6 warps:
-//   warp 0      TMA producer: per 256-element K block, a 128-row P tile and a
-//               BN-row Q tile (128-byte swizzle) plus their scale atoms
-//               (plain bulk copies; the MMA layout makes them contiguous).
-//   warp 1      TMEM allocator and MMA issuer (one thread): copies the scale
-//               atoms smem -> TMEM (tcgen05.cp 32x128b.warpx4) and issues four
+// One CTA per SM, 16 warps in four warpgroups:
+//   warps 0-3   scale writers: one per TMEM lane quarter; per K block they read
+//               the scale atoms the TMA brought into smem and store them into
+//               TMEM (tcgen05.st, the layout the block-scaled MMA reads), so
+//               the tensor pipe is left to the MMAs.
+//   warps 4, 6  TMA producers: per 256-element K block, warp 4 loads a 128-row
+//               P tile and warp 6 a BN-row Q tile (128-byte swizzle), each with
+//               its scale atoms (plain bulk copies; the MMA layout makes them
+//               contiguous).
+//   warp 5      TMEM allocator and MMA issuer (one thread): four
 //               M=128 x N=BN x K=64 block-scaled MMAs per K block.
-//   warps 2-5   epilogue: tcgen05.ld of the fp32 accumulator, alpha, bf16
-//               (or the fused MoE epilogues), global stores.
-// Pipelines: STAGES smem stages (full/empty mbarriers) and 1-2 TMEM
-// accumulator stages (acc_full/acc_empty).  Every wait is bounded.
+//   warps 8-15  epilogue: tcgen05.ld of the fp32 accumulator into registers,
+//               release of the TMEM stage, then alpha, bf16 (or the fused MoE
+//               epilogues) and global stores.
+// Pipelines: STAGES smem stages (full / scales-ready / empty mbarriers) and
+// 1-2 TMEM accumulator stages (acc_full/acc_empty).  Every wait is bounded.
 #pragma once
 
 #include "common.cuh"
@@ -46,7 +51,7 @@ struct GemmCfg {
     static constexpr int STAGES = ST_MIN < 8 ? ST_MIN : 8;
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
     static_assert(STAGES >= 2, "pipeline too shallow");
-    static_assert(2 * STAGES + 5 <= BAR_BYTES / 8 - 2, "barrier area too small");
+    static_assert(3 * STAGES + 5 <= BAR_BYTES / 8 - 2, "barrier area too small");
     static_assert(ACC * BN + STAGES * SF_COLS <= 512, "TMEM budget");
 };
 
@@ -105,7 +110,7 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 }
 
 template <int BN, bool MX, int EPI>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(512, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
                 const GemmLaunch g, const WaitCfg wc) {
     using C = GemmCfg<BN, MX>;
@@ -118,7 +123,8 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(sSFQ + C::STAGES * C::SFQ_BYTES);
     uint64_t* full = bars;
     uint64_t* empty = bars + C::STAGES;
-    uint64_t* accf = bars + 2 * C::STAGES;
+    uint64_t* sfr = bars + 2 * C::STAGES;  // scales of the stage are in TMEM
+    uint64_t* accf = bars + 3 * C::STAGES;
     uint64_t* acce = accf + 2;
     uint64_t* drain = acce + 2;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -127,12 +133,13 @@ __global__ void __launch_bounds__(192, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(full + s, 1);
+            mbar_init(full + s, 2);  // two producers
             mbar_init(empty + s, 1);
+            mbar_init(sfr + s, 4);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(accf + a, 1);
-            mbar_init(acce + a, 4);
+            mbar_init(acce + a, 8);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -140,7 +147,7 @@ __global__ void __launch_bounds__(192, 1)
         prefetch_tensormap(&tmP);
         prefetch_tensormap(&tmQ);
     }
-    if (warp == 1) {
+    if (warp == 5) {
         tmem_alloc(tslot, 512);
         tmem_relinquish();
     }
@@ -154,14 +161,53 @@ __global__ void __launch_bounds__(192, 1)
     const int64_t ksfc = sc.kbt * C::SF_CHUNKS;                 // scale atoms per 128-row tile
     const int64_t q_chunks_total = (g.q_rows + 127) / 128;      // 128-row scale tiles of Q
 
-    if (warp == 0) {
+    if (warp < 4) {
+        // ---------------------------------------------------- scale writers
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        int stage = 0;
+        uint32_t ph = 0;
+        for (int64_t u = blockIdx.x; u < sc.units; u += gridDim.x) {
+            const Unit w = decode_unit<BN>(g, sc, u);
+            bool ok = true;
+            for (int64_t kb = w.kb0; kb < w.kb1; ++kb) {
+                if (!mbar_wait(full + stage, ph, wc, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sfp_t = tmem + lane_base + (uint32_t)(C::ACC * BN + stage * C::SF_COLS);
+                const uint32_t sfq_t = sfp_t + C::SFP_COLS;
+                const uint32_t sp = smem_u32(sSFP + stage * C::SFP_BYTES) + lane * 16;
+                const uint32_t sq = smem_u32(sSFQ + stage * C::SFQ_BYTES) + lane * 16;
+                // lane i holds rows i, 32+i, 64+i, 96+i of an atom: TMEM lane i
+                // of this quarter, columns +0..+3 (every quarter gets the atom)
+#pragma unroll
+                for (int c = 0; c < C::SF_CHUNKS; ++c) tmem_st4(sfp_t + c * 4, lds128(sp + c * 512));
+#pragma unroll
+                for (int rc = 0; rc < C::QCH; ++rc)
+#pragma unroll
+                    for (int c = 0; c < C::SF_CHUNKS; ++c)
+                        tmem_st4(sfq_t + (c * C::QCH + rc) * 4, lds128(sq + (rc * C::SF_CHUNKS + c) * 512));
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sfr + stage);
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+        }
+    } else if (warp == 4 || warp == 6) {
         if (lane == 0) {
-            // ------------------------------------------------ TMA producer
+            // ------------------------------------------------ TMA producers
+            // warp 4 loads the P tile and its scale atoms, warp 6 the Q tile and
+            // its scale atoms; each adds its own bytes to the stage's barrier,
+            // so two threads issue copies in parallel.
+            const bool is_p = warp == 4;
             int stage = 0;
             uint32_t ph = 0;
-            uint32_t issued_ph[C::STAGES];
-            bool issued[C::STAGES];
-            for (int s = 0; s < C::STAGES; ++s) issued[s] = false, issued_ph[s] = 0;
+            uint32_t issued = 0, issued_ph = 0;  // per-stage bits: a copy was issued / its phase parity
             bool ok = true;
             for (int64_t u = blockIdx.x; u < sc.units && ok; u += gridDim.x) {
                 const Unit w = decode_unit<BN>(g, sc, u);
@@ -172,20 +218,27 @@ __global__ void __launch_bounds__(192, 1)
                         ok = false;
                         break;
                     }
-                    uint32_t bytes = C::P_BYTES + C::Q_BYTES + C::SFP_BYTES;
-                    for (int c = 0; c < C::QCH; ++c)
-                        if (qc0 + c < q_chunks_total) bytes += C::SF_CHUNKS * 512;
-                    mbar_arrive_expect_tx(full + stage, bytes);
-                    tma_load_2d(&tmP, full + stage, sP + stage * C::P_BYTES, (int32_t)(kb * 128), (int32_t)w.p_row0);
-                    tma_load_2d(&tmQ, full + stage, sQ + stage * C::Q_BYTES, (int32_t)(kb * 128), (int32_t)w.q_row0);
-                    bulk_load(sSFP + stage * C::SFP_BYTES, sfp + kb * C::SF_CHUNKS * 512, C::SFP_BYTES, full + stage);
-                    for (int c = 0; c < C::QCH; ++c)
-                        if (qc0 + c < q_chunks_total)
-                            bulk_load(sSFQ + stage * C::SFQ_BYTES + c * C::SF_CHUNKS * 512,
-                                      g.q_scales + ((qc0 + c) * ksfc + kb * C::SF_CHUNKS) * 512, C::SF_CHUNKS * 512,
-                                      full + stage);
-                    issued[stage] = true;
-                    issued_ph[stage] = ph;
+                    if (is_p) {
+                        mbar_arrive_expect_tx(full + stage, C::P_BYTES + C::SFP_BYTES);
+                        tma_load_2d(&tmP, full + stage, sP + stage * C::P_BYTES, (int32_t)(kb * 128),
+                                    (int32_t)w.p_row0);
+                        bulk_load(sSFP + stage * C::SFP_BYTES, sfp + kb * C::SF_CHUNKS * 512, C::SFP_BYTES,
+                                  full + stage);
+                    } else {
+                        uint32_t bytes = C::Q_BYTES;
+                        for (int c = 0; c < C::QCH; ++c)
+                            if (qc0 + c < q_chunks_total) bytes += C::SF_CHUNKS * 512;
+                        mbar_arrive_expect_tx(full + stage, bytes);
+                        tma_load_2d(&tmQ, full + stage, sQ + stage * C::Q_BYTES, (int32_t)(kb * 128),
+                                    (int32_t)w.q_row0);
+                        for (int c = 0; c < C::QCH; ++c)
+                            if (qc0 + c < q_chunks_total)
+                                bulk_load(sSFQ + stage * C::SFQ_BYTES + c * C::SF_CHUNKS * 512,
+                                          g.q_scales + ((qc0 + c) * ksfc + kb * C::SF_CHUNKS) * 512,
+                                          C::SF_CHUNKS * 512, full + stage);
+                    }
+                    issued |= 1u << stage;
+                    issued_ph = (issued_ph & ~(1u << stage)) | (ph << stage);
                     if (++stage == C::STAGES) {
                         stage = 0;
                         ph ^= 1u;
@@ -197,10 +250,10 @@ __global__ void __launch_bounds__(192, 1)
                 WaitCfg w2 = wc;
                 volatile int never = 0;
                 for (int s = 0; s < C::STAGES; ++s)
-                    if (issued[s]) mbar_wait(full + s, issued_ph[s], w2, &never);
+                    if ((issued >> s) & 1u) mbar_wait(full + s, (issued_ph >> s) & 1u, w2, &never);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 5) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
             const uint32_t idesc = idesc_mxf4(128, BN, MX);
@@ -219,22 +272,13 @@ __global__ void __launch_bounds__(192, 1)
                 const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
                 const uint32_t q_sub = BN < 128 ? (uint32_t)((w.q_row0 & 127) >> 5) : 0u;
                 for (int64_t kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!mbar_wait(full + stage, ph, wc, abort_flag)) {
+                    if (!mbar_wait(full + stage, ph, wc, abort_flag) || !mbar_wait(sfr + stage, ph, wc, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t sfp_t = tmem + (uint32_t)(C::ACC * BN + stage * C::SF_COLS);
                     const uint32_t sfq_t = sfp_t + C::SFP_COLS;
-#pragma unroll
-                    for (int c = 0; c < C::SF_CHUNKS; ++c)
-                        tmem_cp_sf(sfp_t + c * 4, sdesc_sf(smem_u32(sSFP + stage * C::SFP_BYTES + c * 512)));
-#pragma unroll
-                    for (int rc = 0; rc < C::QCH; ++rc)
-#pragma unroll
-                        for (int c = 0; c < C::SF_CHUNKS; ++c)
-                            tmem_cp_sf(sfq_t + (c * C::QCH + rc) * 4,
-                                       sdesc_sf(smem_u32(sSFQ + stage * C::SFQ_BYTES + (rc * C::SF_CHUNKS + c) * 512)));
                     const uint32_t pa = smem_u32(sP + stage * C::P_BYTES);
                     const uint32_t qa = smem_u32(sQ + stage * C::Q_BYTES);
 #pragma unroll
@@ -276,135 +320,217 @@ __global__ void __launch_bounds__(192, 1)
                 mbar_wait(drain, 0, wc, &never);
             }
         }
-    } else {
+    } else if (warp >= 8) {
         // ---------------------------------------------------- epilogue
+        // 8 warps: warp w owns TMEM lane quarter (w % 4) and column half
+        // (w - 8) / 4.  Each pulls all its accumulator columns into registers
+        // (back-to-back tcgen05.ld, one wait), releases the accumulator stage
+        // at once, then converts and stores while the next tile's MMAs run.
+        constexpr int GRAN = EPI == EPI_SWIGLU ? 64 : 32;
+        constexpr int CPW = BN / 2 > GRAN ? BN / 2 : GRAN;  // columns per warp
+        constexpr int NLD = CPW / 32;
+        static_assert(EPI != EPI_COMBINE || CPW <= 64, "fp32 combine keeps its columns in registers");
         const int qd = warp & 3;  // the TMEM lane quarter this warp may access
+        const int c_begin = ((warp - 8) >> 2) * CPW;
+        const bool has_cols = c_begin < BN;
         int acc = 0;
         uint32_t aph = 0;
         for (int64_t u = blockIdx.x; u < sc.units; u += gridDim.x) {
-            const Unit w = decode_unit<BN>(g, sc, u);
             if (!mbar_wait(accf + acc, aph, wc, abort_flag)) break;
             tc_fence_after();
-            const uint32_t tb = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(acc * BN);
-            const int64_t prow = w.p_row0 + qd * 32 + lane;  // the P row this thread owns
+            const uint32_t tb = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(acc * BN + c_begin);
 
-            if constexpr (EPI == EPI_BF16 || EPI == EPI_BF16_T || EPI == EPI_PARTIAL_T) {
-                float alpha = 1.0f;
-                if (!MX) alpha = __fmul_rn(g.p_global[0], g.q_global[0]);
-                const int64_t q0 = w.qt * BN;  // output column (EPI_BF16) / token (transposed)
-#pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tb + c0, r);
-                    tmem_ld_wait();
-                    if (prow < g.p_rows_valid) {
-                        if constexpr (EPI == EPI_BF16) {
-                            uint16_t* o = reinterpret_cast<uint16_t*>(g.out) + prow * g.ldo + q0 + c0;
-                            if (q0 + c0 + 32 <= g.q_rows_valid) {
-                                uint4* o4 = reinterpret_cast<uint4*>(o);
+            if constexpr (EPI == EPI_BF16) {
+                // chunk by chunk: fp32 -> alpha -> packed bf16 pairs, then release
+                const float alpha = MX ? 1.0f : __fmul_rn(g.p_global[0], g.q_global[0]);
+                uint32_t pk[NLD][16];
+                if (has_cols) {
 #pragma unroll
-                                for (int v = 0; v < 4; ++v) {
-                                    uint4 x;
-                                    x.x = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(r[8 * v + 0])),
-                                                      __fmul_rn(alpha, __uint_as_float(r[8 * v + 1])));
-                                    x.y = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(r[8 * v + 2])),
-                                                      __fmul_rn(alpha, __uint_as_float(r[8 * v + 3])));
-                                    x.z = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(r[8 * v + 4])),
-                                                      __fmul_rn(alpha, __uint_as_float(r[8 * v + 5])));
-                                    x.w = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(r[8 * v + 6])),
-                                                      __fmul_rn(alpha, __uint_as_float(r[8 * v + 7])));
-                                    o4[v] = x;
-                                }
-                            } else {
-                                for (int i = 0; i < 32; ++i)
-                                    if (q0 + c0 + i < g.q_rows_valid) {
-                                        __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(alpha, __uint_as_float(r[i])));
-                                        o[i] = *reinterpret_cast<uint16_t*>(&h);
-                                    }
-                            }
-                        } else if constexpr (EPI == EPI_BF16_T) {
+                    for (int j = 0; j < NLD; ++j) {
+                        uint32_t r[32];
+                        tmem_ld32(tb + j * 32, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            pk[j][i] = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(r[2 * i])),
+                                                   __fmul_rn(alpha, __uint_as_float(r[2 * i + 1])));
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce + acc);
+                const Unit w = decode_unit<BN>(g, sc, u);
+                const int64_t prow = w.p_row0 + qd * 32 + lane;  // the P row this thread owns
+                if (has_cols && prow < g.p_rows_valid) {
+#pragma unroll
+                    for (int j = 0; j < NLD; ++j) {
+                        const int64_t q0 = w.qt * BN + c_begin + j * 32;
+                        uint16_t* o = reinterpret_cast<uint16_t*>(g.out) + prow * g.ldo + q0;
+                        if (q0 + 32 <= g.q_rows_valid) {
+                            uint4* o4 = reinterpret_cast<uint4*>(o);
+#pragma unroll
+                            for (int v = 0; v < 4; ++v)
+                                o4[v] = make_uint4(pk[j][4 * v], pk[j][4 * v + 1], pk[j][4 * v + 2], pk[j][4 * v + 3]);
+                        } else {
+                            for (int i = 0; i < 32; ++i)
+                                if (q0 + i < g.q_rows_valid)
+                                    o[i] = (uint16_t)((i & 1) ? (pk[j][i >> 1] >> 16) : (pk[j][i >> 1] & 0xFFFFu));
+                        }
+                    }
+                }
+            } else if constexpr (EPI == EPI_BF16_T || EPI == EPI_PARTIAL_T) {
+                uint32_t r[NLD][32];
+                if (has_cols) {
+#pragma unroll
+                    for (int j = 0; j < NLD; ++j) tmem_ld32(tb + j * 32, r[j]);
+                    tmem_ld_wait();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce + acc);
+                const Unit w = decode_unit<BN>(g, sc, u);
+                const int64_t prow = w.p_row0 + qd * 32 + lane;
+                const float alpha = MX ? 1.0f : __fmul_rn(g.p_global[0], g.q_global[0]);
+                if (has_cols && prow < g.p_rows_valid) {
+#pragma unroll
+                    for (int j = 0; j < NLD; ++j) {
+                        const int64_t q0 = w.qt * BN + c_begin + j * 32;  // first token of the chunk
+                        if constexpr (EPI == EPI_BF16_T) {
                             uint16_t* o = reinterpret_cast<uint16_t*>(g.out);
 #pragma unroll
                             for (int i = 0; i < 32; ++i) {
-                                const int64_t t = q0 + c0 + i;
+                                const int64_t t = q0 + i;
                                 if (t < g.q_rows_valid) {
-                                    __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(alpha, __uint_as_float(r[i])));
+                                    __nv_bfloat16 h =
+                                        __float2bfloat16_rn(__fmul_rn(alpha, __uint_as_float(r[j][i])));
                                     o[t * g.ldo + prow] = *reinterpret_cast<uint16_t*>(&h);
                                 }
                             }
                         } else {
-                            float* o = reinterpret_cast<float*>(g.out) + (int64_t)w.s * g.q_rows_valid * g.p_rows_valid;
+                            float* o = reinterpret_cast<float*>(g.out) +
+                                       (int64_t)w.s * g.q_rows_valid * g.p_rows_valid;
 #pragma unroll
                             for (int i = 0; i < 32; ++i) {
-                                const int64_t t = q0 + c0 + i;
-                                if (t < g.q_rows_valid) o[t * g.p_rows_valid + prow] = __uint_as_float(r[i]);
+                                const int64_t t = q0 + i;
+                                if (t < g.q_rows_valid) o[t * g.p_rows_valid + prow] = __uint_as_float(r[j][i]);
                             }
                         }
                     }
                 }
+            } else if constexpr (EPI == EPI_PARTIAL) {
+                // split-K partials, row-major; only the warps holding real rows
+                // read TMEM (for decode-sized M that is one lane quarter)
+                const Unit w = decode_unit<BN>(g, sc, u);
+                const int64_t row0 = w.p_row0 + qd * 32;
+                const bool any_rows = has_cols && row0 < g.p_rows_valid;
+                const int64_t prow = row0 + lane;
+                float* o = reinterpret_cast<float*>(g.out) + ((int64_t)w.s * g.p_rows_valid + prow) * g.ldo;
+                if (any_rows) {
+#pragma unroll 1
+                    for (int j = 0; j < NLD; ++j) {
+                        uint32_t r[32];
+                        tmem_ld32(tb + j * 32, r);
+                        tmem_ld_wait();
+                        const int64_t q0 = w.qt * BN + c_begin + j * 32;
+                        if (prow < g.p_rows_valid) {
+                            float4* o4 = reinterpret_cast<float4*>(o + q0);
+                            if (q0 + 32 <= g.q_rows_valid) {
+#pragma unroll
+                                for (int v = 0; v < 8; ++v)
+                                    o4[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                                        __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                            } else {
+                                for (int i = 0; i < 32; ++i)
+                                    if (q0 + i < g.q_rows_valid) o[q0 + i] = __uint_as_float(r[i]);
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce + acc);
             } else if constexpr (EPI == EPI_SWIGLU) {
                 // Q rows are W13 rows interleaved in groups of 32 (gate, up, gate, up, ...):
-                // columns [c0, c0+32) are gate and [c0+32, c0+64) up for the same 32 features.
-                const float alpha = __fmul_rn(g.p_global_per_expert ? g.p_global[w.e] : g.p_global[0], g.q_global[w.e]);
-                const bool valid = prow < (int64_t)g.row_valid_end[w.pt];
-                uint16_t* hrow = reinterpret_cast<uint16_t*>(g.out) + prow * g.ldo;
+                // columns [c, c+32) are gate and [c+32, c+64) up for the same 32 features.
+                const Unit w = decode_unit<BN>(g, sc, u);
+                const int64_t prow = w.p_row0 + qd * 32 + lane;
+                const float alpha =
+                    __fmul_rn(g.p_global_per_expert ? g.p_global[w.e] : g.p_global[0], g.q_global[w.e]);
+                uint32_t hv[NLD / 2][16];
                 uint32_t amax_bits = 0;
-#pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 64) {
-                    uint32_t rg[32], ru[32];
-                    tmem_ld32(tb + c0, rg);
-                    tmem_ld32(tb + c0 + 32, ru);
-                    tmem_ld_wait();
-                    const int64_t f0 = (w.qt * BN + c0) / 2;
-                    uint32_t hv[16];
+                if (has_cols) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float g0 = __fmul_rn(alpha, __uint_as_float(rg[2 * i]));
-                        const float g1 = __fmul_rn(alpha, __uint_as_float(rg[2 * i + 1]));
-                        const float u0 = __fmul_rn(alpha, __uint_as_float(ru[2 * i]));
-                        const float u1 = __fmul_rn(alpha, __uint_as_float(ru[2 * i + 1]));
-                        hv[i] = pack_bf16x2(__fmul_rn(silu_f32(g0), u0), __fmul_rn(silu_f32(g1), u1));
-                        amax_bits = __vmaxu2(amax_bits, hv[i] & 0x7FFF7FFFu);
+                    for (int j = 0; j < NLD; j += 2) {
+                        uint32_t rg[32], ru[32];
+                        tmem_ld32(tb + j * 32, rg);
+                        tmem_ld32(tb + j * 32 + 32, ru);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float g0 = __fmul_rn(alpha, __uint_as_float(rg[2 * i]));
+                            const float g1 = __fmul_rn(alpha, __uint_as_float(rg[2 * i + 1]));
+                            const float u0 = __fmul_rn(alpha, __uint_as_float(ru[2 * i]));
+                            const float u1 = __fmul_rn(alpha, __uint_as_float(ru[2 * i + 1]));
+                            hv[j / 2][i] = pack_bf16x2(__fmul_rn(silu_f32(g0), u0), __fmul_rn(silu_f32(g1), u1));
+                        }
                     }
-                    if (valid) {
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce + acc);
+                const bool valid = has_cols && prow < (int64_t)g.row_valid_end[w.pt];
+                if (valid) {
+                    uint16_t* hrow = reinterpret_cast<uint16_t*>(g.out) + prow * g.ldo;
+#pragma unroll
+                    for (int j = 0; j < NLD; j += 2) {
+                        const int64_t f0 = (w.qt * BN + c_begin + j * 32) / 2;
                         uint4* o4 = reinterpret_cast<uint4*>(hrow + f0);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) o4[v] = make_uint4(hv[4 * v], hv[4 * v + 1], hv[4 * v + 2], hv[4 * v + 3]);
+                        for (int v = 0; v < 4; ++v) {
+                            o4[v] = make_uint4(hv[j / 2][4 * v], hv[j / 2][4 * v + 1], hv[j / 2][4 * v + 2],
+                                               hv[j / 2][4 * v + 3]);
+                            amax_bits = __vmaxu2(amax_bits, hv[j / 2][4 * v] & 0x7FFF7FFFu);
+                            amax_bits = __vmaxu2(amax_bits, hv[j / 2][4 * v + 1] & 0x7FFF7FFFu);
+                            amax_bits = __vmaxu2(amax_bits, hv[j / 2][4 * v + 2] & 0x7FFF7FFFu);
+                            amax_bits = __vmaxu2(amax_bits, hv[j / 2][4 * v + 3] & 0x7FFF7FFFu);
+                        }
                     }
                 }
-                uint32_t m = valid ? max(amax_bits & 0xFFFFu, amax_bits >> 16) : 0u;
+                if (has_cols) {
+                    uint32_t m = max(amax_bits & 0xFFFFu, amax_bits >> 16);
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-                if (lane == 0 && m) atomicMax(reinterpret_cast<unsigned int*>(g.amax_out) + w.e, m << 16);
-            } else if constexpr (EPI == EPI_COMBINE) {
-                const float alpha = __fmul_rn(g.p_global[w.e], g.q_global[w.e]);
-                const bool valid = prow < (int64_t)g.row_valid_end[w.pt];
-                int slot = 0;
-                float wt = 0.0f;
-                if (valid) {
-                    slot = g.row_src[prow];
-                    wt = g.slot_weight[slot];
+                    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+                    if (lane == 0 && m) atomicMax(reinterpret_cast<unsigned int*>(g.amax_out) + w.e, m << 16);
                 }
-                float* yrow = reinterpret_cast<float*>(g.out) + (int64_t)(slot / g.top_k) * g.ldo + w.qt * BN;
-                const float sc = __fmul_rn(wt, alpha);
-#pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tb + c0, r);
+            } else if constexpr (EPI == EPI_COMBINE) {
+                uint32_t r[NLD][32];
+                if (has_cols) {
+#pragma unroll
+                    for (int j = 0; j < NLD; ++j) tmem_ld32(tb + j * 32, r[j]);
                     tmem_ld_wait();
-                    if (valid) {
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce + acc);
+                const Unit w = decode_unit<BN>(g, sc, u);
+                const int64_t prow = w.p_row0 + qd * 32 + lane;
+                const float alpha = __fmul_rn(g.p_global[w.e], g.q_global[w.e]);
+                const bool valid = has_cols && prow < (int64_t)g.row_valid_end[w.pt];
+                if (valid) {
+                    const int slot = g.row_src[prow];
+                    const float sc = __fmul_rn(g.slot_weight[slot], alpha);
+                    float* yrow = reinterpret_cast<float*>(g.out) + (int64_t)(slot / g.top_k) * g.ldo +
+                                  w.qt * BN + c_begin;
+#pragma unroll
+                    for (int j = 0; j < NLD; ++j)
 #pragma unroll
                         for (int v = 0; v < 8; ++v)
-                            red_add_v4(yrow + c0 + 4 * v, __fmul_rn(sc, __uint_as_float(r[4 * v])),
-                                       __fmul_rn(sc, __uint_as_float(r[4 * v + 1])),
-                                       __fmul_rn(sc, __uint_as_float(r[4 * v + 2])),
-                                       __fmul_rn(sc, __uint_as_float(r[4 * v + 3])));
-                    }
+                            red_add_v4(yrow + j * 32 + 4 * v, __fmul_rn(sc, __uint_as_float(r[j][4 * v])),
+                                       __fmul_rn(sc, __uint_as_float(r[j][4 * v + 1])),
+                                       __fmul_rn(sc, __uint_as_float(r[j][4 * v + 2])),
+                                       __fmul_rn(sc, __uint_as_float(r[j][4 * v + 3])));
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acce + acc);
             if (C::ACC == 2) {
                 acc ^= 1;
                 if (acc == 0) aph ^= 1u;
@@ -417,7 +543,7 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_before();
     __syncthreads();
     pdl_launch_dependents();
-    if (warp == 1) {
+    if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }

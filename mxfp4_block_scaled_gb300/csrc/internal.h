@@ -75,6 +75,7 @@ enum Epi : int {
     EPI_PARTIAL_T = 2,  // part[split][q][p] = acc (fp32, alpha applied by the reduction)
     EPI_SWIGLU = 3,     // grouped: h[p][f] = bf16(SiLU(gate) * up), amax per expert
     EPI_COMBINE = 4,    // grouped: y[token][q] += weight * alpha * acc (fp32 atomics)
+    EPI_PARTIAL = 5,    // part[split][p][q] = acc (fp32, P = activations; alpha applied by the reduction)
 };
 
 struct GemmLaunch {

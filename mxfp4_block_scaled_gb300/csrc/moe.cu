@@ -693,8 +693,9 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         GemmLaunch g;
         g.fmt = FP4_NVFP4;
         g.epi = EPI_COMBINE;
-        // the tile width must divide H (output columns of one token row)
-        g.bn = (T * k >= 4 * E * 64 && H % 256 == 0) ? 256 : 64;
+        // the tile width must divide H (output columns of one token row); the
+        // fp32 combine epilogue keeps at most 64 columns per warp in registers
+        g.bn = (T * k >= 4 * E * 64 && H % 128 == 0) ? 128 : 64;
         g.p_codes = h_codes;
         g.p_scales = h_scales;
         g.p_rows = L.R;

@@ -62,13 +62,17 @@ __global__ void __launch_bounds__(QT) amax_partial_kernel(const uint4* __restric
     uint32_t m = 0;
     const int64_t stride = (int64_t)gridDim.x * QT;
     int64_t i = (int64_t)blockIdx.x * QT + threadIdx.x;
-    for (; i + stride < n_vec; i += 2 * stride) {
+    for (; i + 3 * stride < n_vec; i += 4 * stride) {
         const uint4 a = __ldg(x + i);
         const uint4 b = __ldg(x + i + stride);
+        const uint4 c = __ldg(x + i + 2 * stride);
+        const uint4 d = __ldg(x + i + 3 * stride);
         m = absmax8(a, m);
         m = absmax8(b, m);
+        m = absmax8(c, m);
+        m = absmax8(d, m);
     }
-    if (i < n_vec) m = absmax8(__ldg(x + i), m);
+    for (; i < n_vec; i += stride) m = absmax8(__ldg(x + i), m);
     m = max(m & 0xFFFFu, m >> 16);
     m = block_max_u32(m, red);
     if (threadIdx.x == 0) partials[blockIdx.x] = __uint_as_float(m << 16);
@@ -80,7 +84,8 @@ int amax_partials_count(int64_t n_elems) {
     const int sms = d ? d->sm_count : 148;
     int64_t want = (n_elems / 8 + QT * 8 - 1) / (QT * 8);  // >= 8 vectors per thread
     if (want < 1) want = 1;
-    const int64_t cap = (int64_t)sms * 4;
+    int64_t cap = (int64_t)sms * 6;
+    if (cap > 1024) cap = 1024;
     return (int)(want < cap ? want : cap);
 }
 
@@ -111,8 +116,50 @@ cudaError_t launch_amax_partials(const uint16_t* x, int64_t n_elems, float* part
 
 // ------------------------------------------------------------- quantiser
 
+// E2M1 codes of x / d for 8 elements (one 32-bit word), bit-identical to
+// converting the correctly rounded quotients fl(x / d).  With rd = fl(1/d),
+// q = fl(x * rd) is within 1.5 * 2^-23 relative of x / d, and so is fl(x / d);
+// q * (1 - 2^-21) and q * (1 + 2^-21) (each rounded) therefore bracket
+// fl(x / d).  E2M1 rounding is monotone, so when both brackets give the same
+// codes those are the codes of fl(x / d).  Otherwise (a quotient next to a
+// rounding threshold, rare) the codes come from correctly rounded divisions.
+// d must be a normal float whose reciprocal is normal.
+__device__ __forceinline__ uint32_t e2m1_word(const float* f, float d, float rd) {
+    const float lo_s = 1.0f - 4.76837158203125e-07f;  // 1 - 2^-21
+    const float hi_s = 1.0f + 4.76837158203125e-07f;  // 1 + 2^-21
+    float q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(f[i], rd);
+    const uint32_t lo = cvt_e2m1x8(__fmul_rn(q[0], lo_s), __fmul_rn(q[1], lo_s), __fmul_rn(q[2], lo_s),
+                                   __fmul_rn(q[3], lo_s), __fmul_rn(q[4], lo_s), __fmul_rn(q[5], lo_s),
+                                   __fmul_rn(q[6], lo_s), __fmul_rn(q[7], lo_s));
+    const uint32_t hi = cvt_e2m1x8(__fmul_rn(q[0], hi_s), __fmul_rn(q[1], hi_s), __fmul_rn(q[2], hi_s),
+                                   __fmul_rn(q[3], hi_s), __fmul_rn(q[4], hi_s), __fmul_rn(q[5], hi_s),
+                                   __fmul_rn(q[6], hi_s), __fmul_rn(q[7], hi_s));
+    if (lo == hi) return lo;
+    return cvt_e2m1x8(__fdiv_rn(f[0], d), __fdiv_rn(f[1], d), __fdiv_rn(f[2], d), __fdiv_rn(f[3], d),
+                      __fdiv_rn(f[4], d), __fdiv_rn(f[5], d), __fdiv_rn(f[6], d), __fdiv_rn(f[7], d));
+}
+
+__device__ __forceinline__ uint32_t e2m1_word_exact(const float* f, float d) {
+    return cvt_e2m1x8(__fdiv_rn(f[0], d), __fdiv_rn(f[1], d), __fdiv_rn(f[2], d), __fdiv_rn(f[3], d),
+                      __fdiv_rn(f[4], d), __fdiv_rn(f[5], d), __fdiv_rn(f[6], d), __fdiv_rn(f[7], d));
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
+    f[0] = bf16lo(v.x), f[1] = bf16hi(v.x), f[2] = bf16lo(v.y), f[3] = bf16hi(v.y);
+    f[4] = bf16lo(v.z), f[5] = bf16hi(v.z), f[6] = bf16lo(v.w), f[7] = bf16hi(v.w);
+}
+
+// One thread per scale block: 16 elements (NVFP4) or 32 (MXFP4) of one row.
+// A CTA covers `rpi` rows at a time with `bpt` threads per row (consecutive
+// threads take consecutive blocks, so a warp reads a contiguous stretch of the
+// row and writes contiguous codes), and walks rows with a grid stride.  Rows
+// and blocks past the data (padding of the MMA scale layout) get zero scales.
 template <bool MX>
 __global__ void __launch_bounds__(QT) quant_kernel(const QuantLaunch q) {
+    constexpr int BLK = MX ? 32 : 16;
+    constexpr int NV = BLK / 8;  // 16-byte loads per thread
     __shared__ uint32_t red[QT / 32];
     __shared__ float sh_sg;
     pdl_wait();
@@ -134,19 +181,17 @@ __global__ void __launch_bounds__(QT) quant_kernel(const QuantLaunch q) {
                 q.expert_sg_out[e] = __fdiv_rn(q.table[e], 2688.0f);
     }
 
-    const int lane = threadIdx.x & 31;
-    const int64_t chunks = (q.k + 255) / 256;
-    const int64_t ksf_pad = sf_cols_padded(q.k, MX ? 32 : 16);
+    const int nb = (int)sf_cols_padded(q.k, BLK);      // scale blocks per row, padding included
+    const int kblocks = (int)(q.k / BLK);              // blocks holding data
+    const int bpt = nb < QT ? (nb + 31) / 32 * 32 : QT;  // threads per row
+    const int rpi = QT / bpt;                           // rows per CTA iteration
+    const int ty = threadIdx.x / bpt, tx = threadIdx.x - ty * bpt;
+    if (ty >= rpi) return;
     const int64_t row_limit = q.rows_dev ? (int64_t)(*q.rows_dev) : q.rows_pad;
-    const int64_t total = q.rows_pad * chunks;
-    const int64_t warps = (int64_t)gridDim.x * (QT / 32);
-    const int64_t kb = q.k / 2;
+    const int64_t ksf_pad = nb;
+    const bool dyn_sg = !MX && (q.sg_mode == SG_EXPERT_TABLE || q.sg_mode == SG_EXPERT_AMAX);
 
-    for (int64_t item = (int64_t)blockIdx.x * (QT / 32) + (threadIdx.x >> 5); item < total; item += warps) {
-        const int64_t r = item / chunks;
-        const int64_t c = item - r * chunks;
-        if (r >= row_limit) continue;  // warp-uniform
-        const int64_t col = c * 256 + lane * 8;
+    for (int64_t r = (int64_t)blockIdx.x * rpi + ty; r < row_limit; r += (int64_t)gridDim.x * rpi) {
         int64_t src = -1;
         if (r < q.rows) {
             src = r;
@@ -155,36 +200,49 @@ __global__ void __launch_bounds__(QT) quant_kernel(const QuantLaunch q) {
                 src = q.row_map_is_mask ? (m >= 0 ? r : -1) : m;
             }
         }
-        const bool in = (src >= 0) && (col < q.k);
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (in) v = __ldg(reinterpret_cast<const uint4*>(q.x + src * q.x_ld + col));
-        const float f[8] = {bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y),
-                            bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w)};
-        uint32_t am = absmax8(v, 0u);
-        am = max(am & 0xFFFFu, am >> 16);
-        uint32_t sbyte;
-        uint32_t packed = 0;
-        if (!MX) {
-            am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
-            const float amax_b = __uint_as_float(am << 16);
-            float sg = sg_tensor;
-            if (q.sg_mode == SG_EXPERT_TABLE) sg = q.table[q.tile_expert[r >> 7]];
-            else if (q.sg_mode == SG_EXPERT_AMAX) sg = __fdiv_rn(q.table[q.tile_expert[r >> 7]], 2688.0f);
-            const float p = __fmul_rn(sg, 6.0f);
-            sbyte = 0;
-            if (p > 0.0f) sbyte = cvt_e4m3(__fdiv_rn(amax_b, p));
-            const float d = __fmul_rn(e4m3_to_f32(sbyte), sg);
-            if (d != 0.0f) {
+        const uint16_t* xrow = q.x + (src >= 0 ? src : 0) * q.x_ld;
+        uint8_t* crow = q.codes + r * (q.k / 2);
+        float sg = sg_tensor;
+        if (dyn_sg) {
+            const float t = q.table[q.tile_expert[r >> 7]];
+            sg = q.sg_mode == SG_EXPERT_TABLE ? t : __fdiv_rn(t, 2688.0f);
+        }
+        const float p = __fmul_rn(sg, 6.0f);
+        for (int b = tx; b < nb; b += bpt) {
+            const bool in = src >= 0 && b < kblocks;
+            uint4 v[NV];
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    packed |= cvt_e2m1x2(__fdiv_rn(f[2 * i], d), __fdiv_rn(f[2 * i + 1], d)) << (8 * i);
+            for (int i = 0; i < NV; ++i) v[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (in) {
+                const uint4* px = reinterpret_cast<const uint4*>(xrow + b * BLK);
+#pragma unroll
+                for (int i = 0; i < NV; ++i) v[i] = __ldg(px + i);
             }
-        } else {
-            am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
-            am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
-            const float amax_b = __uint_as_float(am << 16);
-            sbyte = 0;
-            if (amax_b > 0.0f) {
+            uint32_t am = 0;
+#pragma unroll
+            for (int i = 0; i < NV; ++i) am = absmax8(v[i], am);
+            const float amax_b = __uint_as_float(max(am & 0xFFFFu, am >> 16) << 16);
+            uint32_t sbyte = 0;
+            uint32_t w[NV];
+#pragma unroll
+            for (int i = 0; i < NV; ++i) w[i] = 0u;
+            if (!MX) {
+                if (p > 0.0f) sbyte = cvt_e4m3(__fdiv_rn(amax_b, p));
+                const float d = __fmul_rn(e4m3_to_f32(sbyte), sg);
+                if (d != 0.0f) {
+                    float f[16];
+                    unpack8(v[0], f);
+                    unpack8(v[1], f + 8);
+                    if (d >= 1.1754944e-38f && d <= 8.5070592e37f) {
+                        const float rd = __frcp_rn(d);
+                        w[0] = e2m1_word(f, d, rd);
+                        w[1] = e2m1_word(f + 8, d, rd);
+                    } else {
+                        w[0] = e2m1_word_exact(f, d);
+                        w[1] = e2m1_word_exact(f + 8, d);
+                    }
+                }
+            } else if (amax_b > 0.0f) {
                 const uint32_t u = __float_as_uint(amax_b);
                 const int fl = (u >> 23) ? (int)(u >> 23) - 127 : (31 - __clz((int)u)) - 149;
                 int e = fl - 2;
@@ -192,30 +250,19 @@ __global__ void __launch_bounds__(QT) quant_kernel(const QuantLaunch q) {
                 sbyte = (uint32_t)(e + 127);
                 const float inv = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e, a normal float here
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    packed |= cvt_e2m1x2(__fmul_rn(f[2 * i], inv), __fmul_rn(f[2 * i + 1], inv)) << (8 * i);
+                for (int i = 0; i < NV; ++i) {
+                    float f[8];
+                    unpack8(v[i], f);
+                    w[i] = cvt_e2m1x8(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv), __fmul_rn(f[2], inv),
+                                      __fmul_rn(f[3], inv), __fmul_rn(f[4], inv), __fmul_rn(f[5], inv),
+                                      __fmul_rn(f[6], inv), __fmul_rn(f[7], inv));
+                }
             }
-        }
-        if (in) *reinterpret_cast<uint32_t*>(q.codes + r * kb + col / 2) = packed;
-        // Gather four consecutive scale bytes into one word of the MMA layout.
-        if (!MX) {
-            const int base = lane & ~7;
-            const uint32_t s0 = __shfl_sync(0xFFFFFFFFu, sbyte, base + 0);
-            const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, sbyte, base + 2);
-            const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, sbyte, base + 4);
-            const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, sbyte, base + 6);
-            if ((lane & 7) == 0)
-                *reinterpret_cast<uint32_t*>(q.scales + sf_offset(r, c * 16 + (lane >> 3) * 4, ksf_pad)) =
-                    s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
-        } else {
-            const int base = lane & ~15;
-            const uint32_t s0 = __shfl_sync(0xFFFFFFFFu, sbyte, base + 0);
-            const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, sbyte, base + 4);
-            const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, sbyte, base + 8);
-            const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, sbyte, base + 12);
-            if ((lane & 15) == 0)
-                *reinterpret_cast<uint32_t*>(q.scales + sf_offset(r, c * 8 + (lane >> 4) * 4, ksf_pad)) =
-                    s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
+            if (in) {
+                if (MX) *reinterpret_cast<uint4*>(crow + b * 16) = make_uint4(w[0], w[1], w[NV > 2 ? 2 : 0], w[NV > 3 ? 3 : 0]);
+                else *reinterpret_cast<uint2*>(crow + b * 8) = make_uint2(w[0], w[1]);
+            }
+            q.scales[sf_offset(r, b, ksf_pad)] = (uint8_t)sbyte;
         }
     }
     pdl_launch_dependents();
@@ -224,10 +271,12 @@ __global__ void __launch_bounds__(QT) quant_kernel(const QuantLaunch q) {
 cudaError_t launch_quant(const QuantLaunch& q, cudaStream_t s) {
     const DeviceInfo* d = current_device();
     const int sms = d ? d->sm_count : 148;
-    const int64_t chunks = (q.k + 255) / 256;
-    const int64_t total = q.rows_pad * chunks;
-    int64_t blocks = (total + (QT / 32) - 1) / (QT / 32);
-    const int64_t cap = (int64_t)sms * (2048 / QT);
+    const int blk = q.fmt == FP4_MXFP4 ? 32 : 16;
+    const int64_t nb = sf_cols_padded(q.k, blk);
+    const int64_t bpt = nb < QT ? (nb + 31) / 32 * 32 : QT;
+    const int64_t rpi = QT / bpt;
+    int64_t blocks = (q.rows_pad + rpi - 1) / rpi;
+    const int64_t cap = (int64_t)sms * 4;  // persistent: one wave at this kernel's occupancy
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     QuantLaunch qq = q;
