@@ -29,6 +29,7 @@ void set_error(const char* fmt, ...) {
 static std::mutex g_dev_mtx;
 static DeviceInfo g_dev[64];
 static int g_arch_override = 0;
+static int g_tile_policy = 0;  // fp4_set_gemm_tile_policy
 static uint64_t g_wait_limit_ns = 4000000000ull;
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns; }
@@ -174,6 +175,12 @@ extern "C" size_t fp4_scales_bytes(int fmt, int64_t rows, int64_t k) {
 
 extern "C" void fp4_set_arch_override(int sm) { g_arch_override = sm; }
 
+extern "C" fp4_status fp4_set_gemm_tile_policy(int policy) {
+    CHECK_OR_RETURN(policy >= 0 && policy <= 2, FP4_ERR_INVALID_ARG, "tile policy %d not in 0..2", policy);
+    g_tile_policy = policy;
+    return FP4_OK;
+}
+
 extern "C" fp4_status fp4_device_status(void* stream) {
     TRY(check_arch());
     const DeviceInfo* d = current_device();
@@ -287,12 +294,14 @@ static const int64_t kDecodeMaxM = 64;
 
 struct GemmPlan {
     bool decode;
+    bool pair;  // CTA-pair kernel (256 x 256 tiles)
     int bn;
     int splits;
 };
 
 static GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int sms) {
     GemmPlan p;
+    p.pair = false;
     const int64_t kbt = gemm_k_blocks(k);
     if (m <= kDecodeMaxM) {
         // decode: one 128-row activation tile (rows beyond m are zero-filled by
@@ -314,6 +323,11 @@ static GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int sms) {
         const int64_t units256 = ((m + 127) / 128) * ((n + 255) / 256);
         p.bn = units256 >= sms ? 256 : 128;
         p.splits = 1;
+        // The CTA-pair kernel is opt-in: on the 8192 x 14336 x 4096 prefill its
+        // K-block loop is bound by the chain operand landing -> scale store in
+        // both CTAs -> cross-CTA arrive -> MMA issue, and it runs slower than
+        // the one-CTA kernel.
+        p.pair = g_tile_policy == 2 && m >= 256 && n >= 256;
     }
     return p;
 }
@@ -376,6 +390,7 @@ static fp4_status enqueue_gemm(int fmt, const uint8_t* ac, const uint8_t* as, co
         g.q_codes = wc, g.q_scales = wsc, g.q_rows = n, g.q_rows_valid = n, g.q_global = wg;
         g.out = out;
         g.ldo = n;
+        if (p.pair) return cuda_status(launch_gemm_pair(g, s), "GEMM launch");
         return cuda_status(launch_gemm(g, s), "GEMM launch");
     }
     // decode: activations on the MMA M side, weights on N, split-K partials

@@ -5,7 +5,7 @@
 
 #include <mutex>
 
-#include "gemm_kernel.cuh"
+#include "gemm_pair.cuh"
 
 namespace fp4 {
 
@@ -87,6 +87,72 @@ static cudaError_t launch_one(const GemmLaunch& g, cudaStream_t s) {
         cfg.numAttrs = 1;
     }
     return cudaLaunchKernelExC(&cfg, (const void*)kern, args);
+}
+
+// CTA-pair GEMM (prefill): clusters of two CTAs, 256 x 256 output tiles.
+template <bool MX>
+static cudaError_t launch_pair(const GemmLaunch& g, cudaStream_t s) {
+    using C = PairCfg<MX>;
+    auto kern = gemm_pair_kernel<MX>;
+    const DeviceInfo* d = current_device();
+    if (!d) return cudaErrorNoDevice;
+    static int max_clusters[64];  // per device: clusters that can be resident at once
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(512);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (max_clusters[d->device] == 0) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+        (void)e;
+        cfg.gridDim = dim3((unsigned)(d->sm_count & ~1));
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, (const void*)kern, &cfg);
+        if (e != cudaSuccess || n < 1) {
+            cudaGetLastError();
+            n = d->sm_count / 2;
+        }
+        max_clusters[d->device] = n;
+    }
+    CUtensorMap tmP, tmQ;
+    if (!make_codes_map(&tmP, g.p_codes, g.p_rows, g.k, 128) || !make_codes_map(&tmQ, g.q_codes, g.q_rows, g.k, 128)) {
+        set_error("cuTensorMapEncodeTiled failed (rows %lld/%lld, k %lld)", (long long)g.p_rows, (long long)g.q_rows,
+                  (long long)g.k);
+        return cudaErrorInvalidValue;
+    }
+    const int64_t units = ((g.p_rows_valid + 255) / 256) * ((g.q_rows_valid + 255) / 256);
+    int64_t clusters = max_clusters[d->device];
+    if (units < clusters) clusters = units;
+    if (clusters < 1) return cudaSuccess;
+    cfg.gridDim = dim3((unsigned)(2 * clusters));
+    if (g.pdl) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
+    }
+    WaitCfg wc;
+    wc.limit_ns = wait_limit_ns();
+    wc.err = d->err_word;
+    GemmLaunch gg = g;
+    void* args[] = {(void*)&tmP, (void*)&tmQ, (void*)&gg, (void*)&wc};
+    return cudaLaunchKernelExC(&cfg, (const void*)kern, args);
+}
+
+cudaError_t launch_gemm_pair(const GemmLaunch& g, cudaStream_t s) {
+    return g.fmt == FP4_MXFP4 ? launch_pair<true>(g, s) : launch_pair<false>(g, s);
+}
+
+int gemm_pair_max_clusters() {
+    const DeviceInfo* d = current_device();
+    return d ? d->sm_count / 2 : 76;
 }
 
 cudaError_t launch_gemm_moe(const GemmLaunch& g, cudaStream_t s);  // moe.cu

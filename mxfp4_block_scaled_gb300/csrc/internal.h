@@ -115,6 +115,8 @@ struct GemmLaunch {
 
 int64_t gemm_k_blocks(int64_t k);
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s);
+// CTA-pair variant (EPI_BF16 only): 256 x 256 tiles on clusters of two CTAs.
+cudaError_t launch_gemm_pair(const GemmLaunch& g, cudaStream_t s);
 cudaError_t launch_splitk_reduce(const float* part, int splits, int64_t m, int64_t n, const float* ga,
                                  const float* gw, bool mx, uint16_t* out, bool pdl, cudaStream_t s);
 

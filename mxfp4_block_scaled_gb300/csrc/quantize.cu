@@ -59,20 +59,23 @@ __global__ void __launch_bounds__(QT) amax_partial_kernel(const uint4* __restric
                                                           float* __restrict__ partials) {
     __shared__ uint32_t red[QT / 32];
     pdl_wait();
+    // Sweep from the end of the tensor to its start, so that the start -- which
+    // the quantise pass reads first -- is the most recently cached.
     uint32_t m = 0;
     const int64_t stride = (int64_t)gridDim.x * QT;
+    const uint4* xe = x + (n_vec - 1);
     int64_t i = (int64_t)blockIdx.x * QT + threadIdx.x;
     for (; i + 3 * stride < n_vec; i += 4 * stride) {
-        const uint4 a = __ldg(x + i);
-        const uint4 b = __ldg(x + i + stride);
-        const uint4 c = __ldg(x + i + 2 * stride);
-        const uint4 d = __ldg(x + i + 3 * stride);
+        const uint4 a = __ldg(xe - i);
+        const uint4 b = __ldg(xe - (i + stride));
+        const uint4 c = __ldg(xe - (i + 2 * stride));
+        const uint4 d = __ldg(xe - (i + 3 * stride));
         m = absmax8(a, m);
         m = absmax8(b, m);
         m = absmax8(c, m);
         m = absmax8(d, m);
     }
-    for (; i < n_vec; i += stride) m = absmax8(__ldg(x + i), m);
+    for (; i < n_vec; i += stride) m = absmax8(__ldg(xe - i), m);
     m = max(m & 0xFFFFu, m >> 16);
     m = block_max_u32(m, red);
     if (threadIdx.x == 0) partials[blockIdx.x] = __uint_as_float(m << 16);
@@ -190,80 +193,114 @@ __global__ void __launch_bounds__(QT) quant_kernel(const QuantLaunch q) {
     const int64_t row_limit = q.rows_dev ? (int64_t)(*q.rows_dev) : q.rows_pad;
     const int64_t ksf_pad = nb;
     const bool dyn_sg = !MX && (q.sg_mode == SG_EXPERT_TABLE || q.sg_mode == SG_EXPERT_AMAX);
+    const int64_t rstride = (int64_t)gridDim.x * rpi;
 
-    for (int64_t r = (int64_t)blockIdx.x * rpi + ty; r < row_limit; r += (int64_t)gridDim.x * rpi) {
-        int64_t src = -1;
-        if (r < q.rows) {
-            src = r;
-            if (q.row_map) {
-                const int64_t m = q.row_map[r];
-                src = q.row_map_is_mask ? (m >= 0 ? r : -1) : m;
-            }
+    // Items (row r, block b) of this thread in order; the loads of the next item
+    // are issued before the current one is converted (two in flight).
+    struct Item {
+        int64_t r, src;
+        int b;
+        uint4 v[NV];
+    };
+    auto source_row = [&](int64_t r) -> int64_t {
+        if (r >= q.rows) return -1;
+        if (!q.row_map) return r;
+        const int64_t m = q.row_map[r];
+        return q.row_map_is_mask ? (m >= 0 ? r : -1) : m;
+    };
+    auto load = [&](Item& it) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) it.v[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (it.src >= 0 && it.b < kblocks) {
+            const uint4* px = reinterpret_cast<const uint4*>(q.x + it.src * q.x_ld + (int64_t)it.b * BLK);
+#pragma unroll
+            for (int i = 0; i < NV; ++i) it.v[i] = __ldg(px + i);
         }
-        const uint16_t* xrow = q.x + (src >= 0 ? src : 0) * q.x_ld;
-        uint8_t* crow = q.codes + r * (q.k / 2);
+    };
+    Item cur;
+    cur.r = (int64_t)blockIdx.x * rpi + ty;
+    cur.b = tx;
+    if (cur.r >= row_limit || cur.b >= nb) {
+        pdl_launch_dependents();
+        return;
+    }
+    cur.src = source_row(cur.r);
+    load(cur);
+    while (true) {
+        Item nxt;
+        nxt.r = cur.r;
+        nxt.b = cur.b + bpt;
+        if (nxt.b >= nb) {
+            nxt.b = tx;
+            nxt.r += rstride;
+        }
+        const bool more = nxt.r < row_limit;
+        if (more) {
+            nxt.src = nxt.r == cur.r ? cur.src : source_row(nxt.r);
+            load(nxt);
+        }
+
+        // ---- convert the current item
+        const int64_t r = cur.r;
+        const int b = cur.b;
+        const bool in = cur.src >= 0 && b < kblocks;
         float sg = sg_tensor;
         if (dyn_sg) {
             const float t = q.table[q.tile_expert[r >> 7]];
             sg = q.sg_mode == SG_EXPERT_TABLE ? t : __fdiv_rn(t, 2688.0f);
         }
-        const float p = __fmul_rn(sg, 6.0f);
-        for (int b = tx; b < nb; b += bpt) {
-            const bool in = src >= 0 && b < kblocks;
-            uint4 v[NV];
+        uint32_t am = 0;
 #pragma unroll
-            for (int i = 0; i < NV; ++i) v[i] = make_uint4(0u, 0u, 0u, 0u);
-            if (in) {
-                const uint4* px = reinterpret_cast<const uint4*>(xrow + b * BLK);
+        for (int i = 0; i < NV; ++i) am = absmax8(cur.v[i], am);
+        const float amax_b = __uint_as_float(max(am & 0xFFFFu, am >> 16) << 16);
+        uint32_t sbyte = 0;
+        uint32_t w[NV];
 #pragma unroll
-                for (int i = 0; i < NV; ++i) v[i] = __ldg(px + i);
-            }
-            uint32_t am = 0;
-#pragma unroll
-            for (int i = 0; i < NV; ++i) am = absmax8(v[i], am);
-            const float amax_b = __uint_as_float(max(am & 0xFFFFu, am >> 16) << 16);
-            uint32_t sbyte = 0;
-            uint32_t w[NV];
-#pragma unroll
-            for (int i = 0; i < NV; ++i) w[i] = 0u;
-            if (!MX) {
-                if (p > 0.0f) sbyte = cvt_e4m3(__fdiv_rn(amax_b, p));
-                const float d = __fmul_rn(e4m3_to_f32(sbyte), sg);
-                if (d != 0.0f) {
-                    float f[16];
-                    unpack8(v[0], f);
-                    unpack8(v[1], f + 8);
-                    if (d >= 1.1754944e-38f && d <= 8.5070592e37f) {
-                        const float rd = __frcp_rn(d);
-                        w[0] = e2m1_word(f, d, rd);
-                        w[1] = e2m1_word(f + 8, d, rd);
-                    } else {
-                        w[0] = e2m1_word_exact(f, d);
-                        w[1] = e2m1_word_exact(f + 8, d);
-                    }
-                }
-            } else if (amax_b > 0.0f) {
-                const uint32_t u = __float_as_uint(amax_b);
-                const int fl = (u >> 23) ? (int)(u >> 23) - 127 : (31 - __clz((int)u)) - 149;
-                int e = fl - 2;
-                e = e < -127 ? -127 : (e > 127 ? 127 : e);
-                sbyte = (uint32_t)(e + 127);
-                const float inv = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e, a normal float here
-#pragma unroll
-                for (int i = 0; i < NV; ++i) {
-                    float f[8];
-                    unpack8(v[i], f);
-                    w[i] = cvt_e2m1x8(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv), __fmul_rn(f[2], inv),
-                                      __fmul_rn(f[3], inv), __fmul_rn(f[4], inv), __fmul_rn(f[5], inv),
-                                      __fmul_rn(f[6], inv), __fmul_rn(f[7], inv));
+        for (int i = 0; i < NV; ++i) w[i] = 0u;
+        if (!MX) {
+            const float p = __fmul_rn(sg, 6.0f);
+            if (p > 0.0f) sbyte = cvt_e4m3(__fdiv_rn(amax_b, p));
+            const float d = __fmul_rn(e4m3_to_f32(sbyte), sg);
+            if (d != 0.0f) {
+                float f[16];
+                unpack8(cur.v[0], f);
+                unpack8(cur.v[1], f + 8);
+                if (d >= 1.1754944e-38f && d <= 8.5070592e37f) {
+                    const float rd = __frcp_rn(d);
+                    w[0] = e2m1_word(f, d, rd);
+                    w[1] = e2m1_word(f + 8, d, rd);
+                } else {
+                    w[0] = e2m1_word_exact(f, d);
+                    w[1] = e2m1_word_exact(f + 8, d);
                 }
             }
-            if (in) {
-                if (MX) *reinterpret_cast<uint4*>(crow + b * 16) = make_uint4(w[0], w[1], w[NV > 2 ? 2 : 0], w[NV > 3 ? 3 : 0]);
-                else *reinterpret_cast<uint2*>(crow + b * 8) = make_uint2(w[0], w[1]);
+        } else if (amax_b > 0.0f) {
+            const uint32_t u = __float_as_uint(amax_b);
+            const int fl = (u >> 23) ? (int)(u >> 23) - 127 : (31 - __clz((int)u)) - 149;
+            int e = fl - 2;
+            e = e < -127 ? -127 : (e > 127 ? 127 : e);
+            sbyte = (uint32_t)(e + 127);
+            const float inv = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e, a normal float here
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                float f[8];
+                unpack8(cur.v[i], f);
+                w[i] = cvt_e2m1x8(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv), __fmul_rn(f[2], inv),
+                                  __fmul_rn(f[3], inv), __fmul_rn(f[4], inv), __fmul_rn(f[5], inv),
+                                  __fmul_rn(f[6], inv), __fmul_rn(f[7], inv));
             }
-            q.scales[sf_offset(r, b, ksf_pad)] = (uint8_t)sbyte;
         }
+        if (in) {
+            uint8_t* c = q.codes + r * (q.k / 2) + (int64_t)b * (BLK / 2);
+            if (MX)
+                *reinterpret_cast<uint4*>(c) = make_uint4(w[0], w[1], w[NV > 2 ? 2 : 0], w[NV > 3 ? 3 : 0]);
+            else
+                *reinterpret_cast<uint2*>(c) = make_uint2(w[0], w[1]);
+        }
+        q.scales[sf_offset(r, b, ksf_pad)] = (uint8_t)sbyte;
+
+        if (!more) break;
+        cur = nxt;
     }
     pdl_launch_dependents();
 }

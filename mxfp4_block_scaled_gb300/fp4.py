@@ -44,6 +44,7 @@ _SIGNATURES = {
     "fp4_scales_bytes": (_SZ, [_INT, _I64, _I64]),
     "fp4_device_status": (_INT, [_P]),
     "fp4_set_arch_override": (None, [_INT]),
+    "fp4_set_gemm_tile_policy": (_INT, [_INT]),
     "fp4_debug_timeout_probe": (_INT, [_I64, _P]),
     "fp4_quantize_workspace_size": (_SZ, [_INT, _I64, _I64]),
     "fp4_quantize_act": (_INT, [_INT, _P, _I64, _I64, _INT, _F, _P, _P, _P, _P, _SZ, _P]),
@@ -187,6 +188,14 @@ def gemm_prequant(aq, wq, out=None, workspace=None, stream=None):
                                _ptr(wq.scales), _ptr(wq.gscale), n, k, _ptr(out), _ptr(ws),
                                0 if ws is None else ws.numel(), _stream(stream)))
     return out
+
+
+TILE_AUTO, TILE_ONE_CTA, TILE_CTA_PAIR = 0, 1, 2
+
+
+def set_gemm_tile_policy(policy):
+    """Choose the prefill GEMM kernel (TILE_AUTO, TILE_ONE_CTA, TILE_CTA_PAIR)."""
+    _check(lib().fp4_set_gemm_tile_policy(int(policy)))
 
 
 def device_status(stream=None):

@@ -105,3 +105,14 @@ def test_python_wrapper_raises(F):
     with pytest.raises(F.FP4Error) as ei:
         F._check(F.lib().fp4_gemm(0, A, 16, 0, 0.0, A, A, A, 256, 48, A, A, 1 << 30, None))
     assert ei.value.name == "FP4_ERR_SHAPE"
+
+
+def test_tile_policy_validation(F):
+    L = F.lib()
+    for p in (F.TILE_ONE_CTA, F.TILE_CTA_PAIR, F.TILE_AUTO):
+        assert L.fp4_set_gemm_tile_policy(p) == 0
+    for bad in (-1, 3):
+        assert L.fp4_set_gemm_tile_policy(bad) == F.STATUS_CODE["FP4_ERR_INVALID_ARG"]
+        assert "tile policy" in L.fp4_last_error_message().decode()
+    with pytest.raises(F.FP4Error):
+        F.set_gemm_tile_policy(7)

@@ -55,6 +55,19 @@ def test_shapes(F, O, m, n, k, fmt):
     check_linear(F, O, I.randn_bf16((m, k), m + n), I.weights_bf16(n, k, k + 3), fmt)
 
 
+# the CTA-pair kernel (forced by the tile policy): more pair tiles than SMs,
+# a ragged M whose last pair tile has an empty odd half, a ragged N, and
+# problems of one or two pair tiles
+@pytest.mark.parametrize("m,n,k", [(2660, 4096, 512), (2395, 4104, 768), (256, 256, 256), (300, 520, 1056)])
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_pair_kernel_shapes(F, O, m, n, k, fmt):
+    F.set_gemm_tile_policy(F.TILE_CTA_PAIR)
+    try:
+        check_linear(F, O, I.randn_bf16((m, k), m), I.weights_bf16(n, k, n), fmt)
+    finally:
+        F.set_gemm_tile_policy(F.TILE_AUTO)
+
+
 def test_static_scale(F, O):
     a = I.randn_bf16((96, 512), 9)
     w = I.weights_bf16(256, 512, 10)
