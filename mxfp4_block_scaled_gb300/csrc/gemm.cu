@@ -23,26 +23,43 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D map over packed codes [rows][k/2] bytes; box = 128 bytes x box_rows,
-// 128-byte swizzle (matches the MMA's K-major SWIZZLE_128B operand layout).
-static bool make_codes_map(CUtensorMap* m, const void* base, int64_t rows, int64_t k, int box_rows) {
+// 2-D map over packed codes [rows][k/2] bytes; box = box_bytes (64 or 128) x
+// box_rows with the swizzle of the same width (the MMA's K-major operand layout).
+static bool make_codes_map(CUtensorMap* m, const void* base, int64_t rows, int64_t k, int box_rows, int box_bytes) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)(k / 2), (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)(k / 2)};
-    cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+    cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)box_rows};
     cuuint32_t es[2] = {1u, 1u};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-int64_t gemm_k_blocks(int64_t k) { return (k + 255) / 256; }
+// 2-D map over the bf16 output [rows][cols] with row pitch ldo elements
+// (ldo % 8 == 0, 16-byte aligned base); box = 64 columns x 128 rows with the
+// 128-byte swizzle of the epilogue's staging buffers.
+static bool make_out_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t ldo) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ldo * 2)};
+    cuuint32_t box[2] = {64u, 128u};
+    cuuint32_t es[2] = {1u, 1u};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int64_t gemm_k_blocks(int64_t k) { return (k + 2 * GEMM_KB_BYTES - 1) / (2 * GEMM_KB_BYTES); }
 
 template <int BN, bool MX, int EPI>
 static cudaError_t launch_one(const GemmLaunch& g, cudaStream_t s) {
-    using C = GemmCfg<BN, MX>;
+    using C = GemmCfg<BN, MX, epi_staging_bytes<EPI>()>;
     auto kern = gemm_kernel<BN, MX, EPI>;
     static bool attr_set = false;  // per instantiation; the attribute is per device function
     if (!attr_set) {
@@ -50,11 +67,21 @@ static cudaError_t launch_one(const GemmLaunch& g, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    CUtensorMap tmP, tmQ;
-    if (!make_codes_map(&tmP, g.p_codes, g.p_rows, g.k, 128) || !make_codes_map(&tmQ, g.q_codes, g.q_rows, g.k, BN)) {
+    CUtensorMap tmP, tmQ, tmO;
+    if (!make_codes_map(&tmP, g.p_codes, g.p_rows, g.k, 128, GEMM_KB_BYTES) ||
+        !make_codes_map(&tmQ, g.q_codes, g.q_rows, g.k, BN, GEMM_KB_BYTES)) {
         set_error("cuTensorMapEncodeTiled failed (rows %lld/%lld, k %lld)", (long long)g.p_rows, (long long)g.q_rows,
                   (long long)g.k);
         return cudaErrorInvalidValue;
+    }
+    if (EPI == EPI_BF16) {
+        if (!make_out_map(&tmO, g.out, g.p_rows_valid, g.q_rows_valid, g.ldo)) {
+            set_error("cuTensorMapEncodeTiled failed for the output (%lld x %lld, ldo %lld)",
+                      (long long)g.p_rows_valid, (long long)g.q_rows_valid, (long long)g.ldo);
+            return cudaErrorInvalidValue;
+        }
+    } else {
+        tmO = tmP;  // unused by the other epilogues
     }
     const DeviceInfo* d = current_device();
     if (!d) return cudaErrorNoDevice;
@@ -73,7 +100,7 @@ static cudaError_t launch_one(const GemmLaunch& g, cudaStream_t s) {
     wc.limit_ns = wait_limit_ns();
     wc.err = d->err_word;
     GemmLaunch gg = g;
-    void* args[] = {(void*)&tmP, (void*)&tmQ, (void*)&gg, (void*)&wc};
+    void* args[] = {(void*)&tmP, (void*)&tmQ, (void*)&tmO, (void*)&gg, (void*)&wc};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(512);
@@ -122,8 +149,9 @@ static cudaError_t launch_pair(const GemmLaunch& g, cudaStream_t s) {
         }
         max_clusters[d->device] = n;
     }
-    CUtensorMap tmP, tmQ;
-    if (!make_codes_map(&tmP, g.p_codes, g.p_rows, g.k, 128) || !make_codes_map(&tmQ, g.q_codes, g.q_rows, g.k, 128)) {
+    CUtensorMap tmP, tmQ, tmO;
+    if (!make_codes_map(&tmP, g.p_codes, g.p_rows, g.k, 128, 128) || !make_codes_map(&tmQ, g.q_codes, g.q_rows, g.k, 128, 128) ||
+        !make_out_map(&tmO, g.out, g.p_rows_valid, g.q_rows_valid, g.ldo)) {
         set_error("cuTensorMapEncodeTiled failed (rows %lld/%lld, k %lld)", (long long)g.p_rows, (long long)g.q_rows,
                   (long long)g.k);
         return cudaErrorInvalidValue;
@@ -142,7 +170,7 @@ static cudaError_t launch_pair(const GemmLaunch& g, cudaStream_t s) {
     wc.limit_ns = wait_limit_ns();
     wc.err = d->err_word;
     GemmLaunch gg = g;
-    void* args[] = {(void*)&tmP, (void*)&tmQ, (void*)&gg, (void*)&wc};
+    void* args[] = {(void*)&tmP, (void*)&tmQ, (void*)&tmO, (void*)&gg, (void*)&wc};
     return cudaLaunchKernelExC(&cfg, (const void*)kern, args);
 }
 

@@ -7,20 +7,29 @@
 //
 // One CTA per SM, 16 warps in four warpgroups:
 //   warps 0-3   scale writers: one per TMEM lane quarter; per K block they read
-//               the scale atoms the TMA brought into smem and store them into
-//               TMEM (tcgen05.st, the layout the block-scaled MMA reads), so
-//               the tensor pipe is left to the MMAs.
+//               the scale atoms from smem and store them into the stage's TMEM
+//               scale columns (tcgen05.st, the layout the block-scaled MMA
+//               reads), so the tensor pipe is left to the MMAs.
 //   warps 4, 6  TMA producers: per 256-element K block, warp 4 loads a 128-row
-//               P tile and warp 6 a BN-row Q tile (128-byte swizzle), each with
-//               its scale atoms (plain bulk copies; the MMA layout makes them
-//               contiguous).
+//               P tile and warp 6 a BN-row Q tile (128-byte swizzle).
+//   warp 7      scale producer: the K block's P and Q scale atoms (plain bulk
+//               copies; the MMA layout makes them contiguous) into a scale ring
+//               with barriers of its own.  The writers need only those atoms
+//               and the stage's TMEM columns free (the MMA's commit of the
+//               previous round), so the scales are in TMEM before the operand
+//               tiles land and the scale path stays off the critical path.
 //   warp 5      TMEM allocator and MMA issuer (one thread): four
 //               M=128 x N=BN x K=64 block-scaled MMAs per K block.
 //   warps 8-15  epilogue: tcgen05.ld of the fp32 accumulator into registers,
 //               release of the TMEM stage, then alpha, bf16 (or the fused MoE
-//               epilogues) and global stores.
-// Pipelines: STAGES smem stages (full / scales-ready / empty mbarriers) and
-// 1-2 TMEM accumulator stages (acc_full/acc_empty).  Every wait is bounded.
+//               epilogues) and global stores.  The bf16 output goes through a
+//               32 KB smem staging area and TMA tensor stores, so whole 128-byte
+//               lines leave the SM (row-per-thread stores from registers would
+//               scatter 16-byte pieces over 32 lines per instruction and load
+//               the L2 with several times as many write requests).
+// Pipelines: STAGES operand stages (full / empty), as many scale slots
+// (scale-full / scale-empty for the smem ring, scales-ready for TMEM) and 1-2
+// TMEM accumulator stages (acc_full / acc_empty).  Every wait is bounded.
 #pragma once
 
 #include "common.cuh"
@@ -28,11 +37,21 @@
 
 namespace fp4 {
 
-template <int BN, bool MX>
+// bf16 epilogue staging: one 16 KB buffer per epilogue warpgroup, 128 rows x
+// 64 bf16 columns in the 128-byte swizzled layout of the output tensor map.
+constexpr int EPI_STAGE_BYTES = 128 * 128;
+
+template <int EPI>
+constexpr int epi_staging_bytes() {
+    return EPI == EPI_BF16 ? 2 * EPI_STAGE_BYTES : 0;
+}
+
+template <int BN, bool MX, int STG = 0>
 struct GemmCfg {
     static constexpr int BM = 128;
-    static constexpr int KB_BYTES = 128;            // one K block = 256 fp4 = 128 bytes per row
-    static constexpr int SF_CHUNKS = MX ? 2 : 4;    // 512-byte scale atoms per 128 rows per K block
+    static constexpr int KB_BYTES = GEMM_KB_BYTES;  // one K block = 2 KB_BYTES fp4 per row
+    static constexpr int KB_MMAS = KB_BYTES / 32;   // K=64 MMAs per K block
+    static constexpr int SF_CHUNKS = KB_BYTES / 64 * (MX ? 1 : 2);  // 512-byte scale atoms per 128 rows per K block
     static constexpr int QCH = BN > 128 ? BN / 128 : 1;
     static constexpr int P_BYTES = BM * KB_BYTES;
     static constexpr int Q_BYTES = BN * KB_BYTES;
@@ -43,15 +62,18 @@ struct GemmCfg {
     static constexpr int SFP_COLS = SF_CHUNKS * 4;
     static constexpr int SFQ_COLS = SF_CHUNKS * 4 * QCH;
     static constexpr int SF_COLS = SFP_COLS + SFQ_COLS;
-    static constexpr int BAR_BYTES = 256;
+    static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM_LIMIT = 227 * 1024;
-    static constexpr int ST_SMEM = (SMEM_LIMIT - 1024 - BAR_BYTES) / STAGE_BYTES;
+    static constexpr int ST_SMEM = (SMEM_LIMIT - 2048 - BAR_BYTES - STG) / STAGE_BYTES;
     static constexpr int ST_TMEM = (512 - ACC * BN) / SF_COLS;
     static constexpr int ST_MIN = ST_SMEM < ST_TMEM ? ST_SMEM : ST_TMEM;
     static constexpr int STAGES = ST_MIN < 8 ? ST_MIN : 8;
-    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    static constexpr int STG_OFFSET = (STAGES * STAGE_BYTES + 1023) / 1024 * 1024;  // 128-byte swizzle alignment
+    static constexpr int SMEM = 1024 + STG_OFFSET + STG + BAR_BYTES;
     static_assert(STAGES >= 2, "pipeline too shallow");
-    static_assert(3 * STAGES + 5 <= BAR_BYTES / 8 - 2, "barrier area too small");
+    static_assert(P_BYTES % 512 == 0 && Q_BYTES % 512 == 0, "64-byte swizzle atoms are 512 bytes");
+    static_assert(SMEM <= SMEM_LIMIT, "shared memory budget");
+    static_assert(5 * STAGES + 5 <= BAR_BYTES / 8 - 2, "barrier area too small");
     static_assert(ACC * BN + STAGES * SF_COLS <= 512, "TMEM budget");
 };
 
@@ -73,7 +95,7 @@ struct Sched {
 template <int BN>
 __device__ __forceinline__ Sched make_sched(const GemmLaunch& g) {
     Sched s;
-    s.kbt = (g.k + 255) / 256;
+    s.kbt = (g.k + 2 * GEMM_KB_BYTES - 1) / (2 * GEMM_KB_BYTES);
     s.splits = g.splits;
     s.kb_per = (s.kbt + g.splits - 1) / g.splits;
     s.n_ptiles = g.grouped ? (int64_t)(*g.n_ptiles_dev) : (g.p_rows_valid + 127) / 128;
@@ -104,6 +126,42 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Stores one epilogue warpgroup's 128 rows x (32 NLD) bf16 columns through its
+// staging buffer `buf` (smem address, 1024-byte aligned) with TMA stores of
+// 128 x 64 boxes at (col0 + 64 h, row0).  Thread (qd, lane) holds row
+// 32 qd + lane; pk[j] = its columns [32 j, 32 j + 32) as packed bf16 pairs.
+// 16-byte piece c of row r sits at piece c ^ (r % 8) of the row (the 128-byte
+// swizzle), which also keeps each st.shared free of bank conflicts.  Named
+// barrier `bar_id` spans the warpgroup; `pending` is the issuing thread's
+// record of a committed store whose smem reads may be in flight.
+template <int NLD>
+__device__ __forceinline__ void epi_store_bf16(const CUtensorMap* tmO, uint32_t buf, const uint32_t (&pk)[NLD][16],
+                                               int qd, int lane, uint32_t bar_id, int64_t col0, int64_t row0,
+                                               int64_t cols_valid, int64_t rows_valid, bool& pending) {
+    static_assert(NLD % 2 == 0, "64-column boxes");
+    const bool issuer = qd == 0 && lane == 0;
+    const uint32_t r = (uint32_t)(qd * 32 + lane);
+    const uint32_t row_addr = buf + r * 128u;
+#pragma unroll
+    for (int h = 0; h < NLD / 2; ++h) {
+        if (issuer && pending) bulk_wait_read_all();
+        named_bar_sync(bar_id, 128);  // the buffer is free
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int j = 2 * h + (c >> 2), i = 4 * (c & 3);
+            sts128(row_addr + (((uint32_t)c ^ (r & 7u)) << 4), pk[j][i], pk[j][i + 1], pk[j][i + 2], pk[j][i + 3]);
+        }
+        fence_proxy_async();          // generic-proxy writes -> visible to the TMA
+        named_bar_sync(bar_id, 128);  // the box is complete
+        if (issuer) {
+            const int64_t c0 = col0 + 64 * h;
+            if (c0 < cols_valid && row0 < rows_valid) tma_store_2d(tmO, buf, (int32_t)c0, (int32_t)row0);
+            bulk_commit();
+            pending = true;
+        }
+    }
+}
+
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                  : "memory");
@@ -112,19 +170,23 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 template <int BN, bool MX, int EPI>
 __global__ void __launch_bounds__(512, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
-                const GemmLaunch g, const WaitCfg wc) {
-    using C = GemmCfg<BN, MX>;
+                const __grid_constant__ CUtensorMap tmO, const GemmLaunch g, const WaitCfg wc) {
+    using C = GemmCfg<BN, MX, epi_staging_bytes<EPI>()>;
+    static_assert(EPI != EPI_BF16 || BN >= 128, "the staged bf16 epilogue stores 64-column boxes");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t* sP = smem;
     uint8_t* sQ = sP + C::STAGES * C::P_BYTES;
     uint8_t* sSFP = sQ + C::STAGES * C::Q_BYTES;
     uint8_t* sSFQ = sSFP + C::STAGES * C::SFP_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sSFQ + C::STAGES * C::SFQ_BYTES);
+    uint8_t* sStg = smem + C::STG_OFFSET;  // bf16 epilogue staging (EPI_BF16)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + epi_staging_bytes<EPI>());
     uint64_t* full = bars;
     uint64_t* empty = bars + C::STAGES;
-    uint64_t* sfr = bars + 2 * C::STAGES;  // scales of the stage are in TMEM
-    uint64_t* accf = bars + 3 * C::STAGES;
+    uint64_t* sfr = bars + 2 * C::STAGES;     // scales of the stage are in TMEM
+    uint64_t* sfull = bars + 3 * C::STAGES;   // scale atoms of the slot landed in smem
+    uint64_t* sempty = bars + 4 * C::STAGES;  // the writers are done with the slot's smem
+    uint64_t* accf = bars + 5 * C::STAGES;
     uint64_t* acce = accf + 2;
     uint64_t* drain = acce + 2;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -133,9 +195,11 @@ __global__ void __launch_bounds__(512, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(full + s, 2);  // two producers
+            mbar_init(full + s, 2);  // two operand producers
             mbar_init(empty + s, 1);
             mbar_init(sfr + s, 4);
+            mbar_init(sfull + s, 1);
+            mbar_init(sempty + s, 4);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(accf + a, 1);
@@ -146,6 +210,7 @@ __global__ void __launch_bounds__(512, 1)
         fence_mbar_init();
         prefetch_tensormap(&tmP);
         prefetch_tensormap(&tmQ);
+        if (EPI == EPI_BF16) prefetch_tensormap(&tmO);
     }
     if (warp == 5) {
         tmem_alloc(tslot, 512);
@@ -158,7 +223,7 @@ __global__ void __launch_bounds__(512, 1)
 
     pdl_wait();
     const Sched sc = make_sched<BN>(g);
-    const int64_t ksfc = sc.kbt * C::SF_CHUNKS;                 // scale atoms per 128-row tile
+    const int64_t ksfc = (g.k + 255) / 256 * (MX ? 2 : 4);      // scale atoms per 128-row tile (K padded to 256)
     const int64_t q_chunks_total = (g.q_rows + 127) / 128;      // 128-row scale tiles of Q
 
     if (warp < 4) {
@@ -170,7 +235,9 @@ __global__ void __launch_bounds__(512, 1)
             const Unit w = decode_unit<BN>(g, sc, u);
             bool ok = true;
             for (int64_t kb = w.kb0; kb < w.kb1; ++kb) {
-                if (!mbar_wait(full + stage, ph, wc, abort_flag)) {
+                // the slot's atoms are in smem, and the MMAs of the stage's
+                // previous round (which read these TMEM columns) are complete
+                if (!mbar_wait(sfull + stage, ph, wc, abort_flag) || !mbar_wait(empty + stage, ph ^ 1u, wc, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -190,7 +257,10 @@ __global__ void __launch_bounds__(512, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(sfr + stage);
+                if (lane == 0) {
+                    mbar_arrive(sfr + stage);
+                    mbar_arrive(sempty + stage);
+                }
                 if (++stage == C::STAGES) {
                     stage = 0;
                     ph ^= 1u;
@@ -198,13 +268,15 @@ __global__ void __launch_bounds__(512, 1)
             }
             if (!ok) break;
         }
-    } else if (warp == 4 || warp == 6) {
+    } else if (warp == 4 || warp == 6 || warp == 7) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producers
-            // warp 4 loads the P tile and its scale atoms, warp 6 the Q tile and
-            // its scale atoms; each adds its own bytes to the stage's barrier,
-            // so two threads issue copies in parallel.
-            const bool is_p = warp == 4;
+            // warp 4 loads the P tile, warp 6 the Q tile (each adds its own
+            // bytes to the stage's barrier), warp 7 both tiles' scale atoms into
+            // the scale ring; three threads issue copies in parallel.
+            const bool is_p = warp == 4, is_sf = warp == 7;
+            uint64_t* const fb = is_sf ? sfull : full;   // barrier the copies complete on
+            uint64_t* const eb = is_sf ? sempty : empty; // barrier that frees the slot
             int stage = 0;
             uint32_t ph = 0;
             uint32_t issued = 0, issued_ph = 0;  // per-stage bits: a copy was issued / its phase parity
@@ -214,28 +286,30 @@ __global__ void __launch_bounds__(512, 1)
                 const uint8_t* sfp = g.p_scales + (w.p_row0 >> 7) * ksfc * 512;
                 const int64_t qc0 = w.q_row0 >> 7;
                 for (int64_t kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!mbar_wait(empty + stage, ph ^ 1u, wc, abort_flag)) {
+                    if (!mbar_wait(eb + stage, ph ^ 1u, wc, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    if (is_p) {
-                        mbar_arrive_expect_tx(full + stage, C::P_BYTES + C::SFP_BYTES);
-                        tma_load_2d(&tmP, full + stage, sP + stage * C::P_BYTES, (int32_t)(kb * 128),
-                                    (int32_t)w.p_row0);
-                        bulk_load(sSFP + stage * C::SFP_BYTES, sfp + kb * C::SF_CHUNKS * 512, C::SFP_BYTES,
-                                  full + stage);
-                    } else {
-                        uint32_t bytes = C::Q_BYTES;
+                    if (is_sf) {
+                        uint32_t bytes = C::SFP_BYTES;
                         for (int c = 0; c < C::QCH; ++c)
                             if (qc0 + c < q_chunks_total) bytes += C::SF_CHUNKS * 512;
-                        mbar_arrive_expect_tx(full + stage, bytes);
-                        tma_load_2d(&tmQ, full + stage, sQ + stage * C::Q_BYTES, (int32_t)(kb * 128),
-                                    (int32_t)w.q_row0);
+                        mbar_arrive_expect_tx(sfull + stage, bytes);
+                        bulk_load(sSFP + stage * C::SFP_BYTES, sfp + kb * C::SF_CHUNKS * 512, C::SFP_BYTES,
+                                  sfull + stage);
                         for (int c = 0; c < C::QCH; ++c)
                             if (qc0 + c < q_chunks_total)
                                 bulk_load(sSFQ + stage * C::SFQ_BYTES + c * C::SF_CHUNKS * 512,
                                           g.q_scales + ((qc0 + c) * ksfc + kb * C::SF_CHUNKS) * 512,
-                                          C::SF_CHUNKS * 512, full + stage);
+                                          C::SF_CHUNKS * 512, sfull + stage);
+                    } else if (is_p) {
+                        mbar_arrive_expect_tx(full + stage, C::P_BYTES);
+                        tma_load_2d(&tmP, full + stage, sP + stage * C::P_BYTES, (int32_t)(kb * C::KB_BYTES),
+                                    (int32_t)w.p_row0);
+                    } else {
+                        mbar_arrive_expect_tx(full + stage, C::Q_BYTES);
+                        tma_load_2d(&tmQ, full + stage, sQ + stage * C::Q_BYTES, (int32_t)(kb * C::KB_BYTES),
+                                    (int32_t)w.q_row0);
                     }
                     issued |= 1u << stage;
                     issued_ph = (issued_ph & ~(1u << stage)) | (ph << stage);
@@ -250,7 +324,7 @@ __global__ void __launch_bounds__(512, 1)
                 WaitCfg w2 = wc;
                 volatile int never = 0;
                 for (int s = 0; s < C::STAGES; ++s)
-                    if ((issued >> s) & 1u) mbar_wait(full + s, (issued_ph >> s) & 1u, w2, &never);
+                    if ((issued >> s) & 1u) mbar_wait(fb + s, (issued_ph >> s) & 1u, w2, &never);
             }
         }
     } else if (warp == 5) {
@@ -282,9 +356,9 @@ __global__ void __launch_bounds__(512, 1)
                     const uint32_t pa = smem_u32(sP + stage * C::P_BYTES);
                     const uint32_t qa = smem_u32(sQ + stage * C::Q_BYTES);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = sdesc_sw128(pa + kk * 32);
-                        const uint64_t bd = sdesc_sw128(qa + kk * 32);
+                    for (int kk = 0; kk < C::KB_MMAS; ++kk) {
+                        const uint64_t ad = C::KB_BYTES == 128 ? sdesc_sw128(pa + kk * 32) : sdesc_sw64(pa + kk * 32);
+                        const uint64_t bd = C::KB_BYTES == 128 ? sdesc_sw128(qa + kk * 32) : sdesc_sw64(qa + kk * 32);
                         uint32_t sfa, sfb, id;
                         if constexpr (!MX) {
                             sfa = sfp_t + kk * 4;
@@ -333,6 +407,8 @@ __global__ void __launch_bounds__(512, 1)
         const int qd = warp & 3;  // the TMEM lane quarter this warp may access
         const int c_begin = ((warp - 8) >> 2) * CPW;
         const bool has_cols = c_begin < BN;
+        const int wg = (warp - 8) >> 2;
+        bool store_pending = false;  // EPI_BF16: this thread issued a TMA store not yet waited for
         int acc = 0;
         uint32_t aph = 0;
         for (int64_t u = blockIdx.x; u < sc.units; u += gridDim.x) {
@@ -360,24 +436,9 @@ __global__ void __launch_bounds__(512, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce + acc);
                 const Unit w = decode_unit<BN>(g, sc, u);
-                const int64_t prow = w.p_row0 + qd * 32 + lane;  // the P row this thread owns
-                if (has_cols && prow < g.p_rows_valid) {
-#pragma unroll
-                    for (int j = 0; j < NLD; ++j) {
-                        const int64_t q0 = w.qt * BN + c_begin + j * 32;
-                        uint16_t* o = reinterpret_cast<uint16_t*>(g.out) + prow * g.ldo + q0;
-                        if (q0 + 32 <= g.q_rows_valid) {
-                            uint4* o4 = reinterpret_cast<uint4*>(o);
-#pragma unroll
-                            for (int v = 0; v < 4; ++v)
-                                o4[v] = make_uint4(pk[j][4 * v], pk[j][4 * v + 1], pk[j][4 * v + 2], pk[j][4 * v + 3]);
-                        } else {
-                            for (int i = 0; i < 32; ++i)
-                                if (q0 + i < g.q_rows_valid)
-                                    o[i] = (uint16_t)((i & 1) ? (pk[j][i >> 1] >> 16) : (pk[j][i >> 1] & 0xFFFFu));
-                        }
-                    }
-                }
+                epi_store_bf16<NLD>(&tmO, smem_u32(sStg) + (uint32_t)(wg * EPI_STAGE_BYTES), pk, qd, lane,
+                                    1u + (uint32_t)wg, w.qt * BN + c_begin, w.p_row0, g.q_rows_valid,
+                                    g.p_rows_valid, store_pending);
             } else if constexpr (EPI == EPI_BF16_T || EPI == EPI_PARTIAL_T) {
                 uint32_t r[NLD][32];
                 if (has_cols) {
@@ -538,6 +599,7 @@ __global__ void __launch_bounds__(512, 1)
                 aph ^= 1u;
             }
         }
+        if (store_pending) bulk_wait_all();
     }
 
     tc_fence_before();

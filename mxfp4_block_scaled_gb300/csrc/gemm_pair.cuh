@@ -42,11 +42,13 @@ struct PairCfg {
     static constexpr int SF_COLS = SFP_COLS + SFQ_COLS;
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM_LIMIT = 227 * 1024;
-    static constexpr int ST_SMEM = (SMEM_LIMIT - 1024 - BAR_BYTES) / STAGE_BYTES;
+    static constexpr int STG = 2 * EPI_STAGE_BYTES;  // bf16 epilogue staging
+    static constexpr int ST_SMEM = (SMEM_LIMIT - 1024 - BAR_BYTES - STG) / STAGE_BYTES;
     static constexpr int ST_TMEM = (512 - BN) / SF_COLS;
     static constexpr int ST_MIN = ST_SMEM < ST_TMEM ? ST_SMEM : ST_TMEM;
     static constexpr int STAGES = ST_MIN < 8 ? ST_MIN : 8;
-    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + STG + BAR_BYTES;
+    static_assert(STAGE_BYTES % 1024 == 0, "staging must stay 1024-byte aligned");
     static_assert(3 * STAGES + 5 <= BAR_BYTES / 8 - 2, "barrier area too small");
     static_assert(BN + STAGES * SF_COLS <= 512, "TMEM budget");
 };
@@ -54,7 +56,7 @@ struct PairCfg {
 template <bool MX>
 __global__ void __launch_bounds__(512, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
-                     const GemmLaunch g, const WaitCfg wc) {
+                     const __grid_constant__ CUtensorMap tmO, const GemmLaunch g, const WaitCfg wc) {
     using C = PairCfg<MX>;
     constexpr int BN = C::BN;
     extern __shared__ uint8_t smem_raw[];
@@ -63,7 +65,8 @@ __global__ void __launch_bounds__(512, 1)
     uint8_t* sQ = sP + C::STAGES * C::P_BYTES;
     uint8_t* sSFP = sQ + C::STAGES * C::Q_BYTES;
     uint8_t* sSFQ = sSFP + C::STAGES * C::SFP_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sSFQ + C::STAGES * C::SFQ_BYTES);
+    uint8_t* sStg = sSFQ + C::STAGES * C::SFQ_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + C::STG);
     uint64_t* full = bars;
     uint64_t* empty = bars + C::STAGES;
     uint64_t* sfr = bars + 2 * C::STAGES;
@@ -89,6 +92,7 @@ __global__ void __launch_bounds__(512, 1)
         fence_mbar_init();
         prefetch_tensormap(&tmP);
         prefetch_tensormap(&tmQ);
+        prefetch_tensormap(&tmO);
     }
     if (warp == 5) {
         tmem_alloc_pair(tslot, 512);
@@ -263,7 +267,9 @@ __global__ void __launch_bounds__(512, 1)
         constexpr int CPW = BN / 2;
         constexpr int NLD = CPW / 32;
         const int qd = warp & 3;
-        const int c_begin = ((warp - 8) >> 2) * CPW;
+        const int wg = (warp - 8) >> 2;
+        const int c_begin = wg * CPW;
+        bool store_pending = false;
         uint32_t aph = 0;
         for (int64_t u = cid; u < units; u += ncl) {
             if (!mbar_wait_cluster(accf, aph, wc, abort_flag)) break;
@@ -286,25 +292,11 @@ __global__ void __launch_bounds__(512, 1)
             if (lane == 0) mbar_arrive_cluster(acce_leader);
             aph ^= 1u;
             const int64_t pm = u % n_pm, qt = u / n_pm;
-            const int64_t prow = pm * 256 + 128 * rank + qd * 32 + lane;
-            if (prow < g.p_rows_valid) {
-#pragma unroll
-                for (int j = 0; j < NLD; ++j) {
-                    const int64_t q0 = qt * BN + c_begin + j * 32;
-                    uint16_t* o = reinterpret_cast<uint16_t*>(g.out) + prow * g.ldo + q0;
-                    if (q0 + 32 <= g.q_rows_valid) {
-                        uint4* o4 = reinterpret_cast<uint4*>(o);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            o4[v] = make_uint4(pk[j][4 * v], pk[j][4 * v + 1], pk[j][4 * v + 2], pk[j][4 * v + 3]);
-                    } else {
-                        for (int i = 0; i < 32; ++i)
-                            if (q0 + i < g.q_rows_valid)
-                                o[i] = (uint16_t)((i & 1) ? (pk[j][i >> 1] >> 16) : (pk[j][i >> 1] & 0xFFFFu));
-                    }
-                }
-            }
+            epi_store_bf16<NLD>(&tmO, smem_u32(sStg) + (uint32_t)(wg * EPI_STAGE_BYTES), pk, qd, lane,
+                                1u + (uint32_t)wg, qt * BN + c_begin, pm * 256 + 128 * rank, g.q_rows_valid,
+                                g.p_rows_valid, store_pending);
         }
+        if (store_pending) bulk_wait_all();
     }
 
     tc_fence_before();
