@@ -41,17 +41,20 @@ static bool make_codes_map(CUtensorMap* m, const void* base, int64_t rows, int64
 }
 
 // 2-D map over the bf16 output [rows][cols] with row pitch ldo elements
-// (ldo % 8 == 0, 16-byte aligned base); box = 64 columns x 128 rows with the
-// 128-byte swizzle of the epilogue's staging buffers.
-static bool make_out_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t ldo) {
+// (ldo % 8 == 0, 16-byte aligned base); box = box_cols (16, 32 or 64) columns
+// x 128 rows with the swizzle of the same width as the epilogue's staging.
+static bool make_out_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t ldo, int box_cols) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)(ldo * 2)};
-    cuuint32_t box[2] = {64u, 128u};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, 128u};
     cuuint32_t es[2] = {1u, 1u};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    box_cols == 16   ? CU_TENSOR_MAP_SWIZZLE_32B
+                    : box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                     : CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -59,7 +62,7 @@ int64_t gemm_k_blocks(int64_t k) { return (k + 2 * GEMM_KB_BYTES - 1) / (2 * GEM
 
 template <int BN, bool MX, int EPI>
 static cudaError_t launch_one(const GemmLaunch& g, cudaStream_t s) {
-    using C = GemmCfg<BN, MX, epi_staging_bytes<EPI>()>;
+    using C = GemmCfg<BN, MX, epi_staging_bytes<EPI, MX>()>;
     auto kern = gemm_kernel<BN, MX, EPI>;
     static bool attr_set = false;  // per instantiation; the attribute is per device function
     if (!attr_set) {
@@ -75,7 +78,7 @@ static cudaError_t launch_one(const GemmLaunch& g, cudaStream_t s) {
         return cudaErrorInvalidValue;
     }
     if (EPI == EPI_BF16) {
-        if (!make_out_map(&tmO, g.out, g.p_rows_valid, g.q_rows_valid, g.ldo)) {
+        if (!make_out_map(&tmO, g.out, g.p_rows_valid, g.q_rows_valid, g.ldo, epi_box_cols<MX>())) {
             set_error("cuTensorMapEncodeTiled failed for the output (%lld x %lld, ldo %lld)",
                       (long long)g.p_rows_valid, (long long)g.q_rows_valid, (long long)g.ldo);
             return cudaErrorInvalidValue;
@@ -151,7 +154,7 @@ static cudaError_t launch_pair(const GemmLaunch& g, cudaStream_t s) {
     }
     CUtensorMap tmP, tmQ, tmO;
     if (!make_codes_map(&tmP, g.p_codes, g.p_rows, g.k, 128, 128) || !make_codes_map(&tmQ, g.q_codes, g.q_rows, g.k, 128, 128) ||
-        !make_out_map(&tmO, g.out, g.p_rows_valid, g.q_rows_valid, g.ldo)) {
+        !make_out_map(&tmO, g.out, g.p_rows_valid, g.q_rows_valid, g.ldo, PairCfg<MX>::BOXC)) {
         set_error("cuTensorMapEncodeTiled failed (rows %lld/%lld, k %lld)", (long long)g.p_rows, (long long)g.q_rows,
                   (long long)g.k);
         return cudaErrorInvalidValue;

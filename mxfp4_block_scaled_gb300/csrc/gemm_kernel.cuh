@@ -27,9 +27,11 @@
 //               lines leave the SM (row-per-thread stores from registers would
 //               scatter 16-byte pieces over 32 lines per instruction and load
 //               the L2 with several times as many write requests).
-// Pipelines: STAGES operand stages (full / empty), as many scale slots
-// (scale-full / scale-empty for the smem ring, scales-ready for TMEM) and 1-2
-// TMEM accumulator stages (acc_full / acc_empty).  Every wait is bounded.
+// Pipelines: STAGES operand stages (full / empty; a stage is full once both
+// operand tiles landed and the four scale writers stored its scales in TMEM,
+// so the MMA thread waits once per K block), as many scale slots (scale-full /
+// scale-empty for the smem ring) and 1-2 TMEM accumulator stages (acc_full /
+// acc_empty).  Every wait is bounded.
 #pragma once
 
 #include "common.cuh"
@@ -37,13 +39,24 @@
 
 namespace fp4 {
 
-// bf16 epilogue staging: one 16 KB buffer per epilogue warpgroup, 128 rows x
-// 64 bf16 columns in the 128-byte swizzled layout of the output tensor map.
-constexpr int EPI_STAGE_BYTES = 128 * 128;
+// bf16 epilogue staging: one buffer per epilogue warpgroup of 128 rows x
+// epi_box_cols bf16 columns, the box of the output tensor map (rows of 32 or
+// 64 bytes with the swizzle of that width).  Narrow boxes keep the staging
+// small enough for four operand stages and a scale ring of four slots
+// (NVFP4 scale slots are twice the MXFP4 ones).
+template <bool MX>
+constexpr int epi_box_cols() {
+    return MX ? 32 : 16;
+}
 
-template <int EPI>
+template <int BOXC>
+constexpr int epi_buffer_bytes() {
+    return 128 * BOXC * 2;
+}
+
+template <int EPI, bool MX>
 constexpr int epi_staging_bytes() {
-    return EPI == EPI_BF16 ? 2 * EPI_STAGE_BYTES : 0;
+    return EPI == EPI_BF16 ? 2 * epi_buffer_bytes<epi_box_cols<MX>()>() : 0;
 }
 
 template <int BN, bool MX, int STG = 0>
@@ -57,23 +70,30 @@ struct GemmCfg {
     static constexpr int Q_BYTES = BN * KB_BYTES;
     static constexpr int SFP_BYTES = SF_CHUNKS * 512;
     static constexpr int SFQ_BYTES = SF_CHUNKS * 512 * QCH;
-    static constexpr int STAGE_BYTES = P_BYTES + Q_BYTES + SFP_BYTES + SFQ_BYTES;
+    static constexpr int OP_BYTES = P_BYTES + Q_BYTES;     // operand stage
+    static constexpr int SF_BYTES = SFP_BYTES + SFQ_BYTES;  // scale slot
     static constexpr int ACC = BN <= 128 ? 2 : 1;
     static constexpr int SFP_COLS = SF_CHUNKS * 4;
     static constexpr int SFQ_COLS = SF_CHUNKS * 4 * QCH;
     static constexpr int SF_COLS = SFP_COLS + SFQ_COLS;
     static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM_LIMIT = 227 * 1024;
-    static constexpr int ST_SMEM = (SMEM_LIMIT - 2048 - BAR_BYTES - STG) / STAGE_BYTES;
+    static constexpr int BUDGET = SMEM_LIMIT - 2048 - BAR_BYTES - STG;
+    // operand stages (each with its TMEM scale columns), keeping room for at
+    // least two scale slots; the scale ring takes what is left, up to STAGES
+    static constexpr int ST_SMEM = (BUDGET - 2 * SF_BYTES) / OP_BYTES;
     static constexpr int ST_TMEM = (512 - ACC * BN) / SF_COLS;
     static constexpr int ST_MIN = ST_SMEM < ST_TMEM ? ST_SMEM : ST_TMEM;
     static constexpr int STAGES = ST_MIN < 8 ? ST_MIN : 8;
-    static constexpr int STG_OFFSET = (STAGES * STAGE_BYTES + 1023) / 1024 * 1024;  // 128-byte swizzle alignment
+    static constexpr int SS_FIT = (BUDGET - STAGES * OP_BYTES) / SF_BYTES;
+    static constexpr int SSLOTS = SS_FIT < STAGES ? SS_FIT : STAGES;
+    static constexpr int STG_OFFSET =
+        (STAGES * OP_BYTES + SSLOTS * SF_BYTES + 1023) / 1024 * 1024;  // swizzle alignment of the staging
     static constexpr int SMEM = 1024 + STG_OFFSET + STG + BAR_BYTES;
-    static_assert(STAGES >= 2, "pipeline too shallow");
+    static_assert(STAGES >= 2 && SSLOTS >= 2, "pipeline too shallow");
     static_assert(P_BYTES % 512 == 0 && Q_BYTES % 512 == 0, "64-byte swizzle atoms are 512 bytes");
     static_assert(SMEM <= SMEM_LIMIT, "shared memory budget");
-    static_assert(5 * STAGES + 5 <= BAR_BYTES / 8 - 2, "barrier area too small");
+    static_assert(2 * STAGES + 2 * SSLOTS + 5 <= BAR_BYTES / 8 - 2, "barrier area too small");
     static_assert(ACC * BN + STAGES * SF_COLS <= 512, "TMEM budget");
 };
 
@@ -128,33 +148,40 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 
 // Stores one epilogue warpgroup's 128 rows x (32 NLD) bf16 columns through its
 // staging buffer `buf` (smem address, 1024-byte aligned) with TMA stores of
-// 128 x 64 boxes at (col0 + 64 h, row0).  Thread (qd, lane) holds row
+// 128 x BOXC boxes at (col0 + BOXC h, row0).  Thread (qd, lane) holds row
 // 32 qd + lane; pk[j] = its columns [32 j, 32 j + 32) as packed bf16 pairs.
-// 16-byte piece c of row r sits at piece c ^ (r % 8) of the row (the 128-byte
-// swizzle), which also keeps each st.shared free of bank conflicts.  Named
-// barrier `bar_id` spans the warpgroup; `pending` is the issuing thread's
-// record of a committed store whose smem reads may be in flight.
-template <int NLD>
+// A box row is BOXC * 2 bytes (32, 64 or 128) in the swizzle of that width:
+// 16-byte piece c of row r sits at piece c ^ (r % 8) (128-byte rows),
+// c ^ ((r / 2) % 4) (64-byte rows) or c ^ ((r / 4) % 2) (32-byte rows), which
+// also keeps each st.shared free of bank conflicts.  Named barrier `bar_id` spans the warpgroup; `pending` is the
+// issuing thread's record of a committed store whose smem reads may be in
+// flight.
+template <int NLD, int BOXC>
 __device__ __forceinline__ void epi_store_bf16(const CUtensorMap* tmO, uint32_t buf, const uint32_t (&pk)[NLD][16],
                                                int qd, int lane, uint32_t bar_id, int64_t col0, int64_t row0,
                                                int64_t cols_valid, int64_t rows_valid, bool& pending) {
-    static_assert(NLD % 2 == 0, "64-column boxes");
+    static_assert(BOXC == 16 || BOXC == 32 || BOXC == 64, "32-, 64- or 128-byte box rows");
+    static_assert((NLD * 32) % BOXC == 0, "whole boxes");
+    constexpr int RB = BOXC * 2;   // bytes per box row
+    constexpr int PIECES = RB / 16;
     const bool issuer = qd == 0 && lane == 0;
     const uint32_t r = (uint32_t)(qd * 32 + lane);
-    const uint32_t row_addr = buf + r * 128u;
+    const uint32_t row_addr = buf + r * (uint32_t)RB;
+    const uint32_t sw = RB == 128 ? (r & 7u) : RB == 64 ? ((r >> 1) & 3u) : ((r >> 2) & 1u);
 #pragma unroll
-    for (int h = 0; h < NLD / 2; ++h) {
+    for (int h = 0; h < NLD * 32 / BOXC; ++h) {
         if (issuer && pending) bulk_wait_read_all();
         named_bar_sync(bar_id, 128);  // the buffer is free
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const int j = 2 * h + (c >> 2), i = 4 * (c & 3);
-            sts128(row_addr + (((uint32_t)c ^ (r & 7u)) << 4), pk[j][i], pk[j][i + 1], pk[j][i + 2], pk[j][i + 3]);
+        for (int c = 0; c < PIECES; ++c) {
+            const int col = h * BOXC + c * 8;  // first of the piece's 8 columns
+            const int j = col / 32, i = (col % 32) / 2;
+            sts128(row_addr + (((uint32_t)c ^ sw) << 4), pk[j][i], pk[j][i + 1], pk[j][i + 2], pk[j][i + 3]);
         }
         fence_proxy_async();          // generic-proxy writes -> visible to the TMA
         named_bar_sync(bar_id, 128);  // the box is complete
         if (issuer) {
-            const int64_t c0 = col0 + 64 * h;
+            const int64_t c0 = col0 + BOXC * h;
             if (c0 < cols_valid && row0 < rows_valid) tma_store_2d(tmO, buf, (int32_t)c0, (int32_t)row0);
             bulk_commit();
             pending = true;
@@ -171,22 +198,21 @@ template <int BN, bool MX, int EPI>
 __global__ void __launch_bounds__(512, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
                 const __grid_constant__ CUtensorMap tmO, const GemmLaunch g, const WaitCfg wc) {
-    using C = GemmCfg<BN, MX, epi_staging_bytes<EPI>()>;
+    using C = GemmCfg<BN, MX, epi_staging_bytes<EPI, MX>()>;
     static_assert(EPI != EPI_BF16 || BN >= 128, "the staged bf16 epilogue stores 64-column boxes");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t* sP = smem;
     uint8_t* sQ = sP + C::STAGES * C::P_BYTES;
-    uint8_t* sSFP = sQ + C::STAGES * C::Q_BYTES;
-    uint8_t* sSFQ = sSFP + C::STAGES * C::SFP_BYTES;
+    uint8_t* sSFP = sQ + C::STAGES * C::Q_BYTES;       // scale ring (SSLOTS slots)
+    uint8_t* sSFQ = sSFP + C::SSLOTS * C::SFP_BYTES;
     uint8_t* sStg = smem + C::STG_OFFSET;  // bf16 epilogue staging (EPI_BF16)
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + epi_staging_bytes<EPI>());
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + epi_staging_bytes<EPI, MX>());
     uint64_t* full = bars;
     uint64_t* empty = bars + C::STAGES;
-    uint64_t* sfr = bars + 2 * C::STAGES;     // scales of the stage are in TMEM
-    uint64_t* sfull = bars + 3 * C::STAGES;   // scale atoms of the slot landed in smem
-    uint64_t* sempty = bars + 4 * C::STAGES;  // the writers are done with the slot's smem
-    uint64_t* accf = bars + 5 * C::STAGES;
+    uint64_t* sfull = bars + 2 * C::STAGES;                // scale atoms of the slot landed in smem
+    uint64_t* sempty = sfull + C::SSLOTS;                  // the writers are done with the slot's smem
+    uint64_t* accf = sempty + C::SSLOTS;
     uint64_t* acce = accf + 2;
     uint64_t* drain = acce + 2;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -195,9 +221,10 @@ __global__ void __launch_bounds__(512, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(full + s, 2);  // two operand producers
+            mbar_init(full + s, 6);  // two operand producers + four scale writers
             mbar_init(empty + s, 1);
-            mbar_init(sfr + s, 4);
+        }
+        for (int s = 0; s < C::SSLOTS; ++s) {
             mbar_init(sfull + s, 1);
             mbar_init(sempty + s, 4);
         }
@@ -229,22 +256,22 @@ __global__ void __launch_bounds__(512, 1)
     if (warp < 4) {
         // ---------------------------------------------------- scale writers
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        int stage = 0;
-        uint32_t ph = 0;
+        int stage = 0, slot = 0;  // operand stage (TMEM scale columns), scale ring slot
+        uint32_t ph = 0, sph = 0;
         for (int64_t u = blockIdx.x; u < sc.units; u += gridDim.x) {
             const Unit w = decode_unit<BN>(g, sc, u);
             bool ok = true;
             for (int64_t kb = w.kb0; kb < w.kb1; ++kb) {
                 // the slot's atoms are in smem, and the MMAs of the stage's
                 // previous round (which read these TMEM columns) are complete
-                if (!mbar_wait(sfull + stage, ph, wc, abort_flag) || !mbar_wait(empty + stage, ph ^ 1u, wc, abort_flag)) {
+                if (!mbar_wait(sfull + slot, sph, wc, abort_flag) || !mbar_wait(empty + stage, ph ^ 1u, wc, abort_flag)) {
                     ok = false;
                     break;
                 }
                 const uint32_t sfp_t = tmem + lane_base + (uint32_t)(C::ACC * BN + stage * C::SF_COLS);
                 const uint32_t sfq_t = sfp_t + C::SFP_COLS;
-                const uint32_t sp = smem_u32(sSFP + stage * C::SFP_BYTES) + lane * 16;
-                const uint32_t sq = smem_u32(sSFQ + stage * C::SFQ_BYTES) + lane * 16;
+                const uint32_t sp = smem_u32(sSFP + slot * C::SFP_BYTES) + lane * 16;
+                const uint32_t sq = smem_u32(sSFQ + slot * C::SFQ_BYTES) + lane * 16;
                 // lane i holds rows i, 32+i, 64+i, 96+i of an atom: TMEM lane i
                 // of this quarter, columns +0..+3 (every quarter gets the atom)
 #pragma unroll
@@ -258,12 +285,16 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(sfr + stage);
-                    mbar_arrive(sempty + stage);
+                    mbar_arrive(full + stage);
+                    mbar_arrive(sempty + slot);
                 }
                 if (++stage == C::STAGES) {
                     stage = 0;
                     ph ^= 1u;
+                }
+                if (++slot == C::SSLOTS) {
+                    slot = 0;
+                    sph ^= 1u;
                 }
             }
             if (!ok) break;
@@ -277,6 +308,7 @@ __global__ void __launch_bounds__(512, 1)
             const bool is_p = warp == 4, is_sf = warp == 7;
             uint64_t* const fb = is_sf ? sfull : full;   // barrier the copies complete on
             uint64_t* const eb = is_sf ? sempty : empty; // barrier that frees the slot
+            const int nst = is_sf ? C::SSLOTS : C::STAGES; // ring length (stage = scale slot for warp 7)
             int stage = 0;
             uint32_t ph = 0;
             uint32_t issued = 0, issued_ph = 0;  // per-stage bits: a copy was issued / its phase parity
@@ -313,7 +345,7 @@ __global__ void __launch_bounds__(512, 1)
                     }
                     issued |= 1u << stage;
                     issued_ph = (issued_ph & ~(1u << stage)) | (ph << stage);
-                    if (++stage == C::STAGES) {
+                    if (++stage == nst) {
                         stage = 0;
                         ph ^= 1u;
                     }
@@ -321,9 +353,13 @@ __global__ void __launch_bounds__(512, 1)
             }
             if (!ok) {
                 // Let every copy already in flight land before the CTA exits.
+                // Copies in flight land within microseconds; an operand stage's
+                // phase may also lack the scale writers' arrivals (they stop
+                // too), so each of these waits is cut short at 1 ms.
                 WaitCfg w2 = wc;
+                if (w2.limit_ns > 1000000ull) w2.limit_ns = 1000000ull;
                 volatile int never = 0;
-                for (int s = 0; s < C::STAGES; ++s)
+                for (int s = 0; s < nst; ++s)
                     if ((issued >> s) & 1u) mbar_wait(fb + s, (issued_ph >> s) & 1u, w2, &never);
             }
         }
@@ -346,7 +382,7 @@ __global__ void __launch_bounds__(512, 1)
                 const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
                 const uint32_t q_sub = BN < 128 ? (uint32_t)((w.q_row0 & 127) >> 5) : 0u;
                 for (int64_t kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!mbar_wait(full + stage, ph, wc, abort_flag) || !mbar_wait(sfr + stage, ph, wc, abort_flag)) {
+                    if (!mbar_wait(full + stage, ph, wc, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -436,7 +472,8 @@ __global__ void __launch_bounds__(512, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce + acc);
                 const Unit w = decode_unit<BN>(g, sc, u);
-                epi_store_bf16<NLD>(&tmO, smem_u32(sStg) + (uint32_t)(wg * EPI_STAGE_BYTES), pk, qd, lane,
+                constexpr int BOXC = epi_box_cols<MX>();
+                epi_store_bf16<NLD, BOXC>(&tmO, smem_u32(sStg) + (uint32_t)(wg * epi_buffer_bytes<BOXC>()), pk, qd, lane,
                                     1u + (uint32_t)wg, w.qt * BN + c_begin, w.p_row0, g.q_rows_valid,
                                     g.p_rows_valid, store_pending);
             } else if constexpr (EPI == EPI_BF16_T || EPI == EPI_PARTIAL_T) {

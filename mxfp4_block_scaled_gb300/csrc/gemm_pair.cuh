@@ -42,7 +42,8 @@ struct PairCfg {
     static constexpr int SF_COLS = SFP_COLS + SFQ_COLS;
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM_LIMIT = 227 * 1024;
-    static constexpr int STG = 2 * EPI_STAGE_BYTES;  // bf16 epilogue staging
+    static constexpr int BOXC = 64;                                // bf16 epilogue box: 128 x 64
+    static constexpr int STG = 2 * epi_buffer_bytes<BOXC>();       // bf16 epilogue staging
     static constexpr int ST_SMEM = (SMEM_LIMIT - 1024 - BAR_BYTES - STG) / STAGE_BYTES;
     static constexpr int ST_TMEM = (512 - BN) / SF_COLS;
     static constexpr int ST_MIN = ST_SMEM < ST_TMEM ? ST_SMEM : ST_TMEM;
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(512, 1)
             if (lane == 0) mbar_arrive_cluster(acce_leader);
             aph ^= 1u;
             const int64_t pm = u % n_pm, qt = u / n_pm;
-            epi_store_bf16<NLD>(&tmO, smem_u32(sStg) + (uint32_t)(wg * EPI_STAGE_BYTES), pk, qd, lane,
+            epi_store_bf16<NLD, C::BOXC>(&tmO, smem_u32(sStg) + (uint32_t)(wg * epi_buffer_bytes<C::BOXC>()), pk, qd, lane,
                                 1u + (uint32_t)wg, qt * BN + c_begin, pm * 256 + 128 * rank, g.q_rows_valid,
                                 g.p_rows_valid, store_pending);
         }
