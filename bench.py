@@ -185,7 +185,8 @@ def profile_traffic(name, kernel_sources):
         return None
 
 
-GEMM_SOURCES = ["mxfp4_block_scaled_gb300/csrc/gemm_kernel.cuh", "mxfp4_block_scaled_gb300/csrc/common.cuh"]
+GEMM_SOURCES = ["mxfp4_block_scaled_gb300/csrc/gemm_kernel.cuh", "mxfp4_block_scaled_gb300/csrc/common.cuh",
+                "mxfp4_block_scaled_gb300/csrc/internal.h", "mxfp4_block_scaled_gb300/csrc/gemm.cu"]
 
 
 # ------------------------------------------------------------ timing

@@ -155,6 +155,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     return false;
 }
 
+// Busy-wait for about `ns` nanoseconds (bounded; used only on abort paths to
+// let copies already in flight land before a CTA exits).
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0; i < 0x40000000u; ++i)
+        if (globaltimer_ns() - t0 > ns) break;
+}
+
 // --------------------------------------------------------- thread clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -206,6 +214,15 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     return false;
 }
 
+// Wait polled at CTA scope (cheap), then one cluster-scope fence so that the
+// remote arrivals' prior writes are ordered before what follows.
+__device__ __forceinline__ bool mbar_wait_then_cluster_fence(uint64_t* bar, uint32_t parity, const WaitCfg& w,
+                                                             volatile int* abort) {
+    if (!mbar_wait(bar, parity, w, abort)) return false;
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+    return true;
+}
+
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -219,6 +236,18 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* ba
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
             smem_u32(dst)),
         "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 2-D tiled load into this CTA's smem whose bytes are counted on an mbarrier
+// in either CTA of the CTA pair (`bar_cluster`: shared::cluster address, e.g.
+// from mapa_shared), so one CTA can wait for both CTAs' operand tiles.
+__device__ __forceinline__ void tma_load_2d_pair(const CUtensorMap* map, uint32_t bar_cluster, void* dst, int32_t c0,
+                                                 int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(bar_cluster)
         : "memory");
 }
 
