@@ -340,8 +340,13 @@ def run_profile_other(args, torch, fp4, L, I, dev):
         hidden = I.randn_bf16((T, MOE_H), 3).to(dev)
         logits = I.router_logits(T, MOE_E, 203).to(dev)
         fn = lambda: fp4.moe(hidden, logits, mw, MOE_K)
-    for _ in range(args.warmup + args.steps):
+    torch.cuda.synchronize()
+    for i in range(args.warmup + args.steps):
+        # an NVTX range per call, so a profiler can skip the set-up launches
+        # (ncu --nvtx --nvtx-include "call/")
+        torch.cuda.nvtx.range_push("call")
         fn()
+        torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     fp4.device_status()
     return {"profile": True, "steps": args.steps, "warmup": args.warmup, "workload": wl}

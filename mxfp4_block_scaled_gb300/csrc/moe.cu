@@ -5,10 +5,12 @@
 // -> quantise/dispatch -> permute, experts, unpermute -> combine) and the
 // expert computation of section 4.3 (two GEMMs, SwiGLU, top-k weighted
 // reduction).  Launch chain on one stream, no host synchronisation:
-//   1 route     top-k per token (warp per token), renormalised weights, expert
-//               bitmap; zeroes the fp32 output accumulator and the h amax
+//   1 route     top-k per token (a thread per token for k <= 8, else a warp
+//               per token), renormalised weights, expert bitmap; zeroes the
+//               fp32 output accumulator and the h amax
 //   2 scan      (one CTA) expert counts, padded offsets (128-row tiles per
-//               expert), tile -> expert map, row -> (token, slot) map
+//               expert), tile -> expert map; then (a thread per assignment)
+//               the row -> (token, slot) map
 //   3 amax      hidden amax partials (dynamic scale)
 //   4 quantise  hidden rows straight into expert-sorted padded order
 //   5 GEMM1     grouped tcgen05 GEMM against the interleaved W13, epilogue
@@ -182,6 +184,118 @@ __device__ __forceinline__ void topk_token(const float* row, int E, int k, int l
     my_w = __fdiv_rn(mine, sum);
 }
 
+// Route with a thread per token (k <= 8, E % 4 == 0), 128 tokens per CTA (4
+// bitmap words per expert).  The CTA stages 32 logits of each of its tokens at
+// a time in shared memory, transposed (a thread reads its token's logits
+// without bank conflicts); each thread keeps its top 8 in registers, sorted:
+// an entry ranks before another if its logit is larger, or equal with a lower
+// expert index, so the selection and its order are those of the warp version
+// (and of a stable sort on the negated logits).  A logit that ranks before
+// the k-th entry is inserted by one pass of compare-and-swap down the list.
+// The loop stays rolled and branch-light: unrolled variants of this scan ran
+// out of the instruction cache.
+constexpr int kRouteTok = 128;
+__global__ void __launch_bounds__(kRouteTok) moe_route_thread_kernel(const RouteArgs a, const StaticScales st) {
+    extern __shared__ uint32_t sbm[];  // [E][4] bitmap words of this block's 128 tokens
+    __shared__ float slog[32][kRouteTok + 1];  // [logit within chunk][token]
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (blockIdx.x == 0) {
+        if (a.zero_outputs)
+            for (int e = threadIdx.x; e < a.E; e += kRouteTok) a.amax_h[e] = 0.0f;
+        if (a.has_static)
+            for (int e = threadIdx.x; e < a.E; e += kRouteTok) {
+                a.static13_out[e] = st.s13[e];
+                a.static2_out[e] = st.s2[e];
+            }
+    }
+    if ((int)blockIdx.x < a.route_blocks) {
+        for (int i = threadIdx.x; i < a.E * 4; i += kRouteTok) sbm[i] = 0u;
+        const int64_t tok0 = (int64_t)blockIdx.x * kRouteTok;
+        const int64_t t = tok0 + threadIdx.x;
+        const int k = a.k;
+        float lv[8];
+        int le[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            lv[j] = -INFINITY;
+            le[j] = 0x7FFFFFFF;  // ranks after every real expert
+        }
+        float tv = -INFINITY;  // the k-th entry: the bar a logit must pass
+        int te = 0x7FFFFFFF;
+        for (int e0 = 0; e0 < a.E; e0 += 32) {
+            __syncthreads();
+            // 128 tokens x 32 logits: thread i loads 16 bytes of token i / 8
+            for (int i = threadIdx.x; i < kRouteTok * 8; i += kRouteTok) {
+                const int tt = i >> 3, c4 = (i & 7) * 4;
+                float4 v4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                if (tok0 + tt < a.T && e0 + c4 < a.E)
+                    v4 = *reinterpret_cast<const float4*>(a.logits + (tok0 + tt) * a.E + e0 + c4);
+                slog[c4][tt] = v4.x;
+                slog[c4 + 1][tt] = v4.y;
+                slog[c4 + 2][tt] = v4.z;
+                slog[c4 + 3][tt] = v4.w;
+            }
+            __syncthreads();
+            const int cn = a.E - e0 < 32 ? a.E - e0 : 32;
+#pragma unroll 1
+            for (int c = 0; c < cn; ++c) {
+                float v = slog[c][threadIdx.x];
+                int e = e0 + c;
+                if (!(v > tv || (v == tv && e < te))) continue;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const bool b = v > lv[j] || (v == lv[j] && e < le[j]);
+                    const float ov = lv[j];
+                    const int oe = le[j];
+                    lv[j] = b ? v : ov;
+                    le[j] = b ? e : oe;
+                    v = b ? ov : v;
+                    e = b ? oe : e;
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j == k - 1) {
+                        tv = lv[j];
+                        te = le[j];
+                    }
+            }
+        }
+        if (t < a.T) {
+            float sum = 0.0f, ex[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                ex[j] = 0.0f;
+                if (j < k) {
+                    ex[j] = expf(lv[j] - lv[0]);
+                    sum += ex[j];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j < k) {
+                    a.ids[t * k + j] = le[j];
+                    a.weights[t * k + j] = __fdiv_rn(ex[j], sum);
+                    atomicOr(&sbm[le[j] * 4 + warp], 1u << lane);
+                }
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < a.E * 4; i += kRouteTok) {
+            const int e = i >> 2, w = i & 3;
+            const int64_t word = (int64_t)blockIdx.x * 4 + w;
+            if (word < a.W) a.bitmap[e * a.W + word] = sbm[i];
+        }
+    } else if (a.zero_outputs) {
+        const int64_t nb = (int64_t)gridDim.x - a.route_blocks;
+        float4* y4 = reinterpret_cast<float4*>(a.y);
+        const int64_t n4 = a.y_elems / 4;
+        for (int64_t i = ((int64_t)blockIdx.x - a.route_blocks) * kRouteTok + threadIdx.x; i < n4;
+             i += nb * kRouteTok)
+            y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    pdl_launch_dependents();
+}
+
 template <int PER_LANE>
 __global__ void __launch_bounds__(256) moe_route_kernel(const RouteArgs a, const StaticScales st) {
     extern __shared__ uint32_t sbm[];  // [E][8] bitmap words of this block's 256 tokens
@@ -242,12 +356,43 @@ struct ScanArgs {
     int32_t* row_tok;        // [R]
 };
 
+// Exclusive scan of v over the 1024 threads of the block (v = 0 past the data);
+// *total receives the sum.
+__device__ __forceinline__ int32_t block_exclusive_scan_1024(int32_t v, int32_t* warp_sums, int32_t* total) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int32_t ws = warp_sums[lane];
+        int32_t wi = ws;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t n = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+            if (lane >= o) wi += n;
+        }
+        warp_sums[lane] = wi - ws;  // exclusive prefix of the warp totals
+        if (lane == 31) *total = wi;
+    }
+    __syncthreads();
+    const int32_t r = warp_sums[warp] + incl - v;
+    __syncthreads();
+    return r;
+}
+
 // One CTA: counts and word-level prefix counts per expert from the bitmap,
-// exclusive scans over experts (plain and padded to 128 rows), the tile map,
-// then every assignment's row = padded[e] + (tokens before it routed to e).
+// exclusive scans over experts (plain and padded to 128 rows), the tile map.
+// The rows of the assignments come from moe_assign_kernel.
 __global__ void __launch_bounds__(1024) moe_scan_kernel(const ScanArgs a) {
     __shared__ int32_t cnt[kMaxExperts];
     __shared__ int32_t pad[kMaxExperts + 1];
+    __shared__ int32_t wsum[32];
+    __shared__ int32_t tot[2];
     pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int e = warp; e < a.E; e += 32) {
@@ -267,19 +412,22 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(const ScanArgs a) {
         if (lane == 0) cnt[e] = base;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int32_t o = 0, p = 0;
-        for (int e = 0; e < a.E; ++e) {
+    {
+        const int e = threadIdx.x;  // E <= 1024 = blockDim
+        const int32_t c = e < a.E ? cnt[e] : 0;
+        const int32_t o = block_exclusive_scan_1024(c, wsum, &tot[0]);
+        const int32_t p = block_exclusive_scan_1024((c + 127) / 128 * 128, wsum, &tot[1]);
+        if (e < a.E) {
             a.offsets[e] = o;
-            pad[e] = p;
             a.padded[e] = p;
-            o += cnt[e];
-            p += (cnt[e] + 127) / 128 * 128;
+            pad[e] = p;
         }
-        a.offsets[a.E] = o;
-        a.padded[a.E] = p;
-        pad[a.E] = p;
-        *a.n_ptiles = p / 128;
+        if (e == 0) {
+            a.offsets[a.E] = tot[0];
+            a.padded[a.E] = tot[1];
+            pad[a.E] = tot[1];
+            *a.n_ptiles = tot[1] / 128;
+        }
     }
     __syncthreads();
     for (int e = warp; e < a.E; e += 32) {
@@ -293,13 +441,20 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(const ScanArgs a) {
             a.row_tok[r] = -1;
         }
     }
+    pdl_launch_dependents();
+}
+
+// A thread per assignment (token t, slot s = t * k + j): its row is
+// padded[e] + (tokens before t routed to e), from the bitmap and its prefix.
+__global__ void __launch_bounds__(256) moe_assign_kernel(const ScanArgs a) {
+    pdl_wait();
     const int64_t slots = a.T * a.k;
-    for (int64_t s = threadIdx.x; s < slots; s += blockDim.x) {
+    for (int64_t s = (int64_t)blockIdx.x * 256 + threadIdx.x; s < slots; s += (int64_t)gridDim.x * 256) {
         const int64_t t = s / a.k;
         const int e = a.ids[s];
         const int64_t w = t >> 5;
         const uint32_t below = a.bitmap[e * a.W + w] & ((1u << (t & 31)) - 1u);
-        const int64_t row = pad[e] + a.wprefix[e * a.W + w] + __popc(below);
+        const int64_t row = a.padded[e] + a.wprefix[e * a.W + w] + __popc(below);
         a.row_src[row] = (int32_t)s;
         a.row_tok[row] = (int32_t)t;
     }
@@ -543,7 +698,8 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         ra.y = y;
         ra.y_elems = T * H;
         ra.amax_h = amax_h;
-        ra.route_blocks = (int)((T + 255) / 256);
+        const bool thread_route = k <= 8 && E % 4 == 0;
+        ra.route_blocks = (int)(thread_route ? (T + kRouteTok - 1) / kRouteTok : (T + 255) / 256);
         ra.has_static = is_static ? 1 : 0;
         ra.static13_out = st13;
         ra.static2_out = st2;
@@ -552,14 +708,16 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         memset(&sc, 0, sizeof(sc));
         if (is_static)
             for (int64_t e = 0; e < E; ++e) sc.s13[e] = s13[e], sc.s2[e] = s2[e];
-        int zero_blocks = full ? (int)std::min<int64_t>((T * H / 4 + 255) / 256, (int64_t)d->sm_count * 4) : 0;
+        const int rt = thread_route ? kRouteTok : 256;  // threads per route CTA
+        int zero_blocks = full ? (int)std::min<int64_t>((T * H / 4 + rt - 1) / rt, (int64_t)d->sm_count * 8) : 0;
         void* args[] = {(void*)&ra, (void*)&sc};
         const int per_lane = (int)((E + 31) / 32);
-        const void* fn = per_lane <= 4 ? (const void*)moe_route_kernel<4>
-                         : per_lane <= 8 ? (const void*)moe_route_kernel<8>
-                         : per_lane <= 16 ? (const void*)moe_route_kernel<16>
-                                          : (const void*)moe_route_kernel<32>;
-        MOE_CUDA(launch_k(fn, dim3(ra.route_blocks + zero_blocks), dim3(256), (size_t)E * 8 * 4, pdl, s, args),
+        const void* fn = thread_route ? (const void*)moe_route_thread_kernel
+                         : per_lane <= 4        ? (const void*)moe_route_kernel<4>
+                         : per_lane <= 8        ? (const void*)moe_route_kernel<8>
+                         : per_lane <= 16       ? (const void*)moe_route_kernel<16>
+                                                : (const void*)moe_route_kernel<32>;
+        MOE_CUDA(launch_k(fn, dim3(ra.route_blocks + zero_blocks), dim3(rt), (size_t)E * (rt / 32) * 4, pdl, s, args),
                  "route launch");
         pdl = true;
         ScanArgs sa;
@@ -579,6 +737,9 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         sa.row_tok = row_tok;
         void* sargs[] = {(void*)&sa};
         MOE_CUDA(launch_k((const void*)moe_scan_kernel, dim3(1), dim3(1024), 0, pdl, s, sargs), "scan launch");
+        const int64_t ab = std::min<int64_t>((T * k + 255) / 256, (int64_t)d->sm_count * 8);
+        MOE_CUDA(launch_k((const void*)moe_assign_kernel, dim3((unsigned)ab), dim3(256), 0, pdl, s, sargs),
+                 "assign launch");
     }
     // 2-3. hidden amax (dynamic) and quantise into expert-sorted padded rows
     if (mask & ST_QUANT) {
