@@ -304,12 +304,13 @@ static GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int sms) {
     p.pair = false;
     const int64_t kbt = gemm_k_blocks(k);
     if (m <= kDecodeMaxM) {
-        // decode: one 128-row activation tile (rows beyond m are zero-filled by
-        // the TMA, not read), 256-wide weight tiles, split-K so that about
-        // three units land on every SM; deterministic reduction afterwards
+        // decode, swap-AB: the weights are the MMA's M side (128-row tiles), the
+        // m activation rows its N side (32 or 64, rows past m zero-filled by
+        // the TMA), split-K so that about three units land on every SM;
+        // deterministic reduction afterwards
         p.decode = true;
-        p.bn = 256;
-        const int64_t qtiles = (n + 255) / 256;
+        p.bn = m <= 32 ? 32 : 64;
+        const int64_t qtiles = (n + 127) / 128;
         int64_t s = (3 * (int64_t)sms + qtiles - 1) / qtiles;
         if (s > kbt / 2) s = kbt / 2;
         if (s > 16) s = 16;
@@ -391,20 +392,23 @@ static fp4_status enqueue_gemm(int fmt, const uint8_t* ac, const uint8_t* as, co
         g.q_codes = wc, g.q_scales = wsc, g.q_rows = n, g.q_rows_valid = n, g.q_global = wg;
         g.out = out;
         g.ldo = n;
+        g.early_q = true;  // weights
         if (p.pair) return cuda_status(launch_gemm_pair(g, s), "GEMM launch");
         return cuda_status(launch_gemm(g, s), "GEMM launch");
     }
-    // decode: activations on the MMA M side, weights on N, split-K partials
-    g.p_codes = ac, g.p_scales = as, g.p_rows = m, g.p_rows_valid = m, g.p_global = ag;
-    g.q_codes = wc, g.q_scales = wsc, g.q_rows = n, g.q_rows_valid = n, g.q_global = wg;
+    // decode: weights on the MMA M side, activations on N, split-K partials
+    // part[split][m][n] (the transposed epilogues write token-major rows)
+    g.p_codes = wc, g.p_scales = wsc, g.p_rows = n, g.p_rows_valid = n, g.p_global = wg;
+    g.q_codes = ac, g.q_scales = as, g.q_rows = m, g.q_rows_valid = m, g.q_global = ag;
     g.splits = p.splits;
+    g.early_p = true;  // weights
     if (p.splits == 1) {
-        g.epi = EPI_BF16;
+        g.epi = EPI_BF16_T;
         g.out = out;
         g.ldo = n;
         return cuda_status(launch_gemm(g, s), "GEMM launch");
     }
-    g.epi = EPI_PARTIAL;
+    g.epi = EPI_PARTIAL_T;
     g.out = part;
     g.ldo = n;
     TRY(cuda_status(launch_gemm(g, s), "GEMM launch"));

@@ -248,13 +248,17 @@ __global__ void __launch_bounds__(512, 1)
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
-    pdl_wait();
+    // Programmatic dependent launch: a grouped GEMM's schedule comes from the
+    // preceding kernels, so every role waits here; otherwise each role waits
+    // just before its first read of their outputs (the weight producer not at
+    // all when early_p / early_q marks its operand).
+    if (g.grouped) pdl_wait();
     const Sched sc = make_sched<BN>(g);
     const int64_t ksfc = (g.k + 255) / 256 * (MX ? 2 : 4);      // scale atoms per 128-row tile (K padded to 256)
     const int64_t q_chunks_total = (g.q_rows + 127) / 128;      // 128-row scale tiles of Q
 
     if (warp < 4) {
-        // ---------------------------------------------------- scale writers
+        // ---------------------------------------------------- scale writers (smem -> TMEM only)
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         int stage = 0, slot = 0;  // operand stage (TMEM scale columns), scale ring slot
         uint32_t ph = 0, sph = 0;
@@ -306,6 +310,7 @@ __global__ void __launch_bounds__(512, 1)
             // bytes to the stage's barrier), warp 7 both tiles' scale atoms into
             // the scale ring; three threads issue copies in parallel.
             const bool is_p = warp == 4, is_sf = warp == 7;
+            if (is_sf || (is_p ? !g.early_p : !g.early_q)) pdl_wait();
             uint64_t* const fb = is_sf ? sfull : full;   // barrier the copies complete on
             uint64_t* const eb = is_sf ? sempty : empty; // barrier that frees the slot
             const int nst = is_sf ? C::SSLOTS : C::STAGES; // ring length (stage = scale slot for warp 7)
@@ -444,6 +449,7 @@ __global__ void __launch_bounds__(512, 1)
         const int c_begin = ((warp - 8) >> 2) * CPW;
         const bool has_cols = c_begin < BN;
         const int wg = (warp - 8) >> 2;
+        pdl_wait();  // global scales and output buffers
         bool store_pending = false;  // EPI_BF16: this thread issued a TMA store not yet waited for
         int acc = 0;
         uint32_t aph = 0;

@@ -111,6 +111,11 @@ struct GemmLaunch {
     float* amax_out = nullptr;              // EPI_SWIGLU: per-expert amax of h (as uint bits, atomicMax)
     int max_ctas = 0;                       // 0 = one per SM
     bool pdl = false;
+    // Operand tiles that do not depend on the preceding kernel (the weights):
+    // their producer starts loading before the programmatic-dependency wait,
+    // overlapping the tail of the activation quantiser.  Non-grouped only.
+    bool early_p = false;
+    bool early_q = false;
 };
 
 // K block of the one-CTA GEMM pipeline: bytes of packed codes per row and

@@ -59,6 +59,9 @@ __global__ void __launch_bounds__(QT) amax_partial_kernel(const uint4* __restric
                                                           float* __restrict__ partials) {
     __shared__ uint32_t red[QT / 32];
     pdl_wait();
+    // the quantiser waits for this grid's completion before reading partials,
+    // so it may be scheduled now
+    pdl_launch_dependents();
     // Sweep from the end of the tensor to its start, so that the start -- which
     // the quantise pass reads first -- is the most recently cached.
     uint32_t m = 0;
@@ -79,7 +82,6 @@ __global__ void __launch_bounds__(QT) amax_partial_kernel(const uint4* __restric
     m = max(m & 0xFFFFu, m >> 16);
     m = block_max_u32(m, red);
     if (threadIdx.x == 0) partials[blockIdx.x] = __uint_as_float(m << 16);
-    pdl_launch_dependents();
 }
 
 int amax_partials_count(int64_t n_elems) {
@@ -166,6 +168,9 @@ __global__ void __launch_bounds__(QT) quant_kernel(const QuantLaunch q) {
     __shared__ uint32_t red[QT / 32];
     __shared__ float sh_sg;
     pdl_wait();
+    // consumers wait for this grid's completion before reading its output, so
+    // they may be scheduled now (a GEMM starts streaming its weights)
+    pdl_launch_dependents();
 
     // Per-tensor global scale (modes that have one).
     float sg_tensor = q.static_scale;
@@ -220,10 +225,7 @@ __global__ void __launch_bounds__(QT) quant_kernel(const QuantLaunch q) {
     Item cur;
     cur.r = (int64_t)blockIdx.x * rpi + ty;
     cur.b = tx;
-    if (cur.r >= row_limit || cur.b >= nb) {
-        pdl_launch_dependents();
-        return;
-    }
+    if (cur.r >= row_limit || cur.b >= nb) return;
     cur.src = source_row(cur.r);
     load(cur);
     while (true) {
@@ -302,7 +304,6 @@ __global__ void __launch_bounds__(QT) quant_kernel(const QuantLaunch q) {
         if (!more) break;
         cur = nxt;
     }
-    pdl_launch_dependents();
 }
 
 cudaError_t launch_quant(const QuantLaunch& q, cudaStream_t s) {
