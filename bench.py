@@ -49,7 +49,8 @@ def parse():
     p.add_argument("--profile", action="store_true",
                    help="only the layer calls (warmup + steps), for ncu captures")
     p.add_argument("--workload", default="prefill",
-                   choices=["prefill", "decode1", "decode8", "decode32", "mxfp4", "moe1", "moe64", "moe4096"],
+                   choices=["prefill", "quant", "decode1", "decode8", "decode32", "mxfp4", "moe1", "moe64",
+                            "moe4096"],
                    help="workload run by --profile")
     return p.parse_args()
 
@@ -329,6 +330,11 @@ def run_profile_other(args, torch, fp4, L, I, dev):
         wq = fp4.prepack_weight(I.weights_bf16(14336, 4096, 101).to(dev))
         a = I.activations_with_outliers(m, 4096, 1).to(dev)
         fn = lambda: fp4.gemm(a, wq)
+    elif wl == "quant":
+        # the prefill activations' dynamic quantisation alone (amax + quantise)
+        a = I.randn_bf16((M, K), 2).to(dev)
+        aq = fp4.empty_qtensor(fp4.NVFP4, M, K, dev)
+        fn = lambda: fp4.quantize(a, out=aq)
     elif wl == "mxfp4":
         wq = fp4.prepack_weight(I.weights_bf16(2048, 7168, 104).to(dev), fp4.MXFP4)
         a = I.randn_bf16((2048, 7168), 4).to(dev)
@@ -416,7 +422,9 @@ def run_secondary(torch, fp4, L, I, dev, peaks):
         byt = wbytes + m * nk * 2 + m * 14336 * 2
         out["decode_m%d" % m] = {"us": round(ms * 1e3, 2), "GB/s": round(byt / (ms * 1e-3) / 1e9, 1),
                                  "frac_hbm": round(byt / (ms * 1e-3) / 1e9 / hbm, 4),
-                                 "note": "quantise + split-K GEMM + reduce, CUDA graph, 8 rotating weight copies"}
+                                 "note": ("one fused launch (activations quantised in the GEMM kernel)" if m <= 8
+                                          else "quantise + split-K GEMM + reduce")
+                                         + ", CUDA graph, 8 rotating weight copies"}
     del copies
     # MXFP4 M=2048 K=7168 N=2048
     a = I.randn_bf16((2048, 7168), 4).to(dev)

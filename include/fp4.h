@@ -103,12 +103,18 @@ fp4_status fp4_device_status(void* stream);
  * for the architecture check; 0 restores the real query.  Host-side only. */
 void fp4_set_arch_override(int sm);
 
-/* Tuning and test hook (no counterpart on the pages): which prefill GEMM
- * kernel fp4_gemm / fp4_gemm_prequant use for m > 64.  0 = automatic (the
- * one-CTA kernel, 128-row tiles), 1 = one-CTA kernel, 2 = the CTA-pair kernel
- * (tcgen05 cta_group::2, 256 x 256 tiles) wherever m >= 256 and n >= 256.
- * Process-wide, host-side; results are identical under every policy.
- * FP4_ERR_INVALID_ARG for a value outside 0..2 (the policy is unchanged). */
+/* Tuning and test hook (no counterpart on the pages): which kernels fp4_gemm /
+ * fp4_gemm_prequant use.  0 = automatic: for m > 64 the one-CTA kernel
+ * (128-row tiles); for fp4_gemm with m <= 8, k <= 8192 and n >= 64 x (SM count) the
+ * fused decode kernel (activation quantisation inside the GEMM launch, one CTA
+ * per 128 weight rows), else quantiser + split-K GEMM + reduction.
+ * 1 = the one-CTA kernel and never the fused decode kernel; 2 = the CTA-pair
+ * kernel (tcgen05 cta_group::2, 256 x 256 tiles) wherever m >= 256 and
+ * n >= 256; 3 = the fused decode kernel for every fp4_gemm with m <= 8 and
+ * k <= 8192.
+ * Process-wide, host-side; results agree within the GEMM tolerance under every
+ * policy (codes and scales are identical).
+ * FP4_ERR_INVALID_ARG for a value outside 0..3 (the policy is unchanged). */
 fp4_status fp4_set_gemm_tile_policy(int policy);
 
 /* Test hook for failure detection: launches one tiny kernel whose thread waits

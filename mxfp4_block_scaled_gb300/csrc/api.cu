@@ -176,7 +176,7 @@ extern "C" size_t fp4_scales_bytes(int fmt, int64_t rows, int64_t k) {
 extern "C" void fp4_set_arch_override(int sm) { g_arch_override = sm; }
 
 extern "C" fp4_status fp4_set_gemm_tile_policy(int policy) {
-    CHECK_OR_RETURN(policy >= 0 && policy <= 2, FP4_ERR_INVALID_ARG, "tile policy %d not in 0..2", policy);
+    CHECK_OR_RETURN(policy >= 0 && policy <= 3, FP4_ERR_INVALID_ARG, "tile policy %d not in 0..3", policy);
     g_tile_policy = policy;
     return FP4_OK;
 }
@@ -455,6 +455,18 @@ extern "C" fp4_status fp4_gemm(int fmt, const void* x, int64_t m, int mode, floa
     uint8_t* as = base;
     base += align256(fp4_scales_bytes(fmt, m, k));
     float* ag = reinterpret_cast<float*>(base);
+    const DeviceInfo* d = current_device();
+    const bool fused = g_tile_policy == 3 || (g_tile_policy == 0 && (n + 127) / 128 >= (int64_t)d->sm_count / 2);
+    if (m <= kDecodeFusedMaxM && k <= kDecodeFusedMaxK && fused) {
+        // decode: one launch (in-kernel activation quantisation, one CTA per
+        // 128 weight rows, no split-K); the activation s_g goes to the workspace
+        return cuda_status(launch_decode_fused(fmt, static_cast<const uint16_t*>(x), (int)m, n, k,
+                                               static_cast<const uint8_t*>(w_codes),
+                                               static_cast<const uint8_t*>(w_scales), w_global,
+                                               mode == FP4_SCALE_DYNAMIC ? 1 : 0, st, ag,
+                                               static_cast<uint16_t*>(out), false, (cudaStream_t)stream),
+                           "decode launch");
+    }
     base += 256;
     float* partials = reinterpret_cast<float*>(base);
     base += 4096;

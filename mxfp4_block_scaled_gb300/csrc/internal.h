@@ -125,6 +125,15 @@ struct GemmLaunch {
 // often; 128 measured faster on the 8192 x 14336 x 4096 prefill.
 constexpr int GEMM_KB_BYTES = 128;
 int64_t gemm_k_blocks(int64_t k);  // K blocks of the one-CTA GEMM
+
+// Small-M linear in one launch (decode_fused.cu): quantises the m <= 8 bf16
+// activation rows in the kernel and streams the weights, one CTA per 128
+// weight rows, bf16 out [m][n].
+constexpr int kDecodeFusedMaxM = 8;
+constexpr int64_t kDecodeFusedMaxK = 8192;
+cudaError_t launch_decode_fused(int fmt, const uint16_t* x, int m, int64_t n, int64_t k, const uint8_t* w_codes,
+                                const uint8_t* w_scales, const float* w_global, int dynamic, float static_scale,
+                                float* a_global_out, uint16_t* out, bool pdl, cudaStream_t s);
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s);
 // CTA-pair variant (EPI_BF16 only): 256 x 256 tiles on clusters of two CTAs.
 cudaError_t launch_gemm_pair(const GemmLaunch& g, cudaStream_t s);

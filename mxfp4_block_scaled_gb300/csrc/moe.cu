@@ -191,7 +191,8 @@ __device__ __forceinline__ void topk_token(const float* row, int E, int k, int l
 // an entry ranks before another if its logit is larger, or equal with a lower
 // expert index, so the selection and its order are those of the warp version
 // (and of a stable sort on the negated logits).  A logit that ranks before
-// the k-th entry is inserted by one pass of compare-and-swap down the list.
+// the 8th entry is inserted by one pass of compare-and-swap down the list (the
+// top 8 contain the top k for any k <= 8).
 // The loop stays rolled and branch-light: unrolled variants of this scan ran
 // out of the instruction cache.
 constexpr int kRouteTok = 128;
@@ -221,7 +222,7 @@ __global__ void __launch_bounds__(kRouteTok) moe_route_thread_kernel(const Route
             lv[j] = -INFINITY;
             le[j] = 0x7FFFFFFF;  // ranks after every real expert
         }
-        float tv = -INFINITY;  // the k-th entry: the bar a logit must pass
+        float tv = -INFINITY;  // the 8th entry: the bar a logit must pass
         int te = 0x7FFFFFFF;
         for (int e0 = 0; e0 < a.E; e0 += 32) {
             __syncthreads();
@@ -253,12 +254,10 @@ __global__ void __launch_bounds__(kRouteTok) moe_route_thread_kernel(const Route
                     v = b ? ov : v;
                     e = b ? oe : e;
                 }
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (j == k - 1) {
-                        tv = lv[j];
-                        te = le[j];
-                    }
+                // the bar is the 8th entry whatever k is: the top 8 contain the top k,
+                // and a fixed index keeps the list in registers
+                tv = lv[7];
+                te = le[7];
             }
         }
         if (t < a.T) {

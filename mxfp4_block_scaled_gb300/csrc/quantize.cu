@@ -7,16 +7,16 @@
 // e = floor(log2 amax_b) - 2 (clamped to [-127, 127]); element =
 // E2M1_rne_satfinite(x * 2^-e) (exact), all-zero blocks give byte 0 and zeros.
 //
-// Layout of the work: one warp quantises a 256-element K tile of one row; lane
-// l holds elements 8l..8l+7 (one 16-byte load), so an NVFP4 block is a lane
-// pair and an MXFP4 block four lanes.  Codes leave as one 32-bit store per
-// lane (128 contiguous bytes per warp); scales are gathered by shuffles into
-// 32-bit words of the MMA layout.  All float operations are single IEEE
-// operations (__fdiv_rn / __fmul_rn), matching the CPU oracle bit for bit.
+// Layout of the work: one thread per scale block (see quant_kernel); the
+// per-block arithmetic is in quant_math.cuh.  Every value that decides a code
+// or a scale byte is the one single IEEE operations (__fdiv_rn / __fmul_rn)
+// give, matching the CPU oracle bit for bit; the faster product with a
+// reciprocal is used only where a bracket proves it gives the same code.
 #include <stdio.h>
 
 #include "common.cuh"
 #include "internal.h"
+#include "quant_math.cuh"
 
 namespace fp4 {
 
@@ -43,16 +43,6 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* red) {
     v = red[0];
     __syncthreads();
     return v;
-}
-
-// |bf16| pair maxima: the sign-cleared bit patterns of non-NaN bf16 values
-// order like their magnitudes, so a 16-bit unsigned max is an exact abs-max.
-__device__ __forceinline__ uint32_t absmax8(const uint4& v, uint32_t m) {
-    m = __vmaxu2(m, v.x & 0x7FFF7FFFu);
-    m = __vmaxu2(m, v.y & 0x7FFF7FFFu);
-    m = __vmaxu2(m, v.z & 0x7FFF7FFFu);
-    m = __vmaxu2(m, v.w & 0x7FFF7FFFu);
-    return m;
 }
 
 __global__ void __launch_bounds__(QT) amax_partial_kernel(const uint4* __restrict__ x, int64_t n_vec,
@@ -120,41 +110,6 @@ cudaError_t launch_amax_partials(const uint16_t* x, int64_t n_elems, float* part
 }
 
 // ------------------------------------------------------------- quantiser
-
-// E2M1 codes of x / d for 8 elements (one 32-bit word), bit-identical to
-// converting the correctly rounded quotients fl(x / d).  With rd = fl(1/d),
-// q = fl(x * rd) is within 1.5 * 2^-23 relative of x / d, and so is fl(x / d);
-// q * (1 - 2^-21) and q * (1 + 2^-21) (each rounded) therefore bracket
-// fl(x / d).  E2M1 rounding is monotone, so when both brackets give the same
-// codes those are the codes of fl(x / d).  Otherwise (a quotient next to a
-// rounding threshold, rare) the codes come from correctly rounded divisions.
-// d must be a normal float whose reciprocal is normal.
-__device__ __forceinline__ uint32_t e2m1_word(const float* f, float d, float rd) {
-    const float lo_s = 1.0f - 4.76837158203125e-07f;  // 1 - 2^-21
-    const float hi_s = 1.0f + 4.76837158203125e-07f;  // 1 + 2^-21
-    float q[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(f[i], rd);
-    const uint32_t lo = cvt_e2m1x8(__fmul_rn(q[0], lo_s), __fmul_rn(q[1], lo_s), __fmul_rn(q[2], lo_s),
-                                   __fmul_rn(q[3], lo_s), __fmul_rn(q[4], lo_s), __fmul_rn(q[5], lo_s),
-                                   __fmul_rn(q[6], lo_s), __fmul_rn(q[7], lo_s));
-    const uint32_t hi = cvt_e2m1x8(__fmul_rn(q[0], hi_s), __fmul_rn(q[1], hi_s), __fmul_rn(q[2], hi_s),
-                                   __fmul_rn(q[3], hi_s), __fmul_rn(q[4], hi_s), __fmul_rn(q[5], hi_s),
-                                   __fmul_rn(q[6], hi_s), __fmul_rn(q[7], hi_s));
-    if (lo == hi) return lo;
-    return cvt_e2m1x8(__fdiv_rn(f[0], d), __fdiv_rn(f[1], d), __fdiv_rn(f[2], d), __fdiv_rn(f[3], d),
-                      __fdiv_rn(f[4], d), __fdiv_rn(f[5], d), __fdiv_rn(f[6], d), __fdiv_rn(f[7], d));
-}
-
-__device__ __forceinline__ uint32_t e2m1_word_exact(const float* f, float d) {
-    return cvt_e2m1x8(__fdiv_rn(f[0], d), __fdiv_rn(f[1], d), __fdiv_rn(f[2], d), __fdiv_rn(f[3], d),
-                      __fdiv_rn(f[4], d), __fdiv_rn(f[5], d), __fdiv_rn(f[6], d), __fdiv_rn(f[7], d));
-}
-
-__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
-    f[0] = bf16lo(v.x), f[1] = bf16hi(v.x), f[2] = bf16lo(v.y), f[3] = bf16hi(v.y);
-    f[4] = bf16lo(v.z), f[5] = bf16hi(v.z), f[6] = bf16lo(v.w), f[7] = bf16hi(v.w);
-}
 
 // One thread per scale block: 16 elements (NVFP4) or 32 (MXFP4) of one row.
 // A CTA covers `rpi` rows at a time with `bpt` threads per row (consecutive

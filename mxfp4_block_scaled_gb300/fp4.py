@@ -190,11 +190,11 @@ def gemm_prequant(aq, wq, out=None, workspace=None, stream=None):
     return out
 
 
-TILE_AUTO, TILE_ONE_CTA, TILE_CTA_PAIR = 0, 1, 2
+TILE_AUTO, TILE_ONE_CTA, TILE_CTA_PAIR, TILE_FUSED_DECODE = 0, 1, 2, 3
 
 
 def set_gemm_tile_policy(policy):
-    """Choose the prefill GEMM kernel (TILE_AUTO, TILE_ONE_CTA, TILE_CTA_PAIR)."""
+    """Choose the GEMM kernels (TILE_AUTO, TILE_ONE_CTA, TILE_CTA_PAIR, TILE_FUSED_DECODE)."""
     _check(lib().fp4_set_gemm_tile_policy(int(policy)))
 
 

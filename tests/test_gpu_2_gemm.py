@@ -68,6 +68,28 @@ def test_pair_kernel_shapes(F, O, m, n, k, fmt):
         F.set_gemm_tile_policy(F.TILE_AUTO)
 
 
+# the fused decode kernel (activation quantisation inside the GEMM launch),
+# forced on small and ragged shapes: n not a multiple of 128, k not of 256
+@pytest.mark.parametrize("m,n,k", [(1, 256, 512), (5, 520, 800), (8, 1000, 1056), (3, 128, 4096)])
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_fused_decode_shapes(F, O, m, n, k, fmt):
+    F.set_gemm_tile_policy(F.TILE_FUSED_DECODE)
+    try:
+        check_linear(F, O, I.activations_with_outliers(m, k, m + k), I.weights_bf16(n, k, n + 7), fmt)
+    finally:
+        F.set_gemm_tile_policy(F.TILE_AUTO)
+
+
+def test_fused_decode_static_scale(F, O):
+    F.set_gemm_tile_policy(F.TILE_FUSED_DECODE)
+    try:
+        a = I.randn_bf16((4, 1024), 21)
+        w = I.weights_bf16(640, 1024, 22)
+        check_linear(F, O, a, w, 0, mode=1, st=3.5 / 2688)
+    finally:
+        F.set_gemm_tile_policy(F.TILE_AUTO)
+
+
 def test_static_scale(F, O):
     a = I.randn_bf16((96, 512), 9)
     w = I.weights_bf16(256, 512, 10)
