@@ -786,8 +786,10 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         GemmLaunch g;
         g.fmt = FP4_NVFP4;
         g.epi = EPI_SWIGLU;
-        // the tile width must divide the expert's 2I rows (tiles never straddle experts)
-        g.bn = (T * k >= 4 * E * 64 && (2 * I) % 256 == 0) ? 256 : 64;
+        // the tile width must divide the expert's 2I rows (tiles never straddle
+        // experts); 128 keeps two TMEM accumulators, so the SwiGLU epilogue of
+        // one tile overlaps the next tile's MMAs (with 256 there is one)
+        g.bn = (T * k >= 4 * E * 64 && (2 * I) % 128 == 0) ? 128 : 64;
         g.p_codes = a_codes;
         g.p_scales = a_scales;
         g.p_rows = L.R;
