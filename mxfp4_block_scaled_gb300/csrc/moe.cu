@@ -12,7 +12,10 @@
 //               expert), tile -> expert map; then (a thread per assignment)
 //               the row -> (token, slot) map
 //   3 amax      hidden amax partials (dynamic scale)
-//   4 quantise  hidden rows straight into expert-sorted padded order
+//   4 quantise  dynamic scale: the T hidden rows once (token order), then a
+//               permute copies each assignment's codes and scale bytes into
+//               the expert-sorted padded rows; static (per-expert) scales:
+//               the rows straight into that order (the codes depend on e)
 //   5 GEMM1     grouped tcgen05 GEMM against the interleaved W13, epilogue
 //               h = bf16(SiLU(gate) * up) and the per-expert amax of h
 //   6 requant   h -> NVFP4 with s_gH[e] = amax_e / 2688
@@ -61,6 +64,8 @@ enum MoeSlot : int {
     MS_PARTIALS,
     MS_STATIC13,
     MS_STATIC2,
+    MS_TOK_CODES,   // dynamic scale: the hidden rows quantised once, token order
+    MS_TOK_SCALES,
     MS_COUNT
 };
 
@@ -104,6 +109,8 @@ static MoeLayout moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
     sz[MS_PARTIALS] = 4096;
     sz[MS_STATIC13] = E * 4;
     sz[MS_STATIC2] = E * 4;
+    sz[MS_TOK_CODES] = T * H / 2;
+    sz[MS_TOK_SCALES] = round_up(T, 128) * sf_cols_padded(H, 16);
     int64_t o = 0;
     for (int i = 0; i < MS_COUNT; ++i) {
         L.off[i] = o;
@@ -460,6 +467,48 @@ __global__ void __launch_bounds__(256) moe_assign_kernel(const ScanArgs a) {
     pdl_launch_dependents();
 }
 
+// Dispatch of the quantised hidden rows: destination row r (expert-sorted,
+// padded) <- token row_tok[r]: its codes and its scale bytes (four adjacent
+// columns are adjacent bytes in the MMA layout of both buffers); padding rows
+// get zero scales.  A warp takes four rows at a time, so four rows' loads are
+// in flight per lane, with no per-element index division.
+__global__ void __launch_bounds__(256) moe_permute_kernel(const uint8_t* __restrict__ tok_codes,
+                                                          const uint8_t* __restrict__ tok_scales,
+                                                          const int32_t* __restrict__ row_tok,
+                                                          const int32_t* __restrict__ rows_dev, int64_t H,
+                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+    pdl_wait();
+    pdl_launch_dependents();  // consumers wait for this grid's completion
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t rows = *rows_dev;
+    const int64_t cb16 = H / 32;                 // 16-byte pieces of codes per row
+    const int64_t ncol = sf_cols_padded(H, 16);  // scale columns per row (padding included)
+    const int64_t nw = ncol / 4;                 // 4-byte scale words per row
+    for (int64_t r0 = ((int64_t)blockIdx.x * 8 + warp) * 4; r0 < rows; r0 += (int64_t)gridDim.x * 32) {
+        int64_t t[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) t[q] = r0 + q < rows ? row_tok[r0 + q] : -2;  // -2: past the rows
+        for (int64_t p = lane; p < cb16; p += 32) {
+            uint4 v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (t[q] >= 0) v[q] = reinterpret_cast<const uint4*>(tok_codes + t[q] * (H / 2))[p];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (t[q] >= 0) reinterpret_cast<uint4*>(codes + (r0 + q) * (H / 2))[p] = v[q];
+        }
+        for (int64_t w = lane; w < nw; w += 32) {
+            uint32_t sv[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                sv[q] = t[q] >= 0 ? *reinterpret_cast<const uint32_t*>(tok_scales + sf_offset(t[q], 4 * w, ncol)) : 0u;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (t[q] != -2) *reinterpret_cast<uint32_t*>(scales + sf_offset(r0 + q, 4 * w, ncol)) = sv[q];
+        }
+    }
+}
+
 // fp32 accumulator -> bf16 output
 __global__ void __launch_bounds__(256) moe_finalize_kernel(const float4* __restrict__ y, uint2* __restrict__ out,
                                                            int64_t n4) {
@@ -679,6 +728,8 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
     float* partials = (float*)at(MS_PARTIALS);
     float* st13 = (float*)at(MS_STATIC13);
     float* st2 = (float*)at(MS_STATIC2);
+    uint8_t* tok_codes = at(MS_TOK_CODES);
+    uint8_t* tok_scales = at(MS_TOK_SCALES);
     const bool is_static = mode == FP4_SCALE_STATIC;
     const bool full = (mask & ST_ALL) == ST_ALL;
     bool pdl = false;  // first launch of the call waits for everything before it
@@ -757,6 +808,7 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         q.tile_expert = tile_expert;
         q.n_experts = (int)E;
         if (!is_static) {
+            // one per-tensor scale: quantise the T rows once, then dispatch
             const int np = amax_partials_count(T * H);
             MOE_CUDA(launch_amax_partials(q.x, T * H, partials, np, pdl, s), "amax launch");
             pdl = true;
@@ -765,13 +817,29 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
             q.partials = partials;
             q.n_partials = np;
             q.global_out = sg_a;
+            q.rows = T;
+            q.rows_pad = round_up(T, 128);
+            q.row_map = nullptr;
+            q.codes = tok_codes;
+            q.scales = tok_scales;
+            MOE_CUDA(launch_quant(q, s), "quantise launch");
+            const uint8_t* tc = tok_codes;
+            const uint8_t* tsc = tok_scales;
+            const int32_t* rt = row_tok;
+            const int32_t* rd = padded + E;  // rows beyond the padded total are not read by GEMM1
+            int64_t hh = H;
+            void* pargs[] = {(void*)&tc, (void*)&tsc, (void*)&rt, (void*)&rd, (void*)&hh, (void*)&a_codes,
+                             (void*)&a_scales};
+            const int64_t pb = (int64_t)d->sm_count * 8;
+            MOE_CUDA(launch_k((const void*)moe_permute_kernel, dim3((unsigned)pb), dim3(256), 0, true, s, pargs),
+                     "permute launch");
         } else {
             q.sg_mode = SG_EXPERT_TABLE;
             q.table = st13;
+            // rows beyond the padded total are skipped: their count is on the device
+            q.rows_dev = padded + E;
+            MOE_CUDA(launch_quant(q, s), "quantise launch");
         }
-        // rows beyond the padded total are skipped: their count is on the device
-        q.rows_dev = padded + E;
-        MOE_CUDA(launch_quant(q, s), "quantise launch");
         pdl = true;
     }
     // 4. GEMM1 + SiLU * up + per-expert amax of h
