@@ -5,9 +5,9 @@
 // -> quantise/dispatch -> permute, experts, unpermute -> combine) and the
 // expert computation of section 4.3 (two GEMMs, SwiGLU, top-k weighted
 // reduction).  Launch chain on one stream, no host synchronisation:
-//   1 route     top-k per token (a thread per token for k <= 8, else a warp
-//               per token), renormalised weights, expert bitmap; zeroes the
-//               fp32 output accumulator and the h amax
+//   1 route     top-k per token (a warp per token, 32 tokens per CTA),
+//               renormalised weights, expert bitmap; zeroes the fp32 output
+//               accumulator and the h amax
 //   2 scan      (one CTA) expert counts, padded offsets (128-row tiles per
 //               expert), tile -> expert map; then (a thread per assignment)
 //               the row -> (token, slot) map
@@ -191,157 +191,45 @@ __device__ __forceinline__ void topk_token(const float* row, int E, int k, int l
     my_w = __fdiv_rn(mine, sum);
 }
 
-// Route with a thread per token (k <= 8, E % 4 == 0), 128 tokens per CTA (4
-// bitmap words per expert).  The CTA stages 32 logits of each of its tokens at
-// a time in shared memory, transposed (a thread reads its token's logits
-// without bank conflicts); each thread keeps its top 8 in registers, sorted:
-// an entry ranks before another if its logit is larger, or equal with a lower
-// expert index, so the selection and its order are those of the warp version
-// (and of a stable sort on the negated logits).  A logit that ranks before
-// the 8th entry is inserted by one pass of compare-and-swap down the list (the
-// top 8 contain the top k for any k <= 8).
-// The loop stays rolled and branch-light: unrolled variants of this scan ran
-// out of the instruction cache.
-constexpr int kRouteTok = 128;
-__global__ void __launch_bounds__(kRouteTok) moe_route_thread_kernel(const RouteArgs a, const StaticScales st) {
-    extern __shared__ uint32_t sbm[];  // [E][4] bitmap words of this block's 128 tokens
-    __shared__ float slog[32][kRouteTok + 1];  // [logit within chunk][token]
-    pdl_wait();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (blockIdx.x == 0) {
-        if (a.zero_outputs)
-            for (int e = threadIdx.x; e < a.E; e += kRouteTok) a.amax_h[e] = 0.0f;
-        if (a.has_static)
-            for (int e = threadIdx.x; e < a.E; e += kRouteTok) {
-                a.static13_out[e] = st.s13[e];
-                a.static2_out[e] = st.s2[e];
-            }
-    }
-    if ((int)blockIdx.x < a.route_blocks) {
-        for (int i = threadIdx.x; i < a.E * 4; i += kRouteTok) sbm[i] = 0u;
-        const int64_t tok0 = (int64_t)blockIdx.x * kRouteTok;
-        const int64_t t = tok0 + threadIdx.x;
-        const int k = a.k;
-        float lv[8];
-        int le[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            lv[j] = -INFINITY;
-            le[j] = 0x7FFFFFFF;  // ranks after every real expert
-        }
-        float tv = -INFINITY;  // the 8th entry: the bar a logit must pass
-        int te = 0x7FFFFFFF;
-        for (int e0 = 0; e0 < a.E; e0 += 32) {
-            __syncthreads();
-            // 128 tokens x 32 logits: thread i loads 16 bytes of token i / 8
-            for (int i = threadIdx.x; i < kRouteTok * 8; i += kRouteTok) {
-                const int tt = i >> 3, c4 = (i & 7) * 4;
-                float4 v4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-                if (tok0 + tt < a.T && e0 + c4 < a.E)
-                    v4 = *reinterpret_cast<const float4*>(a.logits + (tok0 + tt) * a.E + e0 + c4);
-                slog[c4][tt] = v4.x;
-                slog[c4 + 1][tt] = v4.y;
-                slog[c4 + 2][tt] = v4.z;
-                slog[c4 + 3][tt] = v4.w;
-            }
-            __syncthreads();
-            const int cn = a.E - e0 < 32 ? a.E - e0 : 32;
-#pragma unroll 1
-            for (int c = 0; c < cn; ++c) {
-                float v = slog[c][threadIdx.x];
-                int e = e0 + c;
-                if (!(v > tv || (v == tv && e < te))) continue;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const bool b = v > lv[j] || (v == lv[j] && e < le[j]);
-                    const float ov = lv[j];
-                    const int oe = le[j];
-                    lv[j] = b ? v : ov;
-                    le[j] = b ? e : oe;
-                    v = b ? ov : v;
-                    e = b ? oe : e;
-                }
-                // the bar is the 8th entry whatever k is: the top 8 contain the top k,
-                // and a fixed index keeps the list in registers
-                tv = lv[7];
-                te = le[7];
-            }
-        }
-        if (t < a.T) {
-            float sum = 0.0f, ex[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                ex[j] = 0.0f;
-                if (j < k) {
-                    ex[j] = expf(lv[j] - lv[0]);
-                    sum += ex[j];
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (j < k) {
-                    a.ids[t * k + j] = le[j];
-                    a.weights[t * k + j] = __fdiv_rn(ex[j], sum);
-                    atomicOr(&sbm[le[j] * 4 + warp], 1u << lane);
-                }
-        }
-        __syncthreads();
-        for (int i = threadIdx.x; i < a.E * 4; i += kRouteTok) {
-            const int e = i >> 2, w = i & 3;
-            const int64_t word = (int64_t)blockIdx.x * 4 + w;
-            if (word < a.W) a.bitmap[e * a.W + word] = sbm[i];
-        }
-    } else if (a.zero_outputs) {
-        const int64_t nb = (int64_t)gridDim.x - a.route_blocks;
-        float4* y4 = reinterpret_cast<float4*>(a.y);
-        const int64_t n4 = a.y_elems / 4;
-        for (int64_t i = ((int64_t)blockIdx.x - a.route_blocks) * kRouteTok + threadIdx.x; i < n4;
-             i += nb * kRouteTok)
-            y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    pdl_launch_dependents();
-}
-
+// Route with a warp per token: 32 tokens per CTA of 1024 threads, so the CTA
+// owns exactly one 32-token bitmap word per expert (built in smem).  A token's
+// top-k takes k rounds of a warp arg-max (topk_token), short enough that a
+// handful of tokens costs about what one does.
 template <int PER_LANE>
-__global__ void __launch_bounds__(256) moe_route_kernel(const RouteArgs a, const StaticScales st) {
-    extern __shared__ uint32_t sbm[];  // [E][8] bitmap words of this block's 256 tokens
+__global__ void __launch_bounds__(1024) moe_route_kernel(const RouteArgs a, const StaticScales st) {
+    extern __shared__ uint32_t sbm[];  // [E] bitmap words of this block's 32 tokens
     pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (blockIdx.x == 0) {
         if (a.zero_outputs)
-            for (int e = threadIdx.x; e < a.E; e += 256) a.amax_h[e] = 0.0f;
+            for (int e = threadIdx.x; e < a.E; e += 1024) a.amax_h[e] = 0.0f;
         if (a.has_static)
-            for (int e = threadIdx.x; e < a.E; e += 256) {
+            for (int e = threadIdx.x; e < a.E; e += 1024) {
                 a.static13_out[e] = st.s13[e];
                 a.static2_out[e] = st.s2[e];
             }
     }
     if ((int)blockIdx.x < a.route_blocks) {
-        for (int i = threadIdx.x; i < a.E * 8; i += 256) sbm[i] = 0u;
+        for (int i = threadIdx.x; i < a.E; i += 1024) sbm[i] = 0u;
         __syncthreads();
-        for (int i = 0; i < 32; ++i) {
-            const int64_t t = (int64_t)blockIdx.x * 256 + warp * 32 + i;
-            if (t >= a.T) break;
+        const int64_t t = (int64_t)blockIdx.x * 32 + warp;
+        if (t < a.T) {
             int e;
             float w;
             topk_token<PER_LANE>(a.logits + t * a.E, a.E, a.k, lane, e, w);
             if (lane < a.k) {
                 a.ids[t * a.k + lane] = e;
                 a.weights[t * a.k + lane] = w;
-                atomicOr(&sbm[e * 8 + warp], 1u << i);
+                atomicOr(&sbm[e], 1u << warp);
             }
         }
         __syncthreads();
-        for (int i = threadIdx.x; i < a.E * 8; i += 256) {
-            const int e = i >> 3, w = i & 7;
-            const int64_t word = (int64_t)blockIdx.x * 8 + w;
-            if (word < a.W) a.bitmap[e * a.W + word] = sbm[i];
-        }
+        for (int e = threadIdx.x; e < a.E; e += 1024) a.bitmap[e * a.W + blockIdx.x] = sbm[e];
     } else if (a.zero_outputs) {
         const int64_t nb = (int64_t)gridDim.x - a.route_blocks;
         float4* y4 = reinterpret_cast<float4*>(a.y);
         const int64_t n4 = a.y_elems / 4;
-        for (int64_t i = ((int64_t)blockIdx.x - a.route_blocks) * 256 + threadIdx.x; i < n4; i += nb * 256)
+        for (int64_t i = ((int64_t)blockIdx.x - a.route_blocks) * 1024 + threadIdx.x; i < n4; i += nb * 1024)
             y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     pdl_launch_dependents();
@@ -748,8 +636,7 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         ra.y = y;
         ra.y_elems = T * H;
         ra.amax_h = amax_h;
-        const bool thread_route = k <= 8 && E % 4 == 0;
-        ra.route_blocks = (int)(thread_route ? (T + kRouteTok - 1) / kRouteTok : (T + 255) / 256);
+        ra.route_blocks = (int)((T + 31) / 32);  // one CTA (32 warps) per 32 tokens = one bitmap word
         ra.has_static = is_static ? 1 : 0;
         ra.static13_out = st13;
         ra.static2_out = st2;
@@ -758,16 +645,14 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         memset(&sc, 0, sizeof(sc));
         if (is_static)
             for (int64_t e = 0; e < E; ++e) sc.s13[e] = s13[e], sc.s2[e] = s2[e];
-        const int rt = thread_route ? kRouteTok : 256;  // threads per route CTA
-        int zero_blocks = full ? (int)std::min<int64_t>((T * H / 4 + rt - 1) / rt, (int64_t)d->sm_count * 8) : 0;
+        int zero_blocks = full ? (int)std::min<int64_t>((T * H / 4 + 1023) / 1024, (int64_t)d->sm_count * 2) : 0;
         void* args[] = {(void*)&ra, (void*)&sc};
         const int per_lane = (int)((E + 31) / 32);
-        const void* fn = thread_route ? (const void*)moe_route_thread_kernel
-                         : per_lane <= 4        ? (const void*)moe_route_kernel<4>
-                         : per_lane <= 8        ? (const void*)moe_route_kernel<8>
-                         : per_lane <= 16       ? (const void*)moe_route_kernel<16>
-                                                : (const void*)moe_route_kernel<32>;
-        MOE_CUDA(launch_k(fn, dim3(ra.route_blocks + zero_blocks), dim3(rt), (size_t)E * (rt / 32) * 4, pdl, s, args),
+        const void* fn = per_lane <= 4    ? (const void*)moe_route_kernel<4>
+                         : per_lane <= 8  ? (const void*)moe_route_kernel<8>
+                         : per_lane <= 16 ? (const void*)moe_route_kernel<16>
+                                          : (const void*)moe_route_kernel<32>;
+        MOE_CUDA(launch_k(fn, dim3(ra.route_blocks + zero_blocks), dim3(1024), (size_t)E * 4, pdl, s, args),
                  "route launch");
         pdl = true;
         ScanArgs sa;
