@@ -289,21 +289,45 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(const ScanArgs a) {
     __shared__ int32_t tot[2];
     pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int e = warp; e < a.E; e += 32) {
+    // a warp takes experts warp, warp + 32, ...; their 32-word chunks are
+    // walked in order with eight chunks' loads in flight (a chunk's word
+    // prefix needs only the running total of its expert)
+    {
+        const int nch = (int)((a.W + 31) / 32);
+        const int ne = warp < a.E ? (a.E - warp + 31) / 32 : 0;
+        const int nit = ne * nch;
         int32_t base = 0;
-        for (int64_t w0 = 0; w0 < a.W; w0 += 32) {
-            const int64_t w = w0 + lane;
-            const int32_t c = w < a.W ? __popc(a.bitmap[e * a.W + w]) : 0;
-            int32_t incl = c;
+        for (int it0 = 0; it0 < nit; it0 += 8) {
+            uint32_t wv[8];
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int32_t n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                if (lane >= o) incl += n;
+            for (int u = 0; u < 8; ++u) {
+                const int it = it0 + u;
+                wv[u] = 0u;
+                if (it < nit) {
+                    const int e = warp + 32 * (it / nch), ch = it % nch;
+                    const int64_t w = (int64_t)ch * 32 + lane;
+                    if (w < a.W) wv[u] = a.bitmap[e * a.W + w];
+                }
             }
-            if (w < a.W) a.wprefix[e * a.W + w] = base + incl - c;
-            base += __shfl_sync(0xFFFFFFFFu, incl, 31);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int it = it0 + u;
+                if (it >= nit) break;  // warp-uniform
+                const int e = warp + 32 * (it / nch), ch = it % nch;
+                if (ch == 0) base = 0;
+                const int64_t w = (int64_t)ch * 32 + lane;
+                const int32_t c = __popc(wv[u]);
+                int32_t incl = c;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int32_t n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                    if (lane >= o) incl += n;
+                }
+                if (w < a.W) a.wprefix[e * a.W + w] = base + incl - c;
+                base += __shfl_sync(0xFFFFFFFFu, incl, 31);
+                if (ch == nch - 1 && lane == 0) cnt[e] = base;
+            }
         }
-        if (lane == 0) cnt[e] = base;
     }
     __syncthreads();
     {
