@@ -439,6 +439,34 @@ def run_secondary(torch, fp4, L, I, dev, peaks):
                                       "frac_fp4_peak": round(fl / (ms * 1e-3) / 1e12 /
                                                              (peaks["bf16"] * FP4_PER_BF16), 4),
                                       "note": "quantise (one pass) + GEMM, L2 flushed between steps"}
+    # the prefill config's other width: M=8192, K=4096, N=4096, NVFP4; the GEMM on
+    # pre-quantised activations (graded against the tensor roofline) and the
+    # layer call with the activations quantised per call
+    a = I.randn_bf16((M, K), 2).to(dev)
+    wq = fp4.prepack_weight(I.weights_bf16(4096, K, 105).to(dev))
+    aq = fp4.quantize(a)
+    o = torch.empty((M, 4096), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(L.fp4_gemm_workspace_size(0, M, 4096, K), dtype=torch.uint8, device=dev)
+    fl = 2.0 * M * 4096 * K
+    tot, _ = time_steps(torch, 20, 3, lambda _: fp4.gemm_prequant(aq, wq, out=o), flush=flush_buf.zero_)
+    ms_g = statistics.mean(tot)
+    tot, _ = time_steps(torch, 20, 3, lambda _: fp4.gemm(a, wq, out=o, workspace=ws), flush=flush_buf.zero_)
+    ms_q = statistics.mean(tot)
+    peak_s = peaks["bf16_sustained"] * FP4_PER_BF16
+    out["prefill_m8192_k4096_n4096"] = {
+        "gemm_us": round(ms_g * 1e3, 2), "gemm_TFLOP/s": round(fl / (ms_g * 1e-3) / 1e12, 1),
+        "frac_fp4_peak": round(fl / (ms_g * 1e-3) / 1e12 / peak_s, 4),
+        "layer_us": round(ms_q * 1e3, 2), "layer_TFLOP/s": round(fl / (ms_q * 1e-3) / 1e12, 1),
+        "note": "GEMM on pre-quantised activations / quantise + GEMM; L2 flushed between steps; "
+                "fraction of the measured sustained FP4 peak"}
+    del a, aq, o, ws
+    # the single-linear correctness config: A [16, 512], W [256, 512] (latency-bound)
+    a = I.randn_bf16((16, 512), 0).to(dev)
+    wq = fp4.prepack_weight(I.weights_bf16(256, 512, 100).to(dev))
+    o = torch.empty((16, 256), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(L.fp4_gemm_workspace_size(0, 16, 256, 512), dtype=torch.uint8, device=dev)
+    ms = graph_time(torch, [lambda: fp4.gemm(a, wq, out=o, workspace=ws)])
+    out["single_linear_m16_k512_n256"] = {"us": round(ms * 1e3, 2), "note": "quantise + GEMM, CUDA graph"}
     out.update(run_moe(torch, fp4, L, I, dev, peaks))
     return out
 

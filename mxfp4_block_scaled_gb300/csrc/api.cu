@@ -34,6 +34,16 @@ static uint64_t g_wait_limit_ns = 4000000000ull;
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns; }
 
+cudaError_t set_smem_attr_once(const void* fn, int bytes, uint64_t& done) {
+    const DeviceInfo* d = current_device();
+    if (!d) return cudaErrorNoDevice;
+    const uint64_t bit = d->device < 64 ? (1ull << d->device) : 0ull;
+    if (bit && (done & bit)) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done |= bit;
+    return e;
+}
+
 const DeviceInfo* current_device() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {

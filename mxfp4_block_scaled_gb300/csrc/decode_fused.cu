@@ -48,7 +48,7 @@ struct DecCfg {
     static constexpr int SMEM_LIMIT = 227 * 1024;
     static constexpr int MAX_K = (int)kDecodeFusedMaxK;                   // fused path: k <= MAX_K
     static constexpr int COMPACT_MAX = 8 * (MAX_K / 2 + MAX_K / 16);      // m <= 8 rows of codes + scales
-    static constexpr int DTAB = 128 * 8;                                  // NVFP4 (d, 1/d) per scale byte
+    static constexpr int DTAB = 128 * 8;                                  // NVFP4 divisor entry per scale byte
     static constexpr int ST_SMEM = (SMEM_LIMIT - 2048 - BAR_BYTES - COMPACT_MAX - DTAB) / STAGE_BYTES;
     static constexpr int ST_TMEM = (512 - BN) / SF_COLS;
     static constexpr int ST_MIN = ST_SMEM < ST_TMEM ? ST_SMEM : ST_TMEM;
@@ -172,14 +172,10 @@ __global__ void __launch_bounds__(512, 1)
             sg = *s_sg;
         }
         if (blockIdx.x == 0 && ta == 0 && a.a_global_out) *a.a_global_out = MX ? 1.0f : sg;
-        // NVFP4: per scale byte, d = fl(s_b s_g) and fl(1/d) (0: the exact path)
+        // NVFP4: the divisor entry of each scale byte (nvfp4_divisor)
         const float p_t = __fmul_rn(sg, 6.0f);
-        const bool p_fast = p_t >= 2.3509887e-38f && p_t <= 4.2535296e37f;
-        const float inv_p = p_fast ? __frcp_rn(p_t) : 0.0f;
-        if (!MX && ta < 128) {
-            const float d = __fmul_rn(e4m3_to_f32((uint32_t)ta), sg);
-            dtab[ta] = make_float2(d, (d >= 1.1754944e-38f && d <= 8.5070592e37f) ? __frcp_rn(d) : 0.0f);
-        }
+        const float inv_p = nvfp4_inv_p(p_t);
+        if (!MX && ta < 128) dtab[ta] = nvfp4_divisor((uint32_t)ta, sg, true);
         named_bar_sync(1, NT);
         constexpr int LPB = MX ? 4 : 2;  // lanes per block
         const uint32_t cpr = (uint32_t)(a.k / 8);  // chunks per row
@@ -204,18 +200,10 @@ __global__ void __launch_bounds__(512, 1)
                 const float amax_b = __uint_as_float(am << 16);
                 uint32_t sbyte = 0, w = 0;
                 if constexpr (!MX) {
-                    // the arithmetic of nvfp4_scale_byte / nvfp4_codes8, with the
-                    // division bracketed and (d, 1/d) from the table
-                    if (p_fast)
-                        sbyte = e4m3_of_quotient(amax_b, p_t, inv_p);
-                    else if (p_t > 0.0f)
-                        sbyte = cvt_e4m3(__fdiv_rn(amax_b, p_t));
-                    const float2 dr = dtab[sbyte];
-                    if (dr.x != 0.0f) {
-                        float f[8];
-                        unpack8(vb[u], f);
-                        w = dr.y != 0.0f ? e2m1_word(f, dr.x, dr.y) : e2m1_word_exact(f, dr.x);
-                    }
+                    sbyte = nvfp4_scale_byte(amax_b, p_t, inv_p);
+                    float f[8];
+                    unpack8(vb[u], f);
+                    w = nvfp4_word(f, dtab[sbyte]);
                 } else {
                     float inv;
                     sbyte = mxfp4_scale_byte(amax_b, inv);
@@ -450,12 +438,8 @@ template <bool MX>
 static cudaError_t launch_dec(const uint8_t* w_codes, const DecodeArgs& a, bool pdl, cudaStream_t s) {
     using C = DecCfg<MX>;
     auto kern = decode_fused_kernel<MX>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static uint64_t attr_done = 0;  // devices on which this instantiation is opted in
+    if (cudaError_t e = set_smem_attr_once((const void*)kern, C::SMEM, attr_done)) return e;
     auto fn = dec_encode_fn();
     if (!fn) return cudaErrorNotSupported;
     CUtensorMap tm;

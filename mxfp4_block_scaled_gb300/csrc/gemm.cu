@@ -64,12 +64,8 @@ template <int BN, bool MX, int EPI>
 static cudaError_t launch_one(const GemmLaunch& g, cudaStream_t s) {
     using C = GemmCfg<BN, MX, epi_staging_bytes<EPI, MX>()>;
     auto kern = gemm_kernel<BN, MX, EPI>;
-    static bool attr_set = false;  // per instantiation; the attribute is per device function
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static uint64_t attr_done = 0;  // devices on which this instantiation is opted in
+    if (cudaError_t e = set_smem_attr_once((const void*)kern, C::SMEM, attr_done)) return e;
     CUtensorMap tmP, tmQ, tmO;
     if (!make_codes_map(&tmP, g.p_codes, g.p_rows, g.k, 128, GEMM_KB_BYTES) ||
         !make_codes_map(&tmQ, g.q_codes, g.q_rows, g.k, BN, GEMM_KB_BYTES)) {

@@ -23,6 +23,10 @@ const DeviceInfo* current_device();
 // Nanoseconds a device-side wait may spin before giving up.
 uint64_t wait_limit_ns();
 
+// Opt `fn` in to `bytes` of dynamic shared memory on the current device, once
+// per device; `done` is the caller's per-kernel mask of devices already set.
+cudaError_t set_smem_attr_once(const void* fn, int bytes, uint64_t& done);
+
 void set_error(const char* fmt, ...);
 
 // FP4_OK if the current device is sm_103 (honours fp4_set_arch_override).

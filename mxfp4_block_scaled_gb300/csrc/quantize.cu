@@ -10,8 +10,11 @@
 // Layout of the work: one thread per scale block (see quant_kernel); the
 // per-block arithmetic is in quant_math.cuh.  Every value that decides a code
 // or a scale byte is the one single IEEE operations (__fdiv_rn / __fmul_rn)
-// give, matching the CPU oracle bit for bit; the faster product with a
-// reciprocal is used only where a bracket proves it gives the same code.
+// give, matching the CPU oracle bit for bit.  Codes come from products with a
+// reciprocal where that is proven to give the same code: for every input, when
+// the block's divisor passes e2m1_product_exact (one multiply per element), else
+// element by element by a bracket, else by correctly rounded divisions.  With
+// one global scale per tensor the 128 possible divisors are tabulated per CTA.
 #include <stdio.h>
 
 #include "common.cuh"
@@ -45,8 +48,10 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* red) {
     return v;
 }
 
-__global__ void __launch_bounds__(QT) amax_partial_kernel(const uint4* __restrict__ x, int64_t n_vec,
-                                                          float* __restrict__ partials) {
+// Eight 16-byte loads in flight per thread (a thread's loads are one grid
+// stride apart, so each load instruction of a warp reads 512 contiguous bytes).
+__global__ void __launch_bounds__(QT, 6) amax_partial_kernel(const uint4* __restrict__ x, int64_t n_vec,
+                                                             float* __restrict__ partials) {
     __shared__ uint32_t red[QT / 32];
     pdl_wait();
     // the quantiser waits for this grid's completion before reading partials,
@@ -58,17 +63,14 @@ __global__ void __launch_bounds__(QT) amax_partial_kernel(const uint4* __restric
     const int64_t stride = (int64_t)gridDim.x * QT;
     const uint4* xe = x + (n_vec - 1);
     int64_t i = (int64_t)blockIdx.x * QT + threadIdx.x;
-    for (; i + 3 * stride < n_vec; i += 4 * stride) {
-        const uint4 a = __ldg(xe - i);
-        const uint4 b = __ldg(xe - (i + stride));
-        const uint4 c = __ldg(xe - (i + 2 * stride));
-        const uint4 d = __ldg(xe - (i + 3 * stride));
-        m = absmax8(a, m);
-        m = absmax8(b, m);
-        m = absmax8(c, m);
-        m = absmax8(d, m);
+    for (; i < n_vec; i += 8 * stride) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            v[u] = i + u * stride < n_vec ? __ldg(xe - (i + u * stride)) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) m = absmax8(v[u], m);
     }
-    for (; i < n_vec; i += stride) m = absmax8(__ldg(xe - i), m);
     m = max(m & 0xFFFFu, m >> 16);
     m = block_max_u32(m, red);
     if (threadIdx.x == 0) partials[blockIdx.x] = __uint_as_float(m << 16);
@@ -122,6 +124,7 @@ __global__ void __launch_bounds__(QT) quant_kernel(const QuantLaunch q) {
     constexpr int NV = BLK / 8;  // 16-byte loads per thread
     __shared__ uint32_t red[QT / 32];
     __shared__ float sh_sg;
+    __shared__ float2 dtab[128];  // NVFP4, one global scale: divisor entry per scale byte
     pdl_wait();
     // consumers wait for this grid's completion before reading its output, so
     // they may be scheduled now (a GEMM starts streaming its weights)
@@ -143,6 +146,16 @@ __global__ void __launch_bounds__(QT) quant_kernel(const QuantLaunch q) {
             for (int e = threadIdx.x; e < q.n_experts; e += QT)
                 q.expert_sg_out[e] = __fdiv_rn(q.table[e], 2688.0f);
     }
+    const bool dyn_sg = !MX && (q.sg_mode == SG_EXPERT_TABLE || q.sg_mode == SG_EXPERT_AMAX);
+    // one global scale: the 128 divisors (a block's byte is below 0x80) and
+    // 1/fl(6 s_g) once per CTA
+    float p_t = 0.0f, inv_p = 0.0f;
+    if (!MX && !dyn_sg) {
+        if (threadIdx.x < 128) dtab[threadIdx.x] = nvfp4_divisor(threadIdx.x, sg_tensor, true);
+        p_t = __fmul_rn(sg_tensor, 6.0f);
+        inv_p = nvfp4_inv_p(p_t);
+        __syncthreads();
+    }
 
     const int nb = (int)sf_cols_padded(q.k, BLK);      // scale blocks per row, padding included
     const int kblocks = (int)(q.k / BLK);              // blocks holding data
@@ -152,7 +165,6 @@ __global__ void __launch_bounds__(QT) quant_kernel(const QuantLaunch q) {
     if (ty >= rpi) return;
     const int64_t row_limit = q.rows_dev ? (int64_t)(*q.rows_dev) : q.rows_pad;
     const int64_t ksf_pad = nb;
-    const bool dyn_sg = !MX && (q.sg_mode == SG_EXPERT_TABLE || q.sg_mode == SG_EXPERT_AMAX);
     const int64_t rstride = (int64_t)gridDim.x * rpi;
 
     // Items (row r, block b) of this thread in order; the loads of the next item
@@ -201,11 +213,6 @@ __global__ void __launch_bounds__(QT) quant_kernel(const QuantLaunch q) {
         const int64_t r = cur.r;
         const int b = cur.b;
         const bool in = cur.src >= 0 && b < kblocks;
-        float sg = sg_tensor;
-        if (dyn_sg) {
-            const float t = q.table[q.tile_expert[r >> 7]];
-            sg = q.sg_mode == SG_EXPERT_TABLE ? t : __fdiv_rn(t, 2688.0f);
-        }
         uint32_t am = 0;
 #pragma unroll
         for (int i = 0; i < NV; ++i) am = absmax8(cur.v[i], am);
@@ -215,22 +222,23 @@ __global__ void __launch_bounds__(QT) quant_kernel(const QuantLaunch q) {
 #pragma unroll
         for (int i = 0; i < NV; ++i) w[i] = 0u;
         if (!MX) {
-            const float p = __fmul_rn(sg, 6.0f);
-            if (p > 0.0f) sbyte = cvt_e4m3(__fdiv_rn(amax_b, p));
-            const float d = __fmul_rn(e4m3_to_f32(sbyte), sg);
-            if (d != 0.0f) {
-                float f[16];
-                unpack8(cur.v[0], f);
-                unpack8(cur.v[1], f + 8);
-                if (d >= 1.1754944e-38f && d <= 8.5070592e37f) {
-                    const float rd = __frcp_rn(d);
-                    w[0] = e2m1_word(f, d, rd);
-                    w[1] = e2m1_word(f + 8, d, rd);
-                } else {
-                    w[0] = e2m1_word_exact(f, d);
-                    w[1] = e2m1_word_exact(f + 8, d);
-                }
+            float2 e;
+            if (!dyn_sg) {
+                sbyte = nvfp4_scale_byte(amax_b, p_t, inv_p);
+                e = dtab[sbyte];
+            } else {
+                // the row's expert scale (the row's 128-row tile belongs to one expert)
+                const float t = q.table[q.tile_expert[r >> 7]];
+                const float sg = q.sg_mode == SG_EXPERT_TABLE ? t : __fdiv_rn(t, 2688.0f);
+                const float p = __fmul_rn(sg, 6.0f);
+                sbyte = nvfp4_scale_byte(amax_b, p, nvfp4_inv_p(p));
+                e = nvfp4_divisor(sbyte, sg, false);
             }
+            float f[8];
+            unpack8(cur.v[0], f);
+            w[0] = nvfp4_word(f, e);
+            unpack8(cur.v[1], f);
+            w[1] = nvfp4_word(f, e);
         } else if (amax_b > 0.0f) {
             const uint32_t u = __float_as_uint(amax_b);
             const int fl = (u >> 23) ? (int)(u >> 23) - 127 : (31 - __clz((int)u)) - 149;
@@ -261,10 +269,148 @@ __global__ void __launch_bounds__(QT) quant_kernel(const QuantLaunch q) {
     }
 }
 
+// ------------------------------------- NVFP4, one global scale, rows as given
+
+// E2M1 codes of the 8 elements of v times rd, rounded products (a divisor
+// whose table entry proves them exact); paired fp32 multiplies.
+__device__ __forceinline__ uint32_t e2m1_word_rd(const uint4& v, float rd) {
+    const float2 r2 = make_float2(rd, rd);
+    const float2 a = __fmul2_rn(make_float2(bf16lo(v.x), bf16hi(v.x)), r2);
+    const float2 b = __fmul2_rn(make_float2(bf16lo(v.y), bf16hi(v.y)), r2);
+    const float2 c = __fmul2_rn(make_float2(bf16lo(v.z), bf16hi(v.z)), r2);
+    const float2 d = __fmul2_rn(make_float2(bf16lo(v.w), bf16hi(v.w)), r2);
+    return cvt_e2m1x8(a.x, a.y, b.x, b.y, c.x, c.y, d.x, d.y);
+}
+
+// The codes of a block whose divisor is not proven for the product path
+// (bracket or division; rare), out of line.
+__device__ __noinline__ uint2 nvfp4_block_slow(uint4 v0, uint4 v1, float2 e) {
+    float f[8];
+    unpack8(v0, f);
+    const uint32_t w0 = nvfp4_word(f, e);
+    unpack8(v1, f);
+    return make_uint2(w0, nvfp4_word(f, e));
+}
+
+constexpr int QU = 4;        // row groups per thread per iteration: all their loads go out first
+constexpr int QNV_CTAS = 3;  // resident CTAs per SM (register budget of quant_nv_kernel)
+
+// The NVFP4 quantiser for a tensor with one global scale (static, or dynamic
+// from the abs-max partials) and no row map: the dense linear's activations,
+// the MoE hidden states, weight prepack.  Same thread layout as quant_kernel
+// (a thread per 16-element block, `rpi` rows x `bpt` blocks per CTA step);
+// a CTA walks a contiguous range of row groups, QU at a time with all their
+// loads issued before any is converted, and takes the divisor of each scale
+// byte from its table.
+__global__ void __launch_bounds__(QT, QNV_CTAS) quant_nv_kernel(const QuantLaunch q) {
+    __shared__ uint32_t red[QT / 32];
+    __shared__ float sh_sg;
+    __shared__ float2 dtab[128];
+    pdl_wait();
+    pdl_launch_dependents();
+
+    const int nb = (int)sf_cols_padded(q.k, 16);  // scale blocks per row, padding included
+    const int kblocks = (int)(q.k / 16);
+    const int bpt = nb < QT ? (nb + 31) / 32 * 32 : QT;
+    const int rpi = QT / bpt;  // 1, 2, 4 or 8: divides rows_pad (a multiple of 128)
+    const int ty = threadIdx.x / bpt, tx = threadIdx.x - ty * bpt;
+    // this CTA's row groups (rpi rows each): a contiguous range
+    const uint32_t groups = (uint32_t)(q.rows_pad / rpi);
+    const uint32_t per = (groups + gridDim.x - 1) / gridDim.x;
+    const uint32_t g_begin = blockIdx.x * per;
+    const uint32_t g_end = min(groups, g_begin + per);
+    const bool active = ty < rpi && g_begin < g_end;
+    const uint32_t rows = (uint32_t)q.rows;
+    const uint32_t xstep = (uint32_t)(rpi * q.x_ld);  // elements between a thread's rows
+    const uint32_t cstep = (uint32_t)(rpi * (q.k / 2));
+    const uint32_t tile_sf = (uint32_t)nb * 128u;  // scale bytes per 128-row tile
+
+    uint4 v[QU][2];
+    auto load = [&](uint32_t g, uint32_t r, const uint16_t* px, bool bdata) {
+#pragma unroll
+        for (int j = 0; j < QU; ++j) {
+            v[j][0] = v[j][1] = make_uint4(0u, 0u, 0u, 0u);
+            if (g + j < g_end && r + j * rpi < rows && bdata) {
+                const uint4* pv = reinterpret_cast<const uint4*>(px + j * xstep);
+                v[j][0] = __ldg(pv);
+                v[j][1] = __ldg(pv + 1);
+            }
+        }
+    };
+    // the first batch of rows is in flight while the global scale and the
+    // divisor table are formed (neither is needed to load)
+    const uint32_t r_first = g_begin * rpi + ty;
+    if (active) load(g_begin, r_first, q.x + (size_t)r_first * (size_t)q.x_ld + (size_t)tx * 16, tx < kblocks);
+
+    float sg = q.static_scale;
+    if (q.sg_mode == SG_PARTIALS) {
+        uint32_t m = 0;
+        for (int i = threadIdx.x; i < q.n_partials; i += QT) m = max(m, __float_as_uint(q.partials[i]));
+        m = block_max_u32(m, red);
+        if (threadIdx.x == 0) sh_sg = __fdiv_rn(__uint_as_float(m), 2688.0f);
+        __syncthreads();
+        sg = sh_sg;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0 && q.global_out) *q.global_out = sg;
+    if (threadIdx.x < 128) dtab[threadIdx.x] = nvfp4_divisor(threadIdx.x, sg, true);
+    const float p = __fmul_rn(sg, 6.0f);
+    const float inv_p = nvfp4_inv_p(p);
+    __syncthreads();
+    if (!active) return;
+
+    bool first = true;
+    for (int b = tx; b < nb; b += bpt) {
+        const bool bdata = b < kblocks;
+        const uint32_t sf_col = (uint32_t)(b >> 2) * 512u + (uint32_t)(b & 3);
+        uint32_t r = r_first;
+        const uint16_t* px = q.x + (size_t)r * (size_t)q.x_ld + (size_t)b * 16;
+        uint8_t* pc = q.codes + (size_t)r * (size_t)(q.k / 2) + (size_t)b * 8;
+        for (uint32_t g = g_begin; g < g_end; g += QU) {
+            if (!first) load(g, r, px, bdata);
+            first = false;
+#pragma unroll
+            for (int j = 0; j < QU; ++j) {
+                if (g + j >= g_end) break;
+                const uint32_t rj = r + j * rpi;
+                const uint32_t am = absmax8(v[j][1], absmax8(v[j][0], 0u));
+                const float amax_b = __uint_as_float(max(am & 0xFFFFu, am >> 16) << 16);
+                const uint32_t sbyte = nvfp4_scale_byte(amax_b, p, inv_p);
+                const float2 e = dtab[sbyte];
+                uint2 w = make_uint2(0u, 0u);
+                if (e.y > 0.0f)
+                    w = make_uint2(e2m1_word_rd(v[j][0], e.y), e2m1_word_rd(v[j][1], e.y));
+                else if (e.x != 0.0f)
+                    w = nvfp4_block_slow(v[j][0], v[j][1], e);
+                if (rj < rows && bdata) *reinterpret_cast<uint2*>(pc + j * cstep) = w;
+                q.scales[(rj >> 7) * tile_sf + ((rj & 31u) << 4) + (((rj >> 5) & 3u) << 2) + sf_col] = (uint8_t)sbyte;
+            }
+            r += QU * rpi;
+            px += QU * xstep;
+            pc += QU * cstep;
+        }
+    }
+}
+
 cudaError_t launch_quant(const QuantLaunch& q, cudaStream_t s) {
     const DeviceInfo* d = current_device();
     const int sms = d ? d->sm_count : 148;
     const int blk = q.fmt == FP4_MXFP4 ? 32 : 16;
+    const int64_t nb16 = sf_cols_padded(q.k, 16);
+    // quant_nv_kernel keeps rows, row steps and scale offsets in 32 bits
+    const bool fits32 = q.rows_pad < (1LL << 31) && q.x_ld * 8 < (1LL << 32) && q.rows_pad * nb16 < (1LL << 32);
+    const bool one_scale = q.fmt == FP4_NVFP4 && (q.sg_mode == SG_STATIC || q.sg_mode == SG_PARTIALS) && !q.row_map &&
+                           !q.rows_dev && fits32;
+    if (one_scale) {
+        const int64_t nb = nb16;
+        const int64_t bpt = nb < QT ? (nb + 31) / 32 * 32 : QT;
+        const int64_t groups = q.rows_pad / (QT / bpt);
+        int64_t blocks = (groups + QU - 1) / QU;
+        if (blocks > (int64_t)sms * QNV_CTAS) blocks = (int64_t)sms * QNV_CTAS;
+        if (blocks < 1) blocks = 1;
+        QuantLaunch qq = q;
+        void* args[] = {(void*)&qq};
+        return launch_ex((const void*)quant_nv_kernel, dim3((unsigned)blocks), dim3(QT), 0, q.pdl, s, args);
+    }
     const int64_t nb = sf_cols_padded(q.k, blk);
     const int64_t bpt = nb < QT ? (nb + 31) / 32 * 32 : QT;
     const int64_t rpi = QT / bpt;

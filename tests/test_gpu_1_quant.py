@@ -49,7 +49,7 @@ def test_random_normal(F, O, rows, k, fmt):
     check_quant(F, O, I.randn_bf16((rows, k), rows * 7 + k), fmt)
 
 
-@pytest.mark.parametrize("st", [1.0, 0.01, 3.0e-3, 1e-30])
+@pytest.mark.parametrize("st", [1.0, 0.01, 3.0e-3, 1e-30, 5.5 / 2688])
 def test_nvfp4_static(F, O, st):
     check_quant(F, O, I.randn_bf16((64, 512), 5), 0, mode=1, st=st)
 
@@ -95,6 +95,31 @@ def _adversarial(k=512):
 @pytest.mark.parametrize("fmt,mode,st", [(0, 0, 0.0), (0, 1, 1.0), (1, 0, 0.0)])
 def test_adversarial(F, O, fmt, mode, st):
     check_quant(F, O, _adversarial(), fmt, mode, st)
+
+
+def _every_bf16_magnitude(rows, seed):
+    """Rows of 4096: every bf16 value of magnitude in [2^-8, 2^8) with both
+    signs, each row a seeded permutation (so blocks mix binades)."""
+    mags = ((1.0 + np.arange(128)[None, :] / 128.0) * 2.0 ** np.arange(-8, 8)[:, None]).ravel()
+    vals = np.concatenate([mags, -mags]).astype(np.float32)  # 8 significant bits: exact in bf16
+    rng = np.random.default_rng(seed)
+    return torch.from_numpy(np.stack([rng.permutation(vals) for _ in range(rows)])).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("part", range(4))
+def test_nvfp4_global_scale_sweep(F, O, part):
+    """Global scales A / 2688 for every bf16 significand A, as a static scale
+    and as the dynamic scale of a tensor whose abs-max is A: the divisors
+    d = s_b s_g of some of these put E2M1 midpoints times d on bf16 values
+    (the codes then come from the bracket or from divisions), the rest take
+    the one-multiply path.  Every code and scale byte must match the oracle."""
+    x = _every_bf16_magnitude(4, part)
+    for a in range(part * 32, part * 32 + 32):
+        amax = 256.0 + 2.0 * a  # a bf16 value above every element of x
+        check_quant(F, O, x, 0, mode=1, st=float(np.float32(amax / 2688.0)))
+        xd = x.clone()
+        xd[a % 4, (a * 37) % 4096] = -amax
+        check_quant(F, O, xd, 0)
 
 
 def test_all_zero_tensor(F, O):
