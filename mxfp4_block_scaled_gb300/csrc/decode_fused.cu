@@ -125,6 +125,9 @@ __global__ void __launch_bounds__(512, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    // the next kernel may be scheduled now (its weight stream overlaps this
+    // one's tail); it waits for this grid's completion before reading the output
+    pdl_launch_dependents();
 
     const int64_t tile = blockIdx.x;  // 128 weight rows
     const int64_t kbt = (a.k + 255) / 256;
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(512, 1)
         // NVFP4: the divisor entry of each scale byte (nvfp4_divisor)
         const float p_t = __fmul_rn(sg, 6.0f);
         const float inv_p = nvfp4_inv_p(p_t);
-        if (!MX && ta < 128) dtab[ta] = nvfp4_divisor((uint32_t)ta, sg, true);
+        if (!MX && ta < 128) dtab[ta] = nvfp4_divisor((uint32_t)ta, sg, false);
         named_bar_sync(1, NT);
         constexpr int LPB = MX ? 4 : 2;  // lanes per block
         const uint32_t cpr = (uint32_t)(a.k / 8);  // chunks per row
@@ -412,7 +415,6 @@ __global__ void __launch_bounds__(512, 1)
 
     tc_fence_before();
     __syncthreads();
-    pdl_launch_dependents();
     if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);

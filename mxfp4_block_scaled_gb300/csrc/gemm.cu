@@ -85,7 +85,10 @@ static cudaError_t launch_one(const GemmLaunch& g, cudaStream_t s) {
     const DeviceInfo* d = current_device();
     if (!d) return cudaErrorNoDevice;
     int64_t units;
-    if (g.grouped) {
+    if (epi_swapped_grouped<EPI>()) {
+        // upper bound: every 128-row token tile of the capacity, every sub-tile
+        units = ((g.q_rows + 127) / 128) * (128 / BN) * (g.p_rows_valid / 128);
+    } else if (g.grouped) {
         // upper bound: every padded 128-row tile of the capacity
         units = ((g.p_rows + 127) / 128) * ((g.q_rows_valid + BN - 1) / BN) * g.splits;
     } else {
@@ -207,6 +210,8 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
             break;
         case EPI_SWIGLU:
         case EPI_COMBINE:
+        case EPI_SWIGLU_T:
+        case EPI_COMBINE_T:
             return launch_gemm_moe(g, s);
     }
     set_error("no GEMM instantiation for epilogue %d, BN %d", g.epi, g.bn);
@@ -217,6 +222,8 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
 // template's code in one place; moe.cu only builds the launch records).
 cudaError_t launch_gemm_moe(const GemmLaunch& g, cudaStream_t s) {
     if (g.fmt != FP4_NVFP4) return cudaErrorInvalidValue;
+    if (g.epi == EPI_SWIGLU_T && g.bn == 32) return launch_one<32, false, EPI_SWIGLU_T>(g, s);
+    if (g.epi == EPI_COMBINE_T && g.bn == 32) return launch_one<32, false, EPI_COMBINE_T>(g, s);
     if (g.epi == EPI_SWIGLU) {
         if (g.bn == 256) return launch_one<256, false, EPI_SWIGLU>(g, s);
         if (g.bn == 128) return launch_one<128, false, EPI_SWIGLU>(g, s);
@@ -234,6 +241,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4* __rest
                                                             const float* ga, const float* gw, int mx,
                                                             uint2* __restrict__ out) {
     pdl_wait();
+    pdl_launch_dependents();
     const float alpha = mx ? 1.0f : __fmul_rn(gw[0], ga[0]);
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < mn4; i += (int64_t)gridDim.x * blockDim.x) {
         float4 a = part[i];
@@ -247,7 +255,6 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4* __rest
         out[i] = make_uint2(pack_bf16x2(__fmul_rn(alpha, a.x), __fmul_rn(alpha, a.y)),
                             pack_bf16x2(__fmul_rn(alpha, a.z), __fmul_rn(alpha, a.w)));
     }
-    pdl_launch_dependents();
 }
 
 cudaError_t launch_splitk_reduce(const float* part, int splits, int64_t m, int64_t n, const float* ga,

@@ -54,9 +54,30 @@ constexpr int epi_buffer_bytes() {
     return 128 * BOXC * 2;
 }
 
+// EPI_SWIGLU_T: the gate halves handed to the up warps, per unit parity and
+// warp pair, 32 rows x 32 columns of fp32.
+constexpr int kSwigluXBytes = 2 * 2 * 32 * 32 * 4;
+
+template <int EPI>
+constexpr bool epi_swapped_grouped() {
+    return EPI == EPI_SWIGLU_T || EPI == EPI_COMBINE_T;
+}
+
+template <int EPI>
+constexpr bool epi_grouped() {
+    return EPI == EPI_SWIGLU || EPI == EPI_COMBINE || epi_swapped_grouped<EPI>();
+}
+
+// Grouped GEMMs: a CTA's first kUnitTable units' (expert, end of real token
+// rows), read once after the dependency wait; the roles look them up in
+// shared memory instead of each waiting on global loads per unit.
+constexpr int kUnitTable = 64;
+constexpr int kUnitTableBytes = kUnitTable * 8;
+
 template <int EPI, bool MX>
 constexpr int epi_staging_bytes() {
-    return EPI == EPI_BF16 ? 2 * epi_buffer_bytes<epi_box_cols<MX>()>() : 0;
+    return (EPI == EPI_BF16 ? 2 * epi_buffer_bytes<epi_box_cols<MX>()>() : EPI == EPI_SWIGLU_T ? kSwigluXBytes : 0) +
+           (epi_grouped<EPI>() ? kUnitTableBytes : 0);
 }
 
 template <int BN, bool MX, int STG = 0>
@@ -72,7 +93,10 @@ struct GemmCfg {
     static constexpr int SFQ_BYTES = SF_CHUNKS * 512 * QCH;
     static constexpr int OP_BYTES = P_BYTES + Q_BYTES;     // operand stage
     static constexpr int SF_BYTES = SFP_BYTES + SFQ_BYTES;  // scale slot
-    static constexpr int ACC = BN <= 128 ? 2 : 1;
+    // TMEM accumulator stages: the MMAs run up to ACC - 1 units ahead of the
+    // epilogue (four at BN = 32, where a unit's K loop can be shorter than its
+    // epilogue: the grouped GEMM2 with K = 768)
+    static constexpr int ACC = BN <= 32 ? 4 : BN <= 128 ? 2 : 1;
     static constexpr int SFP_COLS = SF_CHUNKS * 4;
     static constexpr int SFQ_COLS = SF_CHUNKS * 4 * QCH;
     static constexpr int SF_COLS = SFP_COLS + SFQ_COLS;
@@ -93,18 +117,20 @@ struct GemmCfg {
     static_assert(STAGES >= 2 && SSLOTS >= 2, "pipeline too shallow");
     static_assert(P_BYTES % 512 == 0 && Q_BYTES % 512 == 0, "64-byte swizzle atoms are 512 bytes");
     static_assert(SMEM <= SMEM_LIMIT, "shared memory budget");
-    static_assert(2 * STAGES + 2 * SSLOTS + 5 <= BAR_BYTES / 8 - 2, "barrier area too small");
+    static_assert(2 * STAGES + 2 * SSLOTS + 2 * ACC + 1 <= BAR_BYTES / 8 - 2, "barrier area too small");
     static_assert(ACC * BN + STAGES * SF_COLS <= 512, "TMEM budget");
 };
 
 // Work unit -> tile coordinates.
 struct Unit {
-    int64_t pt, qt;   // P tile, Q tile (within the expert when grouped)
+    int64_t pt, qt;   // P tile, Q tile (within the expert when grouped); swapped grouped: token tile, weight tile
     int s;            // split index
     int e;            // expert (grouped) or 0
     int64_t p_row0;   // first P row
     int64_t q_row0;   // first Q row in the Q tensor
     int64_t kb0, kb1; // K-block range
+    bool empty;       // swapped grouped: the token sub-tile holds no token (every role skips it)
+    int64_t vend;     // grouped: end of the real rows of the unit's 128-row token tile
 };
 
 struct Sched {
@@ -112,28 +138,73 @@ struct Sched {
     int splits;
 };
 
-template <int BN>
+// Swapped grouped schedule: units = (128 / BN) sub-tiles x token tiles x the
+// expert's weight tiles, weight tile fastest (the CTAs that share a token
+// sub-tile run together and find it in L2) and sub-tile slowest: with a few
+// tokens per expert the later sub-tiles are empty, so the units with work come
+// first and the grid stride spreads them evenly over the CTAs.
+template <int BN, int EPI>
 __device__ __forceinline__ Sched make_sched(const GemmLaunch& g) {
     Sched s;
     s.kbt = (g.k + 2 * GEMM_KB_BYTES - 1) / (2 * GEMM_KB_BYTES);
     s.splits = g.splits;
     s.kb_per = (s.kbt + g.splits - 1) / g.splits;
-    s.n_ptiles = g.grouped ? (int64_t)(*g.n_ptiles_dev) : (g.p_rows_valid + 127) / 128;
-    s.n_qtiles = (g.q_rows_valid + BN - 1) / BN;
-    s.units = s.n_ptiles * s.n_qtiles * g.splits;
+    if constexpr (epi_swapped_grouped<EPI>()) {
+        s.n_ptiles = (int64_t)g.n_ptiles_dev[0];  // token tiles
+        s.n_qtiles = g.p_rows_valid / 128;         // weight tiles per expert
+        // sub-tiles per token tile: no tile holds more than n_ptiles_dev[1]
+        const int64_t subs = min((int64_t)(128 / BN), max((int64_t)1, (int64_t)g.n_ptiles_dev[1]));
+        s.units = s.n_ptiles * subs * s.n_qtiles;
+    } else {
+        s.n_ptiles = epi_grouped<EPI>() ? (int64_t)(*g.n_ptiles_dev) : (g.p_rows_valid + 127) / 128;
+        s.n_qtiles = (g.q_rows_valid + BN - 1) / BN;
+        s.units = s.n_ptiles * s.n_qtiles * g.splits;
+    }
     return s;
 }
 
-template <int BN>
-__device__ __forceinline__ Unit decode_unit(const GemmLaunch& g, const Sched& sc, int64_t u) {
+// The expert and real-row end of token tile pt: from the CTA's unit table
+// when unit u is among its first kUnitTable, else from global memory.
+__device__ __forceinline__ void unit_tile_info(const GemmLaunch& g, const int32_t* ut, int64_t u, int64_t pt,
+                                               int& e, int64_t& vend) {
+    const uint32_t j = (uint32_t)(u - blockIdx.x) / gridDim.x;
+    if (ut && j < (uint32_t)kUnitTable) {
+        e = ut[2 * j];
+        vend = ut[2 * j + 1];
+    } else {
+        e = g.tile_expert[pt];
+        vend = g.row_valid_end[pt];
+    }
+}
+
+template <int BN, int EPI>
+__device__ __forceinline__ Unit decode_unit(const GemmLaunch& g, const Sched& sc, int64_t u,
+                                            const int32_t* ut = nullptr) {
     Unit w;
+    w.empty = false;
+    w.vend = 0;
+    if constexpr (epi_swapped_grouped<EPI>()) {
+        w.s = 0;
+        w.qt = u % sc.n_qtiles;
+        const int64_t r = u / sc.n_qtiles;
+        w.pt = r % sc.n_ptiles;
+        const int sub = (int)(r / sc.n_ptiles);
+        unit_tile_info(g, ut, u, w.pt, w.e, w.vend);
+        w.q_row0 = w.pt * 128 + sub * BN;
+        w.p_row0 = (int64_t)w.e * g.p_rows_valid + w.qt * 128;
+        w.kb0 = 0;
+        w.kb1 = sc.kbt;
+        w.empty = w.q_row0 >= w.vend;
+        return w;
+    }
     w.s = (int)(u % sc.splits);
     const int64_t r = u / sc.splits;
     w.pt = r % sc.n_ptiles;
     w.qt = r / sc.n_ptiles;
-    w.e = g.grouped ? g.tile_expert[w.pt] : 0;
+    w.e = 0;
+    if constexpr (epi_grouped<EPI>()) unit_tile_info(g, ut, u, w.pt, w.e, w.vend);
     w.p_row0 = w.pt * 128;
-    w.q_row0 = (g.grouped ? (int64_t)w.e * g.q_rows_valid : 0) + w.qt * BN;
+    w.q_row0 = (epi_grouped<EPI>() ? (int64_t)w.e * g.q_rows_valid : 0) + w.qt * BN;
     w.kb0 = (int64_t)w.s * sc.kb_per;
     w.kb1 = w.kb0 + sc.kb_per < sc.kbt ? w.kb0 + sc.kb_per : sc.kbt;
     return w;
@@ -218,8 +289,8 @@ __global__ void __launch_bounds__(512, 1)
     uint64_t* sfull = bars + 2 * C::STAGES;                // scale atoms of the slot landed in smem
     uint64_t* sempty = sfull + C::SSLOTS;                  // the writers are done with the slot's smem
     uint64_t* accf = sempty + C::SSLOTS;
-    uint64_t* acce = accf + 2;
-    uint64_t* drain = acce + 2;
+    uint64_t* acce = accf + C::ACC;
+    uint64_t* drain = acce + C::ACC;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
@@ -233,7 +304,7 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(sfull + s, 1);
             mbar_init(sempty + s, 4);
         }
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < C::ACC; ++a) {
             mbar_init(accf + a, 1);
             mbar_init(acce + a, 8);
         }
@@ -252,13 +323,37 @@ __global__ void __launch_bounds__(512, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    // the next kernel may be scheduled now: it waits for this grid's completion
+    // before reading anything this grid writes
+    pdl_launch_dependents();
 
     // Programmatic dependent launch: a grouped GEMM's schedule comes from the
     // preceding kernels, so every role waits here; otherwise each role waits
     // just before its first read of their outputs (the weight producer not at
     // all when early_p / early_q marks its operand).
     if (g.grouped) pdl_wait();
-    const Sched sc = make_sched<BN>(g);
+    const Sched sc = make_sched<BN, EPI>(g);
+    const int32_t* ut = nullptr;  // grouped: this CTA's unit table (expert, real-row end)
+    if constexpr (epi_grouped<EPI>()) {
+        int32_t* t = reinterpret_cast<int32_t*>(sStg + epi_staging_bytes<EPI, MX>() - kUnitTableBytes);
+        for (int j = threadIdx.x; j < kUnitTable; j += blockDim.x) {
+            const int64_t u = blockIdx.x + (int64_t)j * gridDim.x;
+            int32_t e = 0, vend = 0;
+            if (u < sc.units) {
+                int64_t pt;
+                if constexpr (epi_swapped_grouped<EPI>())
+                    pt = (u / sc.n_qtiles) % sc.n_ptiles;
+                else
+                    pt = (u / sc.splits) % sc.n_ptiles;
+                e = g.tile_expert[pt];
+                vend = g.row_valid_end[pt];
+            }
+            t[2 * j] = e;
+            t[2 * j + 1] = vend;
+        }
+        __syncthreads();
+        ut = t;
+    }
     const int64_t ksfc = (g.k + 255) / 256 * (MX ? 2 : 4);      // scale atoms per 128-row tile (K padded to 256)
     const int64_t q_chunks_total = (g.q_rows + 127) / 128;      // 128-row scale tiles of Q
 
@@ -268,7 +363,8 @@ __global__ void __launch_bounds__(512, 1)
         int stage = 0, slot = 0;  // operand stage (TMEM scale columns), scale ring slot
         uint32_t ph = 0, sph = 0;
         for (int64_t u = blockIdx.x; u < sc.units; u += gridDim.x) {
-            const Unit w = decode_unit<BN>(g, sc, u);
+            const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
+            if (w.empty) continue;
             bool ok = true;
             for (int64_t kb = w.kb0; kb < w.kb1; ++kb) {
                 // the slot's atoms are in smem, and the MMAs of the stage's
@@ -324,7 +420,8 @@ __global__ void __launch_bounds__(512, 1)
             uint32_t issued = 0, issued_ph = 0;  // per-stage bits: a copy was issued / its phase parity
             bool ok = true;
             for (int64_t u = blockIdx.x; u < sc.units && ok; u += gridDim.x) {
-                const Unit w = decode_unit<BN>(g, sc, u);
+                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
+                if (w.empty) continue;
                 const uint8_t* sfp = g.p_scales + (w.p_row0 >> 7) * ksfc * 512;
                 const int64_t qc0 = w.q_row0 >> 7;
                 for (int64_t kb = w.kb0; kb < w.kb1; ++kb) {
@@ -383,7 +480,8 @@ __global__ void __launch_bounds__(512, 1)
             uint32_t aph = 0;
             bool ok = true, any = false;
             for (int64_t u = blockIdx.x; u < sc.units && ok; u += gridDim.x) {
-                const Unit w = decode_unit<BN>(g, sc, u);
+                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
+                if (w.empty) continue;
                 if (!mbar_wait(acce + acc, aph ^ 1u, wc, abort_flag)) {
                     ok = false;
                     break;
@@ -426,10 +524,8 @@ __global__ void __launch_bounds__(512, 1)
                 }
                 if (!ok) break;
                 mma_commit(accf + acc);
-                if (C::ACC == 2) {
-                    acc ^= 1;
-                    if (acc == 0) aph ^= 1u;
-                } else {
+                if (++acc == C::ACC) {
+                    acc = 0;
                     aph ^= 1u;
                 }
             }
@@ -446,7 +542,7 @@ __global__ void __launch_bounds__(512, 1)
         // (w - 8) / 4.  Each pulls all its accumulator columns into registers
         // (back-to-back tcgen05.ld, one wait), releases the accumulator stage
         // at once, then converts and stores while the next tile's MMAs run.
-        constexpr int GRAN = EPI == EPI_SWIGLU ? 64 : 32;
+        constexpr int GRAN = EPI == EPI_SWIGLU ? 64 : epi_swapped_grouped<EPI>() ? 16 : 32;
         constexpr int CPW = BN / 2 > GRAN ? BN / 2 : GRAN;  // columns per warp
         constexpr int NLD = CPW / 32;
         static_assert(EPI != EPI_COMBINE || CPW <= 64, "fp32 combine keeps its columns in registers");
@@ -458,7 +554,22 @@ __global__ void __launch_bounds__(512, 1)
         bool store_pending = false;  // EPI_BF16: this thread issued a TMA store not yet waited for
         int acc = 0;
         uint32_t aph = 0;
+        uint32_t n_done = 0;  // units converted by this warp (EPI_SWIGLU_T buffer parity)
         for (int64_t u = blockIdx.x; u < sc.units; u += gridDim.x) {
+            int pf_tok = 0;       // EPI_COMBINE_T: lane i < 16 holds column i's token and routing
+            float pf_w = 0.0f;    // weight, fetched before the wait for the MMAs
+            if constexpr (epi_swapped_grouped<EPI>()) {
+                const Unit wp = decode_unit<BN, EPI>(g, sc, u, ut);
+                if (wp.empty) continue;
+                if constexpr (EPI == EPI_COMBINE_T) {
+                    const int64_t row = wp.q_row0 + c_begin + lane;
+                    if (lane < 16 && row < wp.vend) {
+                        const int slot = g.row_src[row];
+                        pf_tok = slot / g.top_k;
+                        pf_w = g.slot_weight[slot];
+                    }
+                }
+            }
             if (!mbar_wait(accf + acc, aph, wc, abort_flag)) break;
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(acc * BN + c_begin);
@@ -482,7 +593,7 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce + acc);
-                const Unit w = decode_unit<BN>(g, sc, u);
+                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
                 constexpr int BOXC = epi_box_cols<MX>();
                 epi_store_bf16<NLD, BOXC>(&tmO, smem_u32(sStg) + (uint32_t)(wg * epi_buffer_bytes<BOXC>()), pk, qd, lane,
                                     1u + (uint32_t)wg, w.qt * BN + c_begin, w.p_row0, g.q_rows_valid,
@@ -497,7 +608,7 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce + acc);
-                const Unit w = decode_unit<BN>(g, sc, u);
+                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
                 const int64_t prow = w.p_row0 + qd * 32 + lane;
                 const float alpha = MX ? 1.0f : __fmul_rn(g.p_global[0], g.q_global[0]);
                 if (has_cols && prow < g.p_rows_valid) {
@@ -529,7 +640,7 @@ __global__ void __launch_bounds__(512, 1)
             } else if constexpr (EPI == EPI_PARTIAL) {
                 // split-K partials, row-major; only the warps holding real rows
                 // read TMEM (for decode-sized M that is one lane quarter)
-                const Unit w = decode_unit<BN>(g, sc, u);
+                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
                 const int64_t row0 = w.p_row0 + qd * 32;
                 const bool any_rows = has_cols && row0 < g.p_rows_valid;
                 const int64_t prow = row0 + lane;
@@ -561,7 +672,7 @@ __global__ void __launch_bounds__(512, 1)
             } else if constexpr (EPI == EPI_SWIGLU) {
                 // Q rows are W13 rows interleaved in groups of 32 (gate, up, gate, up, ...):
                 // columns [c, c+32) are gate and [c+32, c+64) up for the same 32 features.
-                const Unit w = decode_unit<BN>(g, sc, u);
+                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
                 const int64_t prow = w.p_row0 + qd * 32 + lane;
                 const float alpha =
                     __fmul_rn(g.p_global_per_expert ? g.p_global[w.e] : g.p_global[0], g.q_global[w.e]);
@@ -587,7 +698,7 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce + acc);
-                const bool valid = has_cols && prow < (int64_t)g.row_valid_end[w.pt];
+                const bool valid = has_cols && prow < w.vend;
                 if (valid) {
                     uint16_t* hrow = reinterpret_cast<uint16_t*>(g.out) + prow * g.ldo;
 #pragma unroll
@@ -621,10 +732,10 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce + acc);
-                const Unit w = decode_unit<BN>(g, sc, u);
+                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
                 const int64_t prow = w.p_row0 + qd * 32 + lane;
                 const float alpha = __fmul_rn(g.p_global[w.e], g.q_global[w.e]);
-                const bool valid = has_cols && prow < (int64_t)g.row_valid_end[w.pt];
+                const bool valid = has_cols && prow < w.vend;
                 if (valid) {
                     const int slot = g.row_src[prow];
                     const float sc = __fmul_rn(g.slot_weight[slot], alpha);
@@ -639,11 +750,85 @@ __global__ void __launch_bounds__(512, 1)
                                        __fmul_rn(sc, __uint_as_float(r[j][4 * v + 2])),
                                        __fmul_rn(sc, __uint_as_float(r[j][4 * v + 3])));
                 }
+            } else if constexpr (EPI == EPI_SWIGLU_T) {
+                // P rows are the expert's W13 rows, interleaved in groups of 32
+                // (gate, up, ...): TMEM lane quarters 0 / 1 hold gate / up of
+                // features 64 qt + [0, 32), quarters 2 / 3 of 64 qt + [32, 64);
+                // the 32 columns are the sub-tile's token rows, 16 per warpgroup.
+                // In each gate / up warp pair the gate warp converts the first 8
+                // of its 16 columns and the up warp the last 8; each hands the
+                // other its alpha * acc for the other's columns through smem.
+                static_assert(BN == 32, "16 columns per epilogue warp");
+                uint32_t r[16];
+                tmem_ld16(tb, r);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce + acc);
+                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
+                const float alpha = __fmul_rn(g.q_global[g.q_global_per_expert ? w.e : 0], g.p_global[w.e]);
+                const int pair = qd >> 1, half = wg;
+                const bool is_gate = (qd & 1) == 0;
+                // [parity][half][pair][direction][8 columns][32 lanes]
+                float* xb = reinterpret_cast<float*>(sStg) + ((((n_done & 1u) * 2 + half) * 2 + pair) * 2) * 8 * 32;
+                float* to_up = xb;             // gate of columns 8..15
+                float* to_gate = xb + 8 * 32;  // up of columns 0..7
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (is_gate)
+                        to_up[i * 32 + lane] = __fmul_rn(alpha, __uint_as_float(r[8 + i]));
+                    else
+                        to_gate[i * 32 + lane] = __fmul_rn(alpha, __uint_as_float(r[i]));
+                }
+                named_bar_sync(3u + (uint32_t)(half * 2 + pair), 64);
+                const int64_t f = w.qt * 64 + pair * 32 + lane;
+                const int64_t vend = w.vend;
+                const int64_t row0 = w.q_row0 + c_begin + (is_gate ? 0 : 8);
+                uint16_t* o = reinterpret_cast<uint16_t*>(g.out);
+                uint32_t amax_bits = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float gt = is_gate ? __fmul_rn(alpha, __uint_as_float(r[i])) : to_up[i * 32 + lane];
+                    const float up = is_gate ? to_gate[i * 32 + lane] : __fmul_rn(alpha, __uint_as_float(r[8 + i]));
+                    const int64_t row = row0 + i;
+                    if (row < vend) {
+                        const __nv_bfloat16 hb = __float2bfloat16_rn(__fmul_rn(silu_f32(gt), up));
+                        const uint16_t hbits = *reinterpret_cast<const uint16_t*>(&hb);
+                        o[row * g.ldo + f] = hbits;
+                        amax_bits = max(amax_bits, (uint32_t)(hbits & 0x7FFFu));
+                    }
+                }
+#pragma unroll
+                for (int o2 = 16; o2 > 0; o2 >>= 1) amax_bits = max(amax_bits, __shfl_xor_sync(0xFFFFFFFFu, amax_bits, o2));
+                if (lane == 0 && amax_bits) atomicMax(reinterpret_cast<unsigned int*>(g.amax_out) + w.e, amax_bits << 16);
+                ++n_done;
+            } else if constexpr (EPI == EPI_COMBINE_T) {
+                // P rows are the expert's W2 rows (output features), columns the
+                // sub-tile's token rows (16 per warpgroup):
+                // y[token][feature] += weight * alpha * acc.
+                static_assert(BN == 32, "16 columns per epilogue warp");
+                uint32_t r[16];
+                tmem_ld16(tb, r);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce + acc);
+                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
+                const float alpha = __fmul_rn(g.q_global[w.e], g.p_global[w.e]);
+                const int64_t hd = w.qt * 128 + qd * 32 + lane;
+                const int64_t vend = w.vend;
+                const int64_t row0 = w.q_row0 + c_begin;
+                const float wsc = __fmul_rn(pf_w, alpha);
+                float* y = reinterpret_cast<float*>(g.out) + hd;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int t_i = __shfl_sync(0xFFFFFFFFu, pf_tok, i);
+                    const float s_i = __shfl_sync(0xFFFFFFFFu, wsc, i);
+                    if (row0 + i < vend) atomicAdd(y + (int64_t)t_i * g.ldo, __fmul_rn(s_i, __uint_as_float(r[i])));
+                }
             }
-            if (C::ACC == 2) {
-                acc ^= 1;
-                if (acc == 0) aph ^= 1u;
-            } else {
+            if (++acc == C::ACC) {
+                acc = 0;
                 aph ^= 1u;
             }
         }
@@ -652,7 +837,6 @@ __global__ void __launch_bounds__(512, 1)
 
     tc_fence_before();
     __syncthreads();
-    pdl_launch_dependents();
     if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);

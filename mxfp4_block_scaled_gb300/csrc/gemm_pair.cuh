@@ -124,6 +124,7 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t tmem = *tslot;
 
     pdl_wait();
+    pdl_launch_dependents();  // dependents wait for this grid's completion before reading its output
     const int64_t kbt = (g.k + 255) / 256;
     const int64_t ksfc = kbt * C::SF_CHUNKS;            // scale atoms per 128-row tile
     const int64_t n_pm = (g.p_rows_valid + 255) / 256;  // 256-row pair tiles of P
@@ -350,7 +351,6 @@ __global__ void __launch_bounds__(512, 1)
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // the pair's MMAs, copies and TMEM reads are done in both CTAs
-    pdl_launch_dependents();
     if (warp == 5) {
         tc_fence_after();
         tmem_dealloc_pair(tmem, 512);

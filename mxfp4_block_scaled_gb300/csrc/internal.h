@@ -80,6 +80,10 @@ enum Epi : int {
     EPI_SWIGLU = 3,     // grouped: h[p][f] = bf16(SiLU(gate) * up), amax per expert
     EPI_COMBINE = 4,    // grouped: y[token][q] += weight * alpha * acc (fp32 atomics)
     EPI_PARTIAL = 5,    // part[split][p][q] = acc (fp32, P = activations; alpha applied by the reduction)
+    // grouped with the operands swapped (P = an expert's weight rows, Q = 32-row
+    // tiles of its tokens), for a few tokens per expert:
+    EPI_SWIGLU_T = 6,   // h[q][f] = bf16(SiLU(gate) * up), amax per expert
+    EPI_COMBINE_T = 7,  // y[token of q][p] += weight * alpha * acc (fp32 reductions)
 };
 
 struct GemmLaunch {
@@ -98,18 +102,22 @@ struct GemmLaunch {
     const float* p_global = nullptr;  // NVFP4 global scale(s) of P (per expert when grouped && p_global_per_expert)
     const float* q_global = nullptr;  // NVFP4 global scale(s) of Q (per expert when grouped)
     bool p_global_per_expert = false;
+    bool q_global_per_expert = false;  // EPI_SWIGLU_T / EPI_COMBINE_T: Q (tokens) scale per expert
     // output
     void* out = nullptr;
     int64_t ldo = 0;
     int64_t p_rows_valid = 0;     // rows of P that are real (dense)
     int splits = 1;
-    // grouped (MoE)
+    // grouped (MoE).  The token side is the P operand, or the Q operand with
+    // the swapped epilogues (EPI_SWIGLU_T, EPI_COMBINE_T: P = weights, whose
+    // per-expert row count is p_rows_valid); the tables below always describe
+    // the token rows, in 128-row tiles.
     bool grouped = false;
     int n_experts = 0;
-    const int32_t* tile_expert = nullptr;   // expert of each 128-row P tile
-    const int32_t* n_ptiles_dev = nullptr;  // number of P tiles (device)
-    const int32_t* row_valid_end = nullptr; // per P tile: first padded row index (exclusive end of real rows)
-    const int32_t* row_src = nullptr;       // EPI_COMBINE: source slot (token*k + j) of each P row
+    const int32_t* tile_expert = nullptr;   // expert of each 128-row token tile
+    const int32_t* n_ptiles_dev = nullptr;  // number of token tiles (device)
+    const int32_t* row_valid_end = nullptr; // per token tile: first padded row index (exclusive end of real rows)
+    const int32_t* row_src = nullptr;       // EPI_COMBINE(_T): source slot (token*k + j) of each token row
     const float* slot_weight = nullptr;     // EPI_COMBINE: routing weight of each slot
     int top_k = 0;
     float* amax_out = nullptr;              // EPI_SWIGLU: per-expert amax of h (as uint bits, atomicMax)

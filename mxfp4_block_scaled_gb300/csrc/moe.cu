@@ -103,7 +103,7 @@ static MoeLayout moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
     sz[MS_BITMAP] = E * L.W * 4;
     sz[MS_WPREFIX] = E * L.W * 4;
     sz[MS_TILE_EXPERT] = (L.R / 128) * 4;
-    sz[MS_NPTILES] = 16;
+    sz[MS_NPTILES] = 16;  // [0] token tiles, [1] the most 32-row sub-tiles of a tile
     sz[MS_ROW_VALID_END] = (L.R / 128) * 4;
     sz[MS_ROW_TOK] = L.R * 4;
     sz[MS_PARTIALS] = 4096;
@@ -199,6 +199,7 @@ template <int PER_LANE>
 __global__ void __launch_bounds__(1024) moe_route_kernel(const RouteArgs a, const StaticScales st) {
     extern __shared__ uint32_t sbm[];  // [E] bitmap words of this block's 32 tokens
     pdl_wait();
+    pdl_launch_dependents();  // dependents wait for this grid's completion
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (blockIdx.x == 0) {
         if (a.zero_outputs)
@@ -232,7 +233,6 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const RouteArgs a, cons
         for (int64_t i = ((int64_t)blockIdx.x - a.route_blocks) * 1024 + threadIdx.x; i < n4; i += nb * 1024)
             y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    pdl_launch_dependents();
 }
 
 struct ScanArgs {
@@ -287,7 +287,10 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(const ScanArgs a) {
     __shared__ int32_t pad[kMaxExperts + 1];
     __shared__ int32_t wsum[32];
     __shared__ int32_t tot[2];
+    __shared__ int32_t cmax;  // the largest expert count
     pdl_wait();
+    pdl_launch_dependents();
+    if (threadIdx.x == 0) cmax = 0;  // dependents wait for this grid's completion
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // a warp takes experts warp, warp + 32, ...; their 32-word chunks are
     // walked in order with eight chunks' loads in flight (a chunk's word
@@ -333,6 +336,7 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(const ScanArgs a) {
     {
         const int e = threadIdx.x;  // E <= 1024 = blockDim
         const int32_t c = e < a.E ? cnt[e] : 0;
+        if (c > 0) atomicMax(&cmax, c);
         const int32_t o = block_exclusive_scan_1024(c, wsum, &tot[0]);
         const int32_t p = block_exclusive_scan_1024((c + 127) / 128 * 128, wsum, &tot[1]);
         if (e < a.E) {
@@ -348,6 +352,9 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(const ScanArgs a) {
         }
     }
     __syncthreads();
+    // the most 32-row sub-tiles any 128-row token tile holds (the swapped
+    // grouped GEMMs schedule no sub-tile beyond it)
+    if (threadIdx.x == 0) a.n_ptiles[1] = min(4, (cmax + 31) / 32);
     for (int e = warp; e < a.E; e += 32) {
         const int32_t t0 = pad[e] / 128, t1 = pad[e + 1] / 128;
         for (int32_t t = t0 + lane; t < t1; t += 32) {
@@ -359,13 +366,13 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(const ScanArgs a) {
             a.row_tok[r] = -1;
         }
     }
-    pdl_launch_dependents();
 }
 
 // A thread per assignment (token t, slot s = t * k + j): its row is
 // padded[e] + (tokens before t routed to e), from the bitmap and its prefix.
 __global__ void __launch_bounds__(256) moe_assign_kernel(const ScanArgs a) {
     pdl_wait();
+    pdl_launch_dependents();  // dependents wait for this grid's completion
     const int64_t slots = a.T * a.k;
     for (int64_t s = (int64_t)blockIdx.x * 256 + threadIdx.x; s < slots; s += (int64_t)gridDim.x * 256) {
         const int64_t t = s / a.k;
@@ -376,7 +383,6 @@ __global__ void __launch_bounds__(256) moe_assign_kernel(const ScanArgs a) {
         a.row_src[row] = (int32_t)s;
         a.row_tok[row] = (int32_t)t;
     }
-    pdl_launch_dependents();
 }
 
 // Dispatch of the quantised hidden rows: destination row r (expert-sorted,
@@ -425,20 +431,20 @@ __global__ void __launch_bounds__(256) moe_permute_kernel(const uint8_t* __restr
 __global__ void __launch_bounds__(256) moe_finalize_kernel(const float4* __restrict__ y, uint2* __restrict__ out,
                                                            int64_t n4) {
     pdl_wait();
+    pdl_launch_dependents();  // dependents wait for this grid's completion
     for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n4; i += (int64_t)gridDim.x * 256) {
         const float4 v = y[i];
         __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
         out[i] = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
     }
-    pdl_launch_dependents();
 }
 
 // zero n floats (staged runs)
 __global__ void __launch_bounds__(256) zero_kernel(float4* __restrict__ p, int64_t n4) {
     pdl_wait();
+    pdl_launch_dependents();  // dependents wait for this grid's completion
     for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n4; i += (int64_t)gridDim.x * 256)
         p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    pdl_launch_dependents();
 }
 
 // W13 row interleave for the prepack: destination row r of an expert's
@@ -644,6 +650,10 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
     uint8_t* tok_scales = at(MS_TOK_SCALES);
     const bool is_static = mode == FP4_SCALE_STATIC;
     const bool full = (mask & ST_ALL) == ST_ALL;
+    // A few tokens per expert (at most 16 on average): the grouped GEMMs swap
+    // their operands, so the expert's weight rows fill the 128-row MMA side and
+    // its tokens a 32-column one, instead of padding the tokens to 128 rows.
+    const bool swapped = T * k <= 16 * E;
     bool pdl = false;  // first launch of the call waits for everything before it
 
     // 1. route (+ zeroing of y and amax_h when the whole pipeline runs)
@@ -762,22 +772,38 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         }
         GemmLaunch g;
         g.fmt = FP4_NVFP4;
-        g.epi = EPI_SWIGLU;
-        // the tile width must divide the expert's 2I rows (tiles never straddle
-        // experts); 128 keeps two TMEM accumulators, so the SwiGLU epilogue of
-        // one tile overlaps the next tile's MMAs (with 256 there is one)
-        g.bn = (T * k >= 4 * E * 64 && (2 * I) % 128 == 0) ? 128 : 64;
-        g.p_codes = a_codes;
-        g.p_scales = a_scales;
-        g.p_rows = L.R;
-        g.q_codes = static_cast<const uint8_t*>(w13c);
-        g.q_scales = static_cast<const uint8_t*>(w13s);
-        g.q_rows = E * 2 * I;
-        g.q_rows_valid = 2 * I;
+        if (swapped) {
+            g.epi = EPI_SWIGLU_T;
+            g.bn = 32;
+            g.p_codes = static_cast<const uint8_t*>(w13c);
+            g.p_scales = static_cast<const uint8_t*>(w13s);
+            g.p_rows = E * 2 * I;
+            g.p_rows_valid = 2 * I;
+            g.q_codes = a_codes;
+            g.q_scales = a_scales;
+            g.q_rows = L.R;
+            g.q_rows_valid = L.R;
+            g.p_global = w13g;
+            g.q_global = is_static ? st13 : sg_a;
+            g.q_global_per_expert = is_static;
+        } else {
+            g.epi = EPI_SWIGLU;
+            // the tile width must divide the expert's 2I rows (tiles never straddle
+            // experts); 128 keeps two TMEM accumulators, so the SwiGLU epilogue of
+            // one tile overlaps the next tile's MMAs (with 256 there is one)
+            g.bn = (T * k >= 4 * E * 64 && (2 * I) % 128 == 0) ? 128 : 64;
+            g.p_codes = a_codes;
+            g.p_scales = a_scales;
+            g.p_rows = L.R;
+            g.q_codes = static_cast<const uint8_t*>(w13c);
+            g.q_scales = static_cast<const uint8_t*>(w13s);
+            g.q_rows = E * 2 * I;
+            g.q_rows_valid = 2 * I;
+            g.p_global = is_static ? st13 : sg_a;
+            g.p_global_per_expert = is_static;
+            g.q_global = w13g;
+        }
         g.k = H;
-        g.p_global = is_static ? st13 : sg_a;
-        g.p_global_per_expert = is_static;
-        g.q_global = w13g;
         g.out = h;
         g.ldo = I;
         g.grouped = true;
@@ -831,21 +857,37 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         }
         GemmLaunch g;
         g.fmt = FP4_NVFP4;
-        g.epi = EPI_COMBINE;
-        // the tile width must divide H (output columns of one token row); the
-        // fp32 combine epilogue keeps at most 64 columns per warp in registers
-        g.bn = (T * k >= 4 * E * 64 && H % 128 == 0) ? 128 : 64;
-        g.p_codes = h_codes;
-        g.p_scales = h_scales;
-        g.p_rows = L.R;
-        g.q_codes = static_cast<const uint8_t*>(w2c);
-        g.q_scales = static_cast<const uint8_t*>(w2s);
-        g.q_rows = E * H;
-        g.q_rows_valid = H;
+        if (swapped) {
+            g.epi = EPI_COMBINE_T;
+            g.bn = 32;
+            g.p_codes = static_cast<const uint8_t*>(w2c);
+            g.p_scales = static_cast<const uint8_t*>(w2s);
+            g.p_rows = E * H;
+            g.p_rows_valid = H;
+            g.q_codes = h_codes;
+            g.q_scales = h_scales;
+            g.q_rows = L.R;
+            g.q_rows_valid = L.R;
+            g.p_global = w2g;
+            g.q_global = is_static ? st2 : sg_h;
+            g.q_global_per_expert = true;
+        } else {
+            g.epi = EPI_COMBINE;
+            // the tile width must divide H (output columns of one token row); the
+            // fp32 combine epilogue keeps at most 64 columns per warp in registers
+            g.bn = (T * k >= 4 * E * 64 && H % 128 == 0) ? 128 : 64;
+            g.p_codes = h_codes;
+            g.p_scales = h_scales;
+            g.p_rows = L.R;
+            g.q_codes = static_cast<const uint8_t*>(w2c);
+            g.q_scales = static_cast<const uint8_t*>(w2s);
+            g.q_rows = E * H;
+            g.q_rows_valid = H;
+            g.p_global = is_static ? st2 : sg_h;
+            g.p_global_per_expert = true;
+            g.q_global = w2g;
+        }
         g.k = I;
-        g.p_global = is_static ? st2 : sg_h;
-        g.p_global_per_expert = true;
-        g.q_global = w2g;
         g.out = y;
         g.ldo = H;
         g.grouped = true;
