@@ -29,6 +29,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "quant_math.cuh"
 
 namespace fp4 {
 
@@ -427,6 +428,224 @@ __global__ void __launch_bounds__(256) moe_permute_kernel(const uint8_t* __restr
     }
 }
 
+// ------------------------------------------------ small-T preparation
+
+// For T <= kPrepMaxTokens the route, the expert counts and scans, the row
+// tables and the dispatch-quantisation run in one CTA of 1024 threads (the
+// other CTAs of the launch zero y): at these sizes each is a few microseconds
+// of latency, and one launch replaces six (at T = 64 the one CTA's serial
+// memory round trips already cost more than the six launches).  A 64-bit token mask per expert
+// gives a slot's rank among its expert's tokens directly (rows stay in token
+// order).  Each token's row is quantised once (dynamic scale) and its codes
+// and scale bytes are stored to the rows of its k slots; with static
+// per-expert scales every slot's row is quantised under its expert's scale.
+// The scale bytes of padding rows are not written: only the swapped grouped
+// GEMMs follow this path, and they discard every padding column.
+static constexpr int kPrepMaxTokens = 16;
+
+struct PrepArgs {
+    const float* logits;    // [T][E]
+    const uint16_t* hidden; // [T][H] bf16
+    int64_t T, H;
+    int E, k;
+    int32_t* ids;
+    float* weights;
+    int32_t* offsets;       // [E + 1]
+    int32_t* padded;        // [E + 1]
+    int32_t* n_ptiles;      // [0] token tiles, [1] most 32-row sub-tiles of a tile
+    int32_t* tile_expert;
+    int32_t* row_valid_end;
+    int32_t* row_src;
+    int32_t* row_tok;
+    uint8_t* codes;         // expert-sorted rows [R][H/2]
+    uint8_t* scales;        // their scale bytes, MMA layout
+    float* sg_out;          // dynamic: s_gA
+    int has_static;
+    float* static13_out;
+    float* static2_out;
+    float* amax_h;          // zeroed [E]
+    float* y;               // zeroed [T*H] fp32 by CTAs 1..
+    int64_t y_elems;
+};
+
+template <int PER_LANE>
+__global__ void __launch_bounds__(1024) moe_prep_small_kernel(const PrepArgs a, const StaticScales st) {
+    __shared__ uint64_t tokmask[kMaxExperts];
+    __shared__ int32_t padv[kMaxExperts + 1];
+    __shared__ int32_t s_ids[kPrepMaxTokens * kMaxTopK];
+    __shared__ int32_t s_row[kPrepMaxTokens * kMaxTopK];
+    __shared__ int32_t wsum[32];
+    __shared__ int32_t tot[2];
+    __shared__ int32_t cmax;
+    __shared__ uint32_t red[32];
+    __shared__ float sh_sg;
+    __shared__ float2 dtab[128];
+    pdl_wait();
+    pdl_launch_dependents();  // dependents wait for this grid's completion
+    if (blockIdx.x > 0) {
+        const int64_t nb = (int64_t)gridDim.x - 1;
+        float4* y4 = reinterpret_cast<float4*>(a.y);
+        for (int64_t i = ((int64_t)blockIdx.x - 1) * 1024 + threadIdx.x; i < a.y_elems / 4; i += nb * 1024)
+            y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        return;
+    }
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int E = a.E, k = a.k;
+    const int T = (int)a.T;
+    for (int e = tid; e < E; e += 1024) {
+        tokmask[e] = 0ull;
+        a.amax_h[e] = 0.0f;
+        if (a.has_static) {
+            a.static13_out[e] = st.s13[e];
+            a.static2_out[e] = st.s2[e];
+        }
+    }
+    if (tid == 0) cmax = 0;
+    __syncthreads();
+
+    // 1. route: a warp per token
+    for (int t = warp; t < T; t += 32) {
+        int e;
+        float w;
+        topk_token<PER_LANE>(a.logits + (int64_t)t * E, E, k, lane, e, w);
+        if (lane < k) {
+            a.ids[t * k + lane] = e;
+            a.weights[t * k + lane] = w;
+            s_ids[t * k + lane] = e;
+            atomicOr(reinterpret_cast<unsigned long long*>(&tokmask[e]), 1ull << t);
+        }
+    }
+    __syncthreads();
+
+    // 2. counts, offsets and 128-row padded offsets (thread e)
+    {
+        const int e = tid;
+        const int32_t c = e < E ? __popcll(tokmask[e]) : 0;
+        if (c > 0) atomicMax(&cmax, c);
+        const int32_t o = block_exclusive_scan_1024(c, wsum, &tot[0]);
+        const int32_t p = block_exclusive_scan_1024((c + 127) / 128 * 128, wsum, &tot[1]);
+        if (e < E) {
+            a.offsets[e] = o;
+            a.padded[e] = p;
+            padv[e] = p;
+        }
+        if (e == 0) {
+            a.offsets[E] = tot[0];
+            a.padded[E] = tot[1];
+            padv[E] = tot[1];
+            a.n_ptiles[0] = tot[1] / 128;
+        }
+    }
+    __syncthreads();
+    if (tid == 0) a.n_ptiles[1] = min(4, (cmax + 31) / 32);
+
+    // 3. row tables: tiles, padding rows, and each slot's row (token order)
+    for (int e = warp; e < E; e += 32) {
+        const int32_t c = __popcll(tokmask[e]);
+        const int32_t t0 = padv[e] / 128, t1 = padv[e + 1] / 128;
+        for (int32_t t = t0 + lane; t < t1; t += 32) {
+            a.tile_expert[t] = e;
+            a.row_valid_end[t] = padv[e] + c;
+        }
+        for (int32_t r = padv[e] + c + lane; r < padv[e + 1]; r += 32) {
+            a.row_src[r] = -1;
+            a.row_tok[r] = -1;
+        }
+    }
+    for (int s = tid; s < T * k; s += 1024) {
+        const int t = s / k, e = s_ids[s];
+        const int32_t row = padv[e] + __popcll(tokmask[e] & ((1ull << t) - 1ull));
+        a.row_src[row] = s;
+        a.row_tok[row] = t;
+        s_row[s] = row;
+    }
+
+    // 4. dynamic: s_gA from the abs-max of the T hidden rows, and the divisors
+    const int64_t H = a.H;
+    const int nbp = (int)sf_cols_padded(H, 16);  // scale columns per row (padding included)
+    const int kblocks = (int)(H / 16);
+    if (!a.has_static) {
+        const uint4* xv = reinterpret_cast<const uint4*>(a.hidden);
+        uint32_t m = 0;
+        const int64_t nv = (int64_t)T * H / 8;
+        for (int64_t i = tid; i < nv; i += 4 * 1024) {  // four loads in flight
+            uint4 v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v[q] = i + q * 1024 < nv ? __ldg(xv + i + q * 1024) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) m = absmax8(v[q], m);
+        }
+        m = max(m & 0xFFFFu, m >> 16);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        if (lane == 0) red[warp] = m;
+        __syncthreads();
+        if (tid == 0) {
+            uint32_t v = 0;
+            for (int i = 0; i < 32; ++i) v = max(v, red[i]);
+            sh_sg = __fdiv_rn(__uint_as_float(v << 16), 2688.0f);
+            a.sg_out[0] = sh_sg;
+        }
+        __syncthreads();
+        if (tid < 128) dtab[tid] = nvfp4_divisor((uint32_t)tid, sh_sg, false);
+    }
+    __syncthreads();
+
+    // 5. quantise and dispatch
+    if (!a.has_static) {
+        const float sg = sh_sg;
+        const float p = __fmul_rn(sg, 6.0f);
+        const float inv_p = nvfp4_inv_p(p);
+        for (int item = tid; item < T * nbp; item += 1024) {
+            const int t = item / nbp, b = item - t * nbp;
+            uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+            if (b < kblocks) {
+                const uint4* px = reinterpret_cast<const uint4*>(a.hidden + (int64_t)t * H + (int64_t)b * 16);
+                v0 = __ldg(px);
+                v1 = __ldg(px + 1);
+            }
+            const uint32_t am = absmax8(v1, absmax8(v0, 0u));
+            const uint32_t sbyte = nvfp4_scale_byte(__uint_as_float(max(am & 0xFFFFu, am >> 16) << 16), p, inv_p);
+            const float2 e = dtab[sbyte];
+            float f[8];
+            unpack8(v0, f);
+            const uint32_t w0 = nvfp4_word(f, e);
+            unpack8(v1, f);
+            const uint32_t w1 = nvfp4_word(f, e);
+            for (int j = 0; j < k; ++j) {
+                const int64_t row = s_row[t * k + j];
+                if (b < kblocks) *reinterpret_cast<uint2*>(a.codes + row * (H / 2) + (int64_t)b * 8) = make_uint2(w0, w1);
+                a.scales[sf_offset(row, b, nbp)] = (uint8_t)sbyte;
+            }
+        }
+    } else {
+        for (int item = tid; item < T * k * nbp; item += 1024) {
+            const int s = item / nbp, b = item - s * nbp;
+            const int t = s / k;
+            const float sg = st.s13[s_ids[s]];
+            uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+            if (b < kblocks) {
+                const uint4* px = reinterpret_cast<const uint4*>(a.hidden + (int64_t)t * H + (int64_t)b * 16);
+                v0 = __ldg(px);
+                v1 = __ldg(px + 1);
+            }
+            const uint32_t am = absmax8(v1, absmax8(v0, 0u));
+            const float p = __fmul_rn(sg, 6.0f);
+            const uint32_t sbyte =
+                nvfp4_scale_byte(__uint_as_float(max(am & 0xFFFFu, am >> 16) << 16), p, nvfp4_inv_p(p));
+            const float2 e = nvfp4_divisor(sbyte, sg, false);
+            float f[8];
+            unpack8(v0, f);
+            const uint32_t w0 = nvfp4_word(f, e);
+            unpack8(v1, f);
+            const uint32_t w1 = nvfp4_word(f, e);
+            const int64_t row = s_row[s];
+            if (b < kblocks) *reinterpret_cast<uint2*>(a.codes + row * (H / 2) + (int64_t)b * 8) = make_uint2(w0, w1);
+            a.scales[sf_offset(row, b, nbp)] = (uint8_t)sbyte;
+        }
+    }
+}
+
 // fp32 accumulator -> bf16 output
 __global__ void __launch_bounds__(256) moe_finalize_kernel(const float4* __restrict__ y, uint2* __restrict__ out,
                                                            int64_t n4) {
@@ -654,10 +873,53 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
     // their operands, so the expert's weight rows fill the 128-row MMA side and
     // its tokens a 32-column one, instead of padding the tokens to 128 rows.
     const bool swapped = T * k <= 16 * E;
+    // the whole pipeline for a handful of tokens: one launch prepares it all
+    const bool small_prep = full && swapped && T <= kPrepMaxTokens;
     bool pdl = false;  // first launch of the call waits for everything before it
+    const int per_lane = (int)((E + 31) / 32);
+
+    if (small_prep) {
+        PrepArgs pa;
+        pa.logits = logits;
+        pa.hidden = static_cast<const uint16_t*>(hidden);
+        pa.T = T;
+        pa.H = H;
+        pa.E = (int)E;
+        pa.k = (int)k;
+        pa.ids = ids;
+        pa.weights = wts;
+        pa.offsets = offsets;
+        pa.padded = padded;
+        pa.n_ptiles = n_ptiles;
+        pa.tile_expert = tile_expert;
+        pa.row_valid_end = row_valid_end;
+        pa.row_src = row_src;
+        pa.row_tok = row_tok;
+        pa.codes = a_codes;
+        pa.scales = a_scales;
+        pa.sg_out = sg_a;
+        pa.has_static = is_static ? 1 : 0;
+        pa.static13_out = st13;
+        pa.static2_out = st2;
+        pa.amax_h = amax_h;
+        pa.y = y;
+        pa.y_elems = T * H;
+        StaticScales sc;
+        memset(&sc, 0, sizeof(sc));
+        if (is_static)
+            for (int64_t e = 0; e < E; ++e) sc.s13[e] = s13[e], sc.s2[e] = s2[e];
+        const int zero_blocks = (int)std::min<int64_t>((T * H / 4 + 1023) / 1024, (int64_t)d->sm_count * 2);
+        void* args[] = {(void*)&pa, (void*)&sc};
+        const void* fn = per_lane <= 4    ? (const void*)moe_prep_small_kernel<4>
+                         : per_lane <= 8  ? (const void*)moe_prep_small_kernel<8>
+                         : per_lane <= 16 ? (const void*)moe_prep_small_kernel<16>
+                                          : (const void*)moe_prep_small_kernel<32>;
+        MOE_CUDA(launch_k(fn, dim3(1 + zero_blocks), dim3(1024), 0, pdl, s, args), "prepare launch");
+        pdl = true;
+    }
 
     // 1. route (+ zeroing of y and amax_h when the whole pipeline runs)
-    if (mask & ST_ROUTE) {
+    if ((mask & ST_ROUTE) && !small_prep) {
         RouteArgs ra;
         ra.logits = logits;
         ra.T = T;
@@ -681,7 +943,6 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
             for (int64_t e = 0; e < E; ++e) sc.s13[e] = s13[e], sc.s2[e] = s2[e];
         int zero_blocks = full ? (int)std::min<int64_t>((T * H / 4 + 1023) / 1024, (int64_t)d->sm_count * 2) : 0;
         void* args[] = {(void*)&ra, (void*)&sc};
-        const int per_lane = (int)((E + 31) / 32);
         const void* fn = per_lane <= 4    ? (const void*)moe_route_kernel<4>
                          : per_lane <= 8  ? (const void*)moe_route_kernel<8>
                          : per_lane <= 16 ? (const void*)moe_route_kernel<16>
@@ -711,7 +972,7 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
                  "assign launch");
     }
     // 2-3. hidden amax (dynamic) and quantise into expert-sorted padded rows
-    if (mask & ST_QUANT) {
+    if ((mask & ST_QUANT) && !small_prep) {
         QuantLaunch q;
         q.fmt = FP4_NVFP4;
         q.x = static_cast<const uint16_t*>(hidden);

@@ -144,6 +144,28 @@ def _stage_checks(F, O, c):
     check_close(y, r["y"], r["ymag"], what="y", extra_tau=k * 2.0 ** -23 * r["ymag"])
 
 
+def _prep_checks(O, c, ref=None, dynamic=True):
+    """Route and dispatch-quantise results a full run leaves in the workspace
+    (for a few tokens one launch prepares them): ids, offsets, row order and
+    the expert-sorted rows' codes and scales exact, weights 2e-6 relative."""
+    r = ref if ref is not None else c.ref
+    T, E, k, H = c.T, c.E, c.k, c.H
+    assert np.array_equal(c.view(0, torch.int32, (T, k)).cpu().numpy(), r["ids"])
+    assert np.allclose(c.view(1, torch.float32, (T, k)).cpu().numpy(), r["weights"], rtol=2e-6, atol=0)
+    assert np.array_equal(c.view(2, torch.int32, (E + 1,)).cpu().numpy(), r["offsets"])
+    assert np.array_equal(c.view(3, torch.int32, (E + 1,)).cpu().numpy(), c.padded)
+    rows = c.gpu_rows()
+    row_src = c.view(4, torch.int32, (c.R,)).cpu().numpy()
+    assert np.array_equal(row_src[rows], r["order"])
+    assert np.all(row_src[np.setdiff1d(np.arange(c.padded[-1]), rows)] == -1)
+    codes = c.view(5, torch.uint8, (c.R, H // 2)).cpu().numpy()
+    assert np.array_equal(codes[rows], r["a_codes"])
+    scales = c.view(6, torch.uint8, (c.R * O.scale_cols_padded(H, 0),)).cpu().numpy()
+    assert np.array_equal(O.scales_from_mma(scales, c.R, H, 0)[rows], r["a_scales"])
+    if dynamic:
+        assert np.float32(c.view(7, torch.float32, (E,))[0].item()) == np.float32(r["sgA"])
+
+
 def _end_to_end(F, O, c, max_norm_err=2e-2):
     out = c.run(F)
     y = bf16_to_np(out)
@@ -166,6 +188,7 @@ def test_moe_staged_small(F, O, T, E, k, H, Inter):
     c = Case(F, O, T, E, k, H, Inter, seed=3 + T, std=0.1)
     _stage_checks(F, O, c)
     _end_to_end(F, O, c)
+    _prep_checks(O, c)
 
 
 def test_moe_all_tokens_one_expert(F, O):
@@ -189,6 +212,7 @@ def test_moe_static_scales_and_errors(F, O):
                 static2=st2)
     y = bf16_to_np(out)
     assert np.linalg.norm(y - ref["y"]) / np.linalg.norm(ref["y"]) < 1e-2
+    _prep_checks(O, c, ref=ref, dynamic=False)
     # the zeroed-alpha failure mode is refused: no scales, or a zero scale
     with pytest.raises(F.FP4Error) as e1:
         F.moe(c.hid_d, c.log_d, c.mw, k, mode=1, static13=None, static2=st2, workspace=c.ws)
@@ -249,3 +273,4 @@ def test_moe_full_size(F, O, full_weights, T):
     c.padded = np.concatenate([[0], np.cumsum((c.ref["counts"] + 127) // 128 * 128)]).astype(np.int64)
     _stage_checks(F, O, c)
     _end_to_end(F, O, c)
+    _prep_checks(O, c)
