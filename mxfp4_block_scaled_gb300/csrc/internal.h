@@ -51,6 +51,11 @@ struct QuantLaunch {
     int64_t k = 0;
     const int32_t* row_map = nullptr;  // dest row -> source row (-1: zero row); nullptr = identity
     bool row_map_is_mask = false;      // row_map[r] >= 0 only marks row r as real (source row = r)
+    bool skip_masked_rows = false;     // rows the map marks absent are left untouched (scale bytes too)
+    // with skip_masked_rows and an expert scale: the real rows are those of each
+    // 128-row tile t < *n_tiles_dev below tile_rows_end[t] (the rest are skipped)
+    const int32_t* tile_rows_end = nullptr;
+    const int32_t* n_tiles_dev = nullptr;
     uint8_t* codes = nullptr;
     uint8_t* scales = nullptr;
     int sg_mode = SG_STATIC;

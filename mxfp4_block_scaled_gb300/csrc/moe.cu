@@ -1088,6 +1088,11 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         q.k = I;
         q.row_map = row_tok;
         q.row_map_is_mask = true;
+        // the swapped GEMM2 discards padding columns: their scale bytes need
+        // not be zeroed when the whole pipeline runs
+        q.skip_masked_rows = full && swapped;
+        q.tile_rows_end = row_valid_end;
+        q.n_tiles_dev = n_ptiles;
         q.codes = h_codes;
         q.scales = h_scales;
         q.tile_expert = tile_expert;

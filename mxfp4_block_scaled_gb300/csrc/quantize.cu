@@ -210,6 +210,11 @@ __global__ void __launch_bounds__(QT) quant_kernel(const QuantLaunch q) {
         }
 
         // ---- convert the current item
+        if (q.skip_masked_rows && cur.src < 0) {
+            if (!more) break;
+            cur = nxt;
+            continue;
+        }
         const int64_t r = cur.r;
         const int b = cur.b;
         const bool in = cur.src >= 0 && b < kblocks;
@@ -266,6 +271,54 @@ __global__ void __launch_bounds__(QT) quant_kernel(const QuantLaunch q) {
 
         if (!more) break;
         cur = nxt;
+    }
+}
+
+// ------------------------------ NVFP4, per-expert scale, real rows of tiles
+
+// The MoE requantisation when padding rows may stay untouched: a CTA takes
+// 128-row tiles (one expert each) and only their real rows, so the work
+// follows the tokens rather than the padded capacity; the expert's scale is
+// read once per tile.  Same arithmetic as quant_kernel's expert modes.
+__global__ void __launch_bounds__(QT) quant_tiles_kernel(const QuantLaunch q) {
+    pdl_wait();
+    pdl_launch_dependents();
+    if (blockIdx.x == 0 && q.sg_mode == SG_EXPERT_AMAX && q.expert_sg_out)
+        for (int e = threadIdx.x; e < q.n_experts; e += QT) q.expert_sg_out[e] = __fdiv_rn(q.table[e], 2688.0f);
+    const int nb = (int)sf_cols_padded(q.k, 16);
+    const int kblocks = (int)(q.k / 16);
+    const int bpt = nb < QT ? (nb + 31) / 32 * 32 : QT;
+    const int rpi = QT / bpt;
+    const int ty = threadIdx.x / bpt, tx = threadIdx.x - ty * bpt;
+    if (ty >= rpi) return;
+    const int64_t ntiles = *q.n_tiles_dev;
+    const int64_t cb = q.k / 2;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        const float tv = q.table[q.tile_expert[t]];
+        const float sg = q.sg_mode == SG_EXPERT_TABLE ? tv : __fdiv_rn(tv, 2688.0f);
+        const float p = __fmul_rn(sg, 6.0f);
+        const float inv_p = nvfp4_inv_p(p);
+        const int64_t rend = q.tile_rows_end[t];
+        for (int64_t r = t * 128 + ty; r < rend; r += rpi) {
+            for (int b = tx; b < nb; b += bpt) {
+                uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+                if (b < kblocks) {
+                    const uint4* px = reinterpret_cast<const uint4*>(q.x + r * q.x_ld + (int64_t)b * 16);
+                    v0 = __ldg(px);
+                    v1 = __ldg(px + 1);
+                }
+                const uint32_t am = absmax8(v1, absmax8(v0, 0u));
+                const uint32_t sbyte = nvfp4_scale_byte(__uint_as_float(max(am & 0xFFFFu, am >> 16) << 16), p, inv_p);
+                const float2 e = nvfp4_divisor(sbyte, sg, false);
+                float f[8];
+                unpack8(v0, f);
+                const uint32_t w0 = nvfp4_word(f, e);
+                unpack8(v1, f);
+                const uint32_t w1 = nvfp4_word(f, e);
+                if (b < kblocks) *reinterpret_cast<uint2*>(q.codes + r * cb + (int64_t)b * 8) = make_uint2(w0, w1);
+                q.scales[sf_offset(r, b, nb)] = (uint8_t)sbyte;
+            }
+        }
     }
 }
 
@@ -395,6 +448,15 @@ cudaError_t launch_quant(const QuantLaunch& q, cudaStream_t s) {
     const DeviceInfo* d = current_device();
     const int sms = d ? d->sm_count : 148;
     const int blk = q.fmt == FP4_MXFP4 ? 32 : 16;
+    if (q.fmt == FP4_NVFP4 && q.skip_masked_rows && q.tile_rows_end && q.n_tiles_dev &&
+        (q.sg_mode == SG_EXPERT_TABLE || q.sg_mode == SG_EXPERT_AMAX)) {
+        int64_t blocks = q.rows_pad / 128;  // upper bound on the tiles
+        if (blocks > (int64_t)sms * 4) blocks = (int64_t)sms * 4;
+        if (blocks < 1) blocks = 1;
+        QuantLaunch qq = q;
+        void* args[] = {(void*)&qq};
+        return launch_ex((const void*)quant_tiles_kernel, dim3((unsigned)blocks), dim3(QT), 0, q.pdl, s, args);
+    }
     const int64_t nb16 = sf_cols_padded(q.k, 16);
     // quant_nv_kernel keeps rows, row steps and scale offsets in 32 bits
     const bool fits32 = q.rows_pad < (1LL << 31) && q.x_ld * 8 < (1LL << 32) && q.rows_pad * nb16 < (1LL << 32);
