@@ -265,6 +265,14 @@ __device__ __forceinline__ void epi_store_bf16(const CUtensorMap* tmO, uint32_t 
     }
 }
 
+// Word i of the result is word (i + s) % 4 of v.
+__device__ __forceinline__ uint4 rotate_words(uint4 v, uint32_t s) {
+    if (s == 1) return make_uint4(v.y, v.z, v.w, v.x);
+    if (s == 2) return make_uint4(v.z, v.w, v.x, v.y);
+    if (s == 3) return make_uint4(v.w, v.x, v.y, v.z);
+    return v;
+}
+
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                  : "memory");
@@ -365,6 +373,12 @@ __global__ void __launch_bounds__(512, 1)
         for (int64_t u = blockIdx.x; u < sc.units; u += gridDim.x) {
             const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
             if (w.empty) continue;
+            // A Q tile narrower than 128 rows uses 32-row group(s) q_sub.. of each
+            // scale atom; the words are rotated so those groups sit at column 0
+            // of the atom's four TMEM columns: the MMA always reads the scale
+            // columns from the atom's first (an offset start column at N = 32
+            // faulted with a misaligned address).
+            const uint32_t q_sub = BN < 128 ? (uint32_t)((w.q_row0 & 127) >> 5) : 0u;
             bool ok = true;
             for (int64_t kb = w.kb0; kb < w.kb1; ++kb) {
                 // the slot's atoms are in smem, and the MMAs of the stage's
@@ -385,7 +399,8 @@ __global__ void __launch_bounds__(512, 1)
                 for (int rc = 0; rc < C::QCH; ++rc)
 #pragma unroll
                     for (int c = 0; c < C::SF_CHUNKS; ++c)
-                        tmem_st4(sfq_t + (c * C::QCH + rc) * 4, lds128(sq + (rc * C::SF_CHUNKS + c) * 512));
+                        tmem_st4(sfq_t + (c * C::QCH + rc) * 4,
+                                 rotate_words(lds128(sq + (rc * C::SF_CHUNKS + c) * 512), q_sub));
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -488,7 +503,6 @@ __global__ void __launch_bounds__(512, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
-                const uint32_t q_sub = BN < 128 ? (uint32_t)((w.q_row0 & 127) >> 5) : 0u;
                 for (int64_t kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!mbar_wait(full + stage, ph, wc, abort_flag)) {
                         ok = false;
@@ -506,11 +520,11 @@ __global__ void __launch_bounds__(512, 1)
                         uint32_t sfa, sfb, id;
                         if constexpr (!MX) {
                             sfa = sfp_t + kk * 4;
-                            sfb = sfq_t + kk * 4 * C::QCH + q_sub;
+                            sfb = sfq_t + kk * 4 * C::QCH;
                             id = idesc;
                         } else {
                             sfa = sfp_t + (kk >> 1) * 4;
-                            sfb = sfq_t + (kk >> 1) * 4 * C::QCH + q_sub;
+                            sfb = sfq_t + (kk >> 1) * 4 * C::QCH;
                             id = idesc_with_sf_id(idesc, (uint32_t)(kk & 1) * 2u);
                         }
                         mma_mxf4<MX>(d_tmem, ad, bd, id, sfa, sfb, (kb > w.kb0 || kk > 0) ? 1u : 0u);

@@ -201,6 +201,36 @@ def test_moe_all_tokens_one_expert(F, O):
     _stage_checks(F, O, c)
 
 
+@pytest.mark.parametrize("T", [12, 120])
+def test_moe_one_expert_swapped(F, O, T):
+    """Every token to expert 3 with few tokens per expert overall (T*k <= 16*E):
+    the swapped grouped GEMMs with up to four 32-row sub-tiles in one token tile
+    (T = 120) and, for T = 12, the one-launch preparation."""
+    c = Case(F, O, T, 8, 1, 256, 128, seed=11, std=0.1)
+    c.logits[:, 3] += 100.0
+    c.log_d = c.logits.cuda()
+    c.ref = O.moe(I.u16(c.hidden), c.logits.numpy(), top_k=1, q13=c.q13, q2=c.q2)
+    c.padded = np.concatenate([[0], np.cumsum((c.ref["counts"] + 127) // 128 * 128)]).astype(np.int64)
+    _stage_checks(F, O, c)
+    _end_to_end(F, O, c)
+    _prep_checks(O, c)
+
+
+def test_moe_static_scales_small(F, O):
+    """Static per-expert activation scales through the one-launch preparation."""
+    T, E, k, H, Inter = 9, 8, 2, 256, 128
+    c = Case(F, O, T, E, k, H, Inter, seed=31, std=0.1)
+    st13 = (np.linspace(3.0, 5.0, E) / 2688).astype(np.float32)
+    st2 = (np.linspace(0.4, 0.8, E) / 2688).astype(np.float32)
+    out = F.moe(c.hid_d, c.log_d, c.mw, k, mode=1, static13=st13, static2=st2, workspace=c.ws)
+    torch.cuda.synchronize()
+    ref = O.moe(I.u16(c.hidden), c.logits.numpy(), top_k=k, q13=c.q13, q2=c.q2, mode=1, static13=st13,
+                static2=st2)
+    y = bf16_to_np(out)
+    assert np.linalg.norm(y - ref["y"]) / np.linalg.norm(ref["y"]) < 1e-2
+    _prep_checks(O, c, ref=ref, dynamic=False)
+
+
 def test_moe_static_scales_and_errors(F, O):
     T, E, k, H, Inter = 24, 8, 2, 256, 128
     c = Case(F, O, T, E, k, H, Inter, seed=21, std=0.1)
