@@ -67,6 +67,7 @@ enum MoeSlot : int {
     MS_STATIC2,
     MS_TOK_CODES,   // dynamic scale: the hidden rows quantised once, token order
     MS_TOK_SCALES,
+    MS_SLOT_ROW,    // small-T preparation: the expert-sorted row of each slot
     MS_COUNT
 };
 
@@ -112,6 +113,7 @@ static MoeLayout moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
     sz[MS_STATIC2] = E * 4;
     sz[MS_TOK_CODES] = T * H / 2;
     sz[MS_TOK_SCALES] = round_up(T, 128) * sf_cols_padded(H, 16);
+    sz[MS_SLOT_ROW] = slots * 4;
     int64_t o = 0;
     for (int i = 0; i < MS_COUNT; ++i) {
         L.off[i] = o;
@@ -431,17 +433,20 @@ __global__ void __launch_bounds__(256) moe_permute_kernel(const uint8_t* __restr
 // ------------------------------------------------ small-T preparation
 
 // For T <= kPrepMaxTokens the route, the expert counts and scans, the row
-// tables and the dispatch-quantisation run in one CTA of 1024 threads (the
-// other CTAs of the launch zero y): at these sizes each is a few microseconds
-// of latency, and one launch replaces six (at T = 64 the one CTA's serial
-// memory round trips already cost more than the six launches).  A 64-bit token mask per expert
-// gives a slot's rank among its expert's tokens directly (rows stay in token
-// order).  Each token's row is quantised once (dynamic scale) and its codes
-// and scale bytes are stored to the rows of its k slots; with static
-// per-expert scales every slot's row is quantised under its expert's scale.
-// The scale bytes of padding rows are not written: only the swapped grouped
-// GEMMs follow this path, and they discard every padding column.
-static constexpr int kPrepMaxTokens = 16;
+// tables and the hidden abs-max run in one CTA of 1024 threads (the other
+// CTAs of the launch zero y): at these sizes each is a few microseconds of
+// latency.  A 64-bit token mask per expert gives a slot's rank among its
+// expert's tokens directly (rows stay in token order).  The quantisation and
+// dispatch follow in the same CTA for T <= kPrepInlineTokens (one launch
+// replaces six), else in moe_dispatch_kernel across the GPU (the one CTA's
+// serial memory round trips would cost more than the launch).  Each token's
+// row is quantised once (dynamic scale) and stored to the rows of its k
+// slots; with static per-expert scales every slot's row is quantised under
+// its expert's scale.  The scale bytes of padding rows are not written: only
+// the swapped grouped GEMMs follow this path, and they discard every padding
+// column.
+static constexpr int kPrepMaxTokens = 64;
+static constexpr int kPrepInlineTokens = 16;
 
 struct PrepArgs {
     const float* logits;    // [T][E]
@@ -457,16 +462,44 @@ struct PrepArgs {
     int32_t* row_valid_end;
     int32_t* row_src;
     int32_t* row_tok;
+    int32_t* slot_row;      // [T*k] expert-sorted row of each slot
     uint8_t* codes;         // expert-sorted rows [R][H/2]
     uint8_t* scales;        // their scale bytes, MMA layout
     float* sg_out;          // dynamic: s_gA
     int has_static;
+    int dispatch_inline;    // quantise and dispatch in the preparing CTA
     float* static13_out;
     float* static2_out;
     float* amax_h;          // zeroed [E]
     float* y;               // zeroed [T*H] fp32 by CTAs 1..
     int64_t y_elems;
 };
+
+// One 16-element block (token t, block column b) of the hidden rows:
+// quantised under s_g (divisor entry e, scale-byte divisor p / inv_p) and
+// stored to the expert-sorted rows `rows[0..n)`.
+__device__ __forceinline__ void prep_block(const PrepArgs& a, int t, int b, int kblocks, int nbp, float p,
+                                           float inv_p, float sg, const float2* dtab, const int32_t* rows, int n) {
+    uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+    if (b < kblocks) {
+        const uint4* px = reinterpret_cast<const uint4*>(a.hidden + (int64_t)t * a.H + (int64_t)b * 16);
+        v0 = __ldg(px);
+        v1 = __ldg(px + 1);
+    }
+    const uint32_t am = absmax8(v1, absmax8(v0, 0u));
+    const uint32_t sbyte = nvfp4_scale_byte(__uint_as_float(max(am & 0xFFFFu, am >> 16) << 16), p, inv_p);
+    const float2 e = dtab ? dtab[sbyte] : nvfp4_divisor(sbyte, sg, false);
+    float f[8];
+    unpack8(v0, f);
+    const uint32_t w0 = nvfp4_word(f, e);
+    unpack8(v1, f);
+    const uint32_t w1 = nvfp4_word(f, e);
+    for (int j = 0; j < n; ++j) {
+        const int64_t row = rows[j];
+        if (b < kblocks) *reinterpret_cast<uint2*>(a.codes + row * (a.H / 2) + (int64_t)b * 8) = make_uint2(w0, w1);
+        a.scales[sf_offset(row, b, nbp)] = (uint8_t)sbyte;
+    }
+}
 
 template <int PER_LANE>
 __global__ void __launch_bounds__(1024) moe_prep_small_kernel(const PrepArgs a, const StaticScales st) {
@@ -558,12 +591,11 @@ __global__ void __launch_bounds__(1024) moe_prep_small_kernel(const PrepArgs a, 
         a.row_src[row] = s;
         a.row_tok[row] = t;
         s_row[s] = row;
+        if (!a.dispatch_inline) a.slot_row[s] = row;
     }
 
-    // 4. dynamic: s_gA from the abs-max of the T hidden rows, and the divisors
+    // 4. dynamic: s_gA from the abs-max of the T hidden rows
     const int64_t H = a.H;
-    const int nbp = (int)sf_cols_padded(H, 16);  // scale columns per row (padding included)
-    const int kblocks = (int)(H / 16);
     if (!a.has_static) {
         const uint4* xv = reinterpret_cast<const uint4*>(a.hidden);
         uint32_t m = 0;
@@ -587,61 +619,59 @@ __global__ void __launch_bounds__(1024) moe_prep_small_kernel(const PrepArgs a, 
             a.sg_out[0] = sh_sg;
         }
         __syncthreads();
-        if (tid < 128) dtab[tid] = nvfp4_divisor((uint32_t)tid, sh_sg, false);
+        if (a.dispatch_inline && tid < 128) dtab[tid] = nvfp4_divisor((uint32_t)tid, sh_sg, false);
     }
+    if (!a.dispatch_inline) return;
     __syncthreads();
 
     // 5. quantise and dispatch
+    const int nbp = (int)sf_cols_padded(H, 16);  // scale columns per row (padding included)
+    const int kblocks = (int)(H / 16);
     if (!a.has_static) {
-        const float sg = sh_sg;
-        const float p = __fmul_rn(sg, 6.0f);
+        const float p = __fmul_rn(sh_sg, 6.0f);
         const float inv_p = nvfp4_inv_p(p);
         for (int item = tid; item < T * nbp; item += 1024) {
             const int t = item / nbp, b = item - t * nbp;
-            uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
-            if (b < kblocks) {
-                const uint4* px = reinterpret_cast<const uint4*>(a.hidden + (int64_t)t * H + (int64_t)b * 16);
-                v0 = __ldg(px);
-                v1 = __ldg(px + 1);
-            }
-            const uint32_t am = absmax8(v1, absmax8(v0, 0u));
-            const uint32_t sbyte = nvfp4_scale_byte(__uint_as_float(max(am & 0xFFFFu, am >> 16) << 16), p, inv_p);
-            const float2 e = dtab[sbyte];
-            float f[8];
-            unpack8(v0, f);
-            const uint32_t w0 = nvfp4_word(f, e);
-            unpack8(v1, f);
-            const uint32_t w1 = nvfp4_word(f, e);
-            for (int j = 0; j < k; ++j) {
-                const int64_t row = s_row[t * k + j];
-                if (b < kblocks) *reinterpret_cast<uint2*>(a.codes + row * (H / 2) + (int64_t)b * 8) = make_uint2(w0, w1);
-                a.scales[sf_offset(row, b, nbp)] = (uint8_t)sbyte;
-            }
+            prep_block(a, t, b, kblocks, nbp, p, inv_p, sh_sg, dtab, s_row + t * k, k);
         }
     } else {
         for (int item = tid; item < T * k * nbp; item += 1024) {
             const int s = item / nbp, b = item - s * nbp;
-            const int t = s / k;
             const float sg = st.s13[s_ids[s]];
-            uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
-            if (b < kblocks) {
-                const uint4* px = reinterpret_cast<const uint4*>(a.hidden + (int64_t)t * H + (int64_t)b * 16);
-                v0 = __ldg(px);
-                v1 = __ldg(px + 1);
-            }
-            const uint32_t am = absmax8(v1, absmax8(v0, 0u));
             const float p = __fmul_rn(sg, 6.0f);
-            const uint32_t sbyte =
-                nvfp4_scale_byte(__uint_as_float(max(am & 0xFFFFu, am >> 16) << 16), p, nvfp4_inv_p(p));
-            const float2 e = nvfp4_divisor(sbyte, sg, false);
-            float f[8];
-            unpack8(v0, f);
-            const uint32_t w0 = nvfp4_word(f, e);
-            unpack8(v1, f);
-            const uint32_t w1 = nvfp4_word(f, e);
-            const int64_t row = s_row[s];
-            if (b < kblocks) *reinterpret_cast<uint2*>(a.codes + row * (H / 2) + (int64_t)b * 8) = make_uint2(w0, w1);
-            a.scales[sf_offset(row, b, nbp)] = (uint8_t)sbyte;
+            prep_block(a, s / k, b, kblocks, nbp, p, nvfp4_inv_p(p), sg, nullptr, s_row + s, 1);
+        }
+    }
+}
+
+// The quantisation and dispatch of the small-T preparation across the GPU
+// (T > kPrepInlineTokens): a thread per (token, block column), or per (slot,
+// block column) with static per-expert scales; the slots' rows come from
+// the preparing kernel.
+__global__ void __launch_bounds__(256) moe_dispatch_kernel(const PrepArgs a, const StaticScales st) {
+    __shared__ float2 dtab[128];
+    pdl_wait();
+    pdl_launch_dependents();  // dependents wait for this grid's completion
+    const int64_t H = a.H;
+    const int nbp = (int)sf_cols_padded(H, 16);
+    const int kblocks = (int)(H / 16);
+    const int T = (int)a.T, k = a.k;
+    if (!a.has_static) {
+        const float sg = a.sg_out[0];
+        if (threadIdx.x < 128) dtab[threadIdx.x] = nvfp4_divisor(threadIdx.x, sg, false);
+        __syncthreads();
+        const float p = __fmul_rn(sg, 6.0f);
+        const float inv_p = nvfp4_inv_p(p);
+        for (int item = blockIdx.x * 256 + threadIdx.x; item < T * nbp; item += gridDim.x * 256) {
+            const int t = item / nbp, b = item - t * nbp;
+            prep_block(a, t, b, kblocks, nbp, p, inv_p, sg, dtab, a.slot_row + t * k, k);
+        }
+    } else {
+        for (int item = blockIdx.x * 256 + threadIdx.x; item < T * k * nbp; item += gridDim.x * 256) {
+            const int s = item / nbp, b = item - s * nbp;
+            const float sg = st.s13[a.ids[s]];
+            const float p = __fmul_rn(sg, 6.0f);
+            prep_block(a, s / k, b, kblocks, nbp, p, nvfp4_inv_p(p), sg, nullptr, a.slot_row + s, 1);
         }
     }
 }
@@ -899,6 +929,8 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         pa.scales = a_scales;
         pa.sg_out = sg_a;
         pa.has_static = is_static ? 1 : 0;
+        pa.dispatch_inline = T <= kPrepInlineTokens ? 1 : 0;
+        pa.slot_row = (int32_t*)at(MS_SLOT_ROW);
         pa.static13_out = st13;
         pa.static2_out = st2;
         pa.amax_h = amax_h;
@@ -916,6 +948,12 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
                                           : (const void*)moe_prep_small_kernel<32>;
         MOE_CUDA(launch_k(fn, dim3(1 + zero_blocks), dim3(1024), 0, pdl, s, args), "prepare launch");
         pdl = true;
+        if (!pa.dispatch_inline) {
+            const int64_t items = (is_static ? T * k : T) * sf_cols_padded(H, 16);
+            const int64_t db = std::min<int64_t>((items + 255) / 256, (int64_t)d->sm_count * 4);
+            MOE_CUDA(launch_k((const void*)moe_dispatch_kernel, dim3((unsigned)db), dim3(256), 0, pdl, s, args),
+                     "dispatch launch");
+        }
     }
 
     // 1. route (+ zeroing of y and amax_h when the whole pipeline runs)
