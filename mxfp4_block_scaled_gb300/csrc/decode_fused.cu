@@ -145,16 +145,18 @@ __global__ void __launch_bounds__(512, 1)
         pdl_wait();
         const uint32_t nvec = (uint32_t)((int64_t)a.m * a.k / 8);  // < 2^16 (m <= 8, k <= 8192)
         const uint4* xv = reinterpret_cast<const uint4*>(a.x);
-        // the first four rounds' chunks stay in registers for the quantise pass
-        // (all of them for m k <= 4 x 416 x 8, e.g. one row of 13k elements)
-        uint4 v0[4];
+        // The first R rounds' chunks are loaded at once and stay in registers for
+        // both passes (all of them for m k <= R x 416 x 8 = 39,936 elements,
+        // e.g. 8 rows of 4096): one load latency instead of one per round.
+        constexpr int R = 12;
+        uint4 v0[R];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) v0[u] = ta + u * NT < nvec ? __ldg(xv + ta + u * NT) : make_uint4(0u, 0u, 0u, 0u);
+        for (int u = 0; u < R; ++u) v0[u] = ta + u * NT < nvec ? __ldg(xv + ta + u * NT) : make_uint4(0u, 0u, 0u, 0u);
         if (!MX && a.dynamic) {
             uint32_t mx = 0;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) mx = absmax8(v0[u], mx);
-            for (uint32_t i0 = ta + 4 * NT; i0 < nvec; i0 += 4 * NT) {  // four loads in flight
+            for (int u = 0; u < R; ++u) mx = absmax8(v0[u], mx);
+            for (uint32_t i0 = ta + R * NT; i0 < nvec; i0 += 4 * NT) {  // four loads in flight
                 uint4 v[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) v[u] = i0 + u * NT < nvec ? __ldg(xv + i0 + u * NT) : make_uint4(0u, 0u, 0u, 0u);
@@ -178,19 +180,20 @@ __global__ void __launch_bounds__(512, 1)
         // NVFP4: the divisor entry of each scale byte (nvfp4_divisor)
         const float p_t = __fmul_rn(sg, 6.0f);
         const float inv_p = nvfp4_inv_p(p_t);
-        if (!MX && ta < 128) dtab[ta] = nvfp4_divisor((uint32_t)ta, sg, false);
+        // (the one-value test and neighbour search of the table make almost every
+        // block take the one-multiply path; for a single row the table is on the
+        // critical path and the per-element bracket costs less)
+        if (!MX && ta < 128) dtab[ta] = nvfp4_divisor((uint32_t)ta, sg, a.m > 1);
         named_bar_sync(1, NT);
         constexpr int LPB = MX ? 4 : 2;  // lanes per block
         const uint32_t cpr = (uint32_t)(a.k / 8);  // chunks per row
-        // the trip count follows the warp's first chunk, so it is the same for
-        // all lanes of the warp (the shuffles below need every lane)
-        for (uint32_t jb = (uint32_t)(ta & ~31); jb < nvec; jb += 4 * NT) {
+        // Four rounds of chunks at a time; the trip counts follow the warp's first
+        // chunk, so they are the same for all lanes of the warp (the shuffles
+        // below need every lane).
+        const uint32_t dr = NT / cpr, dc = NT - dr * cpr;  // a round's step in (row, chunk)
+        auto convert4 = [&](const uint4 (&vb)[4], uint32_t jb) {
             const uint32_t j0 = jb + (uint32_t)lane;
-            const bool first = jb == (uint32_t)(ta & ~31);
-            uint4 vb[4];  // four rounds' chunks (the first four from registers)
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                vb[u] = first ? v0[u] : (j0 + u * NT < nvec ? __ldg(xv + j0 + u * NT) : make_uint4(0u, 0u, 0u, 0u));
+            uint32_t r = j0 / cpr, c = j0 - r * cpr;  // row and chunk of round u, stepped below
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const uint32_t i = j0 + u * NT;
@@ -213,11 +216,31 @@ __global__ void __launch_bounds__(512, 1)
                     w = mxfp4_codes8(vb[u], inv);
                 }
                 if (i < nvec) {
-                    const uint32_t r = i / cpr, c = i - r * cpr;
                     *reinterpret_cast<uint32_t*>(xc + (int64_t)r * cb + c * 4) = w;
                     if ((lane & (LPB - 1)) == 0) xs[(int64_t)r * sbpr + c / LPB] = (uint8_t)sbyte;
                 }
+                r += dr;
+                c += dc;
+                if (c >= cpr) {
+                    c -= cpr;
+                    ++r;
+                }
             }
+        };
+        const uint32_t jw = (uint32_t)(ta & ~31);
+#pragma unroll
+        for (int it = 0; it < R / 4; ++it) {  // the rounds held in registers
+            const uint32_t jb = jw + (uint32_t)(it * 4 * NT);
+            if (jb >= nvec) break;  // warp-uniform
+            const uint4 vb[4] = {v0[4 * it], v0[4 * it + 1], v0[4 * it + 2], v0[4 * it + 3]};
+            convert4(vb, jb);
+        }
+        for (uint32_t jb = jw + R * NT; jb < nvec; jb += 4 * NT) {  // the rest, loaded
+            const uint32_t j0 = jb + (uint32_t)lane;
+            uint4 vb[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) vb[u] = j0 + u * NT < nvec ? __ldg(xv + j0 + u * NT) : make_uint4(0u, 0u, 0u, 0u);
+            convert4(vb, jb);
         }
         named_bar_sync(1, NT);  // the compact copy is complete
     }
