@@ -331,8 +331,13 @@ static GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int sms) {
         p.splits = (int)s;
     } else {
         p.decode = false;
-        const int64_t units256 = ((m + 127) / 128) * ((n + 255) / 256);
-        p.bn = units256 >= sms ? 256 : 128;
+        // persistent CTAs take whole tiles, so a launch lasts about (waves of
+        // tiles) x (tile time); a 256-wide tile takes about 1.5x a 128-wide one
+        // (96 KB against 64 KB of shared-memory traffic per K block, which
+        // bounds both)
+        const int64_t w256 = (((m + 127) / 128) * ((n + 255) / 256) + sms - 1) / sms;
+        const int64_t w128 = (((m + 127) / 128) * ((n + 127) / 128) + sms - 1) / sms;
+        p.bn = 3 * w256 <= 2 * w128 ? 256 : 128;
         p.splits = 1;
         // The CTA-pair kernel is opt-in: on the 8192 x 14336 x 4096 prefill its
         // copies (operand tiles and scale atoms alike) take about 8k cycles to

@@ -444,6 +444,71 @@ __global__ void __launch_bounds__(QT, QNV_CTAS) quant_nv_kernel(const QuantLaunc
     }
 }
 
+// ----------------------------------------------- MXFP4, rows as given
+
+constexpr int QU_MX = 2;  // rows in flight per thread (a 32-element block is four 16-byte loads)
+
+// The MXFP4 quantiser without a row map (activations and weight prepack): the
+// layout of quant_nv_kernel with a thread per 32-element block; the scale is
+// an exact power of two, so there is no global scale and no divisor table.
+__global__ void __launch_bounds__(QT, QNV_CTAS) quant_mx_rows_kernel(const QuantLaunch q) {
+    pdl_wait();
+    pdl_launch_dependents();
+    if (blockIdx.x == 0 && threadIdx.x == 0 && q.global_out) *q.global_out = 1.0f;
+    const int nb = (int)sf_cols_padded(q.k, 32);
+    const int kblocks = (int)(q.k / 32);
+    const int bpt = nb < QT ? (nb + 31) / 32 * 32 : QT;
+    const int rpi = QT / bpt;
+    const int ty = threadIdx.x / bpt, tx = threadIdx.x - ty * bpt;
+    const uint32_t groups = (uint32_t)(q.rows_pad / rpi);
+    const uint32_t per = (groups + gridDim.x - 1) / gridDim.x;
+    const uint32_t g_begin = blockIdx.x * per;
+    const uint32_t g_end = min(groups, g_begin + per);
+    if (ty >= rpi || g_begin >= g_end) return;
+    const uint32_t rows = (uint32_t)q.rows;
+    const uint32_t xstep = (uint32_t)(rpi * q.x_ld);
+    const uint32_t cstep = (uint32_t)(rpi * (q.k / 2));
+    const uint32_t tile_sf = (uint32_t)nb * 128u;
+    for (int b = tx; b < nb; b += bpt) {
+        const bool bdata = b < kblocks;
+        const uint32_t sf_col = (uint32_t)(b >> 2) * 512u + (uint32_t)(b & 3);
+        uint32_t r = g_begin * rpi + ty;
+        const uint16_t* px = q.x + (size_t)r * (size_t)q.x_ld + (size_t)b * 32;
+        uint8_t* pc = q.codes + (size_t)r * (size_t)(q.k / 2) + (size_t)b * 16;
+        for (uint32_t g = g_begin; g < g_end; g += QU_MX) {
+            uint4 v[QU_MX][4];
+#pragma unroll
+            for (int j = 0; j < QU_MX; ++j) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) v[j][i] = make_uint4(0u, 0u, 0u, 0u);
+                if (g + j < g_end && r + j * rpi < rows && bdata) {
+                    const uint4* pv = reinterpret_cast<const uint4*>(px + j * xstep);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) v[j][i] = __ldg(pv + i);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < QU_MX; ++j) {
+                if (g + j >= g_end) break;
+                const uint32_t rj = r + j * rpi;
+                uint32_t am = 0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) am = absmax8(v[j][i], am);
+                float inv;
+                const uint32_t sbyte = mxfp4_scale_byte(__uint_as_float(max(am & 0xFFFFu, am >> 16) << 16), inv);
+                if (rj < rows && bdata)
+                    *reinterpret_cast<uint4*>(pc + j * cstep) =
+                        make_uint4(mxfp4_codes8(v[j][0], inv), mxfp4_codes8(v[j][1], inv), mxfp4_codes8(v[j][2], inv),
+                                   mxfp4_codes8(v[j][3], inv));
+                q.scales[(rj >> 7) * tile_sf + ((rj & 31u) << 4) + (((rj >> 5) & 3u) << 2) + sf_col] = (uint8_t)sbyte;
+            }
+            r += QU_MX * rpi;
+            px += QU_MX * xstep;
+            pc += QU_MX * cstep;
+        }
+    }
+}
+
 cudaError_t launch_quant(const QuantLaunch& q, cudaStream_t s) {
     const DeviceInfo* d = current_device();
     const int sms = d ? d->sm_count : 148;
@@ -462,6 +527,18 @@ cudaError_t launch_quant(const QuantLaunch& q, cudaStream_t s) {
     const bool fits32 = q.rows_pad < (1LL << 31) && q.x_ld * 8 < (1LL << 32) && q.rows_pad * nb16 < (1LL << 32);
     const bool one_scale = q.fmt == FP4_NVFP4 && (q.sg_mode == SG_STATIC || q.sg_mode == SG_PARTIALS) && !q.row_map &&
                            !q.rows_dev && fits32;
+    const int64_t nb32 = sf_cols_padded(q.k, 32);
+    if (q.fmt == FP4_MXFP4 && !q.row_map && !q.rows_dev && q.rows_pad < (1LL << 31) && q.x_ld * 8 < (1LL << 32) &&
+        q.rows_pad * nb32 < (1LL << 32)) {
+        const int64_t bpt = nb32 < QT ? (nb32 + 31) / 32 * 32 : QT;
+        const int64_t groups = q.rows_pad / (QT / bpt);
+        int64_t blocks = (groups + QU_MX - 1) / QU_MX;
+        if (blocks > (int64_t)sms * QNV_CTAS) blocks = (int64_t)sms * QNV_CTAS;
+        if (blocks < 1) blocks = 1;
+        QuantLaunch qq = q;
+        void* args[] = {(void*)&qq};
+        return launch_ex((const void*)quant_mx_rows_kernel, dim3((unsigned)blocks), dim3(QT), 0, q.pdl, s, args);
+    }
     if (one_scale) {
         const int64_t nb = nb16;
         const int64_t bpt = nb < QT ? (nb + 31) / 32 * 32 : QT;
