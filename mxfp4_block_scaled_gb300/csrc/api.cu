@@ -321,7 +321,9 @@ static GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int sms) {
         p.decode = true;
         p.bn = m <= 32 ? 32 : 64;
         const int64_t qtiles = (n + 127) / 128;
-        int64_t s = (3 * (int64_t)sms + qtiles - 1) / qtiles;
+        // with weight tiles for at least half the SMs, one K range per tile
+        // (no partials, no reduction launch); fewer tiles are split along K
+        int64_t s = 2 * qtiles >= sms ? 1 : (3 * (int64_t)sms + qtiles - 1) / qtiles;
         if (s > kbt / 2) s = kbt / 2;
         if (s > 16) s = 16;
         if (s < 1) s = 1;
