@@ -473,7 +473,8 @@ extern "C" fp4_status fp4_gemm(int fmt, const void* x, int64_t m, int mode, floa
     base += align256(fp4_scales_bytes(fmt, m, k));
     float* ag = reinterpret_cast<float*>(base);
     const DeviceInfo* d = current_device();
-    const bool fused = g_tile_policy == 3 || (g_tile_policy == 0 && (n + 127) / 128 >= (int64_t)d->sm_count / 2);
+    const bool fused = g_tile_policy == 3 || (g_tile_policy == 0 && m <= kDecodeFusedAutoMaxM &&
+                                              (n + 127) / 128 >= (int64_t)d->sm_count / 2);
     if (m <= kDecodeFusedMaxM && k <= kDecodeFusedMaxK && fused) {
         // decode: one launch (in-kernel activation quantisation, one CTA per
         // 128 weight rows, no split-K); the activation s_g goes to the workspace

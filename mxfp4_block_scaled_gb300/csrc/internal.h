@@ -147,6 +147,11 @@ int64_t gemm_k_blocks(int64_t k);  // K blocks of the one-CTA GEMM
 // activation rows in the kernel and streams the weights, one CTA per 128
 // weight rows, bf16 out [m][n].
 constexpr int kDecodeFusedMaxM = 8;
+// rows up to which the automatic policy takes the fused kernel: on the
+// 14336 x 4096 decode it is 4.3 / 2.0 us faster at m = 1 / 4 than the quantise
+// + GEMM launches, and 0.4 us slower at m = 8 (the in-kernel quantisation of
+// every row by every CTA grows with m)
+constexpr int kDecodeFusedAutoMaxM = 6;
 constexpr int64_t kDecodeFusedMaxK = 8192;
 cudaError_t launch_decode_fused(int fmt, const uint16_t* x, int m, int64_t n, int64_t k, const uint8_t* w_codes,
                                 const uint8_t* w_scales, const float* w_global, int dynamic, float static_scale,
