@@ -570,17 +570,29 @@ __global__ void __launch_bounds__(512, 1)
         uint32_t aph = 0;
         uint32_t n_done = 0;  // units converted by this warp (EPI_SWIGLU_T buffer parity)
         for (int64_t u = blockIdx.x; u < sc.units; u += gridDim.x) {
-            int pf_tok = 0;       // EPI_COMBINE_T: lane i < 16 holds column i's token and routing
-            float pf_w = 0.0f;    // weight, fetched before the wait for the MMAs
+            // EPI_COMBINE_T: lane i of round q holds column 32 q + i's token and
+            // routing weight, fetched before the wait for the MMAs
+            constexpr int NPF = (CPW + 31) / 32;
+            int pf_tok[NPF];
+            float pf_w[NPF];
+#pragma unroll
+            for (int q = 0; q < NPF; ++q) {
+                pf_tok[q] = 0;
+                pf_w[q] = 0.0f;
+            }
             if constexpr (epi_swapped_grouped<EPI>()) {
                 const Unit wp = decode_unit<BN, EPI>(g, sc, u, ut);
                 if (wp.empty) continue;
                 if constexpr (EPI == EPI_COMBINE_T) {
-                    const int64_t row = wp.q_row0 + c_begin + lane;
-                    if (lane < 16 && row < wp.vend) {
-                        const int slot = g.row_src[row];
-                        pf_tok = slot / g.top_k;
-                        pf_w = g.slot_weight[slot];
+#pragma unroll
+                    for (int q = 0; q < NPF; ++q) {
+                        const int col = q * 32 + lane;
+                        const int64_t row = wp.q_row0 + c_begin + col;
+                        if (col < CPW && row < wp.vend) {
+                            const int slot = g.row_src[row];
+                            pf_tok[q] = slot / g.top_k;
+                            pf_w[q] = g.slot_weight[slot];
+                        }
                     }
                 }
             }
@@ -818,11 +830,15 @@ __global__ void __launch_bounds__(512, 1)
                 ++n_done;
             } else if constexpr (EPI == EPI_COMBINE_T) {
                 // P rows are the expert's W2 rows (output features), columns the
-                // sub-tile's token rows (16 per warpgroup):
-                // y[token][feature] += weight * alpha * acc.
-                static_assert(BN == 32, "16 columns per epilogue warp");
-                uint32_t r[16];
-                tmem_ld16(tb, r);
+                // sub-tile's token rows (CPW per warpgroup):
+                // y[token][feature] += weight * alpha * acc.  (At T = 4096 with
+                // 128-token tiles this form ran 157 us against 129 us for the
+                // token-row combine: the L2 reduction rate follows elements,
+                // not requests, and scalar reductions cost 4x the instructions.)
+                static_assert(CPW % 16 == 0, "whole 16-column loads");
+                uint32_t r[CPW / 16][16];
+#pragma unroll
+                for (int c = 0; c < CPW / 16; ++c) tmem_ld16(tb + c * 16, r[c]);
                 tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -832,13 +848,18 @@ __global__ void __launch_bounds__(512, 1)
                 const int64_t hd = w.qt * 128 + qd * 32 + lane;
                 const int64_t vend = w.vend;
                 const int64_t row0 = w.q_row0 + c_begin;
-                const float wsc = __fmul_rn(pf_w, alpha);
                 float* y = reinterpret_cast<float*>(g.out) + hd;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int t_i = __shfl_sync(0xFFFFFFFFu, pf_tok, i);
-                    const float s_i = __shfl_sync(0xFFFFFFFFu, wsc, i);
-                    if (row0 + i < vend) atomicAdd(y + (int64_t)t_i * g.ldo, __fmul_rn(s_i, __uint_as_float(r[i])));
+                for (int q = 0; q < NPF; ++q) {
+                    const float wsc = __fmul_rn(pf_w[q], alpha);
+#pragma unroll
+                    for (int i = 0; i < 32 && q * 32 + i < CPW; ++i) {
+                        const int t_i = __shfl_sync(0xFFFFFFFFu, pf_tok[q], i);
+                        const float s_i = __shfl_sync(0xFFFFFFFFu, wsc, i);
+                        if (row0 + q * 32 + i < vend)
+                            atomicAdd(y + (int64_t)t_i * g.ldo,
+                                      __fmul_rn(s_i, __uint_as_float(r[(q * 32 + i) / 16][(q * 32 + i) % 16])));
+                    }
                 }
             }
             if (++acc == C::ACC) {
