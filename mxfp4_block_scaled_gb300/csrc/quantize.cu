@@ -299,24 +299,35 @@ __global__ void __launch_bounds__(QT) quant_tiles_kernel(const QuantLaunch q) {
         const float p = __fmul_rn(sg, 6.0f);
         const float inv_p = nvfp4_inv_p(p);
         const int64_t rend = q.tile_rows_end[t];
-        for (int64_t r = t * 128 + ty; r < rend; r += rpi) {
-            for (int b = tx; b < nb; b += bpt) {
-                uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
-                if (b < kblocks) {
-                    const uint4* px = reinterpret_cast<const uint4*>(q.x + r * q.x_ld + (int64_t)b * 16);
-                    v0 = __ldg(px);
-                    v1 = __ldg(px + 1);
+        for (int b = tx; b < nb; b += bpt) {
+            for (int64_t r0 = t * 128 + ty; r0 < rend; r0 += 4 * rpi) {  // four rows' loads in flight
+                uint4 v[4][2];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    v[j][0] = v[j][1] = make_uint4(0u, 0u, 0u, 0u);
+                    if (r0 + j * rpi < rend && b < kblocks) {
+                        const uint4* px =
+                            reinterpret_cast<const uint4*>(q.x + (r0 + j * rpi) * q.x_ld + (int64_t)b * 16);
+                        v[j][0] = __ldg(px);
+                        v[j][1] = __ldg(px + 1);
+                    }
                 }
-                const uint32_t am = absmax8(v1, absmax8(v0, 0u));
-                const uint32_t sbyte = nvfp4_scale_byte(__uint_as_float(max(am & 0xFFFFu, am >> 16) << 16), p, inv_p);
-                const float2 e = nvfp4_divisor(sbyte, sg, false);
-                float f[8];
-                unpack8(v0, f);
-                const uint32_t w0 = nvfp4_word(f, e);
-                unpack8(v1, f);
-                const uint32_t w1 = nvfp4_word(f, e);
-                if (b < kblocks) *reinterpret_cast<uint2*>(q.codes + r * cb + (int64_t)b * 8) = make_uint2(w0, w1);
-                q.scales[sf_offset(r, b, nb)] = (uint8_t)sbyte;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int64_t r = r0 + j * rpi;
+                    if (r >= rend) break;
+                    const uint32_t am = absmax8(v[j][1], absmax8(v[j][0], 0u));
+                    const uint32_t sbyte =
+                        nvfp4_scale_byte(__uint_as_float(max(am & 0xFFFFu, am >> 16) << 16), p, inv_p);
+                    const float2 e = nvfp4_divisor(sbyte, sg, false);
+                    float f[8];
+                    unpack8(v[j][0], f);
+                    const uint32_t w0 = nvfp4_word(f, e);
+                    unpack8(v[j][1], f);
+                    const uint32_t w1 = nvfp4_word(f, e);
+                    if (b < kblocks) *reinterpret_cast<uint2*>(q.codes + r * cb + (int64_t)b * 8) = make_uint2(w0, w1);
+                    q.scales[sf_offset(r, b, nb)] = (uint8_t)sbyte;
+                }
             }
         }
     }
