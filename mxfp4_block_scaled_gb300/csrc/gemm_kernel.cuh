@@ -210,12 +210,29 @@ __device__ __forceinline__ Unit decode_unit(const GemmLaunch& g, const Sched& sc
     return w;
 }
 
-// SiLU(g) = g / (1 + exp(-g)) as g times the correctly rounded reciprocal of
-// 1 + expf(-g): one rounding more than a correctly rounded division (within
-// 2^-23 relative, with expf's 2 ulp) at a fraction of its instructions -- this
-// runs for every element of h in the GEMM1 epilogue, and h is requantised to
-// FP4 right after.  A huge 1 + expf(-g) gives a reciprocal of 0 and SiLU 0.
-__device__ __forceinline__ float silu_f32(float g) { return __fmul_rn(g, __frcp_rn(__fadd_rn(1.0f, expf(-g)))); }
+// SiLU(g) = g / (1 + e^-g), for every element of h in the GEMM1 epilogue (h is
+// requantised to FP4 right after).  e^-g = 2^(-g log2 e): the product is
+// carried as p + q, p = fl(-g L) with L = fl(log2 e), q = its rounding error
+// (an FMA) plus -g (log2 e - L) (Cody and Waite's split of the constant);
+// 2^p comes from the hardware's ex2.approx and 2^q is 1 + q ln 2 to well
+// below an ulp (|q| < 2^-16).  Then the hardware's rcp.approx and the
+// product with g.  Relative error about 2^-21 (the two approximate
+// instructions within about 2 ulp each, three roundings), inside the 2^-20
+// the SwiGLU product is given.  For g below about -88, e^-g is +inf, the
+// reciprocal 0 and SiLU 0 (the exact value is below 1e-36 in magnitude).
+__device__ __forceinline__ float silu_f32(float g) {
+    const float kLog2e = 1.44269502163f;        // fl(log2 e)
+    const float kLog2eRest = 1.925963e-08f;      // log2 e - fl(log2 e)
+    const float kLn2 = 0.693147181f;
+    const float p = __fmul_rn(-g, kLog2e);
+    const float q = __fadd_rn(__fmaf_rn(-g, kLog2e, -p), __fmul_rn(-g, kLog2eRest));
+    float e;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(p));
+    e = __fmul_rn(e, __fmaf_rn(q, kLn2, 1.0f));
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(__fadd_rn(1.0f, e)));
+    return __fmul_rn(g, r);
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
