@@ -268,6 +268,20 @@ def linear(fmt, x_u16, w_u16, mode=DYNAMIC, static_scale=0.0):
     return out, mag, qa, qw
 
 
+def linear_w4a16(fmt, x_u16, cw, sw, sgw):
+    """Weight-only FP4 linear ("vLLM on DGX Spark: technical report", section
+    5.3 "Marlin for NVFP4": FP4 weights dequantised to 16 bits, 16-bit
+    activations): out[m, n] = s_gW * sum_k x[m, k] * deqW[n, k] in fp64 with
+    deqW = E2M1 x block scale (exact in bf16, so the 16-bit dequantisation
+    loses nothing) and s_gW the weight's global scale (1 for MXFP4); x is the
+    bf16 activation, not quantised.  Also the magnitude sum that sizes the
+    fp32 accumulation error."""
+    x = bf16_to_f32(x_u16).astype(np.float64)
+    dw = dequantize(fmt, cw, sw, apply_global=False)
+    g = 1.0 if fmt == MXFP4 else float(np.float32(sgw))
+    return g * (x @ dw.T), g * (np.abs(x) @ np.abs(dw).T)
+
+
 def bf16_round(x64):
     """fp64 -> nearest bf16 value (round half to even), as float64.  bf16 keeps
     8 significant bits; its spacing at |x| in [2^(e-1), 2^e) is 2^(e-8), and

@@ -369,6 +369,70 @@ def test_linear_close_to_unquantised_matmul(O, fmt):
     assert 0.01 < rel < 0.2, rel
 
 
+# ------------------------------------------------------------- W4A16 linear
+
+@pytest.mark.parametrize("fmt,M,N,K", [(0, 2, 3, 32), (1, 3, 2, 64)])
+def test_w4a16_brute_force_tiny(O, fmt, M, N, K):
+    """Exact rational sum of x times the hand-decoded weights."""
+    x = I.randn_bf16((M, K), 81 + K)
+    w = I.randn_bf16((N, K), 82 + K, std=0.02)
+    cw, sw, gw = O.quantize(fmt, I.u16(w))
+    out, _ = O.linear_w4a16(fmt, I.u16(x), cw, sw, gw)
+    e2m1 = lambda c: (-1) ** (c >> 3) * [0, 0.5, 1, 1.5, 2, 3, 4, 6][c & 7]
+    blk = 16 if fmt == 0 else 32
+    dec = (lambda b: Fraction(O.e4m3_decode(b))) if fmt == 0 else (lambda b: Fraction(2) ** (b - 127))
+    g = Fraction(1) if fmt == 1 else Fraction(float(np.float32(gw)))
+    xf = x.float().numpy()
+    for m in range(M):
+        for n in range(N):
+            s = Fraction(0)
+            for k in range(K):
+                byte = int(cw[n, k // 2])
+                c = (byte >> 4) if (k & 1) else (byte & 15)
+                s += Fraction(float(xf[m, k])) * Fraction(e2m1(c)) * dec(int(sw[n, k // blk]))
+            want = g * s
+            assert abs(Fraction(out[m, n]) - want) <= abs(want) * Fraction(1, 2 ** 50) + Fraction(1, 2 ** 200)
+
+
+def test_w4a16_one_hot_reads_the_weights(O):
+    """x = e_k selects column k of the dequantised weights, times s_gW."""
+    K, N = 256, 8
+    w = I.randn_bf16((N, K), 91, std=0.02)
+    cw, sw, gw = O.quantize_nvfp4(I.u16(w))
+    dw = O.dequantize(O.NVFP4, cw, sw, gw)
+    for k in (0, 17, 128, 255):
+        x = torch.zeros((1, K), dtype=torch.bfloat16)
+        x[0, k] = 1.0
+        out, _ = O.linear_w4a16(O.NVFP4, I.u16(x), cw, sw, gw)
+        assert np.array_equal(out[0], dw[:, k])
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_w4a16_equals_w4a4_on_fp4_exact_activations(O, fmt):
+    """Activations whose quantisation is exact (FP4 values times a power-of-two
+    block scale) give the same output through the W4A4 oracle."""
+    rng = np.random.default_rng(7)
+    vals = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float32)
+    M, K, N = 4, 256, 6
+    a = rng.choice(vals, size=(M, K)) * rng.choice([-1, 1], size=(M, K))
+    a[:, ::16] = 6.0  # every 16-block holds the largest value
+    x = torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)
+    w = I.randn_bf16((N, K), 93, std=0.02)
+    cw, sw, gw = O.quantize(fmt, I.u16(w))
+    out16, _ = O.linear_w4a16(fmt, I.u16(x), cw, sw, gw)
+    if fmt == 0:
+        # with s_g = 2^-8 every block's scale byte is E4M3(6 / (6 * 2^-8)) = 256,
+        # so the divisor 256 * 2^-8 is exactly 1 and the codes are exact
+        ca, sa, ga = O.quantize_nvfp4(I.u16(x), O.STATIC, 1.0 / 256.0)
+    else:
+        ca, sa = O.quantize_mxfp4(I.u16(x))
+        ga = 1.0
+    deq = O.dequantize(fmt, ca, sa, ga)
+    assert np.array_equal(deq, a.astype(np.float64))  # the activations' quantisation is exact
+    out4, _ = O.gemm(fmt, ca, sa, ga, cw, sw, gw)
+    assert np.allclose(out16, out4, rtol=1e-14, atol=0)
+
+
 # ----------------------------------------------------------- router/permute
 
 def test_router_invariants_and_brute_force(O):
