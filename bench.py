@@ -49,8 +49,8 @@ def parse():
     p.add_argument("--profile", action="store_true",
                    help="only the layer calls (warmup + steps), for ncu captures")
     p.add_argument("--workload", default="prefill",
-                   choices=["prefill", "quant", "decode1", "decode8", "decode32", "mxfp4", "moe1", "moe64",
-                            "moe4096"],
+                   choices=["prefill", "quant", "decode1", "decode8", "decode32", "w4a16_1", "w4a16_4", "mxfp4",
+                            "moe1", "moe64", "moe4096"],
                    help="workload run by --profile")
     return p.parse_args()
 
@@ -330,6 +330,12 @@ def run_profile_other(args, torch, fp4, L, I, dev):
         wq = fp4.prepack_weight(I.weights_bf16(14336, 4096, 101).to(dev))
         a = I.activations_with_outliers(m, 4096, 1).to(dev)
         fn = lambda: fp4.gemm(a, wq)
+    elif wl.startswith("w4a16_"):
+        # weight-only decode on the decode weights
+        m = int(wl[6:])
+        wq = fp4.prepack_weight(I.weights_bf16(14336, 4096, 101).to(dev))
+        a = I.activations_with_outliers(m, 4096, 3).to(dev)
+        fn = lambda: fp4.gemm_w4a16(a, wq)
     elif wl == "quant":
         # the prefill activations' dynamic quantisation alone (amax + quantise)
         a = I.randn_bf16((M, K), 2).to(dev)
@@ -425,6 +431,16 @@ def run_secondary(torch, fp4, L, I, dev, peaks):
                                  "note": ("one fused launch (activations quantised in the GEMM kernel)" if m <= 6
                                           else "quantise (amax + quantise launches) + GEMM")
                                          + ", CUDA graph, 8 rotating weight copies"}
+    # weight-only (W4A16) decode on the same weights: bf16 activations, not quantised
+    for m in (1, 4):
+        a = I.activations_with_outliers(m, nk, 3).to(dev)
+        o = torch.empty((m, 14336), dtype=torch.bfloat16, device=dev)
+        fns = [(lambda wq=wq: fp4.gemm_w4a16(a, wq, out=o)) for wq in copies]
+        ms = graph_time(torch, fns)
+        byt = wbytes + m * nk * 2 + m * 14336 * 2
+        out["w4a16_decode_m%d" % m] = {"us": round(ms * 1e3, 2), "GB/s": round(byt / (ms * 1e-3) / 1e9, 1),
+                                       "frac_hbm": round(byt / (ms * 1e-3) / 1e9 / hbm, 4),
+                                       "note": "weight-only, one launch, CUDA graph, 8 rotating weight copies"}
     del copies
     # MXFP4 M=2048 K=7168 N=2048
     a = I.randn_bf16((2048, 7168), 4).to(dev)

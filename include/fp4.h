@@ -201,6 +201,22 @@ fp4_status fp4_gemm_prequant(int fmt, const void* a_codes, const void* a_scales,
                              const void* w_codes, const void* w_scales, const float* w_global, int64_t n, int64_t k,
                              void* out_bf16, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Weight-only (W4A16) linear for decode: out[m, n] = bf16( s_gW * sum_k
+ * x[m, k] * E2M1(w)[n, k] * s_b[n, k / B] ) with the bf16 activations used as
+ * they are, not quantised ("vLLM on DGX Spark: technical report", section 5.3
+ * "Marlin for NVFP4": the FP4 weight is dequantised to 16 bits and multiplied
+ * with 16-bit activations).  B = 16 (NVFP4, s_gW = *w_global) or 32 (MXFP4,
+ * s_gW = 1, w_global ignored and may be NULL).  Each product of an element and
+ * its block scale is exact in fp32; the sum is fp32 in an unspecified order,
+ * then one bf16 rounding.  The weight is the prepacked one of fp4_gemm.
+ * x_bf16 [m, k], out_bf16 [m, n] row-major, 16-byte aligned.  Requires
+ * m <= 4 and k <= 8192 (FP4_ERR_SHAPE otherwise); no workspace; one launch
+ * that reads every weight byte once.
+ */
+fp4_status fp4_gemm_w4a16(int fmt, const void* x_bf16, int64_t m, const void* w_codes, const void* w_scales,
+                          const float* w_global, int64_t n, int64_t k, void* out_bf16, void* stream);
+
 /* ---------------------------------------------------------- fused MoE */
 
 /*

@@ -10,6 +10,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "w4a16.h"
 
 namespace fp4 {
 
@@ -451,6 +452,23 @@ extern "C" fp4_status fp4_gemm_prequant(int fmt, const void* a_codes, const void
     return enqueue_gemm(fmt, static_cast<const uint8_t*>(a_codes), static_cast<const uint8_t*>(a_scales), a_global,
                         m, static_cast<const uint8_t*>(w_codes), static_cast<const uint8_t*>(w_scales), w_global, n,
                         k, out, static_cast<float*>(ws), false, (cudaStream_t)stream);
+}
+
+extern "C" fp4_status fp4_gemm_w4a16(int fmt, const void* x, int64_t m, const void* w_codes, const void* w_scales,
+                                     const float* w_global, int64_t n, int64_t k, void* out, void* stream) {
+    TRY(validate_gemm_common(fmt, m, w_codes, w_scales, w_global, n, k, out));
+    CHECK_OR_RETURN(m <= kW4A16MaxM, FP4_ERR_SHAPE, "m = %lld: the weight-only path takes at most %d rows",
+                    (long long)m, kW4A16MaxM);
+    CHECK_OR_RETURN(k <= kW4A16MaxK, FP4_ERR_SHAPE, "k = %lld: the weight-only path takes k <= %d", (long long)k,
+                    kW4A16MaxK);
+    if (m == 0 || n == 0) return check_arch();
+    CHECK_OR_RETURN(x, FP4_ERR_INVALID_ARG, "null activation pointer");
+    CHECK_OR_RETURN(aligned16(x), FP4_ERR_ALIGNMENT, "activations must be 16-byte aligned");
+    TRY(check_arch());
+    return cuda_status(launch_w4a16(fmt, static_cast<const uint16_t*>(x), (int)m, n, k,
+                                    static_cast<const uint8_t*>(w_codes), static_cast<const uint8_t*>(w_scales),
+                                    w_global, static_cast<uint16_t*>(out), (cudaStream_t)stream),
+                       "weight-only launch");
 }
 
 extern "C" fp4_status fp4_gemm(int fmt, const void* x, int64_t m, int mode, float st, const void* w_codes,

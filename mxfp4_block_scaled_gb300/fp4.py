@@ -54,6 +54,7 @@ _SIGNATURES = {
     "fp4_gemm": (_INT, [_INT, _P, _I64, _INT, _F, _P, _P, _P, _I64, _I64, _P, _P, _SZ, _P]),
     "fp4_gemm_prequant_workspace_size": (_SZ, [_INT, _I64, _I64, _I64]),
     "fp4_gemm_prequant": (_INT, [_INT, _P, _P, _P, _I64, _P, _P, _P, _I64, _I64, _P, _P, _SZ, _P]),
+    "fp4_gemm_w4a16": (_INT, [_INT, _P, _I64, _P, _P, _P, _I64, _I64, _P, _P]),
     "fp4_moe_prepack_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "fp4_moe_prepack_weights": (_INT, [_P, _P, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "fp4_moe_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I64]),
@@ -187,6 +188,19 @@ def gemm_prequant(aq, wq, out=None, workspace=None, stream=None):
     _check(L.fp4_gemm_prequant(wq.fmt, _ptr(aq.codes), _ptr(aq.scales), _ptr(aq.gscale), m, _ptr(wq.codes),
                                _ptr(wq.scales), _ptr(wq.gscale), n, k, _ptr(out), _ptr(ws),
                                0 if ws is None else ws.numel(), _stream(stream)))
+    return out
+
+
+def gemm_w4a16(x, wq, out=None, stream=None):
+    """Weight-only linear: bf16 x [m, k] (m <= 4, not quantised) times the
+    prepacked FP4 weight [n, k] -> bf16 [m, n]."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()
+    m, k = x.shape
+    n = wq.rows
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
+    _check(lib().fp4_gemm_w4a16(wq.fmt, _ptr(x), m, _ptr(wq.codes), _ptr(wq.scales), _ptr(wq.gscale), n, k,
+                                _ptr(out), _stream(stream)))
     return out
 
 

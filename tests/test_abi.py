@@ -75,6 +75,29 @@ def test_gemm_argument_errors(F):
     assert "multiple of 32" in F.lib().fp4_last_error_message().decode() or True
 
 
+def _w4a16(F, fmt=0, x=A, m=1, wc=A, wsc=A, wg=A, n=256, k=512, out=A):
+    return F.lib().fp4_gemm_w4a16(fmt, x, m, wc, wsc, wg, n, k, out, None)
+
+
+def test_w4a16_argument_errors(F):
+    c = F.STATUS_CODE
+    assert _w4a16(F, m=5) == c["FP4_ERR_SHAPE"]  # more rows than the weight-only path takes
+    assert "at most 4" in F.lib().fp4_last_error_message().decode()
+    assert _w4a16(F, k=8192 + 32) == c["FP4_ERR_SHAPE"]
+    assert _w4a16(F, k=48) == c["FP4_ERR_SHAPE"]
+    assert _w4a16(F, n=12) == c["FP4_ERR_SHAPE"]
+    assert _w4a16(F, m=-1) == c["FP4_ERR_SHAPE"]
+    assert _w4a16(F, fmt=3) == c["FP4_ERR_INVALID_ARG"]
+    assert _w4a16(F, x=0) == c["FP4_ERR_INVALID_ARG"]
+    assert _w4a16(F, wc=0) == c["FP4_ERR_INVALID_ARG"]
+    assert _w4a16(F, wg=0) == c["FP4_ERR_MISSING_SCALE"]
+    assert _w4a16(F, x=A + 4) == c["FP4_ERR_ALIGNMENT"]
+    assert _w4a16(F, out=A + 2) == c["FP4_ERR_ALIGNMENT"]
+    # MXFP4 has no global scale: NULL is accepted (the call then fails only on
+    # the missing GPU, never on the scale)
+    assert _w4a16(F, fmt=1, wg=0) != c["FP4_ERR_MISSING_SCALE"]
+
+
 @pytest.mark.parametrize("st", [0.0, -1.0, float("nan"), float("inf")])
 def test_static_scale_must_be_positive_finite(F, st):
     # the zeroed-alpha failure mode: a missing scale must never become 0

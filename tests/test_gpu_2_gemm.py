@@ -177,3 +177,53 @@ def test_mxfp4_full_size(F, O):
     a = I.randn_bf16((2048, 7168), 4)
     w = I.weights_bf16(2048, 7168, 104)
     check_linear(F, O, a, w, 1)
+
+
+# ------------------------------------------------------ weight-only (W4A16)
+
+def check_w4a16(F, O, x, w, fmt, qw=None):
+    wq = F.prepack_weight(w.cuda(), fmt)
+    got = bf16_to_np(F.gemm_w4a16(x.cuda(), wq))
+    torch.cuda.synchronize()
+    F.device_status()
+    cw, sw, gw = qw if qw is not None else O.quantize(fmt, I.u16(w))
+    ref, mag = O.linear_w4a16(fmt, I.u16(x), cw, sw, gw)
+    check_close(got, ref, mag)
+
+
+# ragged rows of codes (k = 800: a partial 512-byte warp load), the one-lane
+# row (k = 32), rows per CTA not dividing n, and the wide-row kernel
+# (k > 4096: up to eight warp loads per row, k = 4128 needs five)
+@pytest.mark.parametrize("m,n,k", [(1, 256, 512), (2, 520, 800), (3, 1000, 1056), (4, 264, 4096), (1, 8, 32),
+                                   (2, 1032, 4128), (4, 128, 8192)])
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_w4a16_shapes(F, O, m, n, k, fmt):
+    check_w4a16(F, O, I.activations_with_outliers(m, k, m + 5 * k), I.weights_bf16(n, k, n + 11), fmt)
+
+
+def test_w4a16_empty_and_zero(F):
+    w = I.weights_bf16(256, 512, 1).cuda()
+    wq = F.prepack_weight(w)
+    assert F.gemm_w4a16(torch.empty((0, 512), dtype=torch.bfloat16, device="cuda"), wq).shape == (0, 256)
+    out = F.gemm_w4a16(torch.zeros((3, 512), dtype=torch.bfloat16, device="cuda"), wq)
+    torch.cuda.synchronize()
+    assert not out.float().abs().sum().item()
+
+
+def test_w4a16_rejects_five_rows(F):
+    wq = F.prepack_weight(I.weights_bf16(256, 512, 1).cuda())
+    with pytest.raises(F.FP4Error):
+        F.gemm_w4a16(torch.zeros((5, 512), dtype=torch.bfloat16, device="cuda"), wq)
+
+
+@pytest.mark.parametrize("m", [1, 4])
+def test_w4a16_full_size(F, O, decode_weights, m):
+    """Weight-only decode, NVFP4 W [14336, 4096], activations with 0.1%
+    outliers x50: every output element."""
+    w, qw = decode_weights
+    check_w4a16(F, O, I.activations_with_outliers(m, 4096, 3), w, 0, qw)
+
+
+def test_w4a16_mxfp4_full_size(F, O):
+    """Weight-only decode, MXFP4 W [4096, 7168], m = 2: every output element."""
+    check_w4a16(F, O, I.activations_with_outliers(2, 7168, 5), I.weights_bf16(4096, 7168, 105), 1)
