@@ -93,6 +93,14 @@ def reduce_sum(v, ws):
     return float(t[0])
 
 
+def aggregate(units_per_step, steps, ms_local, ws):
+    """Whole-job rate over the ranks (weak scaling, each rank the same work):
+    the units all ranks processed divided by the slowest rank's time.
+    Returns (units per second, that time in ms per step)."""
+    ms_max = reduce_max(ms_local, ws)
+    return reduce_sum(units_per_step * steps, ws) / (ms_max * 1e-3 * steps), ms_max
+
+
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -282,9 +290,9 @@ def run_ours(args, rank, local, ws):
     fp4.device_status()
 
     ms = statistics.mean(tot)
-    ms_max = reduce_max(ms, ws)
     flops = 2.0 * M * N * K
-    value = reduce_sum(flops * args.steps, ws) / (ms_max * 1e-3 * args.steps) / 1e12
+    rate, ms_max = aggregate(flops, args.steps, ms, ws)
+    value = rate / 1e12
     gemm_ms = statistics.mean(pp[1] for pp in parts)
     quant_ms = statistics.mean(pp[0] for pp in parts)
     peak_fp4 = peaks["bf16_sustained"] * FP4_PER_BF16
