@@ -202,6 +202,20 @@ fp4_status fp4_gemm_prequant(int fmt, const void* a_codes, const void* a_scales,
                              void* out_bf16, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * MXFP8 quantiser (E4M3 elements): "vLLM per-format kernel capability
+ * matrix" lists MXFP8 with group size 32.  Per 32-element block of a row,
+ * e = floor(log2 amax_b) - 8 (8 = the largest E4M3 exponent), clamped to
+ * [-127, 127], stored as the E8M0 byte e + 127; each element is
+ * E4M3_rne_satfinite(x * 2^-e) (saturating at +-448, the sign of a value
+ * that rounds to zero kept); an all-zero block gets scale byte 0 and code 0.
+ * x_bf16 [rows, k]; codes [rows, k], one E4M3 byte per element; scales in the
+ * MMA layout of MXFP4 (fp4_scales_bytes(FP4_MXFP4, rows, k) bytes, padding
+ * written as 0).  All 16-byte aligned; k a positive multiple of 32.  No
+ * workspace.  This is the quantiser alone: no GEMM takes MXFP8 operands yet.
+ */
+fp4_status fp4_quantize_mxfp8(const void* x_bf16, int64_t rows, int64_t k, void* codes, void* scales, void* stream);
+
+/*
  * Weight-only (W4A16) linear for decode: out[m, n] = bf16( s_gW * sum_k
  * x[m, k] * E2M1(w)[n, k] * s_b[n, k / B] ) with the bf16 activations used as
  * they are, not quantised ("vLLM on DGX Spark: technical report", section 5.3

@@ -10,6 +10,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "mxfp8.h"
 #include "w4a16.h"
 
 namespace fp4 {
@@ -452,6 +453,21 @@ extern "C" fp4_status fp4_gemm_prequant(int fmt, const void* a_codes, const void
     return enqueue_gemm(fmt, static_cast<const uint8_t*>(a_codes), static_cast<const uint8_t*>(a_scales), a_global,
                         m, static_cast<const uint8_t*>(w_codes), static_cast<const uint8_t*>(w_scales), w_global, n,
                         k, out, static_cast<float*>(ws), false, (cudaStream_t)stream);
+}
+
+extern "C" fp4_status fp4_quantize_mxfp8(const void* x, int64_t rows, int64_t k, void* codes, void* scales,
+                                         void* stream) {
+    TRY(check_rows(rows, "rows"));
+    TRY(check_k(k));
+    if (rows == 0) return check_arch();
+    CHECK_OR_RETURN(x && codes && scales, FP4_ERR_INVALID_ARG, "null input, codes or scales pointer");
+    CHECK_OR_RETURN(aligned16(x) && aligned16(codes) && aligned16(scales), FP4_ERR_ALIGNMENT,
+                    "input, codes and scales must be 16-byte aligned");
+    TRY(check_arch());
+    const DeviceInfo* d = current_device();
+    return cuda_status(launch_mxfp8_quant(static_cast<const uint16_t*>(x), rows, k, static_cast<uint8_t*>(codes),
+                                          static_cast<uint8_t*>(scales), d->sm_count, (cudaStream_t)stream),
+                       "MXFP8 quantise launch");
 }
 
 extern "C" fp4_status fp4_gemm_w4a16(int fmt, const void* x, int64_t m, const void* w_codes, const void* w_scales,

@@ -55,6 +55,7 @@ _SIGNATURES = {
     "fp4_gemm_prequant_workspace_size": (_SZ, [_INT, _I64, _I64, _I64]),
     "fp4_gemm_prequant": (_INT, [_INT, _P, _P, _P, _I64, _P, _P, _P, _I64, _I64, _P, _P, _SZ, _P]),
     "fp4_gemm_w4a16": (_INT, [_INT, _P, _I64, _P, _P, _P, _I64, _I64, _P, _P]),
+    "fp4_quantize_mxfp8": (_INT, [_P, _I64, _I64, _P, _P, _P]),
     "fp4_moe_prepack_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "fp4_moe_prepack_weights": (_INT, [_P, _P, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "fp4_moe_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I64]),
@@ -189,6 +190,18 @@ def gemm_prequant(aq, wq, out=None, workspace=None, stream=None):
                                _ptr(wq.scales), _ptr(wq.gscale), n, k, _ptr(out), _ptr(ws),
                                0 if ws is None else ws.numel(), _stream(stream)))
     return out
+
+
+def quantize_mxfp8(x, stream=None):
+    """bf16 [rows, k] (CUDA) -> (codes [rows, k] uint8 E4M3, scales flat uint8
+    E8M0 in the MMA layout)."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()
+    rows, k = x.shape
+    L = lib()
+    codes = torch.empty((rows, k), dtype=torch.uint8, device=x.device)
+    scales = torch.empty(L.fp4_scales_bytes(MXFP4, rows, k), dtype=torch.uint8, device=x.device)
+    _check(L.fp4_quantize_mxfp8(_ptr(x), rows, k, _ptr(codes), _ptr(scales), _stream(stream)))
+    return codes, scales
 
 
 def gemm_w4a16(x, wq, out=None, stream=None):

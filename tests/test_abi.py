@@ -79,6 +79,17 @@ def _w4a16(F, fmt=0, x=A, m=1, wc=A, wsc=A, wg=A, n=256, k=512, out=A):
     return F.lib().fp4_gemm_w4a16(fmt, x, m, wc, wsc, wg, n, k, out, None)
 
 
+def test_mxfp8_quantize_argument_errors(F):
+    c = F.STATUS_CODE
+    q = lambda x=A, rows=16, k=512, codes=A, scales=A: F.lib().fp4_quantize_mxfp8(x, rows, k, codes, scales, None)
+    assert q(k=48) == c["FP4_ERR_SHAPE"]
+    assert q(k=0) == c["FP4_ERR_SHAPE"]
+    assert q(rows=-1) == c["FP4_ERR_SHAPE"]
+    assert q(x=0) == c["FP4_ERR_INVALID_ARG"]
+    assert q(scales=0) == c["FP4_ERR_INVALID_ARG"]
+    assert q(codes=A + 8) == c["FP4_ERR_ALIGNMENT"]
+
+
 def test_w4a16_argument_errors(F):
     c = F.STATUS_CODE
     assert _w4a16(F, m=5) == c["FP4_ERR_SHAPE"]  # more rows than the weight-only path takes
