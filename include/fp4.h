@@ -150,7 +150,7 @@ fp4_status fp4_quantize_act(int fmt, const void* x_bf16, int64_t rows, int64_t k
  * device memory: code that runs under another component's memory plan (a
  * framework that forbids allocation on its hot path, a pre-built CUDA graph
  * with fixed buffers, a real-time loop) or a C caller with no device
- * allocator.  The paper has no counterpart to this entry point.
+ * allocator.  No layer the source pages describe has this entry point.
  * Same arguments, results and errors as fp4_quantize_act, minus the
  * workspace: the dynamic NVFP4 amax partials go to a static device array of
  * 1024 floats (4 KiB) that every GPU loading the library keeps until the
