@@ -500,6 +500,7 @@ def run_secondary(torch, fp4, L, I, dev, peaks):
                                       "frac_fp4_peak": round(fl / (ms * 1e-3) / 1e12 /
                                                              (peaks["bf16"] * FP4_PER_BF16), 4),
                                       "note": "quantise (one pass) + GEMM, L2 flushed between steps"}
+    out["mxfp8_quant_m8192_k4096"] = run_mxfp8_quant(torch, fp4, L, I, dev, hbm, flush_buf)
     # the prefill config's other width: M=8192, K=4096, N=4096, NVFP4; the GEMM on
     # pre-quantised activations (graded against the tensor roofline) and the
     # layer call with the activations quantised per call
@@ -530,6 +531,31 @@ def run_secondary(torch, fp4, L, I, dev, peaks):
     out["single_linear_m16_k512_n256"] = {"us": round(ms * 1e3, 2), "note": "quantise + GEMM, CUDA graph"}
     out.update(run_moe(torch, fp4, L, I, dev, peaks))
     return out
+
+
+def run_mxfp8_quant(torch, fp4, L, I, dev, hbm, flush_buf):
+    """The MXFP8 (E4M3) quantiser on the prefill activations [8192, 4096],
+    L2 flushed between steps.  Algorithmic bytes: the bf16 input once, one
+    code byte per element and one scale byte per 32 elements.  A failure is
+    recorded in the line instead of ending the bench."""
+    try:
+        a = I.randn_bf16((M, K), 2).to(dev)
+        codes = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        scales = torch.empty(L.fp4_scales_bytes(fp4.MXFP4, M, K), dtype=torch.uint8, device=dev)
+        stream = fp4._stream()
+        p = fp4._ptr
+
+        def step(_):
+            fp4._check(L.fp4_quantize_mxfp8(p(a), M, K, p(codes), p(scales), stream))
+
+        tot, _ = time_steps(torch, 20, 3, step, flush=flush_buf.zero_)
+        ms = statistics.mean(tot)
+        byt = M * K * 2 + M * K + M * K // 32
+        return {"us": round(ms * 1e3, 2), "GB/s": round(byt / (ms * 1e-3) / 1e9, 1),
+                "frac_hbm": round(byt / (ms * 1e-3) / 1e9 / hbm, 4),
+                "note": "one launch, one thread per 32-element block; L2 flushed between steps"}
+    except Exception as e:  # reported, not raised: this line is secondary
+        return {"error": repr(e)[:300]}
 
 
 MOE_E, MOE_K, MOE_H, MOE_I = 128, 8, 2048, 768
