@@ -119,6 +119,14 @@ void fp4_set_arch_override(int sm);
  * FP4_ERR_INVALID_ARG for a value outside 0..3 (the policy is unchanged). */
 fp4_status fp4_set_gemm_tile_policy(int policy);
 
+/* Test hook (host-side, no device needed): the plan fp4_gemm /
+ * fp4_gemm_prequant would use for an m x n x k GEMM on a device with
+ * `sm_count` SMs under the current tile policy.  out[0] = 1 for the
+ * small-m (swapped-operand) path, out[1] = the tile width on the MMA's N side,
+ * out[2] = the number of K splits, out[3] = 1 for the CTA-pair kernel,
+ * out[4] = 1 when fp4_gemm takes the fused decode kernel.  max_out >= 5. */
+fp4_status fp4_debug_plan_gemm(int64_t m, int64_t n, int64_t k, int sm_count, int64_t* out, int max_out);
+
 /* Test hook for failure detection: launches one tiny kernel whose thread waits
  * on a barrier that nothing completes, with a wait limit of `limit_us`
  * microseconds; the wait gives up, sets the device flag and returns, leaving

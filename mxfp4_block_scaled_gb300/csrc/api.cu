@@ -353,6 +353,28 @@ static GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int sms) {
     return p;
 }
 
+// fp4_gemm's choice of the fused decode kernel (activation quantisation
+// inside the GEMM launch): automatic for m <= kDecodeFusedAutoMaxM when the
+// weight has tiles for at least half the SMs, forced by tile policy 3.
+static bool use_fused_decode(int64_t m, int64_t n, int64_t k, int sms) {
+    const bool want = g_tile_policy == 3 ||
+                      (g_tile_policy == 0 && m <= kDecodeFusedAutoMaxM && (n + 127) / 128 >= (int64_t)sms / 2);
+    return m <= kDecodeFusedMaxM && k <= kDecodeFusedMaxK && want;
+}
+
+extern "C" fp4_status fp4_debug_plan_gemm(int64_t m, int64_t n, int64_t k, int sm_count, int64_t* out,
+                                          int max_out) {
+    CHECK_OR_RETURN(m > 0 && n > 0 && k > 0 && sm_count > 0 && out && max_out >= 5, FP4_ERR_INVALID_ARG,
+                    "plan query needs positive sizes, an SM count and room for 5 entries");
+    const GemmPlan p = plan_gemm(m, n, k, sm_count);
+    out[0] = p.decode ? 1 : 0;
+    out[1] = p.bn;
+    out[2] = p.splits;
+    out[3] = p.pair ? 1 : 0;
+    out[4] = use_fused_decode(m, n, k, sm_count) ? 1 : 0;
+    return FP4_OK;
+}
+
 static size_t gemm_prequant_ws(int64_t m, int64_t n, int64_t k, int sms) {
     GemmPlan p = plan_gemm(m, n, k, sms);
     if (p.decode && p.splits > 1) return align256((size_t)p.splits * (size_t)m * (size_t)n * 4);
@@ -507,9 +529,7 @@ extern "C" fp4_status fp4_gemm(int fmt, const void* x, int64_t m, int mode, floa
     base += align256(fp4_scales_bytes(fmt, m, k));
     float* ag = reinterpret_cast<float*>(base);
     const DeviceInfo* d = current_device();
-    const bool fused = g_tile_policy == 3 || (g_tile_policy == 0 && m <= kDecodeFusedAutoMaxM &&
-                                              (n + 127) / 128 >= (int64_t)d->sm_count / 2);
-    if (m <= kDecodeFusedMaxM && k <= kDecodeFusedMaxK && fused) {
+    if (use_fused_decode(m, n, k, d->sm_count)) {
         // decode: one launch (in-kernel activation quantisation, one CTA per
         // 128 weight rows, no split-K); the activation s_g goes to the workspace
         return cuda_status(launch_decode_fused(fmt, static_cast<const uint16_t*>(x), (int)m, n, k,

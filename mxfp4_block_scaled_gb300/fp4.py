@@ -46,6 +46,7 @@ _SIGNATURES = {
     "fp4_set_arch_override": (None, [_INT]),
     "fp4_set_gemm_tile_policy": (_INT, [_INT]),
     "fp4_debug_timeout_probe": (_INT, [_I64, _P]),
+    "fp4_debug_plan_gemm": (_INT, [_I64, _I64, _I64, _INT, ctypes.POINTER(ctypes.c_int64), _INT]),
     "fp4_quantize_workspace_size": (_SZ, [_INT, _I64, _I64]),
     "fp4_quantize_act": (_INT, [_INT, _P, _I64, _I64, _INT, _F, _P, _P, _P, _P, _SZ, _P]),
     "fp4_quantize_act_noalloc": (_INT, [_INT, _P, _I64, _I64, _INT, _F, _P, _P, _P, _P]),
@@ -223,6 +224,13 @@ TILE_AUTO, TILE_ONE_CTA, TILE_CTA_PAIR, TILE_FUSED_DECODE = 0, 1, 2, 3
 def set_gemm_tile_policy(policy):
     """Choose the GEMM kernels (TILE_AUTO, TILE_ONE_CTA, TILE_CTA_PAIR, TILE_FUSED_DECODE)."""
     _check(lib().fp4_set_gemm_tile_policy(int(policy)))
+
+
+def plan_gemm(m, n, k, sm_count):
+    """The GEMM plan for m x n x k on `sm_count` SMs (host-side query)."""
+    out = (ctypes.c_int64 * 5)()
+    _check(lib().fp4_debug_plan_gemm(m, n, k, sm_count, out, 5))
+    return {"small_m": bool(out[0]), "bn": out[1], "splits": out[2], "pair": bool(out[3]), "fused_decode": bool(out[4])}
 
 
 def device_status(stream=None):

@@ -150,3 +150,48 @@ def test_tile_policy_validation(F):
         assert "tile policy" in L.fp4_last_error_message().decode()
     with pytest.raises(F.FP4Error):
         F.set_gemm_tile_policy(7)
+
+
+# ------------------------------------------------------ GEMM planner (host)
+
+SMS = 152  # GB300
+
+
+def test_plan_prefill_tile_width(F):
+    """256-wide tiles when 1.5 x their waves do not exceed the 128-wide waves."""
+    assert F.plan_gemm(8192, 14336, 4096, SMS) == {"small_m": False, "bn": 256, "splits": 1, "pair": False,
+                                                    "fused_decode": False}
+    assert F.plan_gemm(8192, 4096, 4096, SMS)["bn"] == 256    # 7 waves of 256 against 14 of 128
+    assert F.plan_gemm(2048, 2048, 7168, SMS)["bn"] == 256    # one wave of 128 tiles against 1.7 waves
+    assert F.plan_gemm(256, 512, 512, SMS)["bn"] == 128       # one wave either way
+    assert F.plan_gemm(65, 264, 800, SMS)["small_m"] is False  # m > 64 is the prefill kernel
+
+
+def test_plan_decode_split_and_fused(F):
+    p = F.plan_gemm(8, 14336, 4096, SMS)
+    assert p["small_m"] and p["bn"] == 32 and p["splits"] == 1 and not p["fused_decode"]  # 112 tiles >= 76
+    assert F.plan_gemm(40, 14336, 4096, SMS)["bn"] == 64
+    # 32 weight tiles are split along K: ceil(3 x 152 / 32) = 15, at most half the 16 K blocks -> 8
+    assert F.plan_gemm(8, 4096, 4096, SMS)["splits"] == 8
+    assert F.plan_gemm(1, 14336, 4096, SMS)["fused_decode"]          # m <= 6 and tiles for half the SMs
+    assert not F.plan_gemm(1, 4096, 4096, SMS)["fused_decode"]       # 32 tiles < 76
+    assert not F.plan_gemm(7, 14336, 4096, SMS)["fused_decode"]      # above the automatic m limit
+    assert not F.plan_gemm(1, 14336, 8192 + 32, SMS)["fused_decode"]  # k above the fused kernel's limit
+
+
+def test_plan_follows_the_tile_policy(F):
+    try:
+        F.set_gemm_tile_policy(F.TILE_FUSED_DECODE)
+        assert F.plan_gemm(8, 1024, 4096, SMS)["fused_decode"]
+        assert not F.plan_gemm(9, 14336, 4096, SMS)["fused_decode"]
+        F.set_gemm_tile_policy(F.TILE_CTA_PAIR)
+        assert F.plan_gemm(8192, 14336, 4096, SMS)["pair"]
+        assert not F.plan_gemm(128, 14336, 4096, SMS)["pair"]
+        F.set_gemm_tile_policy(F.TILE_ONE_CTA)
+        assert not F.plan_gemm(1, 14336, 4096, SMS)["fused_decode"]
+    finally:
+        F.set_gemm_tile_policy(F.TILE_AUTO)
+    c = F.STATUS_CODE
+    out = (__import__("ctypes").c_int64 * 5)()
+    assert F.lib().fp4_debug_plan_gemm(0, 16, 32, SMS, out, 5) == c["FP4_ERR_INVALID_ARG"]
+    assert F.lib().fp4_debug_plan_gemm(8, 16, 32, SMS, out, 4) == c["FP4_ERR_INVALID_ARG"]
