@@ -195,3 +195,32 @@ def test_plan_follows_the_tile_policy(F):
     out = (__import__("ctypes").c_int64 * 5)()
     assert F.lib().fp4_debug_plan_gemm(0, 16, 32, SMS, out, 5) == c["FP4_ERR_INVALID_ARG"]
     assert F.lib().fp4_debug_plan_gemm(8, 16, 32, SMS, out, 4) == c["FP4_ERR_INVALID_ARG"]
+
+
+# ------------------------------------------------ MoE workspace layout (host)
+
+@pytest.mark.parametrize("T,H,I,E,k", [(0, 256, 128, 8, 2), (1, 2048, 768, 128, 8), (64, 2048, 768, 128, 8),
+                                       (4096, 2048, 768, 128, 8), (5, 256, 128, 8, 2), (40, 512, 192, 16, 4)])
+def test_moe_workspace_layout_holds_its_documented_contents(F, T, H, I, E, k):
+    import ctypes
+    L = F.lib()
+    offs = (ctypes.c_int64 * 32)()
+    n = L.fp4_moe_workspace_layout(T, H, I, E, k, offs, 32)
+    assert n == 15
+    o = [offs[i] for i in range(14)]
+    R = offs[14]
+    slots = T * k
+    # every expert's rows are padded to 128: at most 127 padding rows per expert that has any
+    assert R % 128 == 0 and R >= slots + min(slots, E) * 127 and R >= 128
+    sf = lambda kk: ((kk + 255) // 256) * 16  # NVFP4 scale columns per row, K padded to 256
+    need = [slots * 4, slots * 4, (E + 1) * 4, (E + 1) * 4, R * 4, R * H // 2, R * sf(H), E * 4, R * I * 2, E * 4,
+            E * 4, R * I // 2, R * sf(I), T * H * 4]
+    assert o[0] == 0
+    for i in range(14):
+        assert o[i] % 256 == 0
+    for i in range(13):
+        assert o[i + 1] - o[i] >= need[i], i
+    assert L.fp4_moe_workspace_size(T, H, I, E, k) >= o[13] + need[13]
+    # a short buffer gets the leading entries only
+    assert L.fp4_moe_workspace_layout(T, H, I, E, k, offs, 3) == 3
+    assert L.fp4_moe_workspace_layout(T, H, I, 0, k, offs, 32) == 0
