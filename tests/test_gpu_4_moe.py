@@ -10,6 +10,9 @@ workspace where a stage starts (oracle -> GPU only):
   5 GEMM2 + combine    (oracle requantised h injected) y within tolerance
   6 end to end         norm-wise error and the fraction of flipped requant codes
 """
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -55,7 +58,9 @@ class Case:
         return self.ws[self.off[slot]:self.off[slot] + nbytes].view(dtype).view(shape)
 
     def run(self, F, mask=None):
-        out = F.moe(self.hid_d, self.log_d, self.mw, self.k, workspace=self.ws, stage_mask=mask)
+        st = getattr(self, "static", None)
+        kw = {} if st is None else dict(mode=1, static13=st[0], static2=st[1])
+        out = F.moe(self.hid_d, self.log_d, self.mw, self.k, workspace=self.ws, stage_mask=mask, **kw)
         torch.cuda.synchronize()
         F.device_status()
         return out
@@ -70,8 +75,13 @@ class Case:
 
 
 def _stage_checks(F, O, c):
+    """Stages 1-5 against c.ref; with c.static = (static13, static2) the
+    call runs in static mode (c.ref must then be the oracle's static run):
+    stage 2 quantises each expert's rows under static13[e] and stage 4 under
+    static2[e], so there is no dynamic s_gA / s_gH to compare."""
     T, E, k, H, Inter = c.T, c.E, c.k, c.H, c.I
     r = c.ref
+    is_static = getattr(c, "static", None) is not None
     # 1. route + permute
     c.run(F, mask=1)
     ids = c.view(0, torch.int32, (T, k)).cpu().numpy()
@@ -93,7 +103,8 @@ def _stage_checks(F, O, c):
     canon = O.scales_from_mma(scales, c.R, H, 0)
     assert np.array_equal(canon[rows], r["a_scales"])
     assert np.all(canon[pad_rows] == 0)
-    assert np.float32(c.view(7, torch.float32, (E,))[0].item()) == np.float32(r["sgA"])
+    if not is_static:
+        assert np.float32(c.view(7, torch.float32, (E,))[0].item()) == np.float32(r["sgA"])
     # 3. GEMM1 + SiLU * up
     c.run(F, mask=4)
     h = bf16_to_np(c.view(8, torch.bfloat16, (c.R, Inter)))[rows]
@@ -126,9 +137,10 @@ def _stage_checks(F, O, c):
                            Inter, 0)
     assert np.array_equal(hs[rows], r["h_scales"])
     assert np.all(hs[pad_rows] == 0)
-    sgh = c.view(10, torch.float32, (E,)).cpu().numpy()
     used = r["counts"] > 0
-    assert np.array_equal(sgh[used], r["sgH"][used])
+    if not is_static:
+        sgh = c.view(10, torch.float32, (E,)).cpu().numpy()
+        assert np.array_equal(sgh[used], r["sgH"][used])
     # 5. GEMM2 + combine from the oracle's requantised h
     hcb = np.zeros((c.R, Inter // 2), dtype=np.uint8)
     hcb[rows] = r["h_codes"]
@@ -166,6 +178,15 @@ def _prep_checks(O, c, ref=None, dynamic=True):
         assert np.float32(c.view(7, torch.float32, (E,))[0].item()) == np.float32(r["sgA"])
 
 
+def _report(what, **vals):
+    """Append measured values (error norms, flip rates) as one JSON line to
+    the file named by FP4_TEST_REPORT, when that variable is set."""
+    path = os.environ.get("FP4_TEST_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(dict(test=what, **vals)) + "\n")
+
+
 def _end_to_end(F, O, c, max_norm_err=2e-2):
     out = c.run(F)
     y = bf16_to_np(out)
@@ -178,6 +199,8 @@ def _end_to_end(F, O, c, max_norm_err=2e-2):
     rows = c.gpu_rows()
     hc = c.view(11, torch.uint8, (c.R, c.I // 2)).cpu().numpy()[rows]
     flips = np.mean(hc != c.ref["h_codes"])
+    _report("moe_end_to_end", T=c.T, E=c.E, k=c.k, H=c.H, I=c.I, static=getattr(c, "static", None) is not None,
+            norm_err=float(err), requant_code_flips=float(flips))
     assert flips <= 1e-2, flips
     return err, flips
 
@@ -211,9 +234,27 @@ def test_moe_one_expert_swapped(F, O, T):
     c.log_d = c.logits.cuda()
     c.ref = O.moe(I.u16(c.hidden), c.logits.numpy(), top_k=1, q13=c.q13, q2=c.q2)
     c.padded = np.concatenate([[0], np.cumsum((c.ref["counts"] + 127) // 128 * 128)]).astype(np.int64)
+    return c
+
+
+@pytest.mark.parametrize("T", [1, 64, 4096])
+def test_moe_full_size(F, O, full_weights, T):
+    """128 experts, top-8, hidden 2048, expert intermediate 768."""
+    c = _full_case(F, O, full_weights, T)
     _stage_checks(F, O, c)
     _end_to_end(F, O, c)
     _prep_checks(O, c)
+
+
+@pytest.mark.parametrize("T", [64, 4096])
+def test_moe_static_full_size(F, O, full_weights, T):
+    """The checkpoint path with per-expert static activation scales (all
+    different) at 128 experts, top-8, hidden 2048, intermediate 768: codes
+    bit-exact per stage, h and y within tolerance."""
+    c = _full_case(F, O, full_weights, T, static=_distinct_static(128, 7))
+    _stage_checks(F, O, c)
+    _end_to_end(F, O, c)
+    _prep_checks(O, c, dynamic=False)
 
 
 def test_moe_static_scales_small(F, O):
@@ -229,6 +270,29 @@ def test_moe_static_scales_small(F, O):
     y = bf16_to_np(out)
     assert np.linalg.norm(y - ref["y"]) / np.linalg.norm(ref["y"]) < 1e-2
     _prep_checks(O, c, ref=ref, dynamic=False)
+
+
+def _distinct_static(E, seed):
+    """Per-expert static scales, all different (a swapped pair of arrays or a
+    wrong expert index changes the result): static13 near the hidden rows'
+    amax / 2688, static2 near h's."""
+    rng = np.random.default_rng(seed)
+    st13 = (rng.permutation(np.linspace(3.5, 6.0, E)) / 2688).astype(np.float32)
+    st2 = (rng.permutation(np.linspace(1.5, 5.0, E)) / 2688).astype(np.float32)
+    return st13, st2
+
+
+@pytest.mark.parametrize("T,E,k,H,Inter", [(5, 8, 2, 256, 128), (40, 16, 4, 512, 192), (300, 8, 2, 256, 128)])
+def test_moe_static_staged_small(F, O, T, E, k, H, Inter):
+    """Static mode stage by stage with a different scale per expert, through
+    the swapped (few tokens per expert) and the 128-row grouped GEMMs."""
+    c = Case(F, O, T, E, k, H, Inter, seed=50 + T, std=0.1)
+    c.static = _distinct_static(E, T)
+    c.ref = O.moe(I.u16(c.hidden), c.logits.numpy(), top_k=k, q13=c.q13, q2=c.q2, mode=1, static13=c.static[0],
+                  static2=c.static[1])
+    _stage_checks(F, O, c)
+    _end_to_end(F, O, c)
+    _prep_checks(O, c, dynamic=False)
 
 
 def test_moe_static_scales_and_errors(F, O):
@@ -285,22 +349,43 @@ def full_weights(F, O):
     return w13, w2, mw, O.quantize_experts(I.u16(w13)), O.quantize_experts(I.u16(w2))
 
 
-@pytest.mark.parametrize("T", [1, 64, 4096])
-def test_moe_full_size(F, O, full_weights, T):
-    """128 experts, top-8, hidden 2048, expert intermediate 768."""
+def _full_case(F, O, full_weights, T, static=None):
     w13, w2, mw, q13, q2 = full_weights
     c = Case.__new__(Case)
     c.T, c.E, c.k, c.H, c.I = T, 128, 8, 2048, 768
     c.hidden = I.randn_bf16((T, 2048), 3)
     c.logits = I.router_logits(T, 128, 203)
     c.mw, c.q13, c.q2 = mw, q13, q2
-    c.ref = O.moe(I.u16(c.hidden), c.logits.numpy(), top_k=8, q13=q13, q2=q2)
+    c.static = static
+    if static is None:
+        c.ref = O.moe(I.u16(c.hidden), c.logits.numpy(), top_k=8, q13=q13, q2=q2)
+    else:
+        c.ref = O.moe(I.u16(c.hidden), c.logits.numpy(), top_k=8, q13=q13, q2=q2, mode=1, static13=static[0],
+                      static2=static[1])
     c.hid_d, c.log_d = c.hidden.cuda(), c.logits.cuda()
     L = F.lib()
     c.ws = torch.zeros(L.fp4_moe_workspace_size(T, 2048, 768, 128, 8), dtype=torch.uint8, device="cuda")
     c.off = F.moe_workspace_layout(T, 2048, 768, 128, 8)
     c.R = c.off[14]
     c.padded = np.concatenate([[0], np.cumsum((c.ref["counts"] + 127) // 128 * 128)]).astype(np.int64)
+    return c
+
+
+@pytest.mark.parametrize("T", [1, 64, 4096])
+def test_moe_full_size(F, O, full_weights, T):
+    """128 experts, top-8, hidden 2048, expert intermediate 768."""
+    c = _full_case(F, O, full_weights, T)
     _stage_checks(F, O, c)
     _end_to_end(F, O, c)
     _prep_checks(O, c)
+
+
+@pytest.mark.parametrize("T", [64, 4096])
+def test_moe_static_full_size(F, O, full_weights, T):
+    """The checkpoint path with per-expert static activation scales (all
+    different) at 128 experts, top-8, hidden 2048, intermediate 768: codes
+    bit-exact per stage, h and y within tolerance."""
+    c = _full_case(F, O, full_weights, T, static=_distinct_static(128, 7))
+    _stage_checks(F, O, c)
+    _end_to_end(F, O, c)
+    _prep_checks(O, c, dynamic=False)

@@ -567,3 +567,151 @@ def test_moe_static_scales_path(O):
     r = O.moe(I.u16(hidden), logits, I.u16(w13), I.u16(w2), top_k=2, mode=O.STATIC, static13=st13, static2=st2)
     assert np.all(r["sgH"][r["counts"] > 0] == st2[0])
     assert np.isfinite(r["y"]).all() and np.abs(r["y"]).max() > 0
+
+
+# ---------------------------------------------- MoE with per-expert static scales
+#
+# "GLM-5.3-Flash on vLLM, on GB10", the account of the uninitialised MoE
+# activation scale: a checkpoint's per-expert input_scale sets each expert's
+# activation global scale, and alpha = weight_scale_2 x input_scale.  The pins
+# below use a DIFFERENT scale per expert (and different scales for the two
+# GEMMs), so a swapped pair of arrays or a wrong expert index fails them.
+
+def _distinct_static_scales(E):
+    rng = np.random.default_rng(41)
+    st13 = (rng.permutation(np.linspace(1.5, 6.0, E)) / 2688).astype(np.float32)
+    st2 = (rng.permutation(np.linspace(0.2, 0.9, E)) / 2688).astype(np.float32)
+    assert len(set(st13.tolist())) == E and len(set(st2.tolist())) == E
+    assert not set(st13.tolist()) & set(st2.tolist())
+    return st13, st2
+
+
+def test_moe_static_per_token_loop(O):
+    """Static mode against a loop over (token, slot): the token's row is
+    quantised under its expert's static13[e], GEMM1 takes alpha1 = static13[e]
+    x s_gW13[e], h is requantised under static2[e] and GEMM2 takes alpha2 =
+    static2[e] x s_gW2[e]; the combine sums the k terms by routing weight."""
+    hidden, logits, w13, w2 = _small_moe(T=7, E=4, k=2)
+    k, E = 2, 4
+    st13, st2 = _distinct_static_scales(E)
+    r = O.moe(I.u16(hidden), logits, I.u16(w13), I.u16(w2), top_k=k, mode=O.STATIC, static13=st13, static2=st2)
+    c13, s13, g13 = r["q13"]
+    c2, s2, g2 = r["q2"]
+    T = hidden.shape[0]
+    Inter = w13.shape[1] // 2
+    pos = np.empty(T * k, dtype=np.int64)
+    pos[r["order"]] = np.arange(T * k)
+    y = np.zeros((T, hidden.shape[1]))
+    hu = I.u16(hidden)
+    for t in range(T):
+        for j in range(k):
+            e = int(r["ids"][t, j])
+            ca, sa = O.quantize_nvfp4_given_scale(hu[t:t + 1], st13[e])
+            assert np.array_equal(r["a_codes"][pos[t * k + j]], ca[0])
+            assert np.array_equal(r["a_scales"][pos[t * k + j]], sa[0])
+            g, _ = O.gemm(O.NVFP4, ca, sa, st13[e], c13[e], s13[e], g13[e])
+            h = O.f32_to_bf16_exact(O.silu(g[0, :Inter]) * g[0, Inter:]).reshape(1, -1)
+            ch, sh = O.quantize_nvfp4_given_scale(h, st2[e])
+            assert np.array_equal(r["h_codes"][pos[t * k + j]], ch[0])
+            d, _ = O.gemm(O.NVFP4, ch, sh, st2[e], c2[e], s2[e], g2[e])
+            y[t] += r["weights"][t, j] * d[0]
+    assert np.allclose(r["y"], y, rtol=1e-12, atol=1e-12 * np.abs(y).max())
+    used = r["counts"] > 0
+    assert np.array_equal(r["sgH"][used], st2[used])
+
+
+def test_moe_static_scale_locality(O):
+    """Changing one expert's static13 changes only the dispatched rows of that
+    expert and the outputs of the tokens routed to it; the same for static2
+    and the requantised h.  Exchanging the two arrays changes the result."""
+    hidden, logits, w13, w2 = _small_moe(T=9, E=4, k=2)
+    k, E = 2, 4
+    st13, st2 = _distinct_static_scales(E)
+    kw = dict(top_k=k, mode=O.STATIC)
+    base = O.moe(I.u16(hidden), logits, I.u16(w13), I.u16(w2), static13=st13, static2=st2, **kw)
+    q = dict(q13=base["q13"], q2=base["q2"])
+    offs = base["offsets"]
+    tok = base["order"] // k
+    for e0 in range(E):
+        lo, hi = offs[e0], offs[e0 + 1]
+        if hi == lo:
+            continue
+        routed = np.zeros(hidden.shape[0], dtype=bool)
+        routed[np.unique(tok[lo:hi])] = True
+        rows_other = np.r_[0:lo, hi:offs[-1]]
+        s = st13.copy()
+        s[e0] *= 1.37
+        r = O.moe(I.u16(hidden), logits, static13=s, static2=st2, **q, **kw)
+        assert np.array_equal(r["a_codes"][rows_other], base["a_codes"][rows_other])
+        assert not np.array_equal(r["a_codes"][lo:hi], base["a_codes"][lo:hi])
+        assert np.array_equal(r["y"][~routed], base["y"][~routed])
+        assert not np.allclose(r["y"][routed], base["y"][routed])
+        s = st2.copy()
+        s[e0] *= 1.37
+        r = O.moe(I.u16(hidden), logits, static13=st13, static2=s, **q, **kw)
+        assert np.array_equal(r["a_codes"], base["a_codes"])
+        assert np.array_equal(r["h_codes"][rows_other], base["h_codes"][rows_other])
+        assert not np.array_equal(r["h_codes"][lo:hi], base["h_codes"][lo:hi])
+        assert np.array_equal(r["y"][~routed], base["y"][~routed])
+        assert not np.allclose(r["y"][routed], base["y"][routed])
+    swapped = O.moe(I.u16(hidden), logits, static13=st2, static2=st13, **q, **kw)
+    assert not np.allclose(swapped["y"], base["y"])
+
+
+def test_moe_static_exact_dispatch_round_trip(O):
+    """Hidden blocks on the E2M1 grid times a power of two (block maximum
+    6 x 2^j) and power-of-two static13 scales that differ per expert: every
+    dispatched row then dequantises to the hidden row exactly (the block
+    scale is 2^j / static13[e], an E4M3 power of two), so GEMM1's G equals the
+    fp64 product of the hidden rows with the dequantised W13 of the row's
+    expert, whatever static13[e] is: the per-expert scale cancels between the
+    quantiser and alpha1."""
+    T, E, k, H, Inter = 6, 4, 2, 64, 32
+    _, logits, w13, w2 = _small_moe(T=T, E=E, H=H, Inter=Inter, k=k)
+    rng = np.random.default_rng(5)
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    x = rng.choice(grid, size=(T, H)) * rng.choice([-1, 1], size=(T, H))
+    x[:, ::16] = 6.0  # each 16-element block holds its maximum 6
+    x *= np.repeat(2.0 ** rng.integers(-3, 4, size=(T, H // 16)), 16, axis=1)
+    hidden = torch.tensor(x, dtype=torch.float32).to(torch.bfloat16)
+    assert np.array_equal(hidden.double().numpy(), x)
+    st13 = np.array([2.0 ** -3, 2.0 ** -5, 2.0 ** -1, 2.0 ** -4], dtype=np.float32)
+    st2 = np.full(E, 0.5 / 2688, dtype=np.float32)
+    r = O.moe(I.u16(hidden), logits, I.u16(w13), I.u16(w2), top_k=k, mode=O.STATIC, static13=st13, static2=st2)
+    c13, s13, g13 = r["q13"]
+    tok = r["order"] // k
+    for e in range(E):
+        lo, hi = r["offsets"][e], r["offsets"][e + 1]
+        if hi == lo:
+            continue
+        deq = O.dequantize(O.NVFP4, r["a_codes"][lo:hi], r["a_scales"][lo:hi], st13[e])
+        assert np.array_equal(deq, x[tok[lo:hi]])
+        w = O.dequantize(O.NVFP4, c13[e], s13[e], g13[e])
+        assert np.allclose(r["G"][lo:hi], x[tok[lo:hi]] @ w.T, rtol=1e-12, atol=1e-12)
+
+
+def test_moe_static_scale_far_below_amax_saturates(O):
+    """A static scale far below amax / 2688 saturates: every block scale of the
+    expert's dispatched rows is E4M3 448 (byte 0x7E) and every nonzero element
+    is E2M1 +-6 (codes 0x7 / 0xF); the other experts' rows are unaffected."""
+    hidden, logits, w13, w2 = _small_moe(T=8, E=4, k=2)
+    k, E = 2, 4
+    st13, st2 = _distinct_static_scales(E)
+    base = O.moe(I.u16(hidden), logits, I.u16(w13), I.u16(w2), top_k=k, mode=O.STATIC, static13=st13,
+                 static2=st2)
+    e0 = int(np.argmax(base["counts"]))
+    s = st13.copy()
+    s[e0] = 1e-12
+    r = O.moe(I.u16(hidden), logits, top_k=k, mode=O.STATIC, static13=s, static2=st2, q13=base["q13"],
+              q2=base["q2"])
+    lo, hi = r["offsets"][e0], r["offsets"][e0 + 1]
+    assert hi > lo
+    assert np.all(r["a_scales"][lo:hi] == 0x7E)
+    codes = r["a_codes"][lo:hi]
+    nib = np.stack([codes & 0xF, codes >> 4], axis=-1).reshape(hi - lo, -1)
+    xs = I.u16(hidden)[r["order"][lo:hi] // k]
+    nonzero = (xs & 0x7FFF) != 0
+    assert np.all((nib[nonzero] & 7) == 7)
+    assert np.array_equal((nib >> 3).astype(bool)[nonzero], (xs >> 15).astype(bool)[nonzero])
+    rest = np.r_[0:lo, hi:r["offsets"][-1]]
+    assert np.array_equal(r["a_codes"][rest], base["a_codes"][rest])
