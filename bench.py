@@ -46,6 +46,9 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-secondary", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--oracle-sample-s", type=float, default=None,
+                   help="internal: time the oracle on a sample of about this many seconds in this process "
+                        "(used for the one-thread CPU baseline) and print one JSON line")
     p.add_argument("--profile", action="store_true",
                    help="only the layer calls (warmup + steps), for ncu captures")
     p.add_argument("--workload", default="prefill",
@@ -225,6 +228,43 @@ def time_steps(torch, steps, warmup, step_fn, flush=None, marks=0):
     return tot, parts
 
 
+def sm_count(torch, local):
+    return torch.cuda.get_device_properties(local).multi_processor_count
+
+
+def clock_probe(torch, local, fn, kblocks_per_cta, seconds=0.6):
+    """The kernel launched back to back (no flush) for about `seconds` with
+    nvidia-smi sampling the SM clock every 20 ms: mean kernel time, the
+    median SM clock under load, and their product per K block of the
+    busiest CTA (cycles per K block; a bound that follows the SM clock keeps
+    this constant as the clock moves)."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(10):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    per = e0.elapsed_time(e1) / 10
+    n = max(20, int(seconds * 1e3 / max(per, 1e-3)))
+    cs = ClockSampler(local)
+    cs.start()
+    time.sleep(0.1)
+    e0.record()
+    for _ in range(n):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    ck = cs.stop()
+    us = e0.elapsed_time(e1) / n * 1e3
+    mhz = ck.get("sm_mhz")
+    return {"kernel_us": round(us, 2), "launches": n, "sm_mhz_median": mhz, "samples": ck.get("samples"),
+            "reasons": ck.get("reasons"), "kblocks_per_cta": kblocks_per_cta,
+            "cycles_per_kblock": round(us * mhz / kblocks_per_cta, 1) if mhz else None}
+
+
 # ------------------------------------------------------------ our arm
 
 def run_ours(args, rank, local, ws):
@@ -295,9 +335,17 @@ def run_ours(args, rank, local, ws):
     value = rate / 1e12
     gemm_ms = statistics.mean(pp[1] for pp in parts)
     quant_ms = statistics.mean(pp[0] for pp in parts)
-    peak_fp4 = peaks["bf16_sustained"] * FP4_PER_BF16
+    # the GEMM kernel is timed on its own (a ~0.16 ms launch between flushes):
+    # graded against the burst peak; the sustained one is reported beside it
+    peak_fp4 = peaks["bf16"] * FP4_PER_BF16
+    peak_fp4_sus = peaks["bf16_sustained"] * FP4_PER_BF16
     achieved = flops / (gemm_ms * 1e-3) / 1e12
     traffic = profile_traffic("gemm_nvfp4_prefill_m8192_n14336_k4096.md", GEMM_SOURCES)
+    # SM clock while the GEMM runs: back-to-back launches for ~0.6 s, sampled
+    kb_per_cta = -(-(-(-M // 128) * -(-N // 256)) // sm_count(torch, local)) * -(-K // 256)
+    ck_gemm = clock_probe(torch, local, lambda: fp4._check(L.fp4_gemm_prequant(
+        0, p(aq.codes), p(aq.scales), p(aq.gscale), M, p(wq.codes), p(wq.scales), p(wq.gscale), N, K, p(out),
+        p(gws), gws.numel(), stream)), kb_per_cta)
 
     # end to end through the public API with host buffers
     e2e = run_e2e(torch, fp4, L, a_cpu, wq, dev, max(4, args.steps // 2))
@@ -312,9 +360,12 @@ def run_ours(args, rank, local, ws):
         "roofline": {"bound": "tensor", "kernel": "gemm_kernel<256, NVFP4, bf16 epilogue>",
                      "achieved": round(achieved, 1), "peak": round(peak_fp4, 1), "unit": "TFLOP/s",
                      "frac": round(achieved / peak_fp4, 4), "traffic": traffic,
-                     "peak_source": "%s bf16 sustained %.1f TF/s x %.0f (nominal FP4:bf16)" % (
-                         peaks["source"], peaks["bf16_sustained"], FP4_PER_BF16),
-                     "kernel_ms": round(gemm_ms, 5)},
+                     "peak_source": "%s bf16 burst %.1f TF/s x %.0f (nominal FP4:bf16): the kernel is timed "
+                                    "alone" % (peaks["source"], peaks["bf16"], FP4_PER_BF16),
+                     "frac_of_sustained": round(achieved / peak_fp4_sus, 4),
+                     "sustained_peak": round(peak_fp4_sus, 1),
+                     "kernel_ms": round(gemm_ms, 5),
+                     "sustained_clock": ck_gemm},
         "quantiser": {"ms": round(quant_ms, 5),
                       "gbs": round((M * K * 2 + M * K / 2 + M * K / 16) / (quant_ms * 1e-3) / 1e9, 1),
                       "note": "algorithmic bytes: bf16 read once + codes + scales written"},
@@ -496,10 +547,19 @@ def run_secondary(torch, fp4, L, I, dev, peaks):
     tot, _ = time_steps(torch, 20, 3, lambda _: fp4.gemm(a, wq, out=o, workspace=ws), flush=flush_buf.zero_)
     ms = statistics.mean(tot)
     fl = 2.0 * 2048 * 2048 * 7168
+    aq = fp4.quantize(a, fp4.MXFP4)
+    tot, _ = time_steps(torch, 20, 3, lambda _: fp4.gemm_prequant(aq, wq, out=o), flush=flush_buf.zero_)
+    ms_g = statistics.mean(tot)
+    peak_b = peaks["bf16"] * FP4_PER_BF16
     out["mxfp4_m2048_k7168_n2048"] = {"us": round(ms * 1e3, 2), "TFLOP/s": round(fl / (ms * 1e-3) / 1e12, 1),
-                                      "frac_fp4_peak": round(fl / (ms * 1e-3) / 1e12 /
-                                                             (peaks["bf16"] * FP4_PER_BF16), 4),
-                                      "note": "quantise (one pass) + GEMM, L2 flushed between steps"}
+                                      "frac_fp4_peak": round(fl / (ms * 1e-3) / 1e12 / peak_b, 4),
+                                      "gemm_us": round(ms_g * 1e3, 2),
+                                      "gemm_TFLOP/s": round(fl / (ms_g * 1e-3) / 1e12, 1),
+                                      "gemm_frac_fp4_peak": round(fl / (ms_g * 1e-3) / 1e12 / peak_b, 4),
+                                      "note": "quantise (one pass) + GEMM / GEMM alone on pre-quantised "
+                                              "activations; L2 flushed between steps; fraction of the measured "
+                                              "burst FP4 peak"}
+    del aq
     out["mxfp8_quant_m8192_k4096"] = run_mxfp8_quant(torch, fp4, L, I, dev, hbm, flush_buf)
     # the prefill config's other width: M=8192, K=4096, N=4096, NVFP4; the GEMM on
     # pre-quantised activations (graded against the tensor roofline) and the
@@ -514,13 +574,13 @@ def run_secondary(torch, fp4, L, I, dev, peaks):
     ms_g = statistics.mean(tot)
     tot, _ = time_steps(torch, 20, 3, lambda _: fp4.gemm(a, wq, out=o, workspace=ws), flush=flush_buf.zero_)
     ms_q = statistics.mean(tot)
-    peak_s = peaks["bf16_sustained"] * FP4_PER_BF16
+    peak_b = peaks["bf16"] * FP4_PER_BF16
     out["prefill_m8192_k4096_n4096"] = {
         "gemm_us": round(ms_g * 1e3, 2), "gemm_TFLOP/s": round(fl / (ms_g * 1e-3) / 1e12, 1),
-        "frac_fp4_peak": round(fl / (ms_g * 1e-3) / 1e12 / peak_s, 4),
+        "frac_fp4_peak": round(fl / (ms_g * 1e-3) / 1e12 / peak_b, 4),
         "layer_us": round(ms_q * 1e3, 2), "layer_TFLOP/s": round(fl / (ms_q * 1e-3) / 1e12, 1),
         "note": "GEMM on pre-quantised activations / quantise + GEMM; L2 flushed between steps; "
-                "fraction of the measured sustained FP4 peak"}
+                "fraction of the measured burst FP4 peak"}
     del a, aq, o, ws
     # the single-linear correctness config: A [16, 512], W [256, 512] (latency-bound)
     a = I.randn_bf16((16, 512), 0).to(dev)
@@ -616,7 +676,9 @@ def oracle_sample(rows, a_cpu=None, qw=None):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(target_s=12.0):
+def oracle_timed_sample(target_s):
+    """The oracle on a row sample of the prefill workload sized for about
+    target_s seconds (at most the whole workload): (rows, seconds)."""
     import oracle as O
     from mxfp4_block_scaled_gb300 import inputs as I
     w_cpu = I.weights_bf16(N, K, 102)
@@ -630,12 +692,36 @@ def cpu_baseline(target_s=12.0):
     t256 = oracle_sample(256, a_cpu, qw)
     per_row = max((t256 - t64) / 192.0, 1e-6)
     fixed = max(t64 - 64 * per_row, 0.0)
-    rows = int(min(M, max(256, (target_s - fixed) / per_row)))
+    rows = int(min(M, max(64, (target_s - fixed) / per_row)))
     t = oracle_sample(rows, a_cpu, qw)
-    return {"value": round(2.0 * rows * N * K / t / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
-            "kind": "oracle", "seconds": round(t, 2),
-            "sample": "%d of %d activation rows (quantise + dequantise-and-fp64 GEMM vs pre-quantised W "
-                      "[14336, 4096]); numpy BLAS threads = cores" % (rows, M)}
+    return rows, t
+
+
+ONE_THREAD_ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1",
+                  "BLIS_NUM_THREADS": "1", "VECLIB_MAXIMUM_THREADS": "1", "NUMEXPR_NUM_THREADS": "1"}
+
+
+def cpu_baseline(target_s=12.0, single_s=6.0):
+    """The oracle on all host cores (numpy BLAS threads = cores) and, in a
+    child process with every BLAS / OpenMP thread count set to 1, on one
+    core; each on a row sample of the prefill workload."""
+    rows, t = oracle_timed_sample(target_s)
+    res = {"value": round(2.0 * rows * N * K / t / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+           "kind": "oracle", "seconds": round(t, 2),
+           "sample": "%d of %d activation rows (quantise + dequantise-and-fp64 GEMM vs pre-quantised W "
+                     "[14336, 4096]); numpy BLAS threads = cores" % (rows, M)}
+    env = dict(os.environ)
+    env.update(ONE_THREAD_ENV)
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample-s", str(single_s)],
+                           env=env, capture_output=True, text=True, timeout=600)
+        one = json.loads(r.stdout.strip().splitlines()[-1])
+        res["one_thread"] = {"value": round(2.0 * one["rows"] * N * K / one["seconds"] / 1e12, 6),
+                             "unit": "TFLOP/s", "cores": 1, "seconds": round(one["seconds"], 2),
+                             "sample": "%d of %d activation rows, BLAS and OpenMP threads = 1" % (one["rows"], M)}
+    except Exception as e:  # reported, not raised: the all-cores figure stands alone
+        res["one_thread"] = {"error": repr(e)[:200]}
+    return res
 
 
 def run_reference(args, rank, ws):
@@ -663,6 +749,10 @@ def run_reference(args, rank, ws):
 
 def main():
     args = parse()
+    if args.oracle_sample_s is not None:
+        rows, t = oracle_timed_sample(args.oracle_sample_s)
+        print(json.dumps({"rows": rows, "seconds": t}), flush=True)
+        return
     rank, local, ws = dist_setup(args)
     if args.impl == "reference":
         res = run_reference(args, rank, ws)

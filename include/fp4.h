@@ -11,10 +11,10 @@
  *   MXFP4: E2M1 elements, one E8M0 (power-of-two) scale per 32 elements along
  *          K, no global scale.
  * The GEMM dequantises by alpha = weight global scale x activation global
- * scale ("GLM-5.3-Flash on vLLM, on GB10", section "What the kernel does" and
- * the paragraph on the uninitialised MoE activation scale: alpha =
- * weight_scale_2 x input_scale).  All global scales in this ABI use that
- * dequantisation convention: s_g = amax / (6 x 448) for a dynamic scale.
+ * scale ("GLM-5.3-Flash on vLLM, on GB10", the opening account of the MoE
+ * activation-scale fault: each expert's alpha is weight_scale_2 x
+ * input_scale).  All global scales in this ABI use that dequantisation
+ * convention: s_g = amax / (6 x 448) for a dynamic scale.
  *
  * Memory layouts (all device memory unless stated otherwise):
  *   bf16 tensors   row-major, contiguous, 16-byte aligned base.
@@ -209,19 +209,56 @@ fp4_status fp4_gemm_prequant(int fmt, const void* a_codes, const void* a_scales,
                              const void* w_codes, const void* w_scales, const float* w_global, int64_t n, int64_t k,
                              void* out_bf16, void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------- MXFP8 / MXFP6 (8-bit containers) */
+
+/* Element formats of the wider MX formats ("vLLM per-format kernel capability
+ * matrix": MXFP6 and MXFP8 with group size 32): MXFP8 with E4M3 or E5M2
+ * elements, MXFP6 with E2M3 or E3M2 elements. */
+typedef enum { FP4_MX_E4M3 = 0, FP4_MX_E5M2 = 1, FP4_MX_E2M3 = 2, FP4_MX_E3M2 = 3 } fp4_mx_elem;
+
 /*
- * MXFP8 quantiser (E4M3 elements): "vLLM per-format kernel capability
- * matrix" lists MXFP8 with group size 32.  Per 32-element block of a row,
- * e = floor(log2 amax_b) - 8 (8 = the largest E4M3 exponent), clamped to
- * [-127, 127], stored as the E8M0 byte e + 127; each element is
- * E4M3_rne_satfinite(x * 2^-e) (saturating at +-448, the sign of a value
- * that rounds to zero kept); an all-zero block gets scale byte 0 and code 0.
- * x_bf16 [rows, k]; codes [rows, k], one E4M3 byte per element; scales in the
+ * MX quantiser with 8-bit containers.  Per 32-element block of a row,
+ * e = floor(log2 amax_b) - emax (emax = the element's largest exponent: E4M3
+ * 8, E5M2 15, E2M3 2, E3M2 4), clamped to [-127, 127], stored as the E8M0
+ * byte e + 127 -- the MXFP4 rule of "vLLM on DGX Spark: technical report",
+ * section 6.4, with the element's own emax; each element is
+ * ELEM_rne_satfinite(x * 2^-e) (saturating at the largest finite value:
+ * 448, 57344, 7.5, 28; the sign of a value that rounds to zero kept); an
+ * all-zero block gets scale byte 0 and code 0.
+ * x_bf16 [rows, k]; codes [rows, k], ONE BYTE PER ELEMENT (the FP6 codes in
+ * the low six bits, the top two bits 0: the layout the tensor cores read from
+ * shared memory, so MXFP6 is not packed to 6 bits in memory); scales in the
  * MMA layout of MXFP4 (fp4_scales_bytes(FP4_MXFP4, rows, k) bytes, padding
  * written as 0).  All 16-byte aligned; k a positive multiple of 32.  No
- * workspace.  This is the quantiser alone: no GEMM takes MXFP8 operands yet.
+ * workspace.  FP4_ERR_INVALID_ARG for an unknown element format.
  */
+fp4_status fp4_quantize_mx(int elem, const void* x_bf16, int64_t rows, int64_t k, void* codes, void* scales,
+                           void* stream);
+
+/* fp4_quantize_mx with E4M3 elements (MXFP8). */
 fp4_status fp4_quantize_mxfp8(const void* x_bf16, int64_t rows, int64_t k, void* codes, void* scales, void* stream);
+
+/*
+ * MX linear with 8-bit-container operands (MXFP8 / MXFP6, either element
+ * format on either side): out[m, n] = bf16( sum_k deq(A)[m, k] * deq(W)[n, k] )
+ * with deq = element x 2^(scale byte - 127) per 32-element block, fp32
+ * accumulation on the tensor cores (tcgen05 kind::mxf8f6f4); no global
+ * scale.  a_codes [m, k] / w_codes [n, k] and their scales as written by
+ * fp4_quantize_mx (a_elem / w_elem name their element formats).
+ * out_bf16 [m, n] row-major.  k a multiple of 32 (16-byte code rows), n a
+ * multiple of 8.  No workspace.
+ */
+fp4_status fp4_gemm_mx_prequant(int a_elem, const void* a_codes, const void* a_scales, int64_t m, int w_elem,
+                                const void* w_codes, const void* w_scales, int64_t n, int64_t k, void* out_bf16,
+                                void* stream);
+
+/* The same linear with the bf16 activations x_bf16 [m, k] quantised to a_elem
+ * on the device per call (fp4_quantize_mx into the workspace, then the GEMM).
+ * workspace: fp4_gemm_mx_workspace_size(m, k) bytes, 256-byte aligned. */
+size_t fp4_gemm_mx_workspace_size(int64_t m, int64_t k);
+fp4_status fp4_gemm_mx(int a_elem, const void* x_bf16, int64_t m, int w_elem, const void* w_codes,
+                       const void* w_scales, int64_t n, int64_t k, void* out_bf16, void* workspace,
+                       size_t workspace_bytes, void* stream);
 
 /*
  * Weight-only (W4A16) linear for decode: out[m, n] = bf16( s_gW * sum_k

@@ -25,9 +25,9 @@
 // `acc_full` barriers of both CTAs; both CTAs' epilogues release the
 // accumulator on the even CTA's `acc_empty` barrier.  Every wait is bounded;
 // the CTAs meet at cluster barriers before the first remote arrive or copy and
-// before the Tensor Memory is freed.  Waits poll at CTA scope (barriers
-// completed by the multicast MMA commit need nothing more; those with remote
-// arrivals add one cluster-scope fence after the wait).
+// before the Tensor Memory is freed.  Waits on barriers completed by the
+// multicast MMA commit poll at CTA scope; the MMA issuer's waits on barriers
+// with remote arrivals (full, acc_empty) poll with cluster-scope acquire.
 #pragma once
 
 #include "gemm_kernel.cuh"
@@ -262,13 +262,13 @@ __global__ void __launch_bounds__(512, 1)
             uint32_t ph = 0, aph = 0;
             bool ok = true, any = false;
             for (int64_t u = cid; u < units && ok; u += ncl) {
-                if (!mbar_wait_then_cluster_fence(acce, aph ^ 1u, wc, abort_flag)) {
+                if (!mbar_wait_cluster(acce, aph ^ 1u, wc, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 for (int64_t kb = 0; kb < kbt; ++kb) {
-                    if (!mbar_wait_then_cluster_fence(full + stage, ph, wc, abort_flag)) {
+                    if (!mbar_wait_cluster(full + stage, ph, wc, abort_flag)) {
                         ok = false;
                         break;
                     }

@@ -187,7 +187,7 @@ def _report(what, **vals):
             f.write(json.dumps(dict(test=what, **vals)) + "\n")
 
 
-def _end_to_end(F, O, c, max_norm_err=2e-2):
+def _end_to_end(F, O, c, max_norm_err=3e-3):
     out = c.run(F)
     y = bf16_to_np(out)
     assert np.isfinite(y).all()
@@ -201,7 +201,8 @@ def _end_to_end(F, O, c, max_norm_err=2e-2):
     flips = np.mean(hc != c.ref["h_codes"])
     _report("moe_end_to_end", T=c.T, E=c.E, k=c.k, H=c.H, I=c.I, static=getattr(c, "static", None) is not None,
             norm_err=float(err), requant_code_flips=float(flips))
-    assert flips <= 1e-2, flips
+    # measured: at most 5e-6 of the codes (T = 64), none at most shapes
+    assert flips <= 1e-4, flips
     return err, flips
 
 
@@ -268,7 +269,7 @@ def test_moe_static_scales_small(F, O):
     ref = O.moe(I.u16(c.hidden), c.logits.numpy(), top_k=k, q13=c.q13, q2=c.q2, mode=1, static13=st13,
                 static2=st2)
     y = bf16_to_np(out)
-    assert np.linalg.norm(y - ref["y"]) / np.linalg.norm(ref["y"]) < 1e-2
+    assert np.linalg.norm(y - ref["y"]) / np.linalg.norm(ref["y"]) < 3e-3
     _prep_checks(O, c, ref=ref, dynamic=False)
 
 
@@ -305,7 +306,7 @@ def test_moe_static_scales_and_errors(F, O):
     ref = O.moe(I.u16(c.hidden), c.logits.numpy(), top_k=k, q13=c.q13, q2=c.q2, mode=1, static13=st13,
                 static2=st2)
     y = bf16_to_np(out)
-    assert np.linalg.norm(y - ref["y"]) / np.linalg.norm(ref["y"]) < 1e-2
+    assert np.linalg.norm(y - ref["y"]) / np.linalg.norm(ref["y"]) < 3e-3
     _prep_checks(O, c, ref=ref, dynamic=False)
     # the zeroed-alpha failure mode is refused: no scales, or a zero scale
     with pytest.raises(F.FP4Error) as e1:
