@@ -561,6 +561,7 @@ def run_secondary(torch, fp4, L, I, dev, peaks):
                                               "burst FP4 peak"}
     del aq
     out["mxfp8_quant_m8192_k4096"] = run_mxfp8_quant(torch, fp4, L, I, dev, hbm, flush_buf)
+    out["mxfp8_gemm_m8192_k4096_n14336"] = run_mxfp8_gemm(torch, fp4, L, I, dev, peaks, flush_buf)
     # the prefill config's other width: M=8192, K=4096, N=4096, NVFP4; the GEMM on
     # pre-quantised activations (graded against the tensor roofline) and the
     # layer call with the activations quantised per call
@@ -614,6 +615,37 @@ def run_mxfp8_quant(torch, fp4, L, I, dev, hbm, flush_buf):
         return {"us": round(ms * 1e3, 2), "GB/s": round(byt / (ms * 1e-3) / 1e9, 1),
                 "frac_hbm": round(byt / (ms * 1e-3) / 1e9 / hbm, 4),
                 "note": "one launch, one thread per 32-element block; L2 flushed between steps"}
+    except Exception as e:  # reported, not raised: this line is secondary
+        return {"error": repr(e)[:300]}
+
+
+FP8_PER_BF16 = 4.5 / 2.25  # nominal dense FP8 : bf16 tensor-core throughput
+
+
+def run_mxfp8_gemm(torch, fp4, L, I, dev, peaks, flush_buf):
+    """MXFP8 (E4M3 x E4M3) linear at the prefill shape M=8192, K=4096,
+    N=14336: the GEMM alone on pre-quantised operands, and the layer with
+    the activations quantised per call; L2 flushed between steps; fractions
+    of the dense FP8 peak (measured bf16 burst x 2).  A failure is recorded
+    in the line instead of ending the bench."""
+    try:
+        a = I.randn_bf16((M, K), 2).to(dev)
+        wq = fp4.quantize_mx(I.weights_bf16(N, K, 102).to(dev), fp4.MX_E4M3)
+        aq = fp4.quantize_mx(a, fp4.MX_E4M3)
+        o = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(L.fp4_gemm_mx_workspace_size(M, K), dtype=torch.uint8, device=dev)
+        fl = 2.0 * M * N * K
+        tot, _ = time_steps(torch, 20, 3, lambda _: fp4.gemm_mx_prequant(aq, wq, out=o), flush=flush_buf.zero_)
+        ms_g = statistics.mean(tot)
+        tot, _ = time_steps(torch, 20, 3, lambda _: fp4.gemm_mx(a, wq, fp4.MX_E4M3, out=o, workspace=ws),
+                            flush=flush_buf.zero_)
+        ms_l = statistics.mean(tot)
+        peak8 = peaks["bf16"] * FP8_PER_BF16
+        return {"gemm_us": round(ms_g * 1e3, 2), "gemm_TFLOP/s": round(fl / (ms_g * 1e-3) / 1e12, 1),
+                "gemm_frac_fp8_peak": round(fl / (ms_g * 1e-3) / 1e12 / peak8, 4),
+                "layer_us": round(ms_l * 1e3, 2), "layer_TFLOP/s": round(fl / (ms_l * 1e-3) / 1e12, 1),
+                "note": "tcgen05 kind::mxf8f6f4; GEMM on pre-quantised operands / quantise + GEMM; L2 flushed "
+                        "between steps; fraction of the measured burst bf16 peak x 2"}
     except Exception as e:  # reported, not raised: this line is secondary
         return {"error": repr(e)[:300]}
 

@@ -119,6 +119,16 @@ void fp4_set_arch_override(int sm);
  * FP4_ERR_INVALID_ARG for a value outside 0..3 (the policy is unchanged). */
 fp4_status fp4_set_gemm_tile_policy(int policy);
 
+/* Tuning and test hook (no counterpart on the pages): which implementation
+ * fp4_moe_grouped uses.  0 = automatic: for 1 <= T <= 16 tokens, top_k <= 8,
+ * hidden and inter multiples of 256 and at most 2048, the one-launch MoE (a
+ * memset of its counters, then one cooperative kernel: route, quantise,
+ * GEMM1 + SwiGLU, requantise, GEMM2 and the top-k sum in slot order), else
+ * the launch chain; 1 = always the launch chain.  Results agree within the
+ * MoE tolerance under both.  Process-wide, host-side; FP4_ERR_INVALID_ARG
+ * for a value outside 0..1. */
+fp4_status fp4_set_moe_policy(int policy);
+
 /* Test hook (host-side, no device needed): the plan fp4_gemm /
  * fp4_gemm_prequant would use for an m x n x k GEMM on a device with
  * `sm_count` SMs under the current tile policy.  out[0] = 1 for the
@@ -239,12 +249,13 @@ fp4_status fp4_quantize_mx(int elem, const void* x_bf16, int64_t rows, int64_t k
 fp4_status fp4_quantize_mxfp8(const void* x_bf16, int64_t rows, int64_t k, void* codes, void* scales, void* stream);
 
 /*
- * MX linear with 8-bit-container operands (MXFP8 / MXFP6, either element
- * format on either side): out[m, n] = bf16( sum_k deq(A)[m, k] * deq(W)[n, k] )
- * with deq = element x 2^(scale byte - 127) per 32-element block, fp32
- * accumulation on the tensor cores (tcgen05 kind::mxf8f6f4); no global
- * scale.  a_codes [m, k] / w_codes [n, k] and their scales as written by
- * fp4_quantize_mx (a_elem / w_elem name their element formats).
+ * MXFP8 linear (E4M3 or E5M2 elements, either on either side):
+ * out[m, n] = bf16( sum_k deq(A)[m, k] * deq(W)[n, k] ) with deq = element x
+ * 2^(scale byte - 127) per 32-element block, fp32 accumulation on the tensor
+ * cores (tcgen05 kind::mxf8f6f4); no global scale.  a_codes [m, k] /
+ * w_codes [n, k] and their scales as written by fp4_quantize_mx (a_elem /
+ * w_elem name their element formats: FP4_MX_E4M3 or FP4_MX_E5M2; the MXFP6
+ * formats give FP4_ERR_INVALID_ARG: their codes are quantiser output only).
  * out_bf16 [m, n] row-major.  k a multiple of 32 (16-byte code rows), n a
  * multiple of 8.  No workspace.
  */
@@ -311,8 +322,10 @@ size_t fp4_moe_workspace_size(int64_t tokens, int64_t hidden, int64_t inter, int
  *   5. h requantised to NVFP4 with s_gH[e] = amax_e / 2688 (static:
  *      static_scales2[e]).
  *   6. D = alpha2_e * H_q . W2_e^T (alpha2_e = s_gH[e] * w2_global[e]).
- *   7. out[t] = bf16( sum_j weight[t, j] * D[t, j] ) (fp32 sum; the order of
- *      the top_k terms is not fixed).
+ *   7. out[t] = bf16( sum_j weight[t, j] * D[t, j] ) (fp32 sum; in the
+ *      one-launch form (fp4_set_moe_policy) the terms are added in slot order
+ *      j = 0..top_k-1 and the result is the same bits on every run; in the
+ *      launch chain their order is not fixed).
  * hidden_bf16 [T, H], router_logits fp32 [T, E], out_bf16 [T, H] (device).
  * mode FP4_SCALE_STATIC needs both host arrays static_scales13[E] and
  * static_scales2[E] (each finite and > 0, E <= 256): NULL gives
@@ -339,7 +352,14 @@ fp4_status fp4_moe_grouped(const void* hidden_bf16, const float* router_logits, 
  * R rows), 7 s_gA / static scale per expert fp32 [E], 8 h bf16 [R, I],
  * 9 amax of h per expert fp32 [E], 10 s_gH fp32 [E], 11 h codes [R, I/2],
  * 12 h scales (MMA layout), 13 fp32 output accumulator [T, H]; R = offsets
- * count 14 (the padded row capacity).  Returns the number of entries written. */
+ * count 14 (the padded row capacity).  Entries 15-21 are written by the
+ * one-launch MoE (regions sized only for the shapes it takes), all in slot
+ * order t * top_k + j: 15 h bf16 [T*k, I], 16 the requantised h codes
+ * [T*k, I/2], 17 their scale bytes [T*k, I/16] (row-major, not the MMA
+ * layout), 18 s_gH fp32 [E] (the experts with tokens), 19 D = alpha2 x GEMM2
+ * fp32 [T*k, H], 20 the dispatched hidden codes [T*k, H/2], 21 their scale
+ * bytes [T*k, H/16]; that form also writes entries 0 and 1 and (dynamic
+ * scale) s_gA in entry 7.  Returns the number of entries written. */
 int fp4_moe_workspace_layout(int64_t tokens, int64_t hidden, int64_t inter, int64_t n_experts, int64_t top_k,
                              int64_t* offsets, int max_entries);
 fp4_status fp4_moe_grouped_stages(const void* hidden_bf16, const float* router_logits, int64_t tokens,

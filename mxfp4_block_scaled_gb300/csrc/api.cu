@@ -477,8 +477,15 @@ extern "C" fp4_status fp4_gemm_prequant(int fmt, const void* a_codes, const void
                         k, out, static_cast<float*>(ws), false, (cudaStream_t)stream);
 }
 
-extern "C" fp4_status fp4_quantize_mxfp8(const void* x, int64_t rows, int64_t k, void* codes, void* scales,
-                                         void* stream) {
+static fp4_status check_mx_elem(int elem) {
+    CHECK_OR_RETURN(elem >= FP4_MX_E4M3 && elem <= FP4_MX_E3M2, FP4_ERR_INVALID_ARG, "unknown MX element format %d",
+                    elem);
+    return FP4_OK;
+}
+
+extern "C" fp4_status fp4_quantize_mx(int elem, const void* x, int64_t rows, int64_t k, void* codes, void* scales,
+                                      void* stream) {
+    TRY(check_mx_elem(elem));
     TRY(check_rows(rows, "rows"));
     TRY(check_k(k));
     if (rows == 0) return check_arch();
@@ -487,9 +494,99 @@ extern "C" fp4_status fp4_quantize_mxfp8(const void* x, int64_t rows, int64_t k,
                     "input, codes and scales must be 16-byte aligned");
     TRY(check_arch());
     const DeviceInfo* d = current_device();
-    return cuda_status(launch_mxfp8_quant(static_cast<const uint16_t*>(x), rows, k, static_cast<uint8_t*>(codes),
-                                          static_cast<uint8_t*>(scales), d->sm_count, (cudaStream_t)stream),
-                       "MXFP8 quantise launch");
+    return cuda_status(launch_mx8_quant(elem, static_cast<const uint16_t*>(x), rows, k, static_cast<uint8_t*>(codes),
+                                        static_cast<uint8_t*>(scales), d->sm_count, (cudaStream_t)stream),
+                       "MX quantise launch");
+}
+
+extern "C" fp4_status fp4_quantize_mxfp8(const void* x, int64_t rows, int64_t k, void* codes, void* scales,
+                                         void* stream) {
+    return fp4_quantize_mx(FP4_MX_E4M3, x, rows, k, codes, scales, stream);
+}
+
+// Type code of an MXFP8 element format in the kind::mxf8f6f4 instruction descriptor.
+static int mx8_type_code(int elem) { return elem == FP4_MX_E4M3 ? 0 : 1; }
+
+static fp4_status validate_gemm_mx(int a_elem, int64_t m, int w_elem, const void* w_codes, const void* w_scales,
+                                   int64_t n, int64_t k, void* out) {
+    TRY(check_mx_elem(a_elem));
+    TRY(check_mx_elem(w_elem));
+    CHECK_OR_RETURN(a_elem <= FP4_MX_E5M2 && w_elem <= FP4_MX_E5M2, FP4_ERR_INVALID_ARG,
+                    "the MX GEMM takes MXFP8 operands (E4M3 / E5M2); MXFP6 codes are quantiser output only");
+    TRY(check_rows(m, "m"));
+    TRY(check_rows(n, "n"));
+    TRY(check_k(k));
+    CHECK_OR_RETURN(n % 8 == 0, FP4_ERR_SHAPE, "n = %lld must be a multiple of 8", (long long)n);
+    if (m == 0 || n == 0) return FP4_OK;
+    CHECK_OR_RETURN(w_codes && w_scales && out, FP4_ERR_INVALID_ARG, "null weight or output pointer");
+    CHECK_OR_RETURN(aligned16(w_codes) && aligned16(w_scales) && aligned16(out), FP4_ERR_ALIGNMENT,
+                    "weights / output must be 16-byte aligned");
+    return FP4_OK;
+}
+
+// MX GEMM with 8-bit-container operands: the one-CTA kernel with the bf16
+// epilogue for every m (tile width by the same wave rule as FP4).
+static fp4_status enqueue_gemm_mx(int a_elem, const uint8_t* ac, const uint8_t* as, int64_t m, int w_elem,
+                                  const uint8_t* wc, const uint8_t* wsc, int64_t n, int64_t k, void* out, bool pdl,
+                                  cudaStream_t s) {
+    const DeviceInfo* d = current_device();
+    const int64_t sms = d->sm_count;
+    const int64_t w256 = (((m + 127) / 128) * ((n + 255) / 256) + sms - 1) / sms;
+    const int64_t w128 = (((m + 127) / 128) * ((n + 127) / 128) + sms - 1) / sms;
+    GemmLaunch g;
+    g.fmt = FMT_MX8;
+    g.p_type = mx8_type_code(a_elem);
+    g.q_type = mx8_type_code(w_elem);
+    g.k = k;
+    g.pdl = pdl;
+    g.bn = 3 * w256 <= 2 * w128 ? 256 : 128;
+    g.epi = EPI_BF16;
+    g.p_codes = ac, g.p_scales = as, g.p_rows = m, g.p_rows_valid = m;
+    g.q_codes = wc, g.q_scales = wsc, g.q_rows = n, g.q_rows_valid = n;
+    g.out = out;
+    g.ldo = n;
+    g.early_q = true;  // weights
+    return cuda_status(launch_gemm(g, s), "MX GEMM launch");
+}
+
+extern "C" fp4_status fp4_gemm_mx_prequant(int a_elem, const void* a_codes, const void* a_scales, int64_t m,
+                                           int w_elem, const void* w_codes, const void* w_scales, int64_t n,
+                                           int64_t k, void* out, void* stream) {
+    TRY(validate_gemm_mx(a_elem, m, w_elem, w_codes, w_scales, n, k, out));
+    if (m == 0 || n == 0) return check_arch();
+    CHECK_OR_RETURN(a_codes && a_scales, FP4_ERR_INVALID_ARG, "null activation codes or scales");
+    CHECK_OR_RETURN(aligned16(a_codes) && aligned16(a_scales), FP4_ERR_ALIGNMENT,
+                    "activation codes / scales must be 16-byte aligned");
+    TRY(check_arch());
+    return enqueue_gemm_mx(a_elem, static_cast<const uint8_t*>(a_codes), static_cast<const uint8_t*>(a_scales), m,
+                           w_elem, static_cast<const uint8_t*>(w_codes), static_cast<const uint8_t*>(w_scales), n, k,
+                           out, false, (cudaStream_t)stream);
+}
+
+extern "C" size_t fp4_gemm_mx_workspace_size(int64_t m, int64_t k) {
+    if (m < 0 || k <= 0) return 0;
+    return align256((size_t)m * (size_t)k) + align256(fp4_scales_bytes(FP4_MXFP4, m, k));
+}
+
+extern "C" fp4_status fp4_gemm_mx(int a_elem, const void* x, int64_t m, int w_elem, const void* w_codes,
+                                  const void* w_scales, int64_t n, int64_t k, void* out, void* ws, size_t wsb,
+                                  void* stream) {
+    TRY(validate_gemm_mx(a_elem, m, w_elem, w_codes, w_scales, n, k, out));
+    if (m == 0 || n == 0) return check_arch();
+    CHECK_OR_RETURN(x, FP4_ERR_INVALID_ARG, "null activation pointer");
+    CHECK_OR_RETURN(aligned16(x), FP4_ERR_ALIGNMENT, "activations must be 16-byte aligned");
+    const size_t need = fp4_gemm_mx_workspace_size(m, k);
+    CHECK_OR_RETURN(wsb >= need && ws && (reinterpret_cast<uintptr_t>(ws) & 255) == 0, FP4_ERR_WORKSPACE,
+                    "workspace %zu bytes, need %zu (256-byte aligned)", wsb, need);
+    TRY(check_arch());
+    uint8_t* ac = static_cast<uint8_t*>(ws);
+    uint8_t* as = ac + align256((size_t)m * (size_t)k);
+    const DeviceInfo* d = current_device();
+    cudaStream_t s = (cudaStream_t)stream;
+    TRY(cuda_status(launch_mx8_quant(a_elem, static_cast<const uint16_t*>(x), m, k, ac, as, d->sm_count, s),
+                    "MX quantise launch"));
+    return enqueue_gemm_mx(a_elem, ac, as, m, w_elem, static_cast<const uint8_t*>(w_codes),
+                           static_cast<const uint8_t*>(w_scales), n, k, out, true, s);
 }
 
 extern "C" fp4_status fp4_gemm_w4a16(int fmt, const void* x, int64_t m, const void* w_codes, const void* w_scales,

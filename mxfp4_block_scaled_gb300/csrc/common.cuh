@@ -351,6 +351,11 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, bool ue8m0) {
     return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((ue8m0 ? 1u : 0u) << 23) |
            ((uint32_t)(M >> 4) << 24);
 }
+// The same for kind::mxf8f6f4 (8-bit-container operands, UE8M0 scales):
+// A / B type codes E4M3 0, E5M2 1, E2M3 3, E3M2 4.
+__host__ __device__ constexpr uint32_t idesc_mxf8f6f4(int M, int N, uint32_t atype, uint32_t btype) {
+    return (atype << 7) | (btype << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
+}
 __device__ __forceinline__ uint32_t idesc_with_sf_id(uint32_t idesc, uint32_t id) {
     return idesc | (id << 4) | (id << 29);
 }
@@ -377,6 +382,21 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64
             "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
             : "memory");
     }
+}
+
+// D[tmem] (+)= A[smem] . B[smem]^T for 8-bit-container operands (E4M3, E5M2,
+// E2M3, E3M2 as the instruction descriptor says; K = 32 per instruction) with
+// one UE8M0 scale per 32 elements read from TMEM (the byte the descriptor's
+// scale-factor ids select).
+__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
 }
 
 // CTA-pair (cta_group::2) forms: the allocation is collective over one warp of

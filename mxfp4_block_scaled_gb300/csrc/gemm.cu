@@ -23,13 +23,15 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D map over packed codes [rows][k/2] bytes; box = box_bytes (64 or 128) x
-// box_rows with the swizzle of the same width (the MMA's K-major operand layout).
-static bool make_codes_map(CUtensorMap* m, const void* base, int64_t rows, int64_t k, int box_rows, int box_bytes) {
+// 2-D map over code rows [rows][row_bytes] (packed FP4: k/2 bytes; 8-bit
+// containers: k); box = box_bytes (64 or 128) x box_rows with the swizzle of
+// the same width (the MMA's K-major operand layout).
+static bool make_codes_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes, int box_rows,
+                           int box_bytes) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)(k / 2), (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)(k / 2)};
+    cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
     cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)box_rows};
     cuuint32_t es[2] = {1u, 1u};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
@@ -60,21 +62,22 @@ static bool make_out_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols,
 
 int64_t gemm_k_blocks(int64_t k) { return (k + 2 * GEMM_KB_BYTES - 1) / (2 * GEMM_KB_BYTES); }
 
-template <int BN, bool MX, int EPI>
+template <int BN, int FK, int EPI>
 static cudaError_t launch_one(const GemmLaunch& g, cudaStream_t s) {
-    using C = GemmCfg<BN, MX, epi_staging_bytes<EPI, MX>()>;
-    auto kern = gemm_kernel<BN, MX, EPI>;
+    using C = GemmCfg<BN, FK, epi_staging_bytes<EPI, FK>()>;
+    auto kern = gemm_kernel<BN, FK, EPI>;
     static uint64_t attr_done = 0;  // devices on which this instantiation is opted in
     if (cudaError_t e = set_smem_attr_once((const void*)kern, C::SMEM, attr_done)) return e;
     CUtensorMap tmP, tmQ, tmO;
-    if (!make_codes_map(&tmP, g.p_codes, g.p_rows, g.k, 128, GEMM_KB_BYTES) ||
-        !make_codes_map(&tmQ, g.q_codes, g.q_rows, g.k, BN, GEMM_KB_BYTES)) {
+    const int64_t row_bytes = g.k / fk_elems_per_byte<FK>();
+    if (!make_codes_map(&tmP, g.p_codes, g.p_rows, row_bytes, 128, GEMM_KB_BYTES) ||
+        !make_codes_map(&tmQ, g.q_codes, g.q_rows, row_bytes, BN, GEMM_KB_BYTES)) {
         set_error("cuTensorMapEncodeTiled failed (rows %lld/%lld, k %lld)", (long long)g.p_rows, (long long)g.q_rows,
                   (long long)g.k);
         return cudaErrorInvalidValue;
     }
     if (EPI == EPI_BF16) {
-        if (!make_out_map(&tmO, g.out, g.p_rows_valid, g.q_rows_valid, g.ldo, epi_box_cols<MX>())) {
+        if (!make_out_map(&tmO, g.out, g.p_rows_valid, g.q_rows_valid, g.ldo, epi_box_cols<FK>())) {
             set_error("cuTensorMapEncodeTiled failed for the output (%lld x %lld, ldo %lld)",
                       (long long)g.p_rows_valid, (long long)g.q_rows_valid, (long long)g.ldo);
             return cudaErrorInvalidValue;
@@ -152,7 +155,8 @@ static cudaError_t launch_pair(const GemmLaunch& g, cudaStream_t s) {
         max_clusters[d->device] = n;
     }
     CUtensorMap tmP, tmQ, tmO;
-    if (!make_codes_map(&tmP, g.p_codes, g.p_rows, g.k, 128, 128) || !make_codes_map(&tmQ, g.q_codes, g.q_rows, g.k, 128, 128) ||
+    if (!make_codes_map(&tmP, g.p_codes, g.p_rows, g.k / 2, 128, 128) ||
+        !make_codes_map(&tmQ, g.q_codes, g.q_rows, g.k / 2, 128, 128) ||
         !make_out_map(&tmO, g.out, g.p_rows_valid, g.q_rows_valid, g.ldo, PairCfg<MX>::BOXC)) {
         set_error("cuTensorMapEncodeTiled failed (rows %lld/%lld, k %lld)", (long long)g.p_rows, (long long)g.q_rows,
                   (long long)g.k);
@@ -188,25 +192,38 @@ int gemm_pair_max_clusters() {
 cudaError_t launch_gemm_moe(const GemmLaunch& g, cudaStream_t s);  // moe.cu
 
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
+    if (g.fmt == FMT_MX8) {
+        // 8-bit-container MX operands: the dense bf16 epilogue
+        if (g.epi == EPI_BF16 && g.bn == 256) return launch_one<256, FK_MX8, EPI_BF16>(g, s);
+        if (g.epi == EPI_BF16 && g.bn == 128) return launch_one<128, FK_MX8, EPI_BF16>(g, s);
+        set_error("no MX8 GEMM instantiation for epilogue %d, BN %d", g.epi, g.bn);
+        return cudaErrorInvalidValue;
+    }
     const bool mx = g.fmt == FP4_MXFP4;
     switch (g.epi) {
         case EPI_BF16:
-            if (g.bn == 256) return mx ? launch_one<256, true, EPI_BF16>(g, s) : launch_one<256, false, EPI_BF16>(g, s);
-            if (g.bn == 128) return mx ? launch_one<128, true, EPI_BF16>(g, s) : launch_one<128, false, EPI_BF16>(g, s);
+            if (g.bn == 256)
+                return mx ? launch_one<256, FK_MX4, EPI_BF16>(g, s) : launch_one<256, FK_NV4, EPI_BF16>(g, s);
+            if (g.bn == 128)
+                return mx ? launch_one<128, FK_MX4, EPI_BF16>(g, s) : launch_one<128, FK_NV4, EPI_BF16>(g, s);
             break;
         case EPI_BF16_T:
-            if (g.bn == 32) return mx ? launch_one<32, true, EPI_BF16_T>(g, s) : launch_one<32, false, EPI_BF16_T>(g, s);
-            if (g.bn == 64) return mx ? launch_one<64, true, EPI_BF16_T>(g, s) : launch_one<64, false, EPI_BF16_T>(g, s);
+            if (g.bn == 32)
+                return mx ? launch_one<32, FK_MX4, EPI_BF16_T>(g, s) : launch_one<32, FK_NV4, EPI_BF16_T>(g, s);
+            if (g.bn == 64)
+                return mx ? launch_one<64, FK_MX4, EPI_BF16_T>(g, s) : launch_one<64, FK_NV4, EPI_BF16_T>(g, s);
             break;
         case EPI_PARTIAL:
-            if (g.bn == 256) return mx ? launch_one<256, true, EPI_PARTIAL>(g, s) : launch_one<256, false, EPI_PARTIAL>(g, s);
-            if (g.bn == 128) return mx ? launch_one<128, true, EPI_PARTIAL>(g, s) : launch_one<128, false, EPI_PARTIAL>(g, s);
+            if (g.bn == 256)
+                return mx ? launch_one<256, FK_MX4, EPI_PARTIAL>(g, s) : launch_one<256, FK_NV4, EPI_PARTIAL>(g, s);
+            if (g.bn == 128)
+                return mx ? launch_one<128, FK_MX4, EPI_PARTIAL>(g, s) : launch_one<128, FK_NV4, EPI_PARTIAL>(g, s);
             break;
         case EPI_PARTIAL_T:
             if (g.bn == 32)
-                return mx ? launch_one<32, true, EPI_PARTIAL_T>(g, s) : launch_one<32, false, EPI_PARTIAL_T>(g, s);
+                return mx ? launch_one<32, FK_MX4, EPI_PARTIAL_T>(g, s) : launch_one<32, FK_NV4, EPI_PARTIAL_T>(g, s);
             if (g.bn == 64)
-                return mx ? launch_one<64, true, EPI_PARTIAL_T>(g, s) : launch_one<64, false, EPI_PARTIAL_T>(g, s);
+                return mx ? launch_one<64, FK_MX4, EPI_PARTIAL_T>(g, s) : launch_one<64, FK_NV4, EPI_PARTIAL_T>(g, s);
             break;
         case EPI_SWIGLU:
         case EPI_COMBINE:
@@ -222,15 +239,15 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
 // template's code in one place; moe.cu only builds the launch records).
 cudaError_t launch_gemm_moe(const GemmLaunch& g, cudaStream_t s) {
     if (g.fmt != FP4_NVFP4) return cudaErrorInvalidValue;
-    if (g.epi == EPI_SWIGLU_T && g.bn == 32) return launch_one<32, false, EPI_SWIGLU_T>(g, s);
-    if (g.epi == EPI_COMBINE_T && g.bn == 32) return launch_one<32, false, EPI_COMBINE_T>(g, s);
+    if (g.epi == EPI_SWIGLU_T && g.bn == 32) return launch_one<32, FK_NV4, EPI_SWIGLU_T>(g, s);
+    if (g.epi == EPI_COMBINE_T && g.bn == 32) return launch_one<32, FK_NV4, EPI_COMBINE_T>(g, s);
     if (g.epi == EPI_SWIGLU) {
-        if (g.bn == 256) return launch_one<256, false, EPI_SWIGLU>(g, s);
-        if (g.bn == 128) return launch_one<128, false, EPI_SWIGLU>(g, s);
-        if (g.bn == 64) return launch_one<64, false, EPI_SWIGLU>(g, s);
+        if (g.bn == 256) return launch_one<256, FK_NV4, EPI_SWIGLU>(g, s);
+        if (g.bn == 128) return launch_one<128, FK_NV4, EPI_SWIGLU>(g, s);
+        if (g.bn == 64) return launch_one<64, FK_NV4, EPI_SWIGLU>(g, s);
     } else {
-        if (g.bn == 128) return launch_one<128, false, EPI_COMBINE>(g, s);
-        if (g.bn == 64) return launch_one<64, false, EPI_COMBINE>(g, s);
+        if (g.bn == 128) return launch_one<128, FK_NV4, EPI_COMBINE>(g, s);
+        if (g.bn == 64) return launch_one<64, FK_NV4, EPI_COMBINE>(g, s);
     }
     set_error("no MoE GEMM instantiation for BN %d", g.bn);
     return cudaErrorInvalidValue;

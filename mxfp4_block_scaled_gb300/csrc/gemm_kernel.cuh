@@ -39,14 +39,34 @@
 
 namespace fp4 {
 
+// Operand formats of the GEMM template (FK):
+//   FK_NV4  NVFP4: packed E2M1 pairs, UE4M3 scale per 16 elements, alpha from
+//           the two global scales (kind::mxf4nvf4, scale_vec::4X)
+//   FK_MX4  MXFP4: packed E2M1 pairs, UE8M0 scale per 32 (kind::mxf4nvf4, 2X)
+//   FK_MX8  MXFP8 / MXFP6: one element per byte (E4M3, E5M2, E2M3, E3M2, the
+//           types named at run time in the instruction descriptor), UE8M0
+//           scale per 32 (kind::mxf8f6f4, scale_vec::1X)
+// The MX formats have no global scale (alpha = 1).
+enum : int { FK_NV4 = 0, FK_MX4 = 1, FK_MX8 = 2 };
+
+template <int FK>
+constexpr bool fk_ue8m0() {
+    return FK != FK_NV4;
+}
+// K elements per byte of a code row
+template <int FK>
+constexpr int fk_elems_per_byte() {
+    return FK == FK_MX8 ? 1 : 2;
+}
+
 // bf16 epilogue staging: one buffer per epilogue warpgroup of 128 rows x
 // epi_box_cols bf16 columns, the box of the output tensor map (rows of 32 or
 // 64 bytes with the swizzle of that width).  Narrow boxes keep the staging
 // small enough for four operand stages and a scale ring of four slots
-// (NVFP4 scale slots are twice the MXFP4 ones).
-template <bool MX>
+// (NVFP4 scale slots are twice the MX ones).
+template <int FK>
 constexpr int epi_box_cols() {
-    return MX ? 32 : 16;
+    return FK == FK_NV4 ? 16 : 32;
 }
 
 template <int BOXC>
@@ -74,18 +94,20 @@ constexpr bool epi_grouped() {
 constexpr int kUnitTable = 64;
 constexpr int kUnitTableBytes = kUnitTable * 8;
 
-template <int EPI, bool MX>
+template <int EPI, int FK>
 constexpr int epi_staging_bytes() {
-    return (EPI == EPI_BF16 ? 2 * epi_buffer_bytes<epi_box_cols<MX>()>() : EPI == EPI_SWIGLU_T ? kSwigluXBytes : 0) +
+    return (EPI == EPI_BF16 ? 2 * epi_buffer_bytes<epi_box_cols<FK>()>() : EPI == EPI_SWIGLU_T ? kSwigluXBytes : 0) +
            (epi_grouped<EPI>() ? kUnitTableBytes : 0);
 }
 
-template <int BN, bool MX, int STG = 0>
+template <int BN, int FK, int STG = 0>
 struct GemmCfg {
     static constexpr int BM = 128;
-    static constexpr int KB_BYTES = GEMM_KB_BYTES;  // one K block = 2 KB_BYTES fp4 per row
-    static constexpr int KB_MMAS = KB_BYTES / 32;   // K=64 MMAs per K block
-    static constexpr int SF_CHUNKS = KB_BYTES / 64 * (MX ? 1 : 2);  // 512-byte scale atoms per 128 rows per K block
+    static constexpr int KB_BYTES = GEMM_KB_BYTES;                     // code bytes per row per K block
+    static constexpr int KB_ELEMS = KB_BYTES * fk_elems_per_byte<FK>();  // K elements per K block
+    static constexpr int KB_MMAS = KB_BYTES / 32;  // MMAs per K block (32 bytes of K each: K=64 fp4, K=32 8-bit)
+    static constexpr int SF_BLOCK = FK == FK_NV4 ? 16 : 32;        // elements per block scale
+    static constexpr int SF_CHUNKS = KB_ELEMS / SF_BLOCK / 4;      // 512-byte scale atoms per 128 rows per K block
     static constexpr int QCH = BN > 128 ? BN / 128 : 1;
     static constexpr int P_BYTES = BM * KB_BYTES;
     static constexpr int Q_BYTES = BN * KB_BYTES;
@@ -143,10 +165,10 @@ struct Sched {
 // sub-tile run together and find it in L2) and sub-tile slowest: with a few
 // tokens per expert the later sub-tiles are empty, so the units with work come
 // first and the grid stride spreads them evenly over the CTAs.
-template <int BN, int EPI>
+template <int BN, int EPI, int KB_ELEMS>
 __device__ __forceinline__ Sched make_sched(const GemmLaunch& g) {
     Sched s;
-    s.kbt = (g.k + 2 * GEMM_KB_BYTES - 1) / (2 * GEMM_KB_BYTES);
+    s.kbt = (g.k + KB_ELEMS - 1) / KB_ELEMS;
     s.splits = g.splits;
     s.kb_per = (s.kbt + g.splits - 1) / g.splits;
     if constexpr (epi_swapped_grouped<EPI>()) {
@@ -295,11 +317,12 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                  : "memory");
 }
 
-template <int BN, bool MX, int EPI>
+template <int BN, int FK, int EPI>
 __global__ void __launch_bounds__(512, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
                 const __grid_constant__ CUtensorMap tmO, const GemmLaunch g, const WaitCfg wc) {
-    using C = GemmCfg<BN, MX, epi_staging_bytes<EPI, MX>()>;
+    using C = GemmCfg<BN, FK, epi_staging_bytes<EPI, FK>()>;
+    constexpr bool MX = fk_ue8m0<FK>();  // no global scales
     static_assert(EPI != EPI_BF16 || BN >= 128, "the staged bf16 epilogue stores 64-column boxes");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -308,7 +331,7 @@ __global__ void __launch_bounds__(512, 1)
     uint8_t* sSFP = sQ + C::STAGES * C::Q_BYTES;       // scale ring (SSLOTS slots)
     uint8_t* sSFQ = sSFP + C::SSLOTS * C::SFP_BYTES;
     uint8_t* sStg = smem + C::STG_OFFSET;  // bf16 epilogue staging (EPI_BF16)
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + epi_staging_bytes<EPI, MX>());
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + epi_staging_bytes<EPI, FK>());
     uint64_t* full = bars;
     uint64_t* empty = bars + C::STAGES;
     uint64_t* sfull = bars + 2 * C::STAGES;                // scale atoms of the slot landed in smem
@@ -357,10 +380,10 @@ __global__ void __launch_bounds__(512, 1)
     // just before its first read of their outputs (the weight producer not at
     // all when early_p / early_q marks its operand).
     if (g.grouped) pdl_wait();
-    const Sched sc = make_sched<BN, EPI>(g);
+    const Sched sc = make_sched<BN, EPI, C::KB_ELEMS>(g);
     const int32_t* ut = nullptr;  // grouped: this CTA's unit table (expert, real-row end)
     if constexpr (epi_grouped<EPI>()) {
-        int32_t* t = reinterpret_cast<int32_t*>(sStg + epi_staging_bytes<EPI, MX>() - kUnitTableBytes);
+        int32_t* t = reinterpret_cast<int32_t*>(sStg + epi_staging_bytes<EPI, FK>() - kUnitTableBytes);
         for (int j = threadIdx.x; j < kUnitTable; j += blockDim.x) {
             const int64_t u = blockIdx.x + (int64_t)j * gridDim.x;
             int32_t e = 0, vend = 0;
@@ -380,6 +403,7 @@ __global__ void __launch_bounds__(512, 1)
         ut = t;
     }
     const int64_t ksfc = (g.k + 255) / 256 * (MX ? 2 : 4);      // scale atoms per 128-row tile (K padded to 256)
+    static_assert(FK != FK_MX8 || C::SF_CHUNKS == 1, "an 8-bit K block is one scale atom (K padded to 256 keeps it whole)");
     const int64_t q_chunks_total = (g.q_rows + 127) / 128;      // 128-row scale tiles of Q
 
     if (warp < 4) {
@@ -505,7 +529,8 @@ __global__ void __launch_bounds__(512, 1)
     } else if (warp == 5) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
-            const uint32_t idesc = idesc_mxf4(128, BN, MX);
+            const uint32_t idesc =
+                FK == FK_MX8 ? idesc_mxf8f6f4(128, BN, (uint32_t)g.p_type, (uint32_t)g.q_type) : idesc_mxf4(128, BN, MX);
             int stage = 0;
             uint32_t ph = 0;
             int acc = 0;
@@ -535,16 +560,25 @@ __global__ void __launch_bounds__(512, 1)
                         const uint64_t ad = C::KB_BYTES == 128 ? sdesc_sw128(pa + kk * 32) : sdesc_sw64(pa + kk * 32);
                         const uint64_t bd = C::KB_BYTES == 128 ? sdesc_sw128(qa + kk * 32) : sdesc_sw64(qa + kk * 32);
                         uint32_t sfa, sfb, id;
-                        if constexpr (!MX) {
+                        if constexpr (FK == FK_NV4) {
                             sfa = sfp_t + kk * 4;
                             sfb = sfq_t + kk * 4 * C::QCH;
                             id = idesc;
-                        } else {
+                        } else if constexpr (FK == FK_MX4) {
                             sfa = sfp_t + (kk >> 1) * 4;
                             sfb = sfq_t + (kk >> 1) * 4 * C::QCH;
                             id = idesc_with_sf_id(idesc, (uint32_t)(kk & 1) * 2u);
+                        } else {
+                            // one scale byte per row per K=32 MMA: byte kk of the atom's word
+                            sfa = sfp_t;
+                            sfb = sfq_t;
+                            id = idesc_with_sf_id(idesc, (uint32_t)kk);
                         }
-                        mma_mxf4<MX>(d_tmem, ad, bd, id, sfa, sfb, (kb > w.kb0 || kk > 0) ? 1u : 0u);
+                        const uint32_t acc_in = (kb > w.kb0 || kk > 0) ? 1u : 0u;
+                        if constexpr (FK == FK_MX8)
+                            mma_mxf8f6f4(d_tmem, ad, bd, id, sfa, sfb, acc_in);
+                        else
+                            mma_mxf4<MX>(d_tmem, ad, bd, id, sfa, sfb, acc_in);
                     }
                     any = true;
                     mma_commit(empty + stage);
@@ -637,7 +671,7 @@ __global__ void __launch_bounds__(512, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce + acc);
                 const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
-                constexpr int BOXC = epi_box_cols<MX>();
+                constexpr int BOXC = epi_box_cols<FK>();
                 epi_store_bf16<NLD, BOXC>(&tmO, smem_u32(sStg) + (uint32_t)(wg * epi_buffer_bytes<BOXC>()), pk, qd, lane,
                                     1u + (uint32_t)wg, w.qt * BN + c_begin, w.p_row0, g.q_rows_valid,
                                     g.p_rows_valid, store_pending);

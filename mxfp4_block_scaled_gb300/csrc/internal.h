@@ -91,8 +91,13 @@ enum Epi : int {
     EPI_COMBINE_T = 7,  // y[token of q][p] += weight * alpha * acc (fp32 reductions)
 };
 
+// GemmLaunch::fmt for the 8-bit-container MX formats (MXFP8 / MXFP6; codes
+// one byte per element, UE8M0 scales per 32), beside FP4_NVFP4 / FP4_MXFP4.
+constexpr int FMT_MX8 = 2;
+
 struct GemmLaunch {
     int fmt = FP4_NVFP4;
+    int p_type = 0, q_type = 0;   // FMT_MX8: element type codes of P and Q (kind::mxf8f6f4 descriptor)
     int epi = EPI_BF16;
     int bn = 256;                 // Q tile rows (MMA N): 32, 64, 128 or 256
     // operand P (MMA A, 128-row tiles) and Q (MMA B, bn-row tiles), both K-major

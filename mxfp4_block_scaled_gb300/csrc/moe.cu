@@ -29,13 +29,11 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "moe_common.cuh"
 #include "quant_math.cuh"
 
 namespace fp4 {
 
-static constexpr int kMaxExperts = 1024;
-static constexpr int kMaxTopK = 32;
-static constexpr int kMaxStaticExperts = 256;
 
 // ---------------------------------------------------------------- layout
 
@@ -68,6 +66,15 @@ enum MoeSlot : int {
     MS_TOK_CODES,   // dynamic scale: the hidden rows quantised once, token order
     MS_TOK_SCALES,
     MS_SLOT_ROW,    // small-T preparation: the expert-sorted row of each slot
+    // the one-launch MoE (moe_fused.cu), sized only when its shapes apply
+    MS_F_ZERO,      // counters and h amax, cleared per call
+    MS_F_H,         // bf16 [T k][I], slot order
+    MS_F_HCODES,    // [T k][I/2]
+    MS_F_HSB,       // [T k][I/16] scale bytes, row-major
+    MS_F_SGH,       // fp32 [E]
+    MS_F_D,         // fp32 [T k][H]
+    MS_F_ACODES,    // [T k][H/2]
+    MS_F_ASB,       // [T k][H/16]
     MS_COUNT
 };
 
@@ -114,6 +121,15 @@ static MoeLayout moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
     sz[MS_TOK_CODES] = T * H / 2;
     sz[MS_TOK_SCALES] = round_up(T, 128) * sf_cols_padded(H, 16);
     sz[MS_SLOT_ROW] = slots * 4;
+    const bool fused = moe_fused_supported(T, H, I, E, k);
+    sz[MS_F_ZERO] = fused ? kFusedZeroedBytes : 0;
+    sz[MS_F_H] = fused ? slots * I * 2 : 0;
+    sz[MS_F_HCODES] = fused ? slots * I / 2 : 0;
+    sz[MS_F_HSB] = fused ? slots * I / 16 : 0;
+    sz[MS_F_SGH] = fused ? E * 4 : 0;
+    sz[MS_F_D] = fused ? slots * H * 4 : 0;
+    sz[MS_F_ACODES] = fused ? slots * H / 2 : 0;
+    sz[MS_F_ASB] = fused ? slots * H / 16 : 0;
     int64_t o = 0;
     for (int i = 0; i < MS_COUNT; ++i) {
         L.off[i] = o;
@@ -124,11 +140,6 @@ static MoeLayout moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
 }
 
 // ------------------------------------------------------------ kernels
-
-struct StaticScales {
-    float s13[kMaxStaticExperts];
-    float s2[kMaxStaticExperts];
-};
 
 struct RouteArgs {
     const float* logits;
@@ -147,52 +158,6 @@ struct RouteArgs {
     float* static2_out;
     int zero_outputs;  // 0: route only (staged runs zero in their own stage)
 };
-
-// Warp-cooperative top-k over one token's logits; ties go to the lower
-// expert index.  Lane j < k returns the j-th selection and its weight
-// exp(l_j - l_max) / sum over the selection.
-template <int PER_LANE>
-__device__ __forceinline__ void topk_token(const float* row, int E, int k, int lane, int& my_e, float& my_w) {
-    float v[PER_LANE];
-#pragma unroll
-    for (int q = 0; q < PER_LANE; ++q) {
-        const int e = q * 32 + lane;
-        v[q] = e < E ? row[e] : -INFINITY;
-    }
-    uint32_t taken = 0;
-    float v0 = 0.0f, sum = 0.0f, mine = 0.0f;
-    my_e = 0;
-    for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int be = 0x7FFFFFFF;
-#pragma unroll
-        for (int q = 0; q < PER_LANE; ++q) {
-            const int e = q * 32 + lane;
-            if (e < E && !((taken >> q) & 1u) && (v[q] > bv || be == 0x7FFFFFFF)) {
-                bv = v[q];
-                be = e;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-            const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
-            if (ov > bv || (ov == bv && oe < be)) {
-                bv = ov;
-                be = oe;
-            }
-        }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
-        if (j == 0) v0 = bv;
-        const float ex = expf(bv - v0);
-        sum += ex;
-        if (lane == j) {
-            my_e = be;
-            mine = ex;
-        }
-    }
-    my_w = __fdiv_rn(mine, sum);
-}
 
 // Route with a warp per token: 32 tokens per CTA of 1024 threads, so the CTA
 // owns exactly one 32-token bitmap word per expert (built in smem).  A token's
@@ -828,7 +793,20 @@ extern "C" int fp4_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t
     int n = 0;
     for (int i = 0; i < MS_PUBLIC_END && n < max_entries; ++i) offsets[n++] = L.off[i];
     if (n < max_entries) offsets[n++] = L.R;
+    const int fused[] = {MS_F_H, MS_F_HCODES, MS_F_HSB, MS_F_SGH, MS_F_D, MS_F_ACODES, MS_F_ASB};
+    for (int i = 0; i < 7 && n < max_entries; ++i) offsets[n++] = L.off[fused[i]];
     return n;
+}
+
+static int g_moe_policy = 0;  // fp4_set_moe_policy
+
+extern "C" fp4_status fp4_set_moe_policy(int policy) {
+    if (policy < 0 || policy > 1) {
+        set_error("MoE policy %d not in 0..1", policy);
+        return FP4_ERR_INVALID_ARG;
+    }
+    g_moe_policy = policy;
+    return FP4_OK;
 }
 
 enum : unsigned { ST_ROUTE = 1u, ST_QUANT = 2u, ST_GEMM1 = 4u, ST_REQUANT = 8u, ST_GEMM2 = 16u, ST_ALL = 31u };
@@ -907,6 +885,39 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
     const bool small_prep = full && swapped && T <= kPrepMaxTokens;
     bool pdl = false;  // first launch of the call waits for everything before it
     const int per_lane = (int)((E + 31) / 32);
+
+    if (full && g_moe_policy == 0 && moe_fused_supported(T, H, I, E, k)) {
+        // a few tokens: the whole layer in one launch (after a memset of its counters)
+        FusedMoeLaunch F;
+        F.hidden = static_cast<const uint16_t*>(hidden);
+        F.logits = logits;
+        F.T = T, F.H = H, F.I = I, F.E = E, F.k = k;
+        F.is_static = is_static ? 1 : 0;
+        F.w13_codes = static_cast<const uint8_t*>(w13c);
+        F.w13_scales = static_cast<const uint8_t*>(w13s);
+        F.w13_global = w13g;
+        F.w2_codes = static_cast<const uint8_t*>(w2c);
+        F.w2_scales = static_cast<const uint8_t*>(w2s);
+        F.w2_global = w2g;
+        F.out = static_cast<uint16_t*>(out);
+        F.ids = ids;
+        F.weights = wts;
+        F.sg_a = sg_a;
+        F.zeroed = (uint32_t*)at(MS_F_ZERO);
+        F.h = (uint16_t*)at(MS_F_H);
+        F.a_codes = at(MS_F_ACODES);
+        F.a_sbytes = at(MS_F_ASB);
+        F.h_codes = at(MS_F_HCODES);
+        F.h_sbytes = at(MS_F_HSB);
+        F.sg_h = (float*)at(MS_F_SGH);
+        F.d = (float*)at(MS_F_D);
+        StaticScales sc;
+        memset(&sc, 0, sizeof(sc));
+        if (is_static)
+            for (int64_t e = 0; e < E; ++e) sc.s13[e] = s13[e], sc.s2[e] = s2[e];
+        MOE_CUDA(launch_moe_fused(F, sc, s), "fused MoE launch");
+        return FP4_OK;
+    }
 
     if (small_prep) {
         PrepArgs pa;

@@ -1,0 +1,106 @@
+// moe_common.cuh -- pieces shared by the MoE launch chain (moe.cu) and the
+// one-launch MoE for a few tokens (moe_fused.cu): limits, the static-scale
+// kernel parameter and the warp-cooperative router.
+#pragma once
+
+#include <math.h>
+
+#include "common.cuh"
+
+namespace fp4 {
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int kMaxStaticExperts = 256;
+
+// Per-expert static activation scales, passed by value as a kernel parameter.
+struct StaticScales {
+    float s13[kMaxStaticExperts];
+    float s2[kMaxStaticExperts];
+};
+
+// The one-launch MoE for a few tokens (moe_fused.cu).
+constexpr int kFusedMaxT = 16;                        // tokens
+constexpr int kFusedMaxTopK = 8;
+constexpr int kFusedMaxSlots = kFusedMaxT * kFusedMaxTopK;
+constexpr int kFusedMaxK = 2048;                      // H and I (the two GEMMs' K)
+constexpr int kFusedMaxOutTiles = 32;                 // H / 128
+constexpr int kFusedZeroedBytes = 2048;               // counters + h amax, cleared per call
+
+struct FusedMoeLaunch {
+    const uint16_t* hidden;
+    const float* logits;
+    int64_t T, H, I, E, k;
+    int is_static;
+    const uint8_t* w13_codes;
+    const uint8_t* w13_scales;
+    const float* w13_global;
+    const uint8_t* w2_codes;
+    const uint8_t* w2_scales;
+    const float* w2_global;
+    uint16_t* out;
+    int32_t* ids;
+    float* weights;
+    float* sg_a;
+    uint32_t* zeroed;  // kFusedZeroedBytes, cleared by the launcher
+    uint16_t* h;
+    uint8_t* a_codes;
+    uint8_t* a_sbytes;
+    uint8_t* h_codes;
+    uint8_t* h_sbytes;
+    float* sg_h;
+    float* d;
+};
+
+// The shapes the one-launch MoE takes (else the launch chain runs).
+bool moe_fused_supported(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k);
+// One memset (the counters) and one cooperative kernel launch.
+cudaError_t launch_moe_fused(const FusedMoeLaunch& L, const StaticScales& st, cudaStream_t s);
+
+// Warp-cooperative top-k over one token's logits; ties go to the lower
+// expert index.  Lane j < k returns the j-th selection and its weight
+// exp(l_j - l_max) / sum over the selection.
+template <int PER_LANE>
+__device__ __forceinline__ void topk_token(const float* row, int E, int k, int lane, int& my_e, float& my_w) {
+    float v[PER_LANE];
+#pragma unroll
+    for (int q = 0; q < PER_LANE; ++q) {
+        const int e = q * 32 + lane;
+        v[q] = e < E ? row[e] : -INFINITY;
+    }
+    uint32_t taken = 0;
+    float v0 = 0.0f, sum = 0.0f, mine = 0.0f;
+    my_e = 0;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int be = 0x7FFFFFFF;
+#pragma unroll
+        for (int q = 0; q < PER_LANE; ++q) {
+            const int e = q * 32 + lane;
+            if (e < E && !((taken >> q) & 1u) && (v[q] > bv || be == 0x7FFFFFFF)) {
+                bv = v[q];
+                be = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+            const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
+            if (ov > bv || (ov == bv && oe < be)) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        if (j == 0) v0 = bv;
+        const float ex = expf(bv - v0);
+        sum += ex;
+        if (lane == j) {
+            my_e = be;
+            mine = ex;
+        }
+    }
+    my_w = __fdiv_rn(mine, sum);
+}
+
+}  // namespace fp4

@@ -1,13 +1,17 @@
-// mxfp8.cu -- MXFP8 quantiser with E4M3 elements.  "vLLM per-format kernel
-// capability matrix" lists MXFP8 with group size 32; the scale rule is the
-// MXFP4 one ("vLLM on DGX Spark: technical report", section 6.4) with E4M3's
-// largest exponent (8) in place of E2M1's:
-//   e = floor(log2 amax_b) - 8, clamped to [-127, 127], stored as the E8M0
-//   byte e + 127; element codes E4M3_rne_satfinite(x * 2^-e), one byte each;
-//   an all-zero block gets scale byte 0 and code 0.
-// x * 2^-e is exact wherever it can reach a nonzero E4M3 code (|x| * 2^-e is
-// below 2^9, and every bf16 value at or above E4M3's smallest step keeps
-// all its bits), so the hardware conversion rounds the exact quotient.
+// mxfp8.cu -- MXFP8 / MXFP6 quantisers: E4M3, E5M2, E2M3 or E3M2 elements in
+// 32-element blocks with one E8M0 scale.  "vLLM per-format kernel capability
+// matrix" lists MXFP6 and MXFP8 with group size 32; the scale rule is the
+// MXFP4 one ("vLLM on DGX Spark: technical report", section 6.4) with the
+// element's own largest exponent emax (E4M3 8, E5M2 15, E2M3 2, E3M2 4) in
+// place of E2M1's:
+//   e = floor(log2 amax_b) - emax, clamped to [-127, 127], stored as the E8M0
+//   byte e + 127; element codes ELEM_rne_satfinite(x * 2^-e), one byte each
+//   (the 6-bit codes in the low six bits, the top two bits zero); an
+//   all-zero block gets scale byte 0 and code 0.
+// x * 2^-e is exact: 2^-e is a normal float, |x| * 2^-e < 2^(emax + 1), and a
+// product small enough to lose bits in fp32 lies far below every format's
+// smallest step and rounds to zero either way (keeping its sign), so the
+// hardware conversion rounds the exact quotient.
 //
 // One thread per 32-element block: four 16-byte loads, a 16-bit abs-max
 // over the sign-cleared bf16 patterns, sixteen paired conversions and two
@@ -23,19 +27,30 @@ namespace fp4 {
 
 constexpr int kMx8Threads = 256;
 
-// Two fp32 -> two E4M3 codes in 16 bits, `even` in the low byte.
-__device__ __forceinline__ uint32_t cvt_e4m3x2(float even, float odd) {
+// Two fp32 -> two codes in 16 bits, `even` in the low byte, round to nearest
+// even, saturating at the format's largest finite value.
+template <int ELEM>
+__device__ __forceinline__ uint32_t cvt_mx_x2(float even, float odd) {
     uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(odd), "f"(even));
+    if constexpr (ELEM == MX_ELEM_E4M3)
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(odd), "f"(even));
+    else if constexpr (ELEM == MX_ELEM_E5M2)
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(odd), "f"(even));
+    else if constexpr (ELEM == MX_ELEM_E2M3)
+        asm("cvt.rn.satfinite.e2m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(odd), "f"(even));
+    else
+        asm("cvt.rn.satfinite.e3m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(odd), "f"(even));
     return r;
 }
 
-__global__ void __launch_bounds__(kMx8Threads) mxfp8_quant_kernel(const uint16_t* __restrict__ x, int64_t rows,
-                                                                  int64_t k, int64_t rows_pad, int64_t ksf,
-                                                                  uint8_t* __restrict__ codes,
-                                                                  uint8_t* __restrict__ scales) {
+template <int ELEM>
+__global__ void __launch_bounds__(kMx8Threads) mx8_quant_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                                int64_t k, int64_t rows_pad, int64_t ksf,
+                                                                uint8_t* __restrict__ codes,
+                                                                uint8_t* __restrict__ scales) {
     pdl_wait();
     pdl_launch_dependents();  // dependents wait for this grid's completion
+    constexpr int kEmax = mx_elem_emax(ELEM);
     const int64_t kb = k / 32;  // real blocks per row
     const int64_t total = rows_pad * ksf;
     const int64_t stride = (int64_t)gridDim.x * kMx8Threads;
@@ -56,7 +71,7 @@ __global__ void __launch_bounds__(kMx8Threads) mxfp8_quant_kernel(const uint16_t
                 const uint32_t ab = m << 16;  // fp32 bits of amax_b
                 const uint32_t ef = ab >> 23;
                 const int fl = ef ? (int)ef - 127 : (31 - __clz((int)(ab & 0x7FFFFFu))) - 149;  // floor(log2)
-                const int e = min(max(fl - 8, -127), 127);  // at most 119 for bf16 inputs
+                const int e = min(max(fl - kEmax, -127), 127);
                 sbyte = (uint32_t)(e + 127);
                 const float mult = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e, a normal float
                 const uint32_t xw[16] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w,
@@ -65,8 +80,8 @@ __global__ void __launch_bounds__(kMx8Threads) mxfp8_quant_kernel(const uint16_t
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     const uint32_t a = xw[2 * q], b = xw[2 * q + 1];
-                    w[q] = cvt_e4m3x2(__fmul_rn(bf16lo(a), mult), __fmul_rn(bf16hi(a), mult)) |
-                           (cvt_e4m3x2(__fmul_rn(bf16lo(b), mult), __fmul_rn(bf16hi(b), mult)) << 16);
+                    w[q] = cvt_mx_x2<ELEM>(__fmul_rn(bf16lo(a), mult), __fmul_rn(bf16hi(a), mult)) |
+                           (cvt_mx_x2<ELEM>(__fmul_rn(bf16lo(b), mult), __fmul_rn(bf16hi(b), mult)) << 16);
                 }
                 out[0] = make_uint4(w[0], w[1], w[2], w[3]);
                 out[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -79,14 +94,29 @@ __global__ void __launch_bounds__(kMx8Threads) mxfp8_quant_kernel(const uint16_t
     }
 }
 
-cudaError_t launch_mxfp8_quant(const uint16_t* x, int64_t rows, int64_t k, uint8_t* codes, uint8_t* scales,
-                               int sm_count, cudaStream_t s) {
+cudaError_t launch_mx8_quant(int elem, const uint16_t* x, int64_t rows, int64_t k, uint8_t* codes, uint8_t* scales,
+                             int sm_count, cudaStream_t s) {
     const int64_t rows_pad = round_up(rows, 128);
     const int64_t ksf = sf_cols_padded(k, 32);
     const int64_t total = rows_pad * ksf;
     const int64_t want = (total + kMx8Threads - 1) / kMx8Threads;
-    const int64_t grid = want < (int64_t)sm_count * 8 ? want : (int64_t)sm_count * 8;
-    mxfp8_quant_kernel<<<(unsigned)grid, kMx8Threads, 0, s>>>(x, rows, k, rows_pad, ksf, codes, scales);
+    const unsigned grid = (unsigned)(want < (int64_t)sm_count * 8 ? want : (int64_t)sm_count * 8);
+    switch (elem) {
+        case MX_ELEM_E4M3:
+            mx8_quant_kernel<MX_ELEM_E4M3><<<grid, kMx8Threads, 0, s>>>(x, rows, k, rows_pad, ksf, codes, scales);
+            break;
+        case MX_ELEM_E5M2:
+            mx8_quant_kernel<MX_ELEM_E5M2><<<grid, kMx8Threads, 0, s>>>(x, rows, k, rows_pad, ksf, codes, scales);
+            break;
+        case MX_ELEM_E2M3:
+            mx8_quant_kernel<MX_ELEM_E2M3><<<grid, kMx8Threads, 0, s>>>(x, rows, k, rows_pad, ksf, codes, scales);
+            break;
+        case MX_ELEM_E3M2:
+            mx8_quant_kernel<MX_ELEM_E3M2><<<grid, kMx8Threads, 0, s>>>(x, rows, k, rows_pad, ksf, codes, scales);
+            break;
+        default:
+            return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 

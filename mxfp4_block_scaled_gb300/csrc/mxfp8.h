@@ -1,13 +1,29 @@
-// mxfp8.h -- launcher of the MXFP8 (E4M3) quantiser (mxfp8.cu), for the C ABI.
+// mxfp8.h -- launcher of the MXFP8 / MXFP6 quantisers (mxfp8.cu), for the C ABI.
 #pragma once
 
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "fp4.h"
+
 namespace fp4 {
 
-// x bf16 [rows][k] -> codes [rows][k] E4M3 bytes, scales E8M0 in the MMA layout.
-cudaError_t launch_mxfp8_quant(const uint16_t* x, int64_t rows, int64_t k, uint8_t* codes, uint8_t* scales,
-                               int sm_count, cudaStream_t s);
+// Element formats of the 8-bit-container MX quantisers (the fp4_mx_elem values).
+enum : int {
+    MX_ELEM_E4M3 = FP4_MX_E4M3,
+    MX_ELEM_E5M2 = FP4_MX_E5M2,
+    MX_ELEM_E2M3 = FP4_MX_E2M3,
+    MX_ELEM_E3M2 = FP4_MX_E3M2,
+};
+
+// Exponent of the element format's largest normal value.
+__host__ __device__ constexpr int mx_elem_emax(int elem) {
+    return elem == MX_ELEM_E4M3 ? 8 : elem == MX_ELEM_E5M2 ? 15 : elem == MX_ELEM_E2M3 ? 2 : 4;
+}
+
+// x bf16 [rows][k] -> codes [rows][k], one byte per element, scales E8M0 in
+// the MMA layout.  cudaErrorInvalidValue for an unknown element format.
+cudaError_t launch_mx8_quant(int elem, const uint16_t* x, int64_t rows, int64_t k, uint8_t* codes, uint8_t* scales,
+                             int sm_count, cudaStream_t s);
 
 }  // namespace fp4

@@ -45,6 +45,7 @@ _SIGNATURES = {
     "fp4_device_status": (_INT, [_P]),
     "fp4_set_arch_override": (None, [_INT]),
     "fp4_set_gemm_tile_policy": (_INT, [_INT]),
+    "fp4_set_moe_policy": (_INT, [_INT]),
     "fp4_debug_timeout_probe": (_INT, [_I64, _P]),
     "fp4_debug_plan_gemm": (_INT, [_I64, _I64, _I64, _INT, ctypes.POINTER(ctypes.c_int64), _INT]),
     "fp4_quantize_workspace_size": (_SZ, [_INT, _I64, _I64]),
@@ -57,6 +58,10 @@ _SIGNATURES = {
     "fp4_gemm_prequant": (_INT, [_INT, _P, _P, _P, _I64, _P, _P, _P, _I64, _I64, _P, _P, _SZ, _P]),
     "fp4_gemm_w4a16": (_INT, [_INT, _P, _I64, _P, _P, _P, _I64, _I64, _P, _P]),
     "fp4_quantize_mxfp8": (_INT, [_P, _I64, _I64, _P, _P, _P]),
+    "fp4_quantize_mx": (_INT, [_INT, _P, _I64, _I64, _P, _P, _P]),
+    "fp4_gemm_mx_prequant": (_INT, [_INT, _P, _P, _I64, _INT, _P, _P, _I64, _I64, _P, _P]),
+    "fp4_gemm_mx_workspace_size": (_SZ, [_I64, _I64]),
+    "fp4_gemm_mx": (_INT, [_INT, _P, _I64, _INT, _P, _P, _I64, _I64, _P, _P, _SZ, _P]),
     "fp4_moe_prepack_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "fp4_moe_prepack_weights": (_INT, [_P, _P, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "fp4_moe_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I64]),
@@ -205,6 +210,54 @@ def quantize_mxfp8(x, stream=None):
     return codes, scales
 
 
+MX_E4M3, MX_E5M2, MX_E2M3, MX_E3M2 = 0, 1, 2, 3
+MX_ELEM_NAMES = {MX_E4M3: "e4m3", MX_E5M2: "e5m2", MX_E2M3: "e2m3", MX_E3M2: "e3m2"}
+
+
+class MXTensor:
+    """An MXFP8 / MXFP6 tensor [rows, k]: codes [rows, k] uint8 (one element
+    per byte), E8M0 scales in the MMA layout (flat uint8), element format."""
+
+    def __init__(self, elem, rows, k, codes, scales):
+        self.elem, self.rows, self.k, self.codes, self.scales = elem, rows, k, codes, scales
+
+
+def quantize_mx(x, elem=MX_E4M3, stream=None):
+    """bf16 [rows, k] (CUDA) -> MXTensor via fp4_quantize_mx."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()
+    rows, k = x.shape
+    L = lib()
+    codes = torch.empty((rows, k), dtype=torch.uint8, device=x.device)
+    scales = torch.empty(L.fp4_scales_bytes(MXFP4, rows, k), dtype=torch.uint8, device=x.device)
+    _check(L.fp4_quantize_mx(elem, _ptr(x), rows, k, _ptr(codes), _ptr(scales), _stream(stream)))
+    return MXTensor(elem, rows, k, codes, scales)
+
+
+def gemm_mx_prequant(aq, wq, out=None, stream=None):
+    """MX linear on quantised operands: MXTensor a [m, k] x MXTensor w [n, k] -> bf16 [m, n]."""
+    m, k, n = aq.rows, aq.k, wq.rows
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=aq.codes.device)
+    _check(lib().fp4_gemm_mx_prequant(aq.elem, _ptr(aq.codes), _ptr(aq.scales), m, wq.elem, _ptr(wq.codes),
+                                      _ptr(wq.scales), n, k, _ptr(out), _stream(stream)))
+    return out
+
+
+def gemm_mx(x, wq, elem=MX_E4M3, out=None, workspace=None, stream=None):
+    """MX linear: bf16 x [m, k] quantised to `elem` per call, times the
+    quantised weight MXTensor [n, k] -> bf16 [m, n]."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()
+    m, k = x.shape
+    n = wq.rows
+    L = lib()
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
+    ws = workspace if workspace is not None else _ws(L.fp4_gemm_mx_workspace_size(m, k), x.device)
+    _check(L.fp4_gemm_mx(elem, _ptr(x), m, wq.elem, _ptr(wq.codes), _ptr(wq.scales), n, k, _ptr(out), _ptr(ws),
+                         ws.numel(), _stream(stream)))
+    return out
+
+
 def gemm_w4a16(x, wq, out=None, stream=None):
     """Weight-only linear: bf16 x [m, k] (m <= 4, not quantised) times the
     prepacked FP4 weight [n, k] -> bf16 [m, n]."""
@@ -269,6 +322,14 @@ def _host_scales(a, E):
     arr = np.ascontiguousarray(np.asarray(a, dtype=np.float32).reshape(-1))
     assert arr.size == E
     return arr
+
+
+MOE_AUTO, MOE_CHAIN = 0, 1
+
+
+def set_moe_policy(policy):
+    """Choose the MoE implementation (MOE_AUTO: one launch for a few tokens; MOE_CHAIN)."""
+    _check(lib().fp4_set_moe_policy(int(policy)))
 
 
 def moe_workspace_layout(T, H, I, E, top_k):

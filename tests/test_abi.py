@@ -206,7 +206,7 @@ def test_moe_workspace_layout_holds_its_documented_contents(F, T, H, I, E, k):
     L = F.lib()
     offs = (ctypes.c_int64 * 32)()
     n = L.fp4_moe_workspace_layout(T, H, I, E, k, offs, 32)
-    assert n == 15
+    assert n == 22
     o = [offs[i] for i in range(14)]
     R = offs[14]
     slots = T * k
@@ -221,6 +221,18 @@ def test_moe_workspace_layout_holds_its_documented_contents(F, T, H, I, E, k):
     for i in range(13):
         assert o[i + 1] - o[i] >= need[i], i
     assert L.fp4_moe_workspace_size(T, H, I, E, k) >= o[13] + need[13]
+    # entries 15-21: the one-launch MoE's intermediates, sized when its shapes apply
+    # (1 <= T <= 16, top_k <= 8, H and I multiples of 256 up to 2048), slot order
+    f = [offs[i] for i in range(15, 22)]
+    fused = 1 <= T <= 16 and k <= 8 and H % 256 == 0 and H <= 2048 and I % 256 == 0 and I <= 2048
+    if fused:
+        fneed = [slots * I * 2, slots * I // 2, slots * I // 16, E * 4, slots * H * 4, slots * H // 2, slots * H // 16]
+        for i in range(7):
+            assert f[i] % 256 == 0 and f[i] >= o[13] + need[13]
+            assert L.fp4_moe_workspace_size(T, H, I, E, k) >= f[i] + fneed[i]
+        regions = sorted(zip(f, fneed))
+        for (a0, n0), (a1, _) in zip(regions, regions[1:]):
+            assert a0 + n0 <= a1
     # a short buffer gets the leading entries only
     assert L.fp4_moe_workspace_layout(T, H, I, E, k, offs, 3) == 3
     assert L.fp4_moe_workspace_layout(T, H, I, 0, k, offs, 32) == 0
