@@ -236,3 +236,38 @@ def test_moe_workspace_layout_holds_its_documented_contents(F, T, H, I, E, k):
     # a short buffer gets the leading entries only
     assert L.fp4_moe_workspace_layout(T, H, I, E, k, offs, 3) == 3
     assert L.fp4_moe_workspace_layout(T, H, I, 0, k, offs, 32) == 0
+
+
+# ------------------------------------------- MX (8-bit containers) and policies
+
+def test_mx_argument_errors(F):
+    c = F.STATUS_CODE
+    L = F.lib()
+    q = lambda elem=0, x=A, rows=16, k=512, codes=A, scales=A: L.fp4_quantize_mx(elem, x, rows, k, codes, scales,
+                                                                                  None)
+    assert q(elem=4) == c["FP4_ERR_INVALID_ARG"]
+    assert q(elem=-1) == c["FP4_ERR_INVALID_ARG"]
+    assert q(k=48) == c["FP4_ERR_SHAPE"]
+    assert q(x=0) == c["FP4_ERR_INVALID_ARG"]
+    assert q(codes=A + 8) == c["FP4_ERR_ALIGNMENT"]
+    g = lambda ea=0, ew=0, ac=A, asc=A, m=16, wc=A, wsc=A, n=256, k=512, out=A: L.fp4_gemm_mx_prequant(
+        ea, ac, asc, m, ew, wc, wsc, n, k, out, None)
+    assert g(n=250) == c["FP4_ERR_SHAPE"]
+    assert g(k=48) == c["FP4_ERR_SHAPE"]
+    assert g(ea=9) == c["FP4_ERR_INVALID_ARG"]
+    # MXFP6 codes are quantiser output only: the GEMM refuses them
+    assert g(ea=2) == c["FP4_ERR_INVALID_ARG"] and "MXFP8" in L.fp4_last_error_message().decode()
+    assert g(ew=3) == c["FP4_ERR_INVALID_ARG"]
+    assert g(wc=0) == c["FP4_ERR_INVALID_ARG"]
+    assert g(out=A + 4) == c["FP4_ERR_ALIGNMENT"]
+    assert L.fp4_gemm_mx(0, A, 16, 0, A, A, 256, 512, A, A, 16, None) == c["FP4_ERR_WORKSPACE"]
+    assert L.fp4_gemm_mx_workspace_size(16, 512) >= 16 * 512 + 128 * 16
+
+
+def test_moe_policy_validation(F):
+    L = F.lib()
+    for p in (F.MOE_CHAIN, F.MOE_AUTO):
+        assert L.fp4_set_moe_policy(p) == 0
+    for bad in (-1, 2):
+        assert L.fp4_set_moe_policy(bad) == F.STATUS_CODE["FP4_ERR_INVALID_ARG"]
+        assert "MoE policy" in L.fp4_last_error_message().decode()
