@@ -120,13 +120,14 @@ void fp4_set_arch_override(int sm);
 fp4_status fp4_set_gemm_tile_policy(int policy);
 
 /* Tuning and test hook (no counterpart on the pages): which implementation
- * fp4_moe_grouped uses.  0 = automatic: for 1 <= T <= 16 tokens, top_k <= 8,
- * hidden and inter multiples of 256 and at most 2048, the one-launch MoE (a
- * memset of its counters, then one cooperative kernel: route, quantise,
- * GEMM1 + SwiGLU, requantise, GEMM2 and the top-k sum in slot order), else
- * the launch chain; 1 = always the launch chain.  Results agree within the
- * MoE tolerance under both.  Process-wide, host-side; FP4_ERR_INVALID_ARG
- * for a value outside 0..1. */
+ * fp4_moe_grouped uses.  The one-launch MoE (a memset of its counters, then
+ * one cooperative kernel: route, quantise, GEMM1 + SwiGLU, requantise, GEMM2
+ * and the top-k sum in slot order) takes 1 <= T <= 16 tokens, top_k <= 8,
+ * hidden and inter multiples of 256 and at most 2048; otherwise the launch
+ * chain runs.  0 = automatic: the one launch for T <= 8 (where it is the
+ * faster), else the chain; 1 = always the chain; 2 = the one launch
+ * wherever it applies.  Results agree within the MoE tolerance under all.
+ * Process-wide, host-side; FP4_ERR_INVALID_ARG for a value outside 0..2. */
 fp4_status fp4_set_moe_policy(int policy);
 
 /* Test hook (host-side, no device needed): the plan fp4_gemm /

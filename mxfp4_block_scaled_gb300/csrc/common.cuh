@@ -223,6 +223,11 @@ __device__ __forceinline__ bool mbar_wait_then_cluster_fence(uint64_t* bar, uint
     return true;
 }
 
+// Acquire-release fence at GPU scope (lighter than the sequentially
+// consistent __threadfence()): orders this thread's earlier memory operations,
+// and those ordered before them, before its later ones for every GPU thread.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }

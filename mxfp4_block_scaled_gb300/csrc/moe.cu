@@ -801,8 +801,8 @@ extern "C" int fp4_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int64_t
 static int g_moe_policy = 0;  // fp4_set_moe_policy
 
 extern "C" fp4_status fp4_set_moe_policy(int policy) {
-    if (policy < 0 || policy > 1) {
-        set_error("MoE policy %d not in 0..1", policy);
+    if (policy < 0 || policy > 2) {
+        set_error("MoE policy %d not in 0..2", policy);
         return FP4_ERR_INVALID_ARG;
     }
     g_moe_policy = policy;
@@ -886,7 +886,9 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
     bool pdl = false;  // first launch of the call waits for everything before it
     const int per_lane = (int)((E + 31) / 32);
 
-    if (full && g_moe_policy == 0 && moe_fused_supported(T, H, I, E, k)) {
+    // the one launch where it is faster than the chain (automatic), or whenever it applies (policy 2)
+    const bool fused = g_moe_policy == 2 || (g_moe_policy == 0 && T <= kFusedAutoMaxT);
+    if (full && fused && moe_fused_supported(T, H, I, E, k)) {
         // a few tokens: the whole layer in one launch (after a memset of its counters)
         FusedMoeLaunch F;
         F.hidden = static_cast<const uint16_t*>(hidden);

@@ -21,9 +21,11 @@ struct StaticScales {
 
 // The one-launch MoE for a few tokens (moe_fused.cu).
 constexpr int kFusedMaxT = 16;                        // tokens
+constexpr int kFusedAutoMaxT = 8;                     // tokens up to which fp4_moe_grouped takes it by default
 constexpr int kFusedMaxTopK = 8;
 constexpr int kFusedMaxSlots = kFusedMaxT * kFusedMaxTopK;
 constexpr int kFusedMaxK = 2048;                      // H and I (the two GEMMs' K)
+constexpr int kFusedMaxE = 256;                       // experts
 constexpr int kFusedMaxOutTiles = 32;                 // H / 128
 constexpr int kFusedZeroedBytes = 2048;               // counters + h amax, cleared per call
 
@@ -57,17 +59,13 @@ bool moe_fused_supported(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k);
 // One memset (the counters) and one cooperative kernel launch.
 cudaError_t launch_moe_fused(const FusedMoeLaunch& L, const StaticScales& st, cudaStream_t s);
 
-// Warp-cooperative top-k over one token's logits; ties go to the lower
-// expert index.  Lane j < k returns the j-th selection and its weight
+// Warp-cooperative top-k over one token's logits, lane l holding logits
+// l, 32 + l, 64 + l, ... in v (-inf past E); ties go to the lower expert
+// index.  Lane j < k returns the j-th selection and its weight
 // exp(l_j - l_max) / sum over the selection.
 template <int PER_LANE>
-__device__ __forceinline__ void topk_token(const float* row, int E, int k, int lane, int& my_e, float& my_w) {
-    float v[PER_LANE];
-#pragma unroll
-    for (int q = 0; q < PER_LANE; ++q) {
-        const int e = q * 32 + lane;
-        v[q] = e < E ? row[e] : -INFINITY;
-    }
+__device__ __forceinline__ void topk_regs(const float (&v)[PER_LANE], int E, int k, int lane, int& my_e,
+                                          float& my_w) {
     uint32_t taken = 0;
     float v0 = 0.0f, sum = 0.0f, mine = 0.0f;
     my_e = 0;
@@ -101,6 +99,18 @@ __device__ __forceinline__ void topk_token(const float* row, int E, int k, int l
         }
     }
     my_w = __fdiv_rn(mine, sum);
+}
+
+// The same, loading the token's logits row.
+template <int PER_LANE>
+__device__ __forceinline__ void topk_token(const float* row, int E, int k, int lane, int& my_e, float& my_w) {
+    float v[PER_LANE];
+#pragma unroll
+    for (int q = 0; q < PER_LANE; ++q) {
+        const int e = q * 32 + lane;
+        v[q] = e < E ? row[e] : -INFINITY;
+    }
+    topk_regs<PER_LANE>(v, E, k, lane, my_e, my_w);
 }
 
 }  // namespace fp4

@@ -31,19 +31,22 @@
 // deadlock.  The counters (and the amax) must be zero at launch: the host
 // clears them with one memset before the kernel.
 //
-// Per CTA, 16 warps:
+// Per CTA, 16 warps, the units flowing through them as a pipeline:
 //   warp 4      TMA producer: each unit's weight tile per 256-element K block
 //               (128 rows x 128 B, 128-byte swizzle) and its 4 scale atoms,
 //               on one barrier per stage; it runs ahead through the ring
 //               from the first unit (the weights depend only on the routing)
+//   warps 12-15 the token operand of each unit (the hidden rows quantised
+//               with the unit's global scale, or -- after the expert's GEMM1
+//               units -- its h rows requantised) for the whole K into one of
+//               two shared-memory tiles, so unit n + 1's operand is built
+//               while unit n computes
 //   warps 0-3   scale writers: the stage's weight atoms and the unit's token
 //               atoms of that K block into the stage's TMEM scale columns
 //   warp 5      TMEM allocation and the MMA issuer: swap-AB block-scaled MMAs
-//               (M = 128 weight rows, N = 32 token columns, K = 64)
-//   warps 8-15  per unit: the token operand (the hidden rows quantised with
-//               the unit's global scale, or the expert's h rows requantised)
-//               for the whole K into a shared-memory tile; then warps 8-11
-//               read the accumulator and run the unit's epilogue
+//               (M = 128 weight rows, N = 32 token columns, K = 64) into one
+//               of two TMEM accumulators
+//   warps 8-11  the epilogue of each unit, overlapping the next unit's MMAs
 // Every wait is bounded: on expiry the role sets the device error word and
 // an abort flag that stops the others in the CTA (a CTA waiting on a counter
 // that an aborted CTA never raises gives up at its own limit).
@@ -63,27 +66,31 @@ struct FusedCfg {
     static constexpr int SFP_BYTES = 4 * 512;              // weight scale atoms per K block
     static constexpr int MAX_KB = kFusedMaxK / 256;        // K blocks of the token operand
     static constexpr int QC_BYTES = BN * 128;              // token codes per K block (32 rows x 128 B)
-    static constexpr int QS_BYTES = 4 * 512;               // token scale atoms per K block
-    static constexpr int STAGES = 8;
+    // token scale atoms per K block, compact: the 32 token rows' words of the
+    // four atoms (row r's 4 bytes at c * 128 + r * 4); the scale writers
+    // expand them to the TMEM layout (rows 32-127 of an atom are zero)
+    static constexpr int QS_BYTES = 4 * 128;
+    static constexpr int QBUF = MAX_KB * (QC_BYTES + QS_BYTES);  // one token operand tile (codes, then atoms)
+    static constexpr int STAGES = 7;
     static constexpr int SF_COLS = 32;                     // TMEM scale columns per stage (16 weight + 16 token)
-    static constexpr int XCH_BYTES = 2 * 32 * 32 * 4;      // SwiGLU gate values handed to the up warps
+    static constexpr int XCH_BYTES = 4 * kFusedMaxT * 32 * 4;  // the epilogue's alpha-scaled accumulator columns
     static constexpr int OFF_P = 0;
     static constexpr int OFF_SF = OFF_P + STAGES * P_BYTES;
-    static constexpr int OFF_QC = OFF_SF + STAGES * SFP_BYTES;
-    static constexpr int OFF_QS = OFF_QC + MAX_KB * QC_BYTES;
-    static constexpr int OFF_X = OFF_QS + MAX_KB * QS_BYTES;
-    static constexpr int OFF_DTAB = OFF_X + XCH_BYTES;
-    static constexpr int OFF_TAB = OFF_DTAB + 128 * 8;
-    // routing tables: ids, weights, expert count / active index (E <= 1024),
-    // active experts, their slot lists and token counts
-    static constexpr int TAB_BYTES = kFusedMaxSlots * 4 * 2 + kMaxExperts * 4 + kMaxExperts * 2 +
-                                     kFusedMaxSlots * 4 + kFusedMaxSlots * kFusedMaxT * 2 + kFusedMaxSlots * 4 + 256;
+    static constexpr int OFF_Q = OFF_SF + STAGES * SFP_BYTES;  // two token operand tiles
+    static constexpr int OFF_X = OFF_Q + 2 * QBUF;
+    static constexpr int OFF_DTAB = OFF_X + XCH_BYTES;     // three divisor tables: GEMM1 dynamic, per tile x 2
+    static constexpr int OFF_TAB = OFF_DTAB + 3 * 128 * 8;
+    // routing tables: ids and weights per slot; per expert the token mask,
+    // active index and the two weight global scales; per active expert the
+    // expert, its slot list, token count and s_gH; misc words
+    static constexpr int TAB_BYTES = kFusedMaxSlots * 4 * 2 + kFusedMaxE * (4 + 2 + 4 + 4) +
+                                     kFusedMaxSlots * (4 + kFusedMaxT * 2 + 4 + 4) + 256;
     static constexpr int OFF_BAR = OFF_TAB + TAB_BYTES;
     static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM = 1024 + OFF_BAR + BAR_BYTES;
-    static_assert(OFF_QC % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles are 1024-byte aligned");
+    static_assert(OFF_Q % 1024 == 0 && QBUF % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles are 1024-byte aligned");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
-    static_assert(BN + STAGES * SF_COLS <= 512, "TMEM budget");
+    static_assert(2 * BN + STAGES * SF_COLS <= 512, "TMEM budget");
     static_assert(kFusedMaxT <= BN, "an expert's tokens fit the N side");
 };
 
@@ -119,6 +126,22 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
     return v;
 }
 
+// Bounded wait, by one thread, for a counter another CTA raises; false (and
+// the device error word and the CTA's abort flag set) when it gives up.
+__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t want, const WaitCfg& wc,
+                                           volatile int* abort_flag) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0; it < 0x40000000u; ++it) {
+        if (ld_acquire_u32(p) >= want) return true;
+        if (*abort_flag) return false;
+        __nanosleep(32);
+        if ((it & 15u) == 15u && globaltimer_ns() - t0 > wc.limit_ns) break;
+    }
+    atomicOr(wc.err, DEV_ERR_TIMEOUT);
+    *abort_flag = 1;
+    return false;
+}
+
 template <int PER_LANE>
 __global__ void __launch_bounds__(512, 1)
     moe_fused_kernel(const __grid_constant__ CUtensorMap tm13, const __grid_constant__ CUtensorMap tm2,
@@ -128,52 +151,82 @@ __global__ void __launch_bounds__(512, 1)
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t* sP = smem + C::OFF_P;
     uint8_t* sSF = smem + C::OFF_SF;
-    uint8_t* sQC = smem + C::OFF_QC;
-    uint8_t* sQS = smem + C::OFF_QS;
+    uint8_t* sQ = smem + C::OFF_Q;  // tile b: codes at b * QBUF, atoms at b * QBUF + MAX_KB * QC_BYTES
     float* sX = reinterpret_cast<float*>(smem + C::OFF_X);
-    float2* dtab = reinterpret_cast<float2*>(smem + C::OFF_DTAB);
+    float2* dtab = reinterpret_cast<float2*>(smem + C::OFF_DTAB);  // [3][128]
     int32_t* s_ids = reinterpret_cast<int32_t*>(smem + C::OFF_TAB);
     float* s_w = reinterpret_cast<float*>(s_ids + kFusedMaxSlots);
-    int32_t* s_cnt = reinterpret_cast<int32_t*>(s_w + kFusedMaxSlots);        // [E] tokens per expert
-    int16_t* s_aidx = reinterpret_cast<int16_t*>(s_cnt + kMaxExperts);        // [E] active index
-    int32_t* s_act = reinterpret_cast<int32_t*>(s_aidx + kMaxExperts);        // [E_act] expert
-    int16_t* s_eslot = reinterpret_cast<int16_t*>(s_act + kFusedMaxSlots);    // [E_act][kFusedMaxT] slots
+    uint32_t* s_mask = reinterpret_cast<uint32_t*>(s_w + kFusedMaxSlots);    // [E] tokens of each expert (bit t)
+    float* s_gw13 = reinterpret_cast<float*>(s_mask + kFusedMaxE);           // [E] W13 global scales
+    float* s_gw2 = s_gw13 + kFusedMaxE;                                      // [E] W2 global scales
+    int16_t* s_aidx = reinterpret_cast<int16_t*>(s_gw2 + kFusedMaxE);        // [E] active index
+    int32_t* s_act = reinterpret_cast<int32_t*>(s_aidx + kFusedMaxE);        // [E_act] expert
+    int16_t* s_eslot = reinterpret_cast<int16_t*>(s_act + kFusedMaxSlots);   // [E_act][kFusedMaxT] slots
     int32_t* s_ne = reinterpret_cast<int32_t*>(s_eslot + kFusedMaxSlots * kFusedMaxT);  // [E_act] token count
-    int32_t* s_misc = s_ne + kFusedMaxSlots;  // [0] E_act, [1] amax bits, [2] last-arriver flag, [3] unit s_g,
-                                              // [4..36) per-chunk active counts, then [5] the group's stop flag
+    float* s_sgh = reinterpret_cast<float*>(s_ne + kFusedMaxSlots);          // [E_act] s_gH (quantisers -> epilogue)
+    // [0] E_act, [1] amax bits, [2] last-arriver flag, [3] the quantisers' s_g,
+    // [4..36) per-chunk active counts (prologue), then [4] the quantisers' and
+    // [5] the epilogue's stop flags
+    volatile int32_t* s_misc = reinterpret_cast<int32_t*>(s_sgh + kFusedMaxSlots);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* full = bars;
     uint64_t* empty = bars + C::STAGES;
     uint64_t* tready = bars + 2 * C::STAGES;
-    uint64_t* qready = bars + 3 * C::STAGES;
-    uint64_t* accf = qready + 1;
-    uint64_t* acce = accf + 1;
-    uint64_t* drain = acce + 1;
+    uint64_t* qfull = bars + 3 * C::STAGES;  // [2] token tile written
+    uint64_t* qempty = qfull + 2;            // [2] the MMAs reading the tile are done
+    uint64_t* accf = qempty + 2;             // [2] accumulator complete
+    uint64_t* acce = accf + 2;               // [2] accumulator read by the epilogue
+    uint64_t* drain = acce + 2;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int T = a.T, H = a.H, I = a.I, E = a.E, k = a.k;
+    // The routing and the hidden abs-max need only the inputs: their loads go
+    // out first (after the dependency wait), before the set-up below.
+    pdl_wait();  // hidden and logits come from the preceding kernels
+    float lg[PER_LANE];
+    if (warp < T) {
+#pragma unroll
+        for (int q = 0; q < PER_LANE; ++q) {
+            const int e = q * 32 + lane;
+            lg[q] = e < E ? __ldg(a.logits + (int64_t)warp * E + e) : -INFINITY;
+        }
+    }
+    const float gw = threadIdx.x < E ? __ldg(a.w13_global + threadIdx.x) : 0.0f;
+    const float gw2 = threadIdx.x < E ? __ldg(a.w2_global + threadIdx.x) : 0.0f;
+    uint32_t hm = 0;
+    if (!a.is_static) {
+        const int nv = T * H / 8;
+        const uint4* xv = reinterpret_cast<const uint4*>(a.hidden);
+        for (int i = threadIdx.x; i < nv; i += 512) hm = absmax8(__ldg(xv + i), hm);
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
             mbar_init(tready + s, 4);
         }
-        mbar_init(qready, 1);
-        mbar_init(accf, 1);
-        mbar_init(acce, 4);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(qfull + b, 1);
+            mbar_init(qempty + b, 1);
+            mbar_init(accf + b, 1);
+            mbar_init(acce + b, 4);
+        }
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tensormap(&tm13);
         prefetch_tensormap(&tm2);
     }
-    // token operand tiles and their scale atoms start at zero (rows past an
-    // expert's tokens are never read back; the zeros keep their scales finite)
-    for (int i = threadIdx.x; i < C::MAX_KB * (C::QC_BYTES + C::QS_BYTES) / 16; i += 512)
-        reinterpret_cast<uint4*>(sQC)[i] = make_uint4(0u, 0u, 0u, 0u);
-    for (int i = threadIdx.x; i < E; i += 512) s_cnt[i] = 0;
+    // token operand tiles start at zero (rows past an expert's tokens are never
+    // read back; the zeros keep their scales finite)
+    for (int i = threadIdx.x; i < 2 * C::QBUF / 16; i += 512) reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (threadIdx.x < E) {
+        s_mask[threadIdx.x] = 0u;
+        s_gw13[threadIdx.x] = gw;
+        s_gw2[threadIdx.x] = gw2;
+    }
     fence_proxy_async();
     if (warp == 5) {
         tmem_alloc(tslot, 512);
@@ -183,54 +236,58 @@ __global__ void __launch_bounds__(512, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    pdl_wait();  // hidden and logits come from the preceding kernels
 
     // ---------------------------------------------------------- prologue
-    // route (a warp per token) and the hidden rows' abs-max
+    // route (a warp per token, ties to the lower expert index) and the
+    // hidden rows' abs-max
     if (warp < T) {
         int e;
         float w;
-        topk_token<PER_LANE>(a.logits + (int64_t)warp * E, E, k, lane, e, w);
+        topk_regs<PER_LANE>(lg, E, k, lane, e, w);
         if (lane < k) {
             s_ids[warp * k + lane] = e;
             s_w[warp * k + lane] = w;
         }
     }
     if (!a.is_static) {
-        const int nv = T * H / 8;
-        const uint4* xv = reinterpret_cast<const uint4*>(a.hidden);
-        uint32_t m = 0;
-        for (int i = threadIdx.x; i < nv; i += 512) m = absmax8(__ldg(xv + i), m);
-        m = max(m & 0xFFFFu, m >> 16);
+        hm = max(hm & 0xFFFFu, hm >> 16);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) hm = max(hm, __shfl_xor_sync(0xFFFFFFFFu, hm, o));
+        if (lane == 0) s_misc[4 + warp] = (int32_t)hm;
+    }
+    __syncthreads();
+    if (threadIdx.x < T * k) atomicOr(&s_mask[s_ids[threadIdx.x]], 1u << (threadIdx.x / k));
+    if (!a.is_static && threadIdx.x < 32) {
+        uint32_t m = lane < 16 ? (uint32_t)s_misc[4 + lane] : 0u;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        if (lane == 0) s_misc[4 + warp] = (int32_t)m;
+        if (lane == 0) s_misc[1] = (int32_t)m;
     }
     __syncthreads();
-    if (threadIdx.x < T * k) atomicAdd(&s_cnt[s_ids[threadIdx.x]], 1);
-    if (threadIdx.x == 0 && !a.is_static) {
-        uint32_t m = 0;
-        for (int w = 0; w < 16; ++w) m = max(m, (uint32_t)s_misc[4 + w]);
-        s_misc[1] = (int32_t)m;
-    }
-    __syncthreads();
+    const float sg_a = a.is_static ? 0.0f : __fdiv_rn(__uint_as_float((uint32_t)s_misc[1] << 16), 2688.0f);
+    // the GEMM1 divisor table of the dynamic scale (one for every GEMM1 unit)
+    if (!a.is_static && threadIdx.x >= 384) dtab[threadIdx.x - 384] = nvfp4_divisor(threadIdx.x - 384, sg_a, T > 2);
     // active experts in ascending order: warp w ballots experts 64 w .. 64 w + 63
     uint32_t bal[2];
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
         const int e = warp * 64 + c * 32 + lane;
-        bal[c] = __ballot_sync(0xFFFFFFFFu, e < E && s_cnt[e] > 0);
+        bal[c] = __ballot_sync(0xFFFFFFFFu, e < E && s_mask[e] != 0u);
         if (lane == 0) s_misc[4 + warp * 2 + c] = __popc(bal[c]);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int acc = 0;
-        for (int c = 0; c < 32; ++c) {
-            const int n = s_misc[4 + c];
-            s_misc[4 + c] = acc;
-            acc += n;
+    if (warp == 0) {
+        // exclusive prefix over the 32 chunk counts
+        const int n = s_misc[4 + lane];
+        int incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += y;
         }
-        s_misc[0] = acc;
+        __syncwarp();
+        s_misc[4 + lane] = incl - n;
+        if (lane == 31) s_misc[0] = incl;
     }
     __syncthreads();
 #pragma unroll
@@ -240,65 +297,68 @@ __global__ void __launch_bounds__(512, 1)
             const int idx = s_misc[4 + warp * 2 + c] + __popc(bal[c] & ((1u << lane) - 1u));
             s_act[idx] = e;
             s_aidx[e] = (int16_t)idx;
-            s_ne[idx] = s_cnt[e];
+            s_ne[idx] = __popc(s_mask[e]);
         }
     }
     __syncthreads();
     if (threadIdx.x < T * k) {
         const int i = threadIdx.x, t = i / k, e = s_ids[i];
-        int pos = 0;
-        for (int i2 = 0; i2 < t * k; ++i2) pos += s_ids[i2] == e ? 1 : 0;
+        const int pos = __popc(s_mask[e] & ((1u << t) - 1u));  // the expert's tokens before t
         s_eslot[s_aidx[e] * kFusedMaxT + pos] = (int16_t)i;
         if (blockIdx.x == 0) {
             a.ids[i] = e;
             a.weights[i] = s_w[i];
         }
     }
-    const float sg_a = a.is_static ? 0.0f : __fdiv_rn(__uint_as_float((uint32_t)s_misc[1] << 16), 2688.0f);
     if (blockIdx.x == 0 && threadIdx.x == 0 && !a.is_static) a.sg_a[0] = sg_a;
     __syncthreads();
     const int E_act = s_misc[0];
     const int n1 = 2 * I / 128, n2 = H / 128;
-    const int64_t U1 = (int64_t)E_act * n1, U = U1 + (int64_t)E_act * n2;
+    const int U1 = E_act * n1, U = U1 + E_act * n2;
     const int kb1 = H / 256, kb2 = I / 256;
     const int64_t ksfc13 = (int64_t)(H / 256) * 4, ksfc2 = (int64_t)(I / 256) * 4;
     // (no early trigger of dependent launches: this grid's CTAs wait on one
     // another, so nothing else is invited onto their SMs before they finish)
 
     // unit v -> (GEMM1?, active index, tile)
-    auto unit = [&](int64_t v, bool& g1, int& ai, int& t) {
+    auto unit = [&](int v, bool& g1, int& ai, int& t) {
         g1 = v < U1;
-        const int64_t w = g1 ? v : v - U1;
+        const int w = g1 ? v : v - U1;
         const int n = g1 ? n1 : n2;
-        ai = (int)(w / n);
-        t = (int)(w % n);
+        ai = w / n;
+        t = w - ai * n;
     };
 
     if (warp < 4) {
         // ------------------------------------------------ scale writers
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         int stage = 0;
-        uint32_t ph = 0, uph = 0;
+        uint32_t ph = 0;
         bool ok = true;
-        for (int64_t v = blockIdx.x; v < U && ok; v += gridDim.x, uph ^= 1u) {
+        int n = 0;
+        for (int v = blockIdx.x; v < U && ok; v += gridDim.x, ++n) {
             bool g1;
             int ai, t;
             unit(v, g1, ai, t);
-            if (!mbar_wait(qready, uph, wc, abort_flag)) break;
+            const int qb = n & 1;
+            if (!mbar_wait(qfull + qb, (uint32_t)(n >> 1) & 1u, wc, abort_flag)) break;
             const int kbn = g1 ? kb1 : kb2;
+            const uint32_t qs0 = smem_u32(sQ + qb * C::QBUF + C::MAX_KB * C::QC_BYTES) + lane * 4;
             for (int kb = 0; kb < kbn; ++kb) {
                 if (!mbar_wait(full + stage, ph, wc, abort_flag)) {
                     ok = false;
                     break;
                 }
-                const uint32_t sfp_t = tmem + lane_base + (uint32_t)(C::BN + stage * C::SF_COLS);
+                const uint32_t sfp_t = tmem + lane_base + (uint32_t)(2 * C::BN + stage * C::SF_COLS);
                 const uint32_t sfq_t = sfp_t + 16;
                 const uint32_t sp = smem_u32(sSF + stage * C::SFP_BYTES) + lane * 16;
-                const uint32_t sq = smem_u32(sQS + kb * C::QS_BYTES) + lane * 16;
+                const uint32_t sq = qs0 + kb * C::QS_BYTES;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     tmem_st4(sfp_t + c * 4, lds128(sp + c * 512));
-                    tmem_st4(sfq_t + c * 4, lds128(sq + c * 512));
+                    uint32_t wq;
+                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wq) : "r"(sq + c * 128));
+                    tmem_st4(sfq_t + c * 4, make_uint4(wq, 0u, 0u, 0u));
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -317,7 +377,7 @@ __global__ void __launch_bounds__(512, 1)
             uint32_t ph = 0;
             uint32_t issued = 0, issued_ph = 0;
             bool ok = true;
-            for (int64_t v = blockIdx.x; v < U && ok; v += gridDim.x) {
+            for (int v = blockIdx.x; v < U && ok; v += gridDim.x) {
                 bool g1;
                 int ai, t;
                 unit(v, g1, ai, t);
@@ -355,15 +415,21 @@ __global__ void __launch_bounds__(512, 1)
             // ------------------------------------------------ MMA issuer
             const uint32_t idesc = idesc_mxf4(128, C::BN, false);
             int stage = 0;
-            uint32_t ph = 0, uph = 0;
+            uint32_t ph = 0;
             bool ok = true, any = false;
-            for (int64_t v = blockIdx.x; v < U && ok; v += gridDim.x, uph ^= 1u) {
+            int n = 0;
+            for (int v = blockIdx.x; v < U && ok; v += gridDim.x, ++n) {
                 bool g1;
                 int ai, t;
                 unit(v, g1, ai, t);
-                // the previous unit's accumulator has been read, and this unit's token tile is written
-                if (!mbar_wait(acce, uph ^ 1u, wc, abort_flag) || !mbar_wait(qready, uph, wc, abort_flag)) break;
+                const int b = n & 1;
+                const uint32_t par = (uint32_t)(n >> 1) & 1u;
+                // accumulator b has been read (unit n - 2), token tile b is written (unit n)
+                if (!mbar_wait(acce + b, par ^ 1u, wc, abort_flag) || !mbar_wait(qfull + b, par, wc, abort_flag))
+                    break;
                 tc_fence_after();
+                const uint32_t d_tmem = tmem + (uint32_t)(b * C::BN);
+                const uint32_t qc0 = smem_u32(sQ + b * C::QBUF);
                 const int kbn = g1 ? kb1 : kb2;
                 for (int kb = 0; kb < kbn; ++kb) {
                     if (!mbar_wait(full + stage, ph, wc, abort_flag) ||
@@ -372,13 +438,13 @@ __global__ void __launch_bounds__(512, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sfp_t = tmem + (uint32_t)(C::BN + stage * C::SF_COLS);
+                    const uint32_t sfp_t = tmem + (uint32_t)(2 * C::BN + stage * C::SF_COLS);
                     const uint32_t sfq_t = sfp_t + 16;
                     const uint32_t pa = smem_u32(sP + stage * C::P_BYTES);
-                    const uint32_t qa = smem_u32(sQC + kb * C::QC_BYTES);
+                    const uint32_t qa = qc0 + kb * C::QC_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_mxf4<false>(tmem, sdesc_sw128(pa + kk * 32), sdesc_sw128(qa + kk * 32), idesc,
+                        mma_mxf4<false>(d_tmem, sdesc_sw128(pa + kk * 32), sdesc_sw128(qa + kk * 32), idesc,
                                         sfp_t + kk * 4, sfq_t + kk * 4, (kb > 0 || kk > 0) ? 1u : 0u);
                     any = true;
                     mma_commit(empty + stage);
@@ -388,7 +454,8 @@ __global__ void __launch_bounds__(512, 1)
                     }
                 }
                 if (!ok) break;
-                mma_commit(accf);
+                mma_commit(accf + b);
+                mma_commit(qempty + b);
             }
             if (any && *abort_flag) {
                 // the tensor-core work already issued finishes before TMEM is freed
@@ -397,61 +464,57 @@ __global__ void __launch_bounds__(512, 1)
                 mbar_wait(drain, 0, wc, &never);
             }
         }
-    } else if (warp >= 8) {
-        // ------------------------------------ token operand + epilogue (warps 8-15)
-        const int gt = threadIdx.x - 256;  // 0..255
-        volatile int32_t* vmisc = s_misc;
-        uint32_t uph = 0;
-        for (int64_t v = blockIdx.x; v < U; v += gridDim.x, uph ^= 1u) {
+    } else if (warp >= 12) {
+        // ------------------------------------ token operand tiles (warps 12-15)
+        const int q = threadIdx.x - 384;  // 0..127
+        int n = 0;
+        for (int v = blockIdx.x; v < U; v += gridDim.x, ++n) {
             bool g1;
             int ai, t;
             unit(v, g1, ai, t);
             const int e = s_act[ai];
             const int ne = s_ne[ai];
-            // 1. the unit's global scale (GEMM2: after the expert's GEMM1 units)
-            if (gt == 0) {
-                float sg;
-                if (g1) {
-                    sg = a.is_static ? st.s13[e] : sg_a;
-                } else {
-                    const uint64_t t0 = globaltimer_ns();
-                    bool ready = false;
-                    for (uint32_t it = 0; it < 0x40000000u; ++it) {
-                        if (ld_acquire_u32(a.cnt1 + ai) >= (uint32_t)n1) {
-                            ready = true;
-                            break;
-                        }
-                        if (*abort_flag) break;
-                        __nanosleep(64);
-                        if ((it & 15u) == 15u && globaltimer_ns() - t0 > wc.limit_ns) break;
+            const int qb = n & 1;
+            // 1. tile qb is free (the MMAs of unit n - 2 are done) and the unit's
+            //    global scale is known (GEMM2: after the expert's GEMM1 units)
+            if (q == 0) {
+                bool ok = mbar_wait(qempty + qb, ((uint32_t)(n >> 1) & 1u) ^ 1u, wc, abort_flag);
+                float sg = 0.0f;
+                if (ok) {
+                    if (g1) {
+                        sg = a.is_static ? st.s13[e] : sg_a;
+                    } else {
+                        ok = wait_count(a.cnt1 + ai, (uint32_t)n1, wc, abort_flag);
+                        const float amax = __uint_as_float(ld_acquire_u32(a.amax_h + ai));
+                        sg = a.is_static ? st.s2[e] : __fdiv_rn(amax, 2688.0f);
+                        if (ok && t == 0) a.sg_h[e] = sg;
+                        s_sgh[ai] = sg;  // for the epilogue (ordered by the tile's barriers)
                     }
-                    if (!ready) {
-                        if (!*abort_flag) atomicOr(wc.err, DEV_ERR_TIMEOUT);
-                        *abort_flag = 1;
-                    }
-                    __threadfence();
-                    const float amax = __uint_as_float(ld_acquire_u32(a.amax_h + ai));
-                    sg = a.is_static ? st.s2[e] : __fdiv_rn(amax, 2688.0f);
-                    if (t == 0) a.sg_h[e] = sg;
                 }
-                vmisc[3] = (int32_t)__float_as_uint(sg);
-                vmisc[5] = *abort_flag ? 1 : 0;  // one decision for the whole group (named barriers follow)
+                s_misc[3] = (int32_t)__float_as_uint(sg);
+                s_misc[4] = ok ? 0 : 1;  // one decision for the group (named barriers follow)
             }
-            named_bar_sync(1, 256);
-            if (vmisc[5]) break;
-            const float sg = __uint_as_float((uint32_t)vmisc[3]);
+            named_bar_sync(3, 128);
+            if (s_misc[4]) break;
+            const float sg = __uint_as_float((uint32_t)s_misc[3]);
+            float2* tab = dtab;  // GEMM1, dynamic scale: the prologue's table
+            if (!g1 || a.is_static) {
+                tab = dtab + (1 + qb) * 128;
+                tab[q] = nvfp4_divisor((uint32_t)q, sg, ne > 2);
+                named_bar_sync(3, 128);
+            }
             const float p_t = __fmul_rn(sg, 6.0f);
             const float inv_p = nvfp4_inv_p(p_t);
-            if (gt < 128) dtab[gt] = nvfp4_divisor((uint32_t)gt, sg, true);
-            named_bar_sync(1, 256);
-            // 2. the token operand: ne rows x K, NVFP4 with s_g = sg, straight
-            //    into the MMA's swizzled tile (row r, K block kb, 16-byte piece
-            //    c at piece c ^ (r % 8)) and scale atoms (row r at r * 16)
+            // 2. ne rows x K, NVFP4 with s_g = sg, straight into the MMA's swizzled
+            //    tile (row r, K block kb, 16-byte piece c at piece c ^ (r % 8)) and
+            //    scale atoms (row r at r * 16)
+            uint8_t* qc = sQ + qb * C::QBUF;
+            uint8_t* qs = qc + C::MAX_KB * C::QC_BYTES;
             const int K = g1 ? H : I;
-            const int bpr = K / 16;  // blocks per row
+            const int bpr = K / 16;    // blocks per row
             const bool dump = t == 0;  // one unit per expert leaves the codes in the workspace
-            for (int b = gt; b < ne * bpr; b += 256) {
-                const int r = b / bpr, j = b - r * bpr;
+            for (int bb = q; bb < ne * bpr; bb += 128) {
+                const int r = bb / bpr, j = bb - r * bpr;
                 const int slot = s_eslot[ai * kFusedMaxT + r];
                 uint4 x0, x1;
                 if (g1) {
@@ -468,14 +531,14 @@ __global__ void __launch_bounds__(512, 1)
                 const uint32_t sbyte = nvfp4_scale_byte(__uint_as_float(am << 16), p_t, inv_p);
                 float f[8];
                 unpack8(x0, f);
-                const uint32_t w0 = nvfp4_word(f, dtab[sbyte]);
+                const uint32_t w0 = nvfp4_word(f, tab[sbyte]);
                 unpack8(x1, f);
-                const uint32_t w1 = nvfp4_word(f, dtab[sbyte]);
+                const uint32_t w1 = nvfp4_word(f, tab[sbyte]);
                 const int kb = j >> 4, jj = j & 15;
-                const uint32_t qa = smem_u32(sQC + kb * C::QC_BYTES) + (uint32_t)r * 128u +
+                const uint32_t qa = smem_u32(qc + kb * C::QC_BYTES) + (uint32_t)r * 128u +
                                     ((((uint32_t)jj >> 1) ^ ((uint32_t)r & 7u)) << 4) + (((uint32_t)jj & 1u) << 3);
                 asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(qa), "r"(w0), "r"(w1) : "memory");
-                sQS[kb * C::QS_BYTES + (jj >> 2) * 512 + r * 16 + (jj & 3)] = (uint8_t)sbyte;
+                qs[kb * C::QS_BYTES + (jj >> 2) * 128 + r * 4 + (jj & 3)] = (uint8_t)sbyte;
                 if (dump) {
                     uint8_t* dc = g1 ? a.a_codes + (int64_t)slot * (H / 2) : a.h_codes + (int64_t)slot * (I / 2);
                     uint8_t* ds = g1 ? a.a_sbytes + (int64_t)slot * (H / 16) : a.h_sbytes + (int64_t)slot * (I / 16);
@@ -484,88 +547,100 @@ __global__ void __launch_bounds__(512, 1)
                 }
             }
             fence_proxy_async();  // the tile is read by the tensor cores
-            named_bar_sync(1, 256);
-            // 3. the accumulator: one thread waits for it, the group follows
-            //    (the next unit's tile may be written only once these MMAs are
-            //    complete, and every thread takes the same branch)
-            if (gt == 0) {
-                mbar_arrive(qready);
-                vmisc[5] = mbar_wait(accf, uph, wc, abort_flag) ? 0 : 1;
-            }
-            named_bar_sync(1, 256);
-            if (vmisc[5]) break;
+            named_bar_sync(3, 128);
+            if (q == 0) mbar_arrive(qfull + qb);
+        }
+    } else if (warp >= 8) {
+        // --------------------------------------------------- epilogue (warps 8-11)
+        const int qd = warp - 8;
+        int n = 0;
+        for (int v = blockIdx.x; v < U; v += gridDim.x, ++n) {
+            bool g1;
+            int ai, t;
+            unit(v, g1, ai, t);
+            const int e = s_act[ai];
+            const int ne = s_ne[ai];
+            const int b = n & 1;
+            if (threadIdx.x == 256) s_misc[5] = mbar_wait(accf + b, (uint32_t)(n >> 1) & 1u, wc, abort_flag) ? 0 : 1;
+            named_bar_sync(2, 128);
+            if (s_misc[5]) break;  // one decision for the group
             tc_fence_after();
-            if (warp < 12) {
-                const int qd = warp - 8;
+            {
+                // the accumulator's first kFusedMaxT columns (the expert's tokens) of this
+                // lane quarter, alpha-scaled, into xq[column][lane]: the loops below run
+                // over the unit's tokens only (short code, run once per unit)
                 uint32_t r[32];
-                tmem_ld32(tmem + ((uint32_t)(qd * 32) << 16), r);
+                tmem_ld32(tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(b * C::BN), r);
                 tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(acce);
-                if (g1) {
-                    // W13 rows interleaved in groups of 32: quarters 0 / 1 hold gate / up
-                    // of features 64 t + [0, 32), quarters 2 / 3 of 64 t + [32, 64)
-                    const float alpha = __fmul_rn(sg, a.w13_global[e]);
-                    const int pair = qd >> 1;
-                    float* xg = sX + pair * 32 * 32;  // [column][lane]
-                    if ((qd & 1) == 0) {
+                if (lane == 0) mbar_arrive(acce + b);
+                const float alpha = g1 ? __fmul_rn(a.is_static ? st.s13[e] : sg_a, s_gw13[e])
+                                       : __fmul_rn(s_sgh[ai], s_gw2[e]);
+                float* xq = sX + qd * kFusedMaxT * 32;
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) xg[c * 32 + lane] = __fmul_rn(alpha, __uint_as_float(r[c]));
+                for (int c = 0; c < kFusedMaxT; ++c) xq[c * 32 + lane] = __fmul_rn(alpha, __uint_as_float(r[c]));
+            }
+            named_bar_sync(2, 128);
+            if (g1) {
+                // W13 rows interleaved in groups of 32: quarters 0 / 1 hold gate / up
+                // of features 64 t + [0, 32), quarters 2 / 3 of 64 t + [32, 64)
+                if (qd & 1) {
+                    const float* xg = sX + (qd - 1) * kFusedMaxT * 32;
+                    const float* xu = sX + qd * kFusedMaxT * 32;
+                    const int f = t * 64 + (qd >> 1) * 32 + lane;
+                    uint32_t amax_bits = 0;
+#pragma unroll 1
+                    for (int c = 0; c < ne; ++c) {
+                        const __nv_bfloat16 hb = __float2bfloat16_rn(__fmul_rn(silu_f32(xg[c * 32 + lane]), xu[c * 32 + lane]));
+                        const uint16_t hbits = *reinterpret_cast<const uint16_t*>(&hb);
+                        a.h[(int64_t)s_eslot[ai * kFusedMaxT + c] * I + f] = hbits;
+                        amax_bits = max(amax_bits, (uint32_t)(hbits & 0x7FFFu));
                     }
-                    named_bar_sync(2, 128);
-                    if (qd & 1) {
-                        const int f = t * 64 + pair * 32 + lane;
-                        uint32_t amax_bits = 0;
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            if (c < ne) {
-                                const float g = xg[c * 32 + lane];
-                                const float u = __fmul_rn(alpha, __uint_as_float(r[c]));
-                                const __nv_bfloat16 hb = __float2bfloat16_rn(__fmul_rn(silu_f32(g), u));
-                                const uint16_t hbits = *reinterpret_cast<const uint16_t*>(&hb);
-                                const int slot = s_eslot[ai * kFusedMaxT + c];
-                                a.h[(int64_t)slot * I + f] = hbits;
-                                amax_bits = max(amax_bits, (uint32_t)(hbits & 0x7FFFu));
-                            }
-                        }
+                    for (int o = 16; o > 0; o >>= 1)
+                        amax_bits = max(amax_bits, __shfl_xor_sync(0xFFFFFFFFu, amax_bits, o));
+                    if (lane == 0 && amax_bits) atomicMax(a.amax_h + ai, amax_bits << 16);
+                }
+                named_bar_sync(2, 128);
+                if (threadIdx.x == 256) {
+                    fence_acq_rel_gpu();
+                    atomicAdd(a.cnt1 + ai, 1u);
+                }
+            } else {
+                const float* xq = sX + qd * kFusedMaxT * 32;
+                const int f = t * 128 + qd * 32 + lane;
+#pragma unroll 1
+                for (int c = 0; c < ne; ++c) a.d[(int64_t)s_eslot[ai * kFusedMaxT + c] * H + f] = xq[c * 32 + lane];
+                named_bar_sync(2, 128);
+                if (threadIdx.x == 256) {
+                    fence_acq_rel_gpu();
+                    const uint32_t old = atomicAdd(a.cnt2 + t, 1u);
+                    s_misc[2] = old + 1u == (uint32_t)E_act ? 1 : 0;
+                }
+                named_bar_sync(2, 128);
+                if (s_misc[2]) {
+                    // the last expert of this output tile: the top-k sum in slot order,
+                    // four tokens' loads in flight at a time
+                    fence_acq_rel_gpu();
+                    const int fo = t * 128 + (threadIdx.x - 256);
+                    for (int tok0 = 0; tok0 < T; tok0 += 4) {
+                        float dv[4][kFusedMaxTopK];
 #pragma unroll
-                        for (int o = 16; o > 0; o >>= 1)
-                            amax_bits = max(amax_bits, __shfl_xor_sync(0xFFFFFFFFu, amax_bits, o));
-                        if (lane == 0 && amax_bits) atomicMax(a.amax_h + ai, amax_bits << 16);
-                    }
-                    named_bar_sync(2, 128);
-                    if (threadIdx.x == 256) {
-                        __threadfence();
-                        atomicAdd(a.cnt1 + ai, 1u);
-                    }
-                } else {
-                    const float alpha = __fmul_rn(sg, a.w2_global[e]);
-                    const int f = t * 128 + qd * 32 + lane;
+                        for (int u = 0; u < 4; ++u)
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        if (c < ne) {
-                            const int slot = s_eslot[ai * kFusedMaxT + c];
-                            a.d[(int64_t)slot * H + f] = __fmul_rn(alpha, __uint_as_float(r[c]));
-                        }
-                    }
-                    named_bar_sync(2, 128);
-                    if (threadIdx.x == 256) {
-                        __threadfence();
-                        const uint32_t old = atomicAdd(a.cnt2 + t, 1u);
-                        vmisc[2] = old + 1u == (uint32_t)E_act ? 1 : 0;
-                    }
-                    named_bar_sync(2, 128);
-                    if (vmisc[2]) {
-                        // the last expert of this output tile: the top-k sum in slot order
-                        __threadfence();
-                        const int fo = t * 128 + (threadIdx.x - 256);
-                        for (int tok = 0; tok < T; ++tok) {
+                            for (int j = 0; j < kFusedMaxTopK; ++j)
+                                dv[u][j] = (tok0 + u < T && j < k) ? __ldcg(a.d + (int64_t)((tok0 + u) * k + j) * H + fo)
+                                                                    : 0.0f;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            if (tok0 + u >= T) break;
                             float y = 0.0f;
-                            for (int j = 0; j < k; ++j)
-                                y = __fadd_rn(y, __fmul_rn(s_w[tok * k + j], __ldcg(a.d + (int64_t)(tok * k + j) * H + fo)));
+#pragma unroll
+                            for (int j = 0; j < kFusedMaxTopK; ++j)
+                                if (j < k) y = __fadd_rn(y, __fmul_rn(s_w[(tok0 + u) * k + j], dv[u][j]));
                             const __nv_bfloat16 yb = __float2bfloat16_rn(y);
-                            a.out[(int64_t)tok * H + fo] = *reinterpret_cast<const uint16_t*>(&yb);
+                            a.out[(int64_t)(tok0 + u) * H + fo] = *reinterpret_cast<const uint16_t*>(&yb);
                         }
                     }
                 }
@@ -609,7 +684,7 @@ static bool weight_map(CUtensorMap* m, const void* codes, int64_t rows, int64_t 
 }
 
 bool moe_fused_supported(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
-    return T >= 1 && T <= kFusedMaxT && k >= 1 && k <= kFusedMaxTopK && E <= kMaxExperts && H % 256 == 0 &&
+    return T >= 1 && T <= kFusedMaxT && k >= 1 && k <= kFusedMaxTopK && E <= kFusedMaxE && H % 256 == 0 &&
            H <= kFusedMaxK && H / 128 <= kFusedMaxOutTiles && I % 256 == 0 && I <= kFusedMaxK;
 }
 

@@ -324,11 +324,12 @@ def _host_scales(a, E):
     return arr
 
 
-MOE_AUTO, MOE_CHAIN = 0, 1
+MOE_AUTO, MOE_CHAIN, MOE_FUSED = 0, 1, 2
 
 
 def set_moe_policy(policy):
-    """Choose the MoE implementation (MOE_AUTO: one launch for a few tokens; MOE_CHAIN)."""
+    """Choose the MoE implementation (MOE_AUTO: one launch for a few tokens;
+    MOE_CHAIN; MOE_FUSED: one launch wherever its shapes apply)."""
     _check(lib().fp4_set_moe_policy(int(policy)))
 
 

@@ -266,8 +266,8 @@ def test_mx_argument_errors(F):
 
 def test_moe_policy_validation(F):
     L = F.lib()
-    for p in (F.MOE_CHAIN, F.MOE_AUTO):
+    for p in (F.MOE_CHAIN, F.MOE_FUSED, F.MOE_AUTO):
         assert L.fp4_set_moe_policy(p) == 0
-    for bad in (-1, 2):
+    for bad in (-1, 3):
         assert L.fp4_set_moe_policy(bad) == F.STATUS_CODE["FP4_ERR_INVALID_ARG"]
         assert "MoE policy" in L.fp4_last_error_message().decode()

@@ -58,10 +58,14 @@ class Fused:
         o = self.off[entry]
         return self.ws[o:o + nbytes].view(dtype).view(shape)
 
-    def run(self, F):
+    def run(self, F, policy=None):
         st = self.static
         kw = {} if st is None else dict(mode=1, static13=st[0], static2=st[1])
-        out = F.moe(self.hid_d, self.log_d, self.mw, self.k, workspace=self.ws, **kw)
+        F.set_moe_policy(F.MOE_FUSED if policy is None else policy)
+        try:
+            out = F.moe(self.hid_d, self.log_d, self.mw, self.k, workspace=self.ws, **kw)
+        finally:
+            F.set_moe_policy(F.MOE_AUTO)
         torch.cuda.synchronize()
         F.device_status()
         return out
@@ -155,11 +159,7 @@ def test_moe_fused_matches_chain(F, O):
     """The one-launch MoE and the launch chain agree within the tolerance."""
     c = Fused(F, O, 12, 32, 4, 512, 256, seed=5, std=0.1)
     y_fused = bf16_to_np(c.run(F))
-    F.set_moe_policy(F.MOE_CHAIN)
-    try:
-        y_chain = bf16_to_np(c.run(F))
-    finally:
-        F.set_moe_policy(F.MOE_AUTO)
+    y_chain = bf16_to_np(c.run(F, F.MOE_CHAIN))
     assert np.linalg.norm(y_fused - y_chain) / np.linalg.norm(y_chain) <= 3e-3
 
 
