@@ -686,8 +686,11 @@ def run_moe(torch, fp4, L, I, dev, peaks):
         out["moe_T%d" % T] = {"us": round(ms * 1e3, 2), "GB/s": round(byt / (ms * 1e-3) / 1e9, 1),
                               "frac_hbm": round(byt / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                               "TFLOP/s": round(fl / (ms * 1e-3) / 1e12, 1), "experts_touched": touched,
-                              "note": "route + permute + quantise + GEMM1/SwiGLU + requant + GEMM2/combine, "
-                                      "CUDA graph"}
+                              "note": ("one launch (route, quantise, GEMM1/SwiGLU, requant, GEMM2, slot-order "
+                                       "combine) after a memset of its counters" if T <= 16 else
+                                       "launch chain: route + permute + quantise + GEMM1/SwiGLU + requant + "
+                                       "GEMM2 + slot-order combine")
+                                      + ", CUDA graph" + (", 8 rotating weight copies" if T == 1 else "")}
         del copies
     return out
 

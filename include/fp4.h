@@ -123,10 +123,10 @@ fp4_status fp4_set_gemm_tile_policy(int policy);
  * fp4_moe_grouped uses.  The one-launch MoE (a memset of its counters, then
  * one cooperative kernel: route, quantise, GEMM1 + SwiGLU, requantise, GEMM2
  * and the top-k sum in slot order) takes 1 <= T <= 16 tokens, top_k <= 8,
- * hidden and inter multiples of 256 and at most 2048; otherwise the launch
- * chain runs.  0 = automatic: the one launch for T <= 8 (where it is the
- * faster), else the chain; 1 = always the chain; 2 = the one launch
- * wherever it applies.  Results agree within the MoE tolerance under all.
+ * n_experts <= 256, hidden and inter multiples of 256 and at most 2048;
+ * otherwise the launch chain runs.  0 = automatic: the one launch wherever
+ * it applies (it is the faster there), else the chain; 1 = always the
+ * chain; 2 = the one launch wherever it applies.  Results agree within the MoE tolerance under all.
  * Process-wide, host-side; FP4_ERR_INVALID_ARG for a value outside 0..2. */
 fp4_status fp4_set_moe_policy(int policy);
 
@@ -250,13 +250,25 @@ fp4_status fp4_quantize_mx(int elem, const void* x_bf16, int64_t rows, int64_t k
 fp4_status fp4_quantize_mxfp8(const void* x_bf16, int64_t rows, int64_t k, void* codes, void* scales, void* stream);
 
 /*
- * MXFP8 linear (E4M3 or E5M2 elements, either on either side):
+ * MXFP6 codes (E2M3 or E3M2, one per byte as fp4_quantize_mx writes them) ->
+ * the E4M3 codes of the same values, [rows, k] bytes; out may equal codes
+ * (in place).  Every E2M3 and E3M2 value is an E4M3 value, so this is exact
+ * and the E8M0 scales stay as they are: an MXFP6 operand widened this way
+ * (weights once at load) goes through the MX GEMM as FP4_MX_E4M3 and the
+ * products are those of the MXFP6 values.  FP4_ERR_INVALID_ARG for an MXFP8
+ * element format.
+ */
+fp4_status fp4_mx_widen(int elem, const void* codes, int64_t rows, int64_t k, void* out, void* stream);
+
+/*
+ * MX linear (MXFP8 operands, E4M3 or E5M2 elements, either on either side):
  * out[m, n] = bf16( sum_k deq(A)[m, k] * deq(W)[n, k] ) with deq = element x
  * 2^(scale byte - 127) per 32-element block, fp32 accumulation on the tensor
  * cores (tcgen05 kind::mxf8f6f4); no global scale.  a_codes [m, k] /
  * w_codes [n, k] and their scales as written by fp4_quantize_mx (a_elem /
- * w_elem name their element formats: FP4_MX_E4M3 or FP4_MX_E5M2; the MXFP6
- * formats give FP4_ERR_INVALID_ARG: their codes are quantiser output only).
+ * w_elem name their element formats: FP4_MX_E4M3 or FP4_MX_E5M2; MXFP6
+ * operands are passed widened by fp4_mx_widen as FP4_MX_E4M3, and an
+ * unwidened MXFP6 format gives FP4_ERR_INVALID_ARG).
  * out_bf16 [m, n] row-major.  k a multiple of 32 (16-byte code rows), n a
  * multiple of 8.  No workspace.
  */
@@ -265,7 +277,9 @@ fp4_status fp4_gemm_mx_prequant(int a_elem, const void* a_codes, const void* a_s
                                 void* stream);
 
 /* The same linear with the bf16 activations x_bf16 [m, k] quantised to a_elem
- * on the device per call (fp4_quantize_mx into the workspace, then the GEMM).
+ * on the device per call (fp4_quantize_mx into the workspace, then the GEMM);
+ * a_elem may be an MXFP6 format here (the codes are widened as they are
+ * written), w_elem is E4M3 or E5M2 (MXFP6 weights widened at load).
  * workspace: fp4_gemm_mx_workspace_size(m, k) bytes, 256-byte aligned. */
 size_t fp4_gemm_mx_workspace_size(int64_t m, int64_t k);
 fp4_status fp4_gemm_mx(int a_elem, const void* x_bf16, int64_t m, int w_elem, const void* w_codes,
@@ -323,10 +337,9 @@ size_t fp4_moe_workspace_size(int64_t tokens, int64_t hidden, int64_t inter, int
  *   5. h requantised to NVFP4 with s_gH[e] = amax_e / 2688 (static:
  *      static_scales2[e]).
  *   6. D = alpha2_e * H_q . W2_e^T (alpha2_e = s_gH[e] * w2_global[e]).
- *   7. out[t] = bf16( sum_j weight[t, j] * D[t, j] ) (fp32 sum; in the
- *      one-launch form (fp4_set_moe_policy) the terms are added in slot order
- *      j = 0..top_k-1 and the result is the same bits on every run; in the
- *      launch chain their order is not fixed).
+ *   7. out[t] = bf16( sum_j weight[t, j] * D[t, j] ): D kept in fp32 (one row
+ *      per routing slot), the top_k terms added in fp32 in slot order
+ *      j = 0..top_k-1, so the result is the same bits on every run.
  * hidden_bf16 [T, H], router_logits fp32 [T, E], out_bf16 [T, H] (device).
  * mode FP4_SCALE_STATIC needs both host arrays static_scales13[E] and
  * static_scales2[E] (each finite and > 0, E <= 256): NULL gives
@@ -352,7 +365,8 @@ fp4_status fp4_moe_grouped(const void* hidden_bf16, const float* router_logits, 
  * row int32 [R] (-1 for padding), 5 A codes [R, H/2], 6 A scales (MMA layout,
  * R rows), 7 s_gA / static scale per expert fp32 [E], 8 h bf16 [R, I],
  * 9 amax of h per expert fp32 [E], 10 s_gH fp32 [E], 11 h codes [R, I/2],
- * 12 h scales (MMA layout), 13 fp32 output accumulator [T, H]; R = offsets
+ * 12 h scales (MMA layout), 13 D = alpha2 x GEMM2, fp32 [T*k, H] in slot order
+ * (t * top_k + j); R = offsets
  * count 14 (the padded row capacity).  Entries 15-21 are written by the
  * one-launch MoE (regions sized only for the shapes it takes), all in slot
  * order t * top_k + j: 15 h bf16 [T*k, I], 16 the requantised h codes

@@ -508,11 +508,11 @@ extern "C" fp4_status fp4_quantize_mxfp8(const void* x, int64_t rows, int64_t k,
 static int mx8_type_code(int elem) { return elem == FP4_MX_E4M3 ? 0 : 1; }
 
 static fp4_status validate_gemm_mx(int a_elem, int64_t m, int w_elem, const void* w_codes, const void* w_scales,
-                                   int64_t n, int64_t k, void* out) {
+                                   int64_t n, int64_t k, void* out, bool fp6_a_ok) {
     TRY(check_mx_elem(a_elem));
     TRY(check_mx_elem(w_elem));
-    CHECK_OR_RETURN(a_elem <= FP4_MX_E5M2 && w_elem <= FP4_MX_E5M2, FP4_ERR_INVALID_ARG,
-                    "the MX GEMM takes MXFP8 operands (E4M3 / E5M2); MXFP6 codes are quantiser output only");
+    CHECK_OR_RETURN((a_elem <= FP4_MX_E5M2 || fp6_a_ok) && w_elem <= FP4_MX_E5M2, FP4_ERR_INVALID_ARG,
+                    "the MX GEMM reads E4M3 / E5M2 codes: widen MXFP6 codes first (fp4_mx_widen)");
     TRY(check_rows(m, "m"));
     TRY(check_rows(n, "n"));
     TRY(check_k(k));
@@ -552,7 +552,7 @@ static fp4_status enqueue_gemm_mx(int a_elem, const uint8_t* ac, const uint8_t* 
 extern "C" fp4_status fp4_gemm_mx_prequant(int a_elem, const void* a_codes, const void* a_scales, int64_t m,
                                            int w_elem, const void* w_codes, const void* w_scales, int64_t n,
                                            int64_t k, void* out, void* stream) {
-    TRY(validate_gemm_mx(a_elem, m, w_elem, w_codes, w_scales, n, k, out));
+    TRY(validate_gemm_mx(a_elem, m, w_elem, w_codes, w_scales, n, k, out, false));
     if (m == 0 || n == 0) return check_arch();
     CHECK_OR_RETURN(a_codes && a_scales, FP4_ERR_INVALID_ARG, "null activation codes or scales");
     CHECK_OR_RETURN(aligned16(a_codes) && aligned16(a_scales), FP4_ERR_ALIGNMENT,
@@ -563,6 +563,21 @@ extern "C" fp4_status fp4_gemm_mx_prequant(int a_elem, const void* a_codes, cons
                            out, false, (cudaStream_t)stream);
 }
 
+extern "C" fp4_status fp4_mx_widen(int elem, const void* codes, int64_t rows, int64_t k, void* out, void* stream) {
+    TRY(check_mx_elem(elem));
+    CHECK_OR_RETURN(elem >= FP4_MX_E2M3, FP4_ERR_INVALID_ARG, "only MXFP6 codes (E2M3 / E3M2) are widened");
+    TRY(check_rows(rows, "rows"));
+    TRY(check_k(k));
+    if (rows == 0) return check_arch();
+    CHECK_OR_RETURN(codes && out, FP4_ERR_INVALID_ARG, "null codes or output pointer");
+    CHECK_OR_RETURN(aligned16(codes) && aligned16(out), FP4_ERR_ALIGNMENT, "codes and output must be 16-byte aligned");
+    TRY(check_arch());
+    const DeviceInfo* d = current_device();
+    return cuda_status(launch_mx6_widen(elem, static_cast<const uint8_t*>(codes), static_cast<uint8_t*>(out), rows * k,
+                                        d->sm_count, (cudaStream_t)stream),
+                       "MX widen launch");
+}
+
 extern "C" size_t fp4_gemm_mx_workspace_size(int64_t m, int64_t k) {
     if (m < 0 || k <= 0) return 0;
     return align256((size_t)m * (size_t)k) + align256(fp4_scales_bytes(FP4_MXFP4, m, k));
@@ -571,7 +586,7 @@ extern "C" size_t fp4_gemm_mx_workspace_size(int64_t m, int64_t k) {
 extern "C" fp4_status fp4_gemm_mx(int a_elem, const void* x, int64_t m, int w_elem, const void* w_codes,
                                   const void* w_scales, int64_t n, int64_t k, void* out, void* ws, size_t wsb,
                                   void* stream) {
-    TRY(validate_gemm_mx(a_elem, m, w_elem, w_codes, w_scales, n, k, out));
+    TRY(validate_gemm_mx(a_elem, m, w_elem, w_codes, w_scales, n, k, out, true));
     if (m == 0 || n == 0) return check_arch();
     CHECK_OR_RETURN(x, FP4_ERR_INVALID_ARG, "null activation pointer");
     CHECK_OR_RETURN(aligned16(x), FP4_ERR_ALIGNMENT, "activations must be 16-byte aligned");
@@ -583,9 +598,12 @@ extern "C" fp4_status fp4_gemm_mx(int a_elem, const void* x, int64_t m, int w_el
     uint8_t* as = ac + align256((size_t)m * (size_t)k);
     const DeviceInfo* d = current_device();
     cudaStream_t s = (cudaStream_t)stream;
-    TRY(cuda_status(launch_mx8_quant(a_elem, static_cast<const uint16_t*>(x), m, k, ac, as, d->sm_count, s),
+    // MXFP6 activations: quantised to the 6-bit format, stored as the E4M3
+    // codes of the same values (exact), and multiplied as E4M3
+    const bool fp6 = a_elem >= FP4_MX_E2M3;
+    TRY(cuda_status(launch_mx8_quant(a_elem, static_cast<const uint16_t*>(x), m, k, ac, as, d->sm_count, s, fp6),
                     "MX quantise launch"));
-    return enqueue_gemm_mx(a_elem, ac, as, m, w_elem, static_cast<const uint8_t*>(w_codes),
+    return enqueue_gemm_mx(fp6 ? FP4_MX_E4M3 : a_elem, ac, as, m, w_elem, static_cast<const uint8_t*>(w_codes),
                            static_cast<const uint8_t*>(w_scales), n, k, out, true, s);
 }
 

@@ -229,6 +229,8 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
         case EPI_COMBINE:
         case EPI_SWIGLU_T:
         case EPI_COMBINE_T:
+        case EPI_DSLOT:
+        case EPI_DSLOT_T:
             return launch_gemm_moe(g, s);
     }
     set_error("no GEMM instantiation for epilogue %d, BN %d", g.epi, g.bn);
@@ -241,6 +243,11 @@ cudaError_t launch_gemm_moe(const GemmLaunch& g, cudaStream_t s) {
     if (g.fmt != FP4_NVFP4) return cudaErrorInvalidValue;
     if (g.epi == EPI_SWIGLU_T && g.bn == 32) return launch_one<32, FK_NV4, EPI_SWIGLU_T>(g, s);
     if (g.epi == EPI_COMBINE_T && g.bn == 32) return launch_one<32, FK_NV4, EPI_COMBINE_T>(g, s);
+    if (g.epi == EPI_DSLOT_T && g.bn == 32) return launch_one<32, FK_NV4, EPI_DSLOT_T>(g, s);
+    if (g.epi == EPI_DSLOT) {
+        if (g.bn == 128) return launch_one<128, FK_NV4, EPI_DSLOT>(g, s);
+        if (g.bn == 64) return launch_one<64, FK_NV4, EPI_DSLOT>(g, s);
+    }
     if (g.epi == EPI_SWIGLU) {
         if (g.bn == 256) return launch_one<256, FK_NV4, EPI_SWIGLU>(g, s);
         if (g.bn == 128) return launch_one<128, FK_NV4, EPI_SWIGLU>(g, s);

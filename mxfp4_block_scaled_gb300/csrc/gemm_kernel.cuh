@@ -80,12 +80,12 @@ constexpr int kSwigluXBytes = 2 * 2 * 32 * 32 * 4;
 
 template <int EPI>
 constexpr bool epi_swapped_grouped() {
-    return EPI == EPI_SWIGLU_T || EPI == EPI_COMBINE_T;
+    return EPI == EPI_SWIGLU_T || EPI == EPI_COMBINE_T || EPI == EPI_DSLOT_T;
 }
 
 template <int EPI>
 constexpr bool epi_grouped() {
-    return EPI == EPI_SWIGLU || EPI == EPI_COMBINE || epi_swapped_grouped<EPI>();
+    return EPI == EPI_SWIGLU || EPI == EPI_COMBINE || EPI == EPI_DSLOT || epi_swapped_grouped<EPI>();
 }
 
 // Grouped GEMMs: a CTA's first kUnitTable units' (expert, end of real token
@@ -610,7 +610,8 @@ __global__ void __launch_bounds__(512, 1)
         constexpr int GRAN = EPI == EPI_SWIGLU ? 64 : epi_swapped_grouped<EPI>() ? 16 : 32;
         constexpr int CPW = BN / 2 > GRAN ? BN / 2 : GRAN;  // columns per warp
         constexpr int NLD = CPW / 32;
-        static_assert(EPI != EPI_COMBINE || CPW <= 64, "fp32 combine keeps its columns in registers");
+        static_assert((EPI != EPI_COMBINE && EPI != EPI_DSLOT) || CPW <= 64,
+                      "fp32 combine keeps its columns in registers");
         const int qd = warp & 3;  // the TMEM lane quarter this warp may access
         const int c_begin = ((warp - 8) >> 2) * CPW;
         const bool has_cols = c_begin < BN;
@@ -634,15 +635,19 @@ __global__ void __launch_bounds__(512, 1)
             if constexpr (epi_swapped_grouped<EPI>()) {
                 const Unit wp = decode_unit<BN, EPI>(g, sc, u, ut);
                 if (wp.empty) continue;
-                if constexpr (EPI == EPI_COMBINE_T) {
+                if constexpr (EPI == EPI_COMBINE_T || EPI == EPI_DSLOT_T) {
 #pragma unroll
                     for (int q = 0; q < NPF; ++q) {
                         const int col = q * 32 + lane;
                         const int64_t row = wp.q_row0 + c_begin + col;
                         if (col < CPW && row < wp.vend) {
                             const int slot = g.row_src[row];
-                            pf_tok[q] = slot / g.top_k;
-                            pf_w[q] = g.slot_weight[slot];
+                            if constexpr (EPI == EPI_COMBINE_T) {
+                                pf_tok[q] = slot / g.top_k;
+                                pf_w[q] = g.slot_weight[slot];
+                            } else {
+                                pf_tok[q] = slot;
+                            }
                         }
                     }
                 }
@@ -826,6 +831,60 @@ __global__ void __launch_bounds__(512, 1)
                                        __fmul_rn(sc, __uint_as_float(r[j][4 * v + 1])),
                                        __fmul_rn(sc, __uint_as_float(r[j][4 * v + 2])),
                                        __fmul_rn(sc, __uint_as_float(r[j][4 * v + 3])));
+                }
+            } else if constexpr (EPI == EPI_DSLOT) {
+                // token rows: this row's routing slot gets alpha * acc (fp32, 16-byte stores)
+                uint32_t r[NLD][32];
+                if (has_cols) {
+#pragma unroll
+                    for (int j = 0; j < NLD; ++j) tmem_ld32(tb + j * 32, r[j]);
+                    tmem_ld_wait();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce + acc);
+                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
+                const int64_t prow = w.p_row0 + qd * 32 + lane;
+                const float alpha = __fmul_rn(g.p_global[w.e], g.q_global[w.e]);
+                if (has_cols && prow < w.vend) {
+                    const int slot = g.row_src[prow];
+                    float4* drow = reinterpret_cast<float4*>(reinterpret_cast<float*>(g.out) + (int64_t)slot * g.ldo +
+                                                             w.qt * BN + c_begin);
+#pragma unroll
+                    for (int j = 0; j < NLD; ++j)
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            drow[j * 8 + v] = make_float4(__fmul_rn(alpha, __uint_as_float(r[j][4 * v])),
+                                                          __fmul_rn(alpha, __uint_as_float(r[j][4 * v + 1])),
+                                                          __fmul_rn(alpha, __uint_as_float(r[j][4 * v + 2])),
+                                                          __fmul_rn(alpha, __uint_as_float(r[j][4 * v + 3])));
+                }
+            } else if constexpr (EPI == EPI_DSLOT_T) {
+                // P rows are the expert's W2 rows (output features), columns the
+                // sub-tile's token rows: d[slot of column][feature] = alpha * acc;
+                // the 32 lanes of a column write 32 consecutive features
+                static_assert(CPW % 16 == 0, "whole 16-column loads");
+                uint32_t r[CPW / 16][16];
+#pragma unroll
+                for (int c = 0; c < CPW / 16; ++c) tmem_ld16(tb + c * 16, r[c]);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce + acc);
+                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
+                const float alpha = __fmul_rn(g.q_global[w.e], g.p_global[w.e]);
+                const int64_t hd = w.qt * 128 + qd * 32 + lane;
+                const int64_t vend = w.vend;
+                const int64_t row0 = w.q_row0 + c_begin;
+                float* d = reinterpret_cast<float*>(g.out) + hd;
+#pragma unroll
+                for (int q = 0; q < NPF; ++q) {
+#pragma unroll
+                    for (int i = 0; i < 32 && q * 32 + i < CPW; ++i) {
+                        const int s_i = __shfl_sync(0xFFFFFFFFu, pf_tok[q], i);
+                        if (row0 + q * 32 + i < vend)
+                            d[(int64_t)s_i * g.ldo] = __fmul_rn(alpha, __uint_as_float(r[(q * 32 + i) / 16][(q * 32 + i) % 16]));
+                    }
                 }
             } else if constexpr (EPI == EPI_SWIGLU_T) {
                 // P rows are the expert's W13 rows, interleaved in groups of 32

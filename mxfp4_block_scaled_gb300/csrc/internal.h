@@ -89,6 +89,10 @@ enum Epi : int {
     // tiles of its tokens), for a few tokens per expert:
     EPI_SWIGLU_T = 6,   // h[q][f] = bf16(SiLU(gate) * up), amax per expert
     EPI_COMBINE_T = 7,  // y[token of q][p] += weight * alpha * acc (fp32 reductions)
+    // grouped GEMM2 outputs per routing slot (token * top_k + j), fp32, summed
+    // in slot order by a separate combine (same bits every run):
+    EPI_DSLOT = 8,      // d[slot of p][q] = alpha * acc    (P = token rows)
+    EPI_DSLOT_T = 9,    // d[slot of q][p] = alpha * acc    (swapped: P = an expert's weight rows)
 };
 
 // GemmLaunch::fmt for the 8-bit-container MX formats (MXFP8 / MXFP6; codes

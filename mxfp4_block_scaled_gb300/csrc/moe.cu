@@ -108,7 +108,7 @@ static MoeLayout moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
     sz[MS_SG_H] = E * 4;
     sz[MS_H_CODES] = L.R * I / 2;
     sz[MS_H_SCALES] = L.R * sf_cols_padded(I, 16);
-    sz[MS_Y] = T * H * 4;
+    sz[MS_Y] = slots * H * 4;  // fp32 expert outputs, one row per routing slot
     sz[MS_BITMAP] = E * L.W * 4;
     sz[MS_WPREFIX] = E * L.W * 4;
     sz[MS_TILE_EXPERT] = (L.R / 128) * 4;
@@ -642,13 +642,28 @@ __global__ void __launch_bounds__(256) moe_dispatch_kernel(const PrepArgs a, con
 }
 
 // fp32 accumulator -> bf16 output
-__global__ void __launch_bounds__(256) moe_finalize_kernel(const float4* __restrict__ y, uint2* __restrict__ out,
-                                                           int64_t n4) {
+// out[t][f] = bf16( sum_{j < k} w[t][j] * d[t k + j][f] ), the top-k terms
+// added in slot order in fp32 (a thread per 4 consecutive features), so the
+// output is the same bits on every run.
+__global__ void __launch_bounds__(256) moe_combine_kernel(const float4* __restrict__ d,
+                                                          const float* __restrict__ w, int64_t T, int k,
+                                                          int64_t h4, uint2* __restrict__ out) {
     pdl_wait();
     pdl_launch_dependents();  // dependents wait for this grid's completion
-    for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n4; i += (int64_t)gridDim.x * 256) {
-        const float4 v = y[i];
-        __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    const int64_t n = T * h4;
+    for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256) {
+        const int64_t t = i / h4, f4 = i - t * h4;
+        const float4* dr = d + (t * k) * h4 + f4;
+        float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+            const float wj = w[t * k + j];
+            const float4 v = dr[(int64_t)j * h4];
+            y.x = __fadd_rn(y.x, __fmul_rn(wj, v.x));
+            y.y = __fadd_rn(y.y, __fmul_rn(wj, v.y));
+            y.z = __fadd_rn(y.z, __fmul_rn(wj, v.z));
+            y.w = __fadd_rn(y.w, __fmul_rn(wj, v.w));
+        }
+        __nv_bfloat162 a = __floats2bfloat162_rn(y.x, y.y), b = __floats2bfloat162_rn(y.z, y.w);
         out[i] = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
     }
 }
@@ -948,12 +963,12 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         pa.static2_out = st2;
         pa.amax_h = amax_h;
         pa.y = y;
-        pa.y_elems = T * H;
+        pa.y_elems = 0;  // nothing to clear: GEMM2 writes every slot's row
         StaticScales sc;
         memset(&sc, 0, sizeof(sc));
         if (is_static)
             for (int64_t e = 0; e < E; ++e) sc.s13[e] = s13[e], sc.s2[e] = s2[e];
-        const int zero_blocks = (int)std::min<int64_t>((T * H / 4 + 1023) / 1024, (int64_t)d->sm_count * 2);
+        const int zero_blocks = 0;
         void* args[] = {(void*)&pa, (void*)&sc};
         const void* fn = per_lane <= 4    ? (const void*)moe_prep_small_kernel<4>
                          : per_lane <= 8  ? (const void*)moe_prep_small_kernel<8>
@@ -981,7 +996,7 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         ra.bitmap = bitmap;
         ra.W = L.W;
         ra.y = y;
-        ra.y_elems = T * H;
+        ra.y_elems = 0;  // nothing to clear: GEMM2 writes every slot's row
         ra.amax_h = amax_h;
         ra.route_blocks = (int)((T + 31) / 32);  // one CTA (32 warps) per 32 tokens = one bitmap word
         ra.has_static = is_static ? 1 : 0;
@@ -992,7 +1007,7 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         memset(&sc, 0, sizeof(sc));
         if (is_static)
             for (int64_t e = 0; e < E; ++e) sc.s13[e] = s13[e], sc.s2[e] = s2[e];
-        int zero_blocks = full ? (int)std::min<int64_t>((T * H / 4 + 1023) / 1024, (int64_t)d->sm_count * 2) : 0;
+        const int zero_blocks = 0;
         void* args[] = {(void*)&ra, (void*)&sc};
         const void* fn = per_lane <= 4    ? (const void*)moe_route_kernel<4>
                          : per_lane <= 8  ? (const void*)moe_route_kernel<8>
@@ -1164,21 +1179,12 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         MOE_CUDA(launch_quant(q, s), "requantise launch");
         pdl = true;
     }
-    // 6. GEMM2 + weighted combine into y, then y -> bf16
+    // 6. GEMM2 into one fp32 row per routing slot, then the top-k sum in slot order -> bf16
     if (mask & ST_GEMM2) {
-        if (!full) {
-            float4* z = reinterpret_cast<float4*>(y);
-            int64_t n4 = T * H / 4;
-            void* zargs[] = {(void*)&z, (void*)&n4};
-            int64_t zb = std::min<int64_t>((n4 + 255) / 256, (int64_t)d->sm_count * 4);
-            MOE_CUDA(launch_k((const void*)zero_kernel, dim3((unsigned)zb), dim3(256), 0, pdl, s, zargs),
-                     "zero launch");
-            pdl = true;
-        }
         GemmLaunch g;
         g.fmt = FP4_NVFP4;
         if (swapped) {
-            g.epi = EPI_COMBINE_T;
+            g.epi = EPI_DSLOT_T;
             g.bn = 32;
             g.p_codes = static_cast<const uint8_t*>(w2c);
             g.p_scales = static_cast<const uint8_t*>(w2s);
@@ -1192,9 +1198,9 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
             g.q_global = is_static ? st2 : sg_h;
             g.q_global_per_expert = true;
         } else {
-            g.epi = EPI_COMBINE;
+            g.epi = EPI_DSLOT;
             // the tile width must divide H (output columns of one token row); the
-            // fp32 combine epilogue keeps at most 64 columns per warp in registers
+            // fp32 epilogue keeps at most 64 columns per warp in registers
             g.bn = (T * k >= 4 * E * 64 && H % 128 == 0) ? 128 : 64;
             g.p_codes = h_codes;
             g.p_scales = h_scales;
@@ -1220,13 +1226,15 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         g.top_k = (int)k;
         g.pdl = pdl;
         MOE_CUDA(launch_gemm(g, s), "GEMM2 launch");
-        const float4* y4 = reinterpret_cast<const float4*>(y);
+        const float4* d4 = reinterpret_cast<const float4*>(y);
+        const float* wv = wts;
         uint2* o2 = reinterpret_cast<uint2*>(out);
-        int64_t n4 = T * H / 4;
-        void* fargs[] = {(void*)&y4, (void*)&o2, (void*)&n4};
-        int64_t fb = std::min<int64_t>((n4 + 255) / 256, (int64_t)d->sm_count * 4);
-        MOE_CUDA(launch_k((const void*)moe_finalize_kernel, dim3((unsigned)fb), dim3(256), 0, true, s, fargs),
-                 "finalise launch");
+        int64_t TT = T, h4 = H / 4;
+        int kk = (int)k;
+        void* fargs[] = {(void*)&d4, (void*)&wv, (void*)&TT, (void*)&kk, (void*)&h4, (void*)&o2};
+        int64_t fb = std::min<int64_t>((T * h4 + 255) / 256, (int64_t)d->sm_count * 8);
+        MOE_CUDA(launch_k((const void*)moe_combine_kernel, dim3((unsigned)fb), dim3(256), 0, true, s, fargs),
+                 "combine launch");
     }
     return FP4_OK;
 }

@@ -21,7 +21,7 @@ struct StaticScales {
 
 // The one-launch MoE for a few tokens (moe_fused.cu).
 constexpr int kFusedMaxT = 16;                        // tokens
-constexpr int kFusedAutoMaxT = 8;                     // tokens up to which fp4_moe_grouped takes it by default
+constexpr int kFusedAutoMaxT = 16;                    // tokens up to which fp4_moe_grouped takes it by default
 constexpr int kFusedMaxTopK = 8;
 constexpr int kFusedMaxSlots = kFusedMaxT * kFusedMaxTopK;
 constexpr int kFusedMaxK = 2048;                      // H and I (the two GEMMs' K)

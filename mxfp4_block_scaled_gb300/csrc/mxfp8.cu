@@ -43,7 +43,44 @@ __device__ __forceinline__ uint32_t cvt_mx_x2(float even, float odd) {
     return r;
 }
 
+// The E4M3 code of the same value as a 6-bit code (E2M3 or E3M2; the low six
+// bits of the byte): every E2M3 and E3M2 value is an E4M3 value (E4M3 has as
+// many or more mantissa bits and a wider exponent range), so the widening is
+// exact.  E2M3 (bias 1): exponent field e > 0 is 2^(e-1) (1 + m/8) -> E4M3
+// field e + 6, mantissa m; e = 0 is m 2^-3 (m = 1: 2^-3; 2-3: 2^-2 (1 + (m-2)/2);
+// 4-7: 2^-1 (1 + (m-4)/4)).  E3M2 (bias 3): e > 0 is 2^(e-3) (1 + m/4) -> field
+// e + 4, mantissa 2m; e = 0 is m 2^-4.  Zero keeps its sign.
 template <int ELEM>
+__device__ __forceinline__ uint32_t fp6_to_e4m3(uint32_t c) {
+    const uint32_t sign = (c & 0x20u) << 2;
+    uint32_t mag;
+    if constexpr (ELEM == MX_ELEM_E2M3) {
+        const uint32_t e = (c >> 3) & 3u, m = c & 7u;
+        if (e) {
+            mag = ((e + 6u) << 3) | m;
+        } else {
+            // subnormal m * 2^-3: exponent of the leading bit, then the rest
+            mag = m == 0u ? 0u : m == 1u ? 0x20u : m < 4u ? (0x28u | ((m & 1u) << 2)) : (0x30u | ((m & 3u) << 1));
+        }
+    } else {
+        const uint32_t e = (c >> 2) & 7u, m = c & 3u;
+        if (e) {
+            mag = ((e + 4u) << 3) | (m << 1);
+        } else {
+            mag = m == 0u ? 0u : m == 1u ? 0x18u : m == 2u ? 0x20u : 0x24u;  // m * 2^-4
+        }
+    }
+    return sign | mag;
+}
+
+// Four 6-bit codes (one per byte) -> four E4M3 codes.
+template <int ELEM>
+__device__ __forceinline__ uint32_t widen4(uint32_t w) {
+    return fp6_to_e4m3<ELEM>(w & 0x3Fu) | (fp6_to_e4m3<ELEM>((w >> 8) & 0x3Fu) << 8) |
+           (fp6_to_e4m3<ELEM>((w >> 16) & 0x3Fu) << 16) | (fp6_to_e4m3<ELEM>((w >> 24) & 0x3Fu) << 24);
+}
+
+template <int ELEM, bool WIDEN>
 __global__ void __launch_bounds__(kMx8Threads) mx8_quant_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                                 int64_t k, int64_t rows_pad, int64_t ksf,
                                                                 uint8_t* __restrict__ codes,
@@ -82,6 +119,7 @@ __global__ void __launch_bounds__(kMx8Threads) mx8_quant_kernel(const uint16_t* 
                     const uint32_t a = xw[2 * q], b = xw[2 * q + 1];
                     w[q] = cvt_mx_x2<ELEM>(__fmul_rn(bf16lo(a), mult), __fmul_rn(bf16hi(a), mult)) |
                            (cvt_mx_x2<ELEM>(__fmul_rn(bf16lo(b), mult), __fmul_rn(bf16hi(b), mult)) << 16);
+                    if constexpr (WIDEN) w[q] = widen4<ELEM>(w[q]);
                 }
                 out[0] = make_uint4(w[0], w[1], w[2], w[3]);
                 out[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -94,8 +132,31 @@ __global__ void __launch_bounds__(kMx8Threads) mx8_quant_kernel(const uint16_t* 
     }
 }
 
+// in may equal out: each thread reads, then writes, its own 16 bytes
+__global__ void __launch_bounds__(kMx8Threads) mx6_widen_kernel(int elem, const uint4* in, uint4* out, int64_t n16) {
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int64_t i = (int64_t)blockIdx.x * kMx8Threads + threadIdx.x; i < n16; i += (int64_t)gridDim.x * kMx8Threads) {
+        const uint4 v = in[i];
+        out[i] = elem == MX_ELEM_E2M3
+                     ? make_uint4(widen4<MX_ELEM_E2M3>(v.x), widen4<MX_ELEM_E2M3>(v.y), widen4<MX_ELEM_E2M3>(v.z),
+                                  widen4<MX_ELEM_E2M3>(v.w))
+                     : make_uint4(widen4<MX_ELEM_E3M2>(v.x), widen4<MX_ELEM_E3M2>(v.y), widen4<MX_ELEM_E3M2>(v.z),
+                                  widen4<MX_ELEM_E3M2>(v.w));
+    }
+}
+
+cudaError_t launch_mx6_widen(int elem, const uint8_t* in, uint8_t* out, int64_t bytes, int sm_count, cudaStream_t s) {
+    const int64_t n16 = bytes / 16;
+    const int64_t want = (n16 + kMx8Threads - 1) / kMx8Threads;
+    const unsigned grid = (unsigned)(want < (int64_t)sm_count * 8 ? (want > 0 ? want : 1) : (int64_t)sm_count * 8);
+    mx6_widen_kernel<<<grid, kMx8Threads, 0, s>>>(elem, reinterpret_cast<const uint4*>(in), reinterpret_cast<uint4*>(out),
+                                                   n16);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_mx8_quant(int elem, const uint16_t* x, int64_t rows, int64_t k, uint8_t* codes, uint8_t* scales,
-                             int sm_count, cudaStream_t s) {
+                             int sm_count, cudaStream_t s, bool widen) {
     const int64_t rows_pad = round_up(rows, 128);
     const int64_t ksf = sf_cols_padded(k, 32);
     const int64_t total = rows_pad * ksf;
@@ -103,16 +164,22 @@ cudaError_t launch_mx8_quant(int elem, const uint16_t* x, int64_t rows, int64_t 
     const unsigned grid = (unsigned)(want < (int64_t)sm_count * 8 ? want : (int64_t)sm_count * 8);
     switch (elem) {
         case MX_ELEM_E4M3:
-            mx8_quant_kernel<MX_ELEM_E4M3><<<grid, kMx8Threads, 0, s>>>(x, rows, k, rows_pad, ksf, codes, scales);
+            mx8_quant_kernel<MX_ELEM_E4M3, false><<<grid, kMx8Threads, 0, s>>>(x, rows, k, rows_pad, ksf, codes, scales);
             break;
         case MX_ELEM_E5M2:
-            mx8_quant_kernel<MX_ELEM_E5M2><<<grid, kMx8Threads, 0, s>>>(x, rows, k, rows_pad, ksf, codes, scales);
+            mx8_quant_kernel<MX_ELEM_E5M2, false><<<grid, kMx8Threads, 0, s>>>(x, rows, k, rows_pad, ksf, codes, scales);
             break;
         case MX_ELEM_E2M3:
-            mx8_quant_kernel<MX_ELEM_E2M3><<<grid, kMx8Threads, 0, s>>>(x, rows, k, rows_pad, ksf, codes, scales);
+            if (widen)
+                mx8_quant_kernel<MX_ELEM_E2M3, true><<<grid, kMx8Threads, 0, s>>>(x, rows, k, rows_pad, ksf, codes, scales);
+            else
+                mx8_quant_kernel<MX_ELEM_E2M3, false><<<grid, kMx8Threads, 0, s>>>(x, rows, k, rows_pad, ksf, codes, scales);
             break;
         case MX_ELEM_E3M2:
-            mx8_quant_kernel<MX_ELEM_E3M2><<<grid, kMx8Threads, 0, s>>>(x, rows, k, rows_pad, ksf, codes, scales);
+            if (widen)
+                mx8_quant_kernel<MX_ELEM_E3M2, true><<<grid, kMx8Threads, 0, s>>>(x, rows, k, rows_pad, ksf, codes, scales);
+            else
+                mx8_quant_kernel<MX_ELEM_E3M2, false><<<grid, kMx8Threads, 0, s>>>(x, rows, k, rows_pad, ksf, codes, scales);
             break;
         default:
             return cudaErrorInvalidValue;

@@ -22,8 +22,14 @@ __host__ __device__ constexpr int mx_elem_emax(int elem) {
 }
 
 // x bf16 [rows][k] -> codes [rows][k], one byte per element, scales E8M0 in
-// the MMA layout.  cudaErrorInvalidValue for an unknown element format.
+// the MMA layout; with `widen` (E2M3 / E3M2 only) each 6-bit code is written
+// as the E4M3 code of the same value.  cudaErrorInvalidValue for an unknown
+// element format.
 cudaError_t launch_mx8_quant(int elem, const uint16_t* x, int64_t rows, int64_t k, uint8_t* codes, uint8_t* scales,
-                             int sm_count, cudaStream_t s);
+                             int sm_count, cudaStream_t s, bool widen = false);
+
+// 6-bit codes (E2M3 / E3M2, one per byte) -> the E4M3 codes of the same
+// values; bytes % 16 == 0, in may equal out.
+cudaError_t launch_mx6_widen(int elem, const uint8_t* in, uint8_t* out, int64_t bytes, int sm_count, cudaStream_t s);
 
 }  // namespace fp4

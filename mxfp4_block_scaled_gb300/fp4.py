@@ -61,6 +61,7 @@ _SIGNATURES = {
     "fp4_quantize_mx": (_INT, [_INT, _P, _I64, _I64, _P, _P, _P]),
     "fp4_gemm_mx_prequant": (_INT, [_INT, _P, _P, _I64, _INT, _P, _P, _I64, _I64, _P, _P]),
     "fp4_gemm_mx_workspace_size": (_SZ, [_I64, _I64]),
+    "fp4_mx_widen": (_INT, [_INT, _P, _I64, _I64, _P, _P]),
     "fp4_gemm_mx": (_INT, [_INT, _P, _I64, _INT, _P, _P, _I64, _I64, _P, _P, _SZ, _P]),
     "fp4_moe_prepack_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "fp4_moe_prepack_weights": (_INT, [_P, _P, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -231,6 +232,14 @@ def quantize_mx(x, elem=MX_E4M3, stream=None):
     scales = torch.empty(L.fp4_scales_bytes(MXFP4, rows, k), dtype=torch.uint8, device=x.device)
     _check(L.fp4_quantize_mx(elem, _ptr(x), rows, k, _ptr(codes), _ptr(scales), _stream(stream)))
     return MXTensor(elem, rows, k, codes, scales)
+
+
+def mx_widen(q, stream=None):
+    """An MXFP6 MXTensor -> the same values as an E4M3 MXTensor (exact; the
+    scales are shared), the form the MX GEMM reads."""
+    codes = torch.empty_like(q.codes)
+    _check(lib().fp4_mx_widen(q.elem, _ptr(q.codes), q.rows, q.k, _ptr(codes), _stream(stream)))
+    return MXTensor(MX_E4M3, q.rows, q.k, codes, q.scales)
 
 
 def gemm_mx_prequant(aq, wq, out=None, stream=None):

@@ -214,7 +214,7 @@ def test_moe_workspace_layout_holds_its_documented_contents(F, T, H, I, E, k):
     assert R % 128 == 0 and R >= slots + min(slots, E) * 127 and R >= 128
     sf = lambda kk: ((kk + 255) // 256) * 16  # NVFP4 scale columns per row, K padded to 256
     need = [slots * 4, slots * 4, (E + 1) * 4, (E + 1) * 4, R * 4, R * H // 2, R * sf(H), E * 4, R * I * 2, E * 4,
-            E * 4, R * I // 2, R * sf(I), T * H * 4]
+            E * 4, R * I // 2, R * sf(I), slots * H * 4]
     assert o[0] == 0
     for i in range(14):
         assert o[i] % 256 == 0
@@ -255,9 +255,17 @@ def test_mx_argument_errors(F):
     assert g(n=250) == c["FP4_ERR_SHAPE"]
     assert g(k=48) == c["FP4_ERR_SHAPE"]
     assert g(ea=9) == c["FP4_ERR_INVALID_ARG"]
-    # MXFP6 codes are quantiser output only: the GEMM refuses them
-    assert g(ea=2) == c["FP4_ERR_INVALID_ARG"] and "MXFP8" in L.fp4_last_error_message().decode()
+    # the GEMM reads E4M3 / E5M2 codes: MXFP6 operands are widened first
+    assert g(ea=2) == c["FP4_ERR_INVALID_ARG"] and "widen" in L.fp4_last_error_message().decode()
     assert g(ew=3) == c["FP4_ERR_INVALID_ARG"]
+    # per call, MXFP6 activations are accepted (widened as they are quantised); weights are not
+    assert L.fp4_gemm_mx(2, A, 16, 3, A, A, 256, 512, A, A, 1 << 30, None) == c["FP4_ERR_INVALID_ARG"]
+    wd = lambda elem=2, codes=A, rows=16, k=512, out=A: L.fp4_mx_widen(elem, codes, rows, k, out, None)
+    assert wd(elem=0) == c["FP4_ERR_INVALID_ARG"]  # only MXFP6 codes are widened
+    assert wd(elem=1) == c["FP4_ERR_INVALID_ARG"]
+    assert wd(k=48) == c["FP4_ERR_SHAPE"]
+    assert wd(codes=0) == c["FP4_ERR_INVALID_ARG"]
+    assert wd(out=A + 8) == c["FP4_ERR_ALIGNMENT"]
     assert g(wc=0) == c["FP4_ERR_INVALID_ARG"]
     assert g(out=A + 4) == c["FP4_ERR_ALIGNMENT"]
     assert L.fp4_gemm_mx(0, A, 16, 0, A, A, 256, 512, A, A, 16, None) == c["FP4_ERR_WORKSPACE"]

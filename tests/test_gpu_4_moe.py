@@ -152,8 +152,15 @@ def _stage_checks(F, O, c):
     c.view(10, torch.float32, (E,)).copy_(torch.from_numpy(r["sgH"]))
     out = c.run(F, mask=16)
     y = bf16_to_np(out)
-    # fp32 combine of k terms in any order: k * 2^-24 of the magnitude on top
+    # fp32 sum of the k terms in slot order: k * 2^-24 of the magnitude on top
     check_close(y, r["y"], r["ymag"], what="y", extra_tau=k * 2.0 ** -23 * r["ymag"])
+    # D, one fp32 row per routing slot (workspace entry 13), within the GEMM tolerance
+    S = T * k
+    D = c.view(13, torch.float32, (S, H)).cpu().numpy().astype(np.float64)[r["order"]]
+    tau_d = 2.0 ** -18 * r["Dmag"] + 2.0 ** -22 * np.abs(r["D"])
+    assert np.all(np.abs(D - r["D"]) <= tau_d + 1e-30), "D"
+    # the combine has a fixed order: the same bits on a second run
+    assert torch.equal(c.run(F, mask=16), out)
 
 
 def _prep_checks(O, c, ref=None, dynamic=True):
@@ -191,6 +198,7 @@ def _end_to_end(F, O, c, max_norm_err=3e-3):
     out = c.run(F)
     y = bf16_to_np(out)
     assert np.isfinite(y).all()
+    assert torch.equal(c.run(F), out), "the output differs between two runs"
     ny = np.linalg.norm(c.ref["y"])
     err = np.linalg.norm(y - c.ref["y"]) / ny
     assert err <= max_norm_err, err

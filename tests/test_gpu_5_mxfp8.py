@@ -4,7 +4,9 @@ Quantisers (E4M3, E5M2, E2M3, E3M2 elements): codes and the whole scale
 buffer (padding included) bit for bit.  MXFP8 GEMM (E4M3 / E5M2 operands,
 tcgen05 kind::mxf8f6f4): every output element, or sampled rows and columns at
 the full prefill size, within the tolerance of tests/util.py (no global
-scale: alpha = 1).  MXFP6 operands are refused by the GEMM."""
+scale: alpha = 1).  MXFP6: the exact widening of every 6-bit code to E4M3,
+and MXFP6 (or mixed) linears through the E4M3 GEMM against the oracle's
+products of the 6-bit values."""
 import numpy as np
 import pytest
 import torch
@@ -139,12 +141,57 @@ def test_mx_gemm_prequant_matches_per_call(F, O):
     assert torch.equal(o1, o2)
 
 
-def test_mx_gemm_rejects_fp6(F, O):
+@pytest.mark.parametrize("elem", [2, 3])
+def test_mx_widen_is_exact(F, O, elem):
+    """Every 6-bit code (both signs) widens to the E4M3 code of the same
+    value, in place and out of place."""
+    codes = np.tile(np.arange(64, dtype=np.uint8), 32).reshape(4, 512)
+    q = F.MXTensor(elem, 4, 512, torch.from_numpy(codes).cuda(), torch.zeros(512, dtype=torch.uint8, device="cuda"))
+    wide = F.mx_widen(q).codes.cpu().numpy()
+    want = X.decode(NAME[elem], codes.astype(np.int64))
+    got = X.decode("e4m3", wide.astype(np.int64))
+    assert np.array_equal(got, want)
+    assert np.array_equal(np.signbit(got), np.signbit(want))  # -0 stays -0
+    F.lib().fp4_mx_widen(elem, q.codes.data_ptr(), 4, 512, q.codes.data_ptr(), None)  # in place
+    torch.cuda.synchronize()
+    assert np.array_equal(q.codes.cpu().numpy(), wide)
+
+
+def mx6_linear(F, a, w, ea, ew):
+    """MXFP6 (or mixed) linear: W quantised to ew and, if MXFP6, widened;
+    activations quantised to ea per call by fp4_gemm_mx."""
+    wq = F.quantize_mx(w.cuda(), ew)
+    if ew >= 2:
+        wq = F.mx_widen(wq)
+    got = bf16_to_np(F.gemm_mx(a.cuda(), wq, ea))
+    torch.cuda.synchronize()
+    F.device_status()
+    ca, sa = X.quantize(NAME[ea], I.u16(a))
+    cw, sw = X.quantize(NAME[ew], I.u16(w))
+    ref, mag = X.gemm(NAME[ea], ca, sa, NAME[ew], cw, sw)
+    return got, ref, mag
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 256, 512), (33, 264, 800), (130, 520, 1056), (300, 1280, 2048)])
+@pytest.mark.parametrize("ea,ew", [(2, 2), (3, 3), (2, 3), (0, 2), (3, 1)])
+def test_mxfp6_gemm_shapes(F, O, m, n, k, ea, ew):
+    """MXFP6 operands through the E4M3 GEMM after the exact widening: the
+    products are those of the MXFP6 values (the oracle computes them from the
+    6-bit codes)."""
+    a = I.randn_bf16((m, k), m + n + 7 * ea)
+    w = I.weights_bf16(n, k, k + 5 + ew)
+    got, ref, mag = mx6_linear(F, a, w, ea, ew)
+    check_close(got, ref, mag)
+
+
+def test_mx_gemm_refuses_unwidened_fp6(F, O):
     x = torch.zeros((4, 64), dtype=torch.bfloat16, device="cuda")
     wq = F.quantize_mx(torch.zeros((8, 64), dtype=torch.bfloat16, device="cuda"), 2)
     with pytest.raises(F.FP4Error) as e:
         F.gemm_mx(x, wq, 0)
     assert e.value.name == "FP4_ERR_INVALID_ARG"
+    with pytest.raises(F.FP4Error):
+        F.gemm_mx_prequant(F.quantize_mx(x, 2), F.mx_widen(wq))
 
 
 def test_mxfp8_prefill_full_size_sampled(F, O):
