@@ -94,9 +94,16 @@ constexpr bool epi_grouped() {
 constexpr int kUnitTable = 64;
 constexpr int kUnitTableBytes = kUnitTable * 8;
 
+// EPI_DSLOT: each epilogue warp turns its 32 rows x 32 columns of fp32 around
+// through 4 KB of shared memory, so that its stores cover whole rows.
+constexpr int kDslotXBytes = 8 * 32 * 32 * 4;
+
 template <int EPI, int FK>
 constexpr int epi_staging_bytes() {
-    return (EPI == EPI_BF16 ? 2 * epi_buffer_bytes<epi_box_cols<FK>()>() : EPI == EPI_SWIGLU_T ? kSwigluXBytes : 0) +
+    return (EPI == EPI_BF16       ? 2 * epi_buffer_bytes<epi_box_cols<FK>()>()
+            : EPI == EPI_SWIGLU_T ? kSwigluXBytes
+            : EPI == EPI_DSLOT    ? kDslotXBytes
+                                  : 0) +
            (epi_grouped<EPI>() ? kUnitTableBytes : 0);
 }
 
@@ -833,7 +840,11 @@ __global__ void __launch_bounds__(512, 1)
                                        __fmul_rn(sc, __uint_as_float(r[j][4 * v + 3])));
                 }
             } else if constexpr (EPI == EPI_DSLOT) {
-                // token rows: this row's routing slot gets alpha * acc (fp32, 16-byte stores)
+                // token rows: each row's routing slot gets alpha * acc (fp32).  The warp
+                // holds 32 rows x 32 columns per chunk; it writes them to its 4 KB of
+                // shared memory (row r's 16-byte piece v at piece v ^ (r % 8): no bank
+                // conflicts either way) and stores them back four rows per instruction,
+                // eight lanes x 16 bytes = one whole 128-byte line of a row each.
                 uint32_t r[NLD][32];
                 if (has_cols) {
 #pragma unroll
@@ -844,20 +855,32 @@ __global__ void __launch_bounds__(512, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce + acc);
                 const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
-                const int64_t prow = w.p_row0 + qd * 32 + lane;
+                const int64_t prow0 = w.p_row0 + qd * 32;
                 const float alpha = __fmul_rn(g.p_global[w.e], g.q_global[w.e]);
-                if (has_cols && prow < w.vend) {
-                    const int slot = g.row_src[prow];
-                    float4* drow = reinterpret_cast<float4*>(reinterpret_cast<float*>(g.out) + (int64_t)slot * g.ldo +
-                                                             w.qt * BN + c_begin);
+                const int slot = prow0 + lane < w.vend ? g.row_src[prow0 + lane] : -1;
+                const uint32_t xs = smem_u32(sStg) + (uint32_t)(warp - 8) * 4096u;
+                float* dbase = reinterpret_cast<float*>(g.out) + w.qt * BN + c_begin;
+                if (has_cols) {
 #pragma unroll
-                    for (int j = 0; j < NLD; ++j)
+                    for (int j = 0; j < NLD; ++j) {
 #pragma unroll
                         for (int v = 0; v < 8; ++v)
-                            drow[j * 8 + v] = make_float4(__fmul_rn(alpha, __uint_as_float(r[j][4 * v])),
-                                                          __fmul_rn(alpha, __uint_as_float(r[j][4 * v + 1])),
-                                                          __fmul_rn(alpha, __uint_as_float(r[j][4 * v + 2])),
-                                                          __fmul_rn(alpha, __uint_as_float(r[j][4 * v + 3])));
+                            sts128(xs + (uint32_t)lane * 128u + ((uint32_t)(v ^ (lane & 7)) << 4),
+                                   __float_as_uint(__fmul_rn(alpha, __uint_as_float(r[j][4 * v]))),
+                                   __float_as_uint(__fmul_rn(alpha, __uint_as_float(r[j][4 * v + 1]))),
+                                   __float_as_uint(__fmul_rn(alpha, __uint_as_float(r[j][4 * v + 2]))),
+                                   __float_as_uint(__fmul_rn(alpha, __uint_as_float(r[j][4 * v + 3]))));
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int row = i * 4 + (lane >> 3), c4 = lane & 7;
+                            const int srow = __shfl_sync(0xFFFFFFFFu, slot, row);
+                            const uint4 v4 = lds128(xs + (uint32_t)row * 128u + ((uint32_t)(c4 ^ (row & 7)) << 4));
+                            if (srow >= 0)
+                                *reinterpret_cast<uint4*>(dbase + (int64_t)srow * g.ldo + j * 32 + c4 * 4) = v4;
+                        }
+                        __syncwarp();
+                    }
                 }
             } else if constexpr (EPI == EPI_DSLOT_T) {
                 // P rows are the expert's W2 rows (output features), columns the
