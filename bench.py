@@ -53,7 +53,7 @@ def parse():
                    help="only the layer calls (warmup + steps), for ncu captures")
     p.add_argument("--workload", default="prefill",
                    choices=["prefill", "quant", "decode1", "decode8", "decode32", "w4a16_1", "w4a16_4", "mxfp4",
-                            "moe1", "moe64", "moe4096"],
+                            "mxfp8", "moe1", "moe64", "moe4096"],
                    help="workload run by --profile")
     return p.parse_args()
 
@@ -404,6 +404,12 @@ def run_profile_other(args, torch, fp4, L, I, dev):
         wq = fp4.prepack_weight(I.weights_bf16(2048, 7168, 104).to(dev), fp4.MXFP4)
         a = I.randn_bf16((2048, 7168), 4).to(dev)
         fn = lambda: fp4.gemm(a, wq)
+    elif wl == "mxfp8":
+        # the MXFP8 (E4M3) linear at the prefill shape, GEMM on pre-quantised operands
+        wq = fp4.quantize_mx(I.weights_bf16(N, K, 102).to(dev), fp4.MX_E4M3)
+        aq = fp4.quantize_mx(I.randn_bf16((M, K), 2).to(dev), fp4.MX_E4M3)
+        o = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        fn = lambda: fp4.gemm_mx_prequant(aq, wq, out=o)
     else:
         T = int(wl[3:])
         mw = fp4.moe_prepack(I.expert_weights_bf16(MOE_E, 2 * MOE_I, MOE_H, 103).to(dev),
