@@ -178,9 +178,15 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
     return r;
 }
 
-// Arrive on an mbarrier given by its shared::cluster address (any CTA of the cluster).
+// Arrive on an mbarrier given by its shared::cluster address (any CTA of the
+// cluster), with the default release semantics at CTA scope.  A release at
+// cluster scope makes every arrive wait for a cluster-wide memory fence (in
+// the CTA-pair GEMM that fence, once per K block in each scale writer, paced
+// the whole pipeline); the arrivals here only order Tensor Memory stores that
+// tcgen05.wait::st has already completed and shared-memory reads of the
+// arriving CTA, which need no cluster-wide visibility of generic memory.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {

@@ -59,42 +59,58 @@ bool moe_fused_supported(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k);
 // One memset (the counters) and one cooperative kernel launch.
 cudaError_t launch_moe_fused(const FusedMoeLaunch& L, const StaticScales& st, cudaStream_t s);
 
+// Order-preserving 32-bit key of a logit: a larger float has a larger key.
+// -0 ranks with +0 (the two compare equal), and a NaN ranks below every
+// number (a stable descending sort of the logits puts it last); key 0 is
+// left for "no candidate".
+__device__ __forceinline__ uint32_t route_key(float x) {
+    uint32_t b = __float_as_uint(x);
+    if (b == 0x80000000u) b = 0u;
+    if ((b & 0x7FFFFFFFu) > 0x7F800000u) return 1u;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// The logit of a key (route_key's inverse on numbers).
+__device__ __forceinline__ float route_val(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
 // Warp-cooperative top-k over one token's logits, lane l holding logits
-// l, 32 + l, 64 + l, ... in v (-inf past E); ties go to the lower expert
+// l, 32 + l, 64 + l, ... in v (ignored past E); ties go to the lower expert
 // index.  Lane j < k returns the j-th selection and its weight
-// exp(l_j - l_max) / sum over the selection.
+// exp(l_j - l_max) / sum over the selection.  Each round takes the largest
+// key with one warp max-reduction and, among the lanes holding it, the
+// lowest expert index with one min-reduction (a lane's own candidate is
+// its first register with its largest key, so its lowest index).
 template <int PER_LANE>
 __device__ __forceinline__ void topk_regs(const float (&v)[PER_LANE], int E, int k, int lane, int& my_e,
                                           float& my_w) {
-    uint32_t taken = 0;
+    uint32_t key[PER_LANE];
+#pragma unroll
+    for (int q = 0; q < PER_LANE; ++q) key[q] = q * 32 + lane < E ? route_key(v[q]) : 0u;
     float v0 = 0.0f, sum = 0.0f, mine = 0.0f;
     my_e = 0;
     for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int be = 0x7FFFFFFF;
+        uint32_t bk = key[0], bq = 0;
 #pragma unroll
-        for (int q = 0; q < PER_LANE; ++q) {
-            const int e = q * 32 + lane;
-            if (e < E && !((taken >> q) & 1u) && (v[q] > bv || be == 0x7FFFFFFF)) {
-                bv = v[q];
-                be = e;
+        for (int q = 1; q < PER_LANE; ++q)
+            if (key[q] > bk) {
+                bk = key[q];
+                bq = (uint32_t)q;
             }
-        }
+        const uint32_t mk = __reduce_max_sync(0xFFFFFFFFu, bk);
+        const uint32_t be = __reduce_min_sync(0xFFFFFFFFu, bk == mk ? bq * 32u + (uint32_t)lane : 0xFFFFFFFFu);
+        if ((be & 31u) == (uint32_t)lane) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-            const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
-            if (ov > bv || (ov == bv && oe < be)) {
-                bv = ov;
-                be = oe;
-            }
+            for (int q = 0; q < PER_LANE; ++q)
+                if ((uint32_t)q == (be >> 5)) key[q] = 0u;
         }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        const float bv = route_val(mk);
         if (j == 0) v0 = bv;
         const float ex = expf(bv - v0);
         sum += ex;
         if (lane == j) {
-            my_e = be;
+            my_e = (int)be;
             mine = ex;
         }
     }
