@@ -98,11 +98,17 @@ constexpr int kUnitTableBytes = kUnitTable * 8;
 // through 4 KB of shared memory, so that its stores cover whole rows.
 constexpr int kDslotXBytes = 8 * 32 * 32 * 4;
 
+// EPI_SWIGLU: each epilogue warp turns its 32 rows x 32 h columns (bf16)
+// around through 2 KB of shared memory, so that its stores cover whole
+// 64-byte row pieces.
+constexpr int kSwigluStgBytes = 8 * 32 * 32 * 2;
+
 template <int EPI, int FK>
 constexpr int epi_staging_bytes() {
     return (EPI == EPI_BF16       ? 2 * epi_buffer_bytes<epi_box_cols<FK>()>()
             : EPI == EPI_SWIGLU_T ? kSwigluXBytes
             : EPI == EPI_DSLOT    ? kDslotXBytes
+            : EPI == EPI_SWIGLU   ? kSwigluStgBytes
                                   : 0) +
            (epi_grouped<EPI>() ? kUnitTableBytes : 0);
 }
@@ -787,22 +793,37 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce + acc);
-                const bool valid = has_cols && prow < w.vend;
-                if (valid) {
-                    uint16_t* hrow = reinterpret_cast<uint16_t*>(g.out) + prow * g.ldo;
+                // the amax of the row's h values (bf16 bits, sign cleared)
+                if (has_cols && prow < w.vend) {
 #pragma unroll
-                    for (int j = 0; j < NLD; j += 2) {
-                        const int64_t f0 = (w.qt * BN + c_begin + j * 32) / 2;
-                        uint4* o4 = reinterpret_cast<uint4*>(hrow + f0);
+                    for (int jp = 0; jp < NLD / 2; ++jp)
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            o4[v] = make_uint4(hv[j / 2][4 * v], hv[j / 2][4 * v + 1], hv[j / 2][4 * v + 2],
-                                               hv[j / 2][4 * v + 3]);
-                            amax_bits = __vmaxu2(amax_bits, hv[j / 2][4 * v] & 0x7FFF7FFFu);
-                            amax_bits = __vmaxu2(amax_bits, hv[j / 2][4 * v + 1] & 0x7FFF7FFFu);
-                            amax_bits = __vmaxu2(amax_bits, hv[j / 2][4 * v + 2] & 0x7FFF7FFFu);
-                            amax_bits = __vmaxu2(amax_bits, hv[j / 2][4 * v + 3] & 0x7FFF7FFFu);
+                        for (int i = 0; i < 16; ++i) amax_bits = __vmaxu2(amax_bits, hv[jp][i] & 0x7FFF7FFFu);
+                }
+                // rows through shared memory: lane i writes row i's 64 bytes (16-byte
+                // piece v at v ^ ((i / 2) % 4): the eight lanes of a store phase hit
+                // distinct banks), then each store instruction covers 8 rows x 64
+                // contiguous bytes
+                if (has_cols) {
+                    const uint32_t xs = smem_u32(sStg) + (uint32_t)(warp - 8) * 2048u;
+                    const int64_t prow0 = w.p_row0 + qd * 32;
+                    uint16_t* hbase = reinterpret_cast<uint16_t*>(g.out);
+#pragma unroll
+                    for (int jp = 0; jp < NLD / 2; ++jp) {
+                        const int64_t f0 = (w.qt * BN + c_begin + jp * 64) / 2;  // first h column of the pair
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            sts128(xs + (uint32_t)lane * 64u + ((uint32_t)(v ^ ((lane >> 1) & 3)) << 4), hv[jp][4 * v],
+                                   hv[jp][4 * v + 1], hv[jp][4 * v + 2], hv[jp][4 * v + 3]);
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int row = i * 8 + (lane >> 2), c4 = lane & 3;
+                            const uint4 v4 = lds128(xs + (uint32_t)row * 64u + ((uint32_t)(c4 ^ ((row >> 1) & 3)) << 4));
+                            if (prow0 + row < w.vend)
+                                *reinterpret_cast<uint4*>(hbase + (prow0 + row) * g.ldo + f0 + c4 * 8) = v4;
                         }
+                        __syncwarp();
                     }
                 }
                 if (has_cols) {

@@ -6,22 +6,24 @@
 // expert computation of section 4.3 (two GEMMs, SwiGLU, top-k weighted
 // reduction).  Launch chain on one stream, no host synchronisation:
 //   1 route     top-k per token (a warp per token, 32 tokens per CTA),
-//               renormalised weights, expert bitmap; zeroes the fp32 output
-//               accumulator and the h amax
+//               renormalised weights, expert bitmap; zeroes the h amax
 //   2 scan      (one CTA) expert counts, padded offsets (128-row tiles per
 //               expert), tile -> expert map; then (a thread per assignment)
-//               the row -> (token, slot) map
+//               the row -> (token, slot) and slot -> row maps
 //   3 amax      hidden amax partials (dynamic scale)
-//   4 quantise  dynamic scale: the T hidden rows once (token order), then a
-//               permute copies each assignment's codes and scale bytes into
-//               the expert-sorted padded rows; static (per-expert) scales:
-//               the rows straight into that order (the codes depend on e)
+//   4 dispatch  dynamic scale: each token row quantised once into the rows
+//               of its k slots (expert-sorted, padded), padding rows' scale
+//               bytes zeroed; static (per-expert) scales: the rows straight
+//               into that order under their expert's scale
 //   5 GEMM1     grouped tcgen05 GEMM against the interleaved W13, epilogue
 //               h = bf16(SiLU(gate) * up) and the per-expert amax of h
 //   6 requant   h -> NVFP4 with s_gH[e] = amax_e / 2688
-//   7 GEMM2     grouped tcgen05 GEMM against W2, epilogue
-//               y[token] += weight * alpha2 * D (fp32 reductions)
-//   8 finalise  y -> bf16
+//   7 GEMM2     grouped tcgen05 GEMM against W2, epilogue D[slot] =
+//               alpha2 * acc (fp32, one row per routing slot)
+//   8 combine   y[t] = bf16(sum over j in slot order of w[t][j] D[t k + j])
+// A few tokens (T <= 64) take a one-CTA preparation (route, counts, tables)
+// and the swapped grouped GEMMs instead of steps 1-4; at most 16 tokens go to
+// the one-launch kernel of moe_fused.cu by default.
 #include <math.h>
 #include <string.h>
 
@@ -63,9 +65,7 @@ enum MoeSlot : int {
     MS_PARTIALS,
     MS_STATIC13,
     MS_STATIC2,
-    MS_TOK_CODES,   // dynamic scale: the hidden rows quantised once, token order
-    MS_TOK_SCALES,
-    MS_SLOT_ROW,    // small-T preparation: the expert-sorted row of each slot
+    MS_SLOT_ROW,    // the expert-sorted row of each slot
     // the one-launch MoE (moe_fused.cu), sized only when its shapes apply
     MS_F_ZERO,      // counters and h amax, cleared per call
     MS_F_H,         // bf16 [T k][I], slot order
@@ -118,8 +118,6 @@ static MoeLayout moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
     sz[MS_PARTIALS] = 4096;
     sz[MS_STATIC13] = E * 4;
     sz[MS_STATIC2] = E * 4;
-    sz[MS_TOK_CODES] = T * H / 2;
-    sz[MS_TOK_SCALES] = round_up(T, 128) * sf_cols_padded(H, 16);
     sz[MS_SLOT_ROW] = slots * 4;
     const bool fused = moe_fused_supported(T, H, I, E, k);
     sz[MS_F_ZERO] = fused ? kFusedZeroedBytes : 0;
@@ -216,6 +214,7 @@ struct ScanArgs {
     int32_t* row_valid_end;  // [R/128]
     int32_t* row_src;        // [R]
     int32_t* row_tok;        // [R]
+    int32_t* slot_row;       // [T*k] the row of each routing slot
 };
 
 // Exclusive scan of v over the 1024 threads of the block (v = 0 past the data);
@@ -260,41 +259,50 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(const ScanArgs a) {
     pdl_launch_dependents();
     if (threadIdx.x == 0) cmax = 0;  // dependents wait for this grid's completion
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // a warp takes experts warp, warp + 32, ...; their 32-word chunks are
-    // walked in order with eight chunks' loads in flight (a chunk's word
-    // prefix needs only the running total of its expert)
+    // a warp takes experts warp, warp + 32, ...; their 128-word chunks (four
+    // consecutive words a lane) are walked in order with four chunks' loads in
+    // flight (a chunk's word prefix needs only the running total of its expert)
     {
-        const int nch = (int)((a.W + 31) / 32);
+        const int nch = (int)((a.W + 127) / 128);
         const int ne = warp < a.E ? (a.E - warp + 31) / 32 : 0;
         const int nit = ne * nch;
         int32_t base = 0;
-        for (int it0 = 0; it0 < nit; it0 += 8) {
-            uint32_t wv[8];
+        for (int it0 = 0; it0 < nit; it0 += 4) {
+            uint32_t wv[4][4];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < 4; ++u) {
                 const int it = it0 + u;
-                wv[u] = 0u;
-                if (it < nit) {
-                    const int e = warp + 32 * (it / nch), ch = it % nch;
-                    const int64_t w = (int64_t)ch * 32 + lane;
-                    if (w < a.W) wv[u] = a.bitmap[e * a.W + w];
-                }
+                const int e = warp + 32 * (it / nch), ch = it % nch;
+                const int64_t w0 = (int64_t)ch * 128 + lane * 4;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    wv[u][i] = it < nit && w0 + i < a.W ? a.bitmap[(int64_t)e * a.W + w0 + i] : 0u;
             }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < 4; ++u) {
                 const int it = it0 + u;
                 if (it >= nit) break;  // warp-uniform
                 const int e = warp + 32 * (it / nch), ch = it % nch;
                 if (ch == 0) base = 0;
-                const int64_t w = (int64_t)ch * 32 + lane;
-                const int32_t c = __popc(wv[u]);
-                int32_t incl = c;
+                const int64_t w0 = (int64_t)ch * 128 + lane * 4;
+                int32_t c[4], lsum = 0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    c[i] = __popc(wv[u][i]);
+                    lsum += c[i];
+                }
+                int32_t incl = lsum;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
                     const int32_t n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
                     if (lane >= o) incl += n;
                 }
-                if (w < a.W) a.wprefix[e * a.W + w] = base + incl - c;
+                int32_t pre = base + incl - lsum;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (w0 + i < a.W) a.wprefix[(int64_t)e * a.W + w0 + i] = pre;
+                    pre += c[i];
+                }
                 base += __shfl_sync(0xFFFFFFFFu, incl, 31);
                 if (ch == nch - 1 && lane == 0) cnt[e] = base;
             }
@@ -350,48 +358,7 @@ __global__ void __launch_bounds__(256) moe_assign_kernel(const ScanArgs a) {
         const int64_t row = a.padded[e] + a.wprefix[e * a.W + w] + __popc(below);
         a.row_src[row] = (int32_t)s;
         a.row_tok[row] = (int32_t)t;
-    }
-}
-
-// Dispatch of the quantised hidden rows: destination row r (expert-sorted,
-// padded) <- token row_tok[r]: its codes and its scale bytes (four adjacent
-// columns are adjacent bytes in the MMA layout of both buffers); padding rows
-// get zero scales.  A warp takes four rows at a time, so four rows' loads are
-// in flight per lane, with no per-element index division.
-__global__ void __launch_bounds__(256) moe_permute_kernel(const uint8_t* __restrict__ tok_codes,
-                                                          const uint8_t* __restrict__ tok_scales,
-                                                          const int32_t* __restrict__ row_tok,
-                                                          const int32_t* __restrict__ rows_dev, int64_t H,
-                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
-    pdl_wait();
-    pdl_launch_dependents();  // consumers wait for this grid's completion
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t rows = *rows_dev;
-    const int64_t cb16 = H / 32;                 // 16-byte pieces of codes per row
-    const int64_t ncol = sf_cols_padded(H, 16);  // scale columns per row (padding included)
-    const int64_t nw = ncol / 4;                 // 4-byte scale words per row
-    for (int64_t r0 = ((int64_t)blockIdx.x * 8 + warp) * 4; r0 < rows; r0 += (int64_t)gridDim.x * 32) {
-        int64_t t[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) t[q] = r0 + q < rows ? row_tok[r0 + q] : -2;  // -2: past the rows
-        for (int64_t p = lane; p < cb16; p += 32) {
-            uint4 v[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (t[q] >= 0) v[q] = reinterpret_cast<const uint4*>(tok_codes + t[q] * (H / 2))[p];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (t[q] >= 0) reinterpret_cast<uint4*>(codes + (r0 + q) * (H / 2))[p] = v[q];
-        }
-        for (int64_t w = lane; w < nw; w += 32) {
-            uint32_t sv[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                sv[q] = t[q] >= 0 ? *reinterpret_cast<const uint32_t*>(tok_scales + sf_offset(t[q], 4 * w, ncol)) : 0u;
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (t[q] != -2) *reinterpret_cast<uint32_t*>(scales + sf_offset(r0 + q, 4 * w, ncol)) = sv[q];
-        }
+        a.slot_row[s] = (int32_t)row;
     }
 }
 
@@ -438,6 +405,10 @@ struct PrepArgs {
     float* amax_h;          // zeroed [E]
     float* y;               // zeroed [T*H] fp32 by CTAs 1..
     int64_t y_elems;
+    float* amax_part;       // [n_amax_ctas] abs-max of a slice of the hidden rows (CTAs 1..)
+    int n_amax_ctas;        // dynamic scale, dispatch in moe_dispatch_kernel: CTAs 1.. take the abs-max
+    int mark_pad_rows;      // moe_dispatch_kernel: row_src / row_tok = -1 on the tiles' padding rows
+    int zero_pad_scales;    // moe_dispatch_kernel: zero scale bytes on the tiles' padding rows
 };
 
 // One 16-element block (token t, block column b) of the hidden rows:
@@ -481,10 +452,31 @@ __global__ void __launch_bounds__(1024) moe_prep_small_kernel(const PrepArgs a, 
     pdl_wait();
     pdl_launch_dependents();  // dependents wait for this grid's completion
     if (blockIdx.x > 0) {
-        const int64_t nb = (int64_t)gridDim.x - 1;
-        float4* y4 = reinterpret_cast<float4*>(a.y);
-        for (int64_t i = ((int64_t)blockIdx.x - 1) * 1024 + threadIdx.x; i < a.y_elems / 4; i += nb * 1024)
-            y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (a.n_amax_ctas > 0) {
+            // the abs-max of one slice of the hidden rows (the dispatch reduces the slices)
+            const int64_t nv = a.T * a.H / 8;
+            const int64_t per = (nv + a.n_amax_ctas - 1) / a.n_amax_ctas;
+            const int64_t b0 = ((int64_t)blockIdx.x - 1) * per;
+            const int64_t b1 = b0 + per < nv ? b0 + per : nv;
+            const uint4* xv = reinterpret_cast<const uint4*>(a.hidden);
+            uint32_t m = 0;
+            for (int64_t i = b0 + threadIdx.x; i < b1; i += 2 * 1024) {
+                const uint4 v0 = __ldg(xv + i);
+                const uint4 v1 = i + 1024 < b1 ? __ldg(xv + i + 1024) : make_uint4(0u, 0u, 0u, 0u);
+                m = absmax8(v1, absmax8(v0, m));
+            }
+            m = max(m & 0xFFFFu, m >> 16);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+            if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+            __syncthreads();
+            if (threadIdx.x < 32) {
+                uint32_t v = red[threadIdx.x];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+                if (threadIdx.x == 0) a.amax_part[blockIdx.x - 1] = __uint_as_float(v << 16);
+            }
+        }
         return;
     }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -501,16 +493,39 @@ __global__ void __launch_bounds__(1024) moe_prep_small_kernel(const PrepArgs a, 
     if (tid == 0) cmax = 0;
     __syncthreads();
 
-    // 1. route: a warp per token
-    for (int t = warp; t < T; t += 32) {
-        int e;
-        float w;
-        topk_token<PER_LANE>(a.logits + (int64_t)t * E, E, k, lane, e, w);
-        if (lane < k) {
-            a.ids[t * k + lane] = e;
-            a.weights[t * k + lane] = w;
-            s_ids[t * k + lane] = e;
-            atomicOr(reinterpret_cast<unsigned long long*>(&tokmask[e]), 1ull << t);
+    // 1. route: a warp per token (both of a warp's tokens' logits loaded first
+    // when they fit the registers)
+    {
+        constexpr int RT = kPrepMaxTokens / 32;     // tokens per warp at most
+        constexpr bool PRE = PER_LANE <= 8;         // all of them loaded first
+        float lg[PRE ? RT : 1][PER_LANE];
+        if constexpr (PRE) {
+#pragma unroll
+            for (int i = 0; i < RT; ++i) {
+                const int t = warp + 32 * i;
+#pragma unroll
+                for (int q = 0; q < PER_LANE; ++q) {
+                    const int e = q * 32 + lane;
+                    lg[i][q] = t < T && e < E ? __ldg(a.logits + (int64_t)t * E + e) : -INFINITY;
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < RT; ++i) {
+            const int t = warp + 32 * i;
+            if (t >= T) break;
+            int e;
+            float w;
+            if constexpr (PRE)
+                topk_regs<PER_LANE>(lg[i], E, k, lane, e, w);
+            else
+                topk_token<PER_LANE>(a.logits + (int64_t)t * E, E, k, lane, e, w);
+            if (lane < k) {
+                a.ids[t * k + lane] = e;
+                a.weights[t * k + lane] = w;
+                s_ids[t * k + lane] = e;
+                atomicOr(reinterpret_cast<unsigned long long*>(&tokmask[e]), 1ull << t);
+            }
         }
     }
     __syncthreads();
@@ -537,7 +552,9 @@ __global__ void __launch_bounds__(1024) moe_prep_small_kernel(const PrepArgs a, 
     __syncthreads();
     if (tid == 0) a.n_ptiles[1] = min(4, (cmax + 31) / 32);
 
-    // 3. row tables: tiles, padding rows, and each slot's row (token order)
+    // 3. row tables: tiles, padding rows (here only when the dispatch is
+    // inline: moe_dispatch_kernel marks them across the GPU), and each slot's
+    // row (token order)
     for (int e = warp; e < E; e += 32) {
         const int32_t c = __popcll(tokmask[e]);
         const int32_t t0 = padv[e] / 128, t1 = padv[e + 1] / 128;
@@ -545,10 +562,11 @@ __global__ void __launch_bounds__(1024) moe_prep_small_kernel(const PrepArgs a, 
             a.tile_expert[t] = e;
             a.row_valid_end[t] = padv[e] + c;
         }
-        for (int32_t r = padv[e] + c + lane; r < padv[e + 1]; r += 32) {
-            a.row_src[r] = -1;
-            a.row_tok[r] = -1;
-        }
+        if (a.dispatch_inline)
+            for (int32_t r = padv[e] + c + lane; r < padv[e + 1]; r += 32) {
+                a.row_src[r] = -1;
+                a.row_tok[r] = -1;
+            }
     }
     for (int s = tid; s < T * k; s += 1024) {
         const int t = s / k, e = s_ids[s];
@@ -559,9 +577,10 @@ __global__ void __launch_bounds__(1024) moe_prep_small_kernel(const PrepArgs a, 
         if (!a.dispatch_inline) a.slot_row[s] = row;
     }
 
-    // 4. dynamic: s_gA from the abs-max of the T hidden rows
+    // 4. dynamic: s_gA from the abs-max of the T hidden rows (unless CTAs 1..
+    // take it in slices)
     const int64_t H = a.H;
-    if (!a.has_static) {
+    if (!a.has_static && a.n_amax_ctas == 0) {
         const uint4* xv = reinterpret_cast<const uint4*>(a.hidden);
         uint32_t m = 0;
         const int64_t nv = (int64_t)T * H / 8;
@@ -615,14 +634,43 @@ __global__ void __launch_bounds__(1024) moe_prep_small_kernel(const PrepArgs a, 
 // the preparing kernel.
 __global__ void __launch_bounds__(256) moe_dispatch_kernel(const PrepArgs a, const StaticScales st) {
     __shared__ float2 dtab[128];
+    __shared__ float sh_sg;
     pdl_wait();
     pdl_launch_dependents();  // dependents wait for this grid's completion
     const int64_t H = a.H;
     const int nbp = (int)sf_cols_padded(H, 16);
     const int kblocks = (int)(H / 16);
     const int T = (int)a.T, k = a.k;
+    // padding rows of the expert tiles (rows past each tile's real rows)
+    if (a.mark_pad_rows || a.zero_pad_scales) {
+        const int64_t n = (int64_t)a.n_ptiles[0] * 128;
+        for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256)
+            if (i >= a.row_valid_end[i >> 7]) {
+                if (a.mark_pad_rows) {
+                    a.row_src[i] = -1;
+                    a.row_tok[i] = -1;
+                }
+                if (a.zero_pad_scales)
+                    for (int c = 0; c < nbp; c += 4)
+                        *reinterpret_cast<uint32_t*>(a.scales + sf_offset(i, c, nbp)) = 0u;
+            }
+    }
     if (!a.has_static) {
-        const float sg = a.sg_out[0];
+        // s_gA = max over the slices' abs-maxima / 2688
+        uint32_t m = 0;
+        for (int i = threadIdx.x; i < a.n_amax_ctas; i += 256) m = max(m, __float_as_uint(a.amax_part[i]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        __shared__ uint32_t red[8];
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int w = 1; w < 8; ++w) m = max(m, red[w]);
+            sh_sg = a.n_amax_ctas > 0 ? __fdiv_rn(__uint_as_float(m), 2688.0f) : a.sg_out[0];
+            if (blockIdx.x == 0 && a.n_amax_ctas > 0) a.sg_out[0] = sh_sg;
+        }
+        __syncthreads();
+        const float sg = sh_sg;
         if (threadIdx.x < 128) dtab[threadIdx.x] = nvfp4_divisor(threadIdx.x, sg, false);
         __syncthreads();
         const float p = __fmul_rn(sg, 6.0f);
@@ -888,8 +936,6 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
     float* partials = (float*)at(MS_PARTIALS);
     float* st13 = (float*)at(MS_STATIC13);
     float* st2 = (float*)at(MS_STATIC2);
-    uint8_t* tok_codes = at(MS_TOK_CODES);
-    uint8_t* tok_scales = at(MS_TOK_SCALES);
     const bool is_static = mode == FP4_SCALE_STATIC;
     const bool full = (mask & ST_ALL) == ST_ALL;
     // A few tokens per expert (at most 16 on average): the grouped GEMMs swap
@@ -964,11 +1010,18 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         pa.amax_h = amax_h;
         pa.y = y;
         pa.y_elems = 0;  // nothing to clear: GEMM2 writes every slot's row
+        // the hidden abs-max in slices of 2048 16-byte vectors, one CTA each
+        pa.amax_part = partials;
+        pa.n_amax_ctas = (!is_static && !pa.dispatch_inline)
+                             ? (int)std::min<int64_t>(32, std::max<int64_t>(1, (T * H / 8 + 2047) / 2048))
+                             : 0;
         StaticScales sc;
         memset(&sc, 0, sizeof(sc));
         if (is_static)
             for (int64_t e = 0; e < E; ++e) sc.s13[e] = s13[e], sc.s2[e] = s2[e];
-        const int zero_blocks = 0;
+        pa.mark_pad_rows = 1;    // the swapped GEMMs never read the padding rows' scales
+        pa.zero_pad_scales = 0;
+        const int zero_blocks = pa.n_amax_ctas;
         void* args[] = {(void*)&pa, (void*)&sc};
         const void* fn = per_lane <= 4    ? (const void*)moe_prep_small_kernel<4>
                          : per_lane <= 8  ? (const void*)moe_prep_small_kernel<8>
@@ -1031,6 +1084,7 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         sa.row_valid_end = row_valid_end;
         sa.row_src = row_src;
         sa.row_tok = row_tok;
+        sa.slot_row = (int32_t*)at(MS_SLOT_ROW);
         void* sargs[] = {(void*)&sa};
         MOE_CUDA(launch_k((const void*)moe_scan_kernel, dim3(1), dim3(1024), 0, pdl, s, sargs), "scan launch");
         const int64_t ab = std::min<int64_t>((T * k + 255) / 256, (int64_t)d->sm_count * 8);
@@ -1054,31 +1108,38 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         q.tile_expert = tile_expert;
         q.n_experts = (int)E;
         if (!is_static) {
-            // one per-tensor scale: quantise the T rows once, then dispatch
+            // one per-tensor scale: the abs-max in partials, then each token row
+            // quantised once into the rows of its k routing slots; the tiles'
+            // padding rows get zero scale bytes (GEMM1 reads them)
             const int np = amax_partials_count(T * H);
             MOE_CUDA(launch_amax_partials(q.x, T * H, partials, np, pdl, s), "amax launch");
-            pdl = true;
-            q.pdl = true;
-            q.sg_mode = SG_PARTIALS;
-            q.partials = partials;
-            q.n_partials = np;
-            q.global_out = sg_a;
-            q.rows = T;
-            q.rows_pad = round_up(T, 128);
-            q.row_map = nullptr;
-            q.codes = tok_codes;
-            q.scales = tok_scales;
-            MOE_CUDA(launch_quant(q, s), "quantise launch");
-            const uint8_t* tc = tok_codes;
-            const uint8_t* tsc = tok_scales;
-            const int32_t* rt = row_tok;
-            const int32_t* rd = padded + E;  // rows beyond the padded total are not read by GEMM1
-            int64_t hh = H;
-            void* pargs[] = {(void*)&tc, (void*)&tsc, (void*)&rt, (void*)&rd, (void*)&hh, (void*)&a_codes,
-                             (void*)&a_scales};
-            const int64_t pb = (int64_t)d->sm_count * 8;
-            MOE_CUDA(launch_k((const void*)moe_permute_kernel, dim3((unsigned)pb), dim3(256), 0, true, s, pargs),
-                     "permute launch");
+            PrepArgs pa;
+            memset(&pa, 0, sizeof(pa));
+            pa.hidden = static_cast<const uint16_t*>(hidden);
+            pa.T = T;
+            pa.H = H;
+            pa.E = (int)E;
+            pa.k = (int)k;
+            pa.ids = ids;
+            pa.n_ptiles = n_ptiles;
+            pa.row_valid_end = row_valid_end;
+            pa.row_src = row_src;
+            pa.row_tok = row_tok;
+            pa.slot_row = (int32_t*)at(MS_SLOT_ROW);
+            pa.codes = a_codes;
+            pa.scales = a_scales;
+            pa.sg_out = sg_a;
+            pa.amax_part = partials;
+            pa.n_amax_ctas = np;
+            pa.mark_pad_rows = 0;  // the scan marked them
+            pa.zero_pad_scales = 1;
+            StaticScales sc;
+            memset(&sc, 0, sizeof(sc));
+            void* dargs[] = {(void*)&pa, (void*)&sc};
+            const int64_t items = T * sf_cols_padded(H, 16);
+            const int64_t db = std::min<int64_t>((items + 255) / 256, (int64_t)d->sm_count * 4);
+            MOE_CUDA(launch_k((const void*)moe_dispatch_kernel, dim3((unsigned)db), dim3(256), 0, true, s, dargs),
+                     "dispatch launch");
         } else {
             q.sg_mode = SG_EXPERT_TABLE;
             q.table = st13;
