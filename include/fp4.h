@@ -338,8 +338,9 @@ size_t fp4_moe_workspace_size(int64_t tokens, int64_t hidden, int64_t inter, int
  *      static_scales2[e]).
  *   6. D = alpha2_e * H_q . W2_e^T (alpha2_e = s_gH[e] * w2_global[e]).
  *   7. out[t] = bf16( sum_j weight[t, j] * D[t, j] ): D kept in fp32 (one row
- *      per routing slot), the top_k terms added in fp32 in slot order
- *      j = 0..top_k-1, so the result is the same bits on every run.
+ *      per routing slot, in the expert-sorted row order), the top_k terms
+ *      added in fp32 in slot order j = 0..top_k-1, so the result is the same
+ *      bits on every run.
  * hidden_bf16 [T, H], router_logits fp32 [T, E], out_bf16 [T, H] (device).
  * mode FP4_SCALE_STATIC needs both host arrays static_scales13[E] and
  * static_scales2[E] (each finite and > 0, E <= 256): NULL gives
@@ -365,8 +366,8 @@ fp4_status fp4_moe_grouped(const void* hidden_bf16, const float* router_logits, 
  * row int32 [R] (-1 for padding), 5 A codes [R, H/2], 6 A scales (MMA layout,
  * R rows), 7 s_gA / static scale per expert fp32 [E], 8 h bf16 [R, I],
  * 9 amax of h per expert fp32 [E], 10 s_gH fp32 [E], 11 h codes [R, I/2],
- * 12 h scales (MMA layout), 13 D = alpha2 x GEMM2, fp32 [T*k, H] in slot order
- * (t * top_k + j); R = offsets
+ * 12 h scales (MMA layout), 13 D = alpha2 x GEMM2, fp32 [R, H], one row per
+ * padded row (the row of slot t * top_k + j is the one entry 4 maps to it); R = offsets
  * count 14 (the padded row capacity).  Entries 15-21 are written by the
  * one-launch MoE (regions sized only for the shapes it takes), all in slot
  * order t * top_k + j: 15 h bf16 [T*k, I], 16 the requantised h codes

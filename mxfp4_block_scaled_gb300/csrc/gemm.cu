@@ -60,6 +60,21 @@ static bool make_out_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols,
     return r == CUDA_SUCCESS;
 }
 
+// 2-D map over an fp32 output [rows][cols] with row pitch ldo elements
+// (ldo % 4 == 0, 16-byte aligned base); box = 32 columns (128 bytes) x 32
+// rows, 128-byte swizzle (one epilogue warp's staging).
+static bool make_f32_out_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t ldo) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ldo * 4)};
+    cuuint32_t box[2] = {32u, 32u};
+    cuuint32_t es[2] = {1u, 1u};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int64_t gemm_k_blocks(int64_t k) { return (k + 2 * GEMM_KB_BYTES - 1) / (2 * GEMM_KB_BYTES); }
 
 template <int BN, int FK, int EPI>
@@ -80,6 +95,13 @@ static cudaError_t launch_one(const GemmLaunch& g, cudaStream_t s) {
         if (!make_out_map(&tmO, g.out, g.p_rows_valid, g.q_rows_valid, g.ldo, epi_box_cols<FK>())) {
             set_error("cuTensorMapEncodeTiled failed for the output (%lld x %lld, ldo %lld)",
                       (long long)g.p_rows_valid, (long long)g.q_rows_valid, (long long)g.ldo);
+            return cudaErrorInvalidValue;
+        }
+    } else if (EPI == EPI_DSLOT) {
+        // D [p_rows][q_rows_valid] fp32, the expert-sorted padded token rows
+        if (!make_f32_out_map(&tmO, g.out, g.p_rows, g.q_rows_valid, g.ldo)) {
+            set_error("cuTensorMapEncodeTiled failed for D (%lld x %lld, ldo %lld)", (long long)g.p_rows,
+                      (long long)g.q_rows_valid, (long long)g.ldo);
             return cudaErrorInvalidValue;
         }
     } else {

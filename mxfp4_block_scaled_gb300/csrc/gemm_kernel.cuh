@@ -648,19 +648,15 @@ __global__ void __launch_bounds__(512, 1)
             if constexpr (epi_swapped_grouped<EPI>()) {
                 const Unit wp = decode_unit<BN, EPI>(g, sc, u, ut);
                 if (wp.empty) continue;
-                if constexpr (EPI == EPI_COMBINE_T || EPI == EPI_DSLOT_T) {
+                if constexpr (EPI == EPI_COMBINE_T) {
 #pragma unroll
                     for (int q = 0; q < NPF; ++q) {
                         const int col = q * 32 + lane;
                         const int64_t row = wp.q_row0 + c_begin + col;
                         if (col < CPW && row < wp.vend) {
                             const int slot = g.row_src[row];
-                            if constexpr (EPI == EPI_COMBINE_T) {
-                                pf_tok[q] = slot / g.top_k;
-                                pf_w[q] = g.slot_weight[slot];
-                            } else {
-                                pf_tok[q] = slot;
-                            }
+                            pf_tok[q] = slot / g.top_k;
+                            pf_w[q] = g.slot_weight[slot];
                         }
                     }
                 }
@@ -670,19 +666,29 @@ __global__ void __launch_bounds__(512, 1)
             const uint32_t tb = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(acc * BN + c_begin);
 
             if constexpr (EPI == EPI_BF16) {
-                // chunk by chunk: fp32 -> alpha -> packed bf16 pairs, then release
+                // two chunks per round (one tcgen05.wait::ld each): fp32 -> alpha ->
+                // packed bf16 pairs, then release.  The MMAs of the next tile wait
+                // for the release, so its latency is paid at every tile boundary
+                // (one round per chunk cost ~1,000 cycles there, 8 % of the prefill).
                 const float alpha = MX ? 1.0f : __fmul_rn(g.p_global[0], g.q_global[0]);
                 uint32_t pk[NLD][16];
                 if (has_cols) {
 #pragma unroll
-                    for (int j = 0; j < NLD; ++j) {
-                        uint32_t r[32];
-                        tmem_ld32(tb + j * 32, r);
+                    for (int j = 0; j < NLD; j += 2) {
+                        uint32_t r0[32], r1[32];
+                        tmem_ld32(tb + j * 32, r0);
+                        if (j + 1 < NLD) tmem_ld32(tb + (j + 1) * 32, r1);
                         tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            pk[j][i] = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(r[2 * i])),
-                                                   __fmul_rn(alpha, __uint_as_float(r[2 * i + 1])));
+                            pk[j][i] = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(r0[2 * i])),
+                                                   __fmul_rn(alpha, __uint_as_float(r0[2 * i + 1])));
+                        if (j + 1 < NLD) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                pk[j + 1][i] = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(r1[2 * i])),
+                                                           __fmul_rn(alpha, __uint_as_float(r1[2 * i + 1])));
+                        }
                     }
                 }
                 tc_fence_before();
@@ -861,11 +867,11 @@ __global__ void __launch_bounds__(512, 1)
                                        __fmul_rn(sc, __uint_as_float(r[j][4 * v + 3])));
                 }
             } else if constexpr (EPI == EPI_DSLOT) {
-                // token rows: each row's routing slot gets alpha * acc (fp32).  The warp
-                // holds 32 rows x 32 columns per chunk; it writes them to its 4 KB of
-                // shared memory (row r's 16-byte piece v at piece v ^ (r % 8): no bank
-                // conflicts either way) and stores them back four rows per instruction,
-                // eight lanes x 16 bytes = one whole 128-byte line of a row each.
+                // token rows (expert-sorted, padded): D[row][feature] = alpha * acc
+                // (fp32).  Per 32-column chunk the warp writes its 32 rows to its
+                // 4 KB of shared memory in the 128-byte swizzle (row r's 16-byte
+                // piece v at piece v ^ (r % 8): no bank conflicts) and one TMA store
+                // takes the 32 x 32 box out; a box of padding rows only is skipped.
                 uint32_t r[NLD][32];
                 if (has_cols) {
 #pragma unroll
@@ -878,12 +884,12 @@ __global__ void __launch_bounds__(512, 1)
                 const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
                 const int64_t prow0 = w.p_row0 + qd * 32;
                 const float alpha = __fmul_rn(g.p_global[w.e], g.q_global[w.e]);
-                const int slot = prow0 + lane < w.vend ? g.row_src[prow0 + lane] : -1;
                 const uint32_t xs = smem_u32(sStg) + (uint32_t)(warp - 8) * 4096u;
-                float* dbase = reinterpret_cast<float*>(g.out) + w.qt * BN + c_begin;
-                if (has_cols) {
+                if (has_cols && prow0 < w.vend) {
 #pragma unroll
                     for (int j = 0; j < NLD; ++j) {
+                        if (lane == 0 && store_pending) bulk_wait_read_all();  // the buffer is free
+                        __syncwarp();
 #pragma unroll
                         for (int v = 0; v < 8; ++v)
                             sts128(xs + (uint32_t)lane * 128u + ((uint32_t)(v ^ (lane & 7)) << 4),
@@ -891,22 +897,19 @@ __global__ void __launch_bounds__(512, 1)
                                    __float_as_uint(__fmul_rn(alpha, __uint_as_float(r[j][4 * v + 1]))),
                                    __float_as_uint(__fmul_rn(alpha, __uint_as_float(r[j][4 * v + 2]))),
                                    __float_as_uint(__fmul_rn(alpha, __uint_as_float(r[j][4 * v + 3]))));
+                        fence_proxy_async();  // generic-proxy writes -> visible to the TMA
                         __syncwarp();
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const int row = i * 4 + (lane >> 3), c4 = lane & 7;
-                            const int srow = __shfl_sync(0xFFFFFFFFu, slot, row);
-                            const uint4 v4 = lds128(xs + (uint32_t)row * 128u + ((uint32_t)(c4 ^ (row & 7)) << 4));
-                            if (srow >= 0)
-                                *reinterpret_cast<uint4*>(dbase + (int64_t)srow * g.ldo + j * 32 + c4 * 4) = v4;
+                        if (lane == 0) {
+                            tma_store_2d(&tmO, xs, (int32_t)(w.qt * BN + c_begin + j * 32), (int32_t)prow0);
+                            bulk_commit();
+                            store_pending = true;
                         }
-                        __syncwarp();
                     }
                 }
             } else if constexpr (EPI == EPI_DSLOT_T) {
                 // P rows are the expert's W2 rows (output features), columns the
-                // sub-tile's token rows: d[slot of column][feature] = alpha * acc;
-                // the 32 lanes of a column write 32 consecutive features
+                // sub-tile's token rows (expert-sorted): d[row of column][feature] =
+                // alpha * acc; the 32 lanes of a column write 32 consecutive features
                 static_assert(CPW % 16 == 0, "whole 16-column loads");
                 uint32_t r[CPW / 16][16];
 #pragma unroll
@@ -922,14 +925,8 @@ __global__ void __launch_bounds__(512, 1)
                 const int64_t row0 = w.q_row0 + c_begin;
                 float* d = reinterpret_cast<float*>(g.out) + hd;
 #pragma unroll
-                for (int q = 0; q < NPF; ++q) {
-#pragma unroll
-                    for (int i = 0; i < 32 && q * 32 + i < CPW; ++i) {
-                        const int s_i = __shfl_sync(0xFFFFFFFFu, pf_tok[q], i);
-                        if (row0 + q * 32 + i < vend)
-                            d[(int64_t)s_i * g.ldo] = __fmul_rn(alpha, __uint_as_float(r[(q * 32 + i) / 16][(q * 32 + i) % 16]));
-                    }
-                }
+                for (int c = 0; c < CPW; ++c)
+                    if (row0 + c < vend) d[(row0 + c) * g.ldo] = __fmul_rn(alpha, __uint_as_float(r[c / 16][c % 16]));
             } else if constexpr (EPI == EPI_SWIGLU_T) {
                 // P rows are the expert's W13 rows, interleaved in groups of 32
                 // (gate, up, ...): TMEM lane quarters 0 / 1 hold gate / up of

@@ -326,15 +326,23 @@ __global__ void __launch_bounds__(512, 1)
             const uint32_t tb = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)c_begin;
             const float alpha = MX ? 1.0f : __fmul_rn(g.p_global[0], g.q_global[0]);
             uint32_t pk[NLD][16];
+            // two chunks per tcgen05.wait::ld (the next tile's MMAs wait for the release)
 #pragma unroll
-            for (int j = 0; j < NLD; ++j) {
-                uint32_t r[32];
-                tmem_ld32(tb + j * 32, r);
+            for (int j = 0; j < NLD; j += 2) {
+                uint32_t r0[32], r1[32];
+                tmem_ld32(tb + j * 32, r0);
+                if (j + 1 < NLD) tmem_ld32(tb + (j + 1) * 32, r1);
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
-                    pk[j][i] = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(r[2 * i])),
-                                           __fmul_rn(alpha, __uint_as_float(r[2 * i + 1])));
+                    pk[j][i] = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(r0[2 * i])),
+                                           __fmul_rn(alpha, __uint_as_float(r0[2 * i + 1])));
+                if (j + 1 < NLD) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        pk[j + 1][i] = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(r1[2 * i])),
+                                                   __fmul_rn(alpha, __uint_as_float(r1[2 * i + 1])));
+                }
             }
             tc_fence_before();
             __syncwarp();

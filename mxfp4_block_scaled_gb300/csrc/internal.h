@@ -68,8 +68,12 @@ struct QuantLaunch {
     float* expert_sg_out = nullptr;     // SG_EXPERT_AMAX: s_g[e] written here (n_experts entries)
     int n_experts = 0;
     const int32_t* rows_dev = nullptr;  // optional device row count bound (grouped): rows beyond are skipped
+    float2* etab = nullptr;             // expert modes, every tile row: scratch of n_experts x kEtabStride entries
     bool pdl = false;
 };
+
+// Entries per expert of the per-expert divisor tables (128 divisors, then (p, 1/p)).
+constexpr int kEtabStride = 130;
 
 int amax_partials_count(int64_t n_elems);
 cudaError_t launch_amax_partials(const uint16_t* x, int64_t n_elems, float* partials, int n_part, bool pdl,
@@ -91,8 +95,8 @@ enum Epi : int {
     EPI_COMBINE_T = 7,  // y[token of q][p] += weight * alpha * acc (fp32 reductions)
     // grouped GEMM2 outputs per routing slot (token * top_k + j), fp32, summed
     // in slot order by a separate combine (same bits every run):
-    EPI_DSLOT = 8,      // d[slot of p][q] = alpha * acc    (P = token rows)
-    EPI_DSLOT_T = 9,    // d[slot of q][p] = alpha * acc    (swapped: P = an expert's weight rows)
+    EPI_DSLOT = 8,      // d[p][q] = alpha * acc (fp32, TMA stores; P = expert-sorted token rows)
+    EPI_DSLOT_T = 9,    // d[q][p] = alpha * acc (swapped: P = an expert's weight rows)
 };
 
 // GemmLaunch::fmt for the 8-bit-container MX formats (MXFP8 / MXFP6; codes

@@ -66,6 +66,7 @@ enum MoeSlot : int {
     MS_STATIC13,
     MS_STATIC2,
     MS_SLOT_ROW,    // the expert-sorted row of each slot
+    MS_ETAB,        // per-expert divisor tables of the expert-scale quantisers
     // the one-launch MoE (moe_fused.cu), sized only when its shapes apply
     MS_F_ZERO,      // counters and h amax, cleared per call
     MS_F_H,         // bf16 [T k][I], slot order
@@ -108,7 +109,7 @@ static MoeLayout moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
     sz[MS_SG_H] = E * 4;
     sz[MS_H_CODES] = L.R * I / 2;
     sz[MS_H_SCALES] = L.R * sf_cols_padded(I, 16);
-    sz[MS_Y] = slots * H * 4;  // fp32 expert outputs, one row per routing slot
+    sz[MS_Y] = L.R * H * 4;  // fp32 expert outputs, one row per expert-sorted padded row
     sz[MS_BITMAP] = E * L.W * 4;
     sz[MS_WPREFIX] = E * L.W * 4;
     sz[MS_TILE_EXPERT] = (L.R / 128) * 4;
@@ -119,6 +120,7 @@ static MoeLayout moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
     sz[MS_STATIC13] = E * 4;
     sz[MS_STATIC2] = E * 4;
     sz[MS_SLOT_ROW] = slots * 4;
+    sz[MS_ETAB] = E * kEtabStride * 8;
     const bool fused = moe_fused_supported(T, H, I, E, k);
     sz[MS_F_ZERO] = fused ? kFusedZeroedBytes : 0;
     sz[MS_F_H] = fused ? slots * I * 2 : 0;
@@ -574,7 +576,7 @@ __global__ void __launch_bounds__(1024) moe_prep_small_kernel(const PrepArgs a, 
         a.row_src[row] = s;
         a.row_tok[row] = t;
         s_row[s] = row;
-        if (!a.dispatch_inline) a.slot_row[s] = row;
+        a.slot_row[s] = row;
     }
 
     // 4. dynamic: s_gA from the abs-max of the T hidden rows (unless CTAs 1..
@@ -689,23 +691,23 @@ __global__ void __launch_bounds__(256) moe_dispatch_kernel(const PrepArgs a, con
     }
 }
 
-// fp32 accumulator -> bf16 output
-// out[t][f] = bf16( sum_{j < k} w[t][j] * d[t k + j][f] ), the top-k terms
-// added in slot order in fp32 (a thread per 4 consecutive features), so the
-// output is the same bits on every run.
+// out[t][f] = bf16( sum_{j < k} w[t][j] * d[row of slot t k + j][f] ), the
+// top-k terms added in slot order in fp32 (a thread per 4 consecutive
+// features; d holds one fp32 row per expert-sorted padded row), so the output
+// is the same bits on every run.
 __global__ void __launch_bounds__(256) moe_combine_kernel(const float4* __restrict__ d,
-                                                          const float* __restrict__ w, int64_t T, int k,
+                                                          const float* __restrict__ w,
+                                                          const int32_t* __restrict__ slot_row, int64_t T, int k,
                                                           int64_t h4, uint2* __restrict__ out) {
     pdl_wait();
     pdl_launch_dependents();  // dependents wait for this grid's completion
     const int64_t n = T * h4;
     for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256) {
         const int64_t t = i / h4, f4 = i - t * h4;
-        const float4* dr = d + (t * k) * h4 + f4;
         float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int j = 0; j < k; ++j) {
             const float wj = w[t * k + j];
-            const float4 v = dr[(int64_t)j * h4];
+            const float4 v = d[(int64_t)slot_row[t * k + j] * h4 + f4];
             y.x = __fadd_rn(y.x, __fmul_rn(wj, v.x));
             y.y = __fadd_rn(y.y, __fmul_rn(wj, v.y));
             y.z = __fadd_rn(y.z, __fmul_rn(wj, v.z));
@@ -1143,6 +1145,7 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         } else {
             q.sg_mode = SG_EXPERT_TABLE;
             q.table = st13;
+            q.etab = (float2*)at(MS_ETAB);
             // rows beyond the padded total are skipped: their count is on the device
             q.rows_dev = padded + E;
             MOE_CUDA(launch_quant(q, s), "quantise launch");
@@ -1233,9 +1236,11 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
             q.sg_mode = SG_EXPERT_AMAX;
             q.table = amax_h;
             q.expert_sg_out = sg_h;
+            q.etab = (float2*)at(MS_ETAB);
         } else {
             q.sg_mode = SG_EXPERT_TABLE;
             q.table = st2;
+            q.etab = (float2*)at(MS_ETAB);
         }
         MOE_CUDA(launch_quant(q, s), "requantise launch");
         pdl = true;
@@ -1289,10 +1294,11 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         MOE_CUDA(launch_gemm(g, s), "GEMM2 launch");
         const float4* d4 = reinterpret_cast<const float4*>(y);
         const float* wv = wts;
+        const int32_t* sr = (const int32_t*)at(MS_SLOT_ROW);
         uint2* o2 = reinterpret_cast<uint2*>(out);
         int64_t TT = T, h4 = H / 4;
         int kk = (int)k;
-        void* fargs[] = {(void*)&d4, (void*)&wv, (void*)&TT, (void*)&kk, (void*)&h4, (void*)&o2};
+        void* fargs[] = {(void*)&d4, (void*)&wv, (void*)&sr, (void*)&TT, (void*)&kk, (void*)&h4, (void*)&o2};
         int64_t fb = std::min<int64_t>((T * h4 + 255) / 256, (int64_t)d->sm_count * 8);
         MOE_CUDA(launch_k((const void*)moe_combine_kernel, dim3((unsigned)fb), dim3(256), 0, true, s, fargs),
                  "combine launch");

@@ -214,7 +214,7 @@ def test_moe_workspace_layout_holds_its_documented_contents(F, T, H, I, E, k):
     assert R % 128 == 0 and R >= slots + min(slots, E) * 127 and R >= 128
     sf = lambda kk: ((kk + 255) // 256) * 16  # NVFP4 scale columns per row, K padded to 256
     need = [slots * 4, slots * 4, (E + 1) * 4, (E + 1) * 4, R * 4, R * H // 2, R * sf(H), E * 4, R * I * 2, E * 4,
-            E * 4, R * I // 2, R * sf(I), slots * H * 4]
+            E * 4, R * I // 2, R * sf(I), R * H * 4]
     assert o[0] == 0
     for i in range(14):
         assert o[i] % 256 == 0

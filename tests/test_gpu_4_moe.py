@@ -154,9 +154,8 @@ def _stage_checks(F, O, c):
     y = bf16_to_np(out)
     # fp32 sum of the k terms in slot order: k * 2^-24 of the magnitude on top
     check_close(y, r["y"], r["ymag"], what="y", extra_tau=k * 2.0 ** -23 * r["ymag"])
-    # D, one fp32 row per routing slot (workspace entry 13), within the GEMM tolerance
-    S = T * k
-    D = c.view(13, torch.float32, (S, H)).cpu().numpy().astype(np.float64)[r["order"]]
+    # D, one fp32 row per expert-sorted padded row (workspace entry 13), within the GEMM tolerance
+    D = c.view(13, torch.float32, (c.R, H)).cpu().numpy().astype(np.float64)[c.gpu_rows()]
     tau_d = 2.0 ** -18 * r["Dmag"] + 2.0 ** -22 * np.abs(r["D"])
     assert np.all(np.abs(D - r["D"]) <= tau_d + 1e-30), "D"
     # the combine has a fixed order: the same bits on a second run
