@@ -113,10 +113,12 @@ void fp4_set_arch_override(int sm);
  * 1 = the one-CTA kernel and never the fused decode kernel; 2 = the CTA-pair
  * kernel (tcgen05 cta_group::2, 256 x 256 tiles) wherever m >= 256 and
  * n >= 256; 3 = the fused decode kernel for every fp4_gemm with m <= 8 and
- * k <= 8192.
+ * k <= 8192; 4 = fp4_gemm_w4a16 always on its tensor-core kernel (policy 0
+ * takes it for m >= 3 when the weight's 128-row tiles fill at least half the
+ * SMs, else the CUDA-core kernel).
  * Process-wide, host-side; results agree within the GEMM tolerance under every
  * policy (codes and scales are identical).
- * FP4_ERR_INVALID_ARG for a value outside 0..3 (the policy is unchanged). */
+ * FP4_ERR_INVALID_ARG for a value outside 0..4 (the policy is unchanged). */
 fp4_status fp4_set_gemm_tile_policy(int policy);
 
 /* Tuning and test hook (no counterpart on the pages): which implementation

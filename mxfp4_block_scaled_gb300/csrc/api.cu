@@ -188,7 +188,7 @@ extern "C" size_t fp4_scales_bytes(int fmt, int64_t rows, int64_t k) {
 extern "C" void fp4_set_arch_override(int sm) { g_arch_override = sm; }
 
 extern "C" fp4_status fp4_set_gemm_tile_policy(int policy) {
-    CHECK_OR_RETURN(policy >= 0 && policy <= 3, FP4_ERR_INVALID_ARG, "tile policy %d not in 0..3", policy);
+    CHECK_OR_RETURN(policy >= 0 && policy <= 4, FP4_ERR_INVALID_ARG, "tile policy %d not in 0..4", policy);
     g_tile_policy = policy;
     return FP4_OK;
 }
@@ -618,9 +618,17 @@ extern "C" fp4_status fp4_gemm_w4a16(int fmt, const void* x, int64_t m, const vo
     CHECK_OR_RETURN(x, FP4_ERR_INVALID_ARG, "null activation pointer");
     CHECK_OR_RETURN(aligned16(x), FP4_ERR_ALIGNMENT, "activations must be 16-byte aligned");
     TRY(check_arch());
-    return cuda_status(launch_w4a16(fmt, static_cast<const uint16_t*>(x), (int)m, n, k,
-                                    static_cast<const uint8_t*>(w_codes), static_cast<const uint8_t*>(w_scales),
-                                    w_global, static_cast<uint16_t*>(out), (cudaStream_t)stream),
+    const DeviceInfo* d = current_device();
+    const int sms = d ? d->sm_count : 148;
+    // the tensor-core kernel takes one CTA per 128 weight rows and runs at a
+    // near-constant time paced by its 256 small (N = 16) MMAs per CTA: automatic
+    // for 3-4 activation rows when the tiles fill at least half the SMs (the
+    // CUDA-core kernel's time grows with the rows, the tensor-core one's does not)
+    const bool tc = g_tile_policy == 4 || (g_tile_policy == 0 && m >= 3 && 2 * ((n + 127) / 128) >= sms);
+    auto launch = tc ? launch_w4a16_tc : launch_w4a16;
+    return cuda_status(launch(fmt, static_cast<const uint16_t*>(x), (int)m, n, k, static_cast<const uint8_t*>(w_codes),
+                              static_cast<const uint8_t*>(w_scales), w_global, static_cast<uint16_t*>(out),
+                              (cudaStream_t)stream),
                        "weight-only launch");
 }
 

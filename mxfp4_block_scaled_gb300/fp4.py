@@ -280,11 +280,11 @@ def gemm_w4a16(x, wq, out=None, stream=None):
     return out
 
 
-TILE_AUTO, TILE_ONE_CTA, TILE_CTA_PAIR, TILE_FUSED_DECODE = 0, 1, 2, 3
+TILE_AUTO, TILE_ONE_CTA, TILE_CTA_PAIR, TILE_FUSED_DECODE, TILE_W4A16_TC = 0, 1, 2, 3, 4
 
 
 def set_gemm_tile_policy(policy):
-    """Choose the GEMM kernels (TILE_AUTO, TILE_ONE_CTA, TILE_CTA_PAIR, TILE_FUSED_DECODE)."""
+    """Choose the GEMM kernels (TILE_AUTO, TILE_ONE_CTA, TILE_CTA_PAIR, TILE_FUSED_DECODE, TILE_W4A16_TC)."""
     _check(lib().fp4_set_gemm_tile_policy(int(policy)))
 
 

@@ -143,9 +143,9 @@ def test_python_wrapper_raises(F):
 
 def test_tile_policy_validation(F):
     L = F.lib()
-    for p in (F.TILE_ONE_CTA, F.TILE_CTA_PAIR, F.TILE_FUSED_DECODE, F.TILE_AUTO):
+    for p in (F.TILE_ONE_CTA, F.TILE_CTA_PAIR, F.TILE_FUSED_DECODE, F.TILE_W4A16_TC, F.TILE_AUTO):
         assert L.fp4_set_gemm_tile_policy(p) == 0
-    for bad in (-1, 4):
+    for bad in (-1, 5):
         assert L.fp4_set_gemm_tile_policy(bad) == F.STATUS_CODE["FP4_ERR_INVALID_ARG"]
         assert "tile policy" in L.fp4_last_error_message().decode()
     with pytest.raises(F.FP4Error):

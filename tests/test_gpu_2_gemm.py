@@ -201,6 +201,28 @@ def test_w4a16_shapes(F, O, m, n, k, fmt):
     check_w4a16(F, O, I.activations_with_outliers(m, k, m + 5 * k), I.weights_bf16(n, k, n + 11), fmt)
 
 
+@pytest.mark.parametrize("m,n,k", [(1, 256, 512), (2, 520, 800), (3, 1000, 1056), (4, 264, 4096), (1, 8, 32),
+                                   (2, 1032, 4128), (4, 128, 8192)])
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_w4a16_tensor_core_shapes(F, O, m, n, k, fmt):
+    """The same shapes forced onto the tensor-core kernel (weights dequantised
+    to bf16 in shared memory, kind::f16 MMAs): ragged n and k, one K block."""
+    F.set_gemm_tile_policy(F.TILE_W4A16_TC)
+    try:
+        check_w4a16(F, O, I.activations_with_outliers(m, k, m + 5 * k), I.weights_bf16(n, k, n + 11), fmt)
+    finally:
+        F.set_gemm_tile_policy(F.TILE_AUTO)
+
+
+def test_w4a16_tensor_core_mxfp4_full_size(F, O):
+    """MXFP4 W [4096, 7168], m = 3, on the tensor-core kernel."""
+    F.set_gemm_tile_policy(F.TILE_W4A16_TC)
+    try:
+        check_w4a16(F, O, I.activations_with_outliers(3, 7168, 6), I.weights_bf16(4096, 7168, 105), 1)
+    finally:
+        F.set_gemm_tile_policy(F.TILE_AUTO)
+
+
 def test_w4a16_empty_and_zero(F):
     w = I.weights_bf16(256, 512, 1).cuda()
     wq = F.prepack_weight(w)
