@@ -68,12 +68,8 @@ struct QuantLaunch {
     float* expert_sg_out = nullptr;     // SG_EXPERT_AMAX: s_g[e] written here (n_experts entries)
     int n_experts = 0;
     const int32_t* rows_dev = nullptr;  // optional device row count bound (grouped): rows beyond are skipped
-    float2* etab = nullptr;             // expert modes, every tile row: scratch of n_experts x kEtabStride entries
     bool pdl = false;
 };
-
-// Entries per expert of the per-expert divisor tables (128 divisors, then (p, 1/p)).
-constexpr int kEtabStride = 130;
 
 int amax_partials_count(int64_t n_elems);
 cudaError_t launch_amax_partials(const uint16_t* x, int64_t n_elems, float* partials, int n_part, bool pdl,

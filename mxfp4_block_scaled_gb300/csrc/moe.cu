@@ -66,7 +66,6 @@ enum MoeSlot : int {
     MS_STATIC13,
     MS_STATIC2,
     MS_SLOT_ROW,    // the expert-sorted row of each slot
-    MS_ETAB,        // per-expert divisor tables of the expert-scale quantisers
     // the one-launch MoE (moe_fused.cu), sized only when its shapes apply
     MS_F_ZERO,      // counters and h amax, cleared per call
     MS_F_H,         // bf16 [T k][I], slot order
@@ -120,7 +119,6 @@ static MoeLayout moe_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
     sz[MS_STATIC13] = E * 4;
     sz[MS_STATIC2] = E * 4;
     sz[MS_SLOT_ROW] = slots * 4;
-    sz[MS_ETAB] = E * kEtabStride * 8;
     const bool fused = moe_fused_supported(T, H, I, E, k);
     sz[MS_F_ZERO] = fused ? kFusedZeroedBytes : 0;
     sz[MS_F_H] = fused ? slots * I * 2 : 0;
@@ -432,10 +430,20 @@ __device__ __forceinline__ void prep_block(const PrepArgs& a, int t, int b, int 
     const uint32_t w0 = nvfp4_word(f, e);
     unpack8(v1, f);
     const uint32_t w1 = nvfp4_word(f, e);
-    for (int j = 0; j < n; ++j) {
-        const int64_t row = rows[j];
-        if (b < kblocks) *reinterpret_cast<uint2*>(a.codes + row * (a.H / 2) + (int64_t)b * 8) = make_uint2(w0, w1);
-        a.scales[sf_offset(row, b, nbp)] = (uint8_t)sbyte;
+    // the rows are read eight at a time before the stores (`rows` is global or
+    // shared memory; read one by one between stores, no read could move above
+    // the store before it, so each read's latency was paid in turn)
+    for (int j0 = 0; j0 < n; j0 += 8) {
+        int64_t rr[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) rr[u] = j0 + u < n ? (int64_t)rows[j0 + u] : -1;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (rr[u] < 0) break;
+            if (b < kblocks)
+                *reinterpret_cast<uint2*>(a.codes + rr[u] * (a.H / 2) + (int64_t)b * 8) = make_uint2(w0, w1);
+            a.scales[sf_offset(rr[u], b, nbp)] = (uint8_t)sbyte;
+        }
     }
 }
 
@@ -1145,7 +1153,6 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         } else {
             q.sg_mode = SG_EXPERT_TABLE;
             q.table = st13;
-            q.etab = (float2*)at(MS_ETAB);
             // rows beyond the padded total are skipped: their count is on the device
             q.rows_dev = padded + E;
             MOE_CUDA(launch_quant(q, s), "quantise launch");
@@ -1236,11 +1243,9 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
             q.sg_mode = SG_EXPERT_AMAX;
             q.table = amax_h;
             q.expert_sg_out = sg_h;
-            q.etab = (float2*)at(MS_ETAB);
         } else {
             q.sg_mode = SG_EXPERT_TABLE;
             q.table = st2;
-            q.etab = (float2*)at(MS_ETAB);
         }
         MOE_CUDA(launch_quant(q, s), "requantise launch");
         pdl = true;

@@ -457,89 +457,110 @@ __global__ void __launch_bounds__(QT, QNV_CTAS) quant_nv_kernel(const QuantLaunc
 
 // ------------------------- NVFP4, per-expert scale, every row of the tiles
 
-// Per expert e: the 128 divisor entries of its global scale (nvfp4_divisor
-// without the refinement: the product path where the plain reciprocal is
-// proven, else the bracket, so the launch runs no division loop) and (p, 1/p)
-// of its scale bytes, at
-// etab[e * kEtabStride ...]; for SG_EXPERT_AMAX also s_g[e] = amax_e / 2688.
-__global__ void __launch_bounds__(128) expert_tables_kernel(const QuantLaunch q) {
-    pdl_wait();
-    pdl_launch_dependents();
-    const int e = blockIdx.x;
-    const float tv = q.table[e];
-    const float sg = q.sg_mode == SG_EXPERT_TABLE ? tv : __fdiv_rn(tv, 2688.0f);
-    float2* t = q.etab + (int64_t)e * kEtabStride;
-    t[threadIdx.x] = nvfp4_divisor(threadIdx.x, sg, false);
-    if (threadIdx.x == 0) {
-        const float p = __fmul_rn(sg, 6.0f);
-        t[128] = make_float2(p, nvfp4_inv_p(p));
-        if (q.sg_mode == SG_EXPERT_AMAX && q.expert_sg_out) q.expert_sg_out[e] = sg;
-    }
-}
+constexpr int QE_ROWS = 64;  // rows per work item (half a 128-row tile: one expert)
 
 // Rows of 128-row expert tiles quantised with the tile's expert scale, every
 // row of the tiles written: the MoE requantisation of h when the grouped
 // GEMM2 has tokens on the 128-row side (it reads the padding rows' zero scale
 // bytes), and the dispatch with static per-expert scales (row_map gives each
-// row's token).  The divisors come from expert_tables_kernel: a thread takes
-// one 16-element block column of `rpi` rows at a time (QU of them in flight),
-// looks its divisor up in the tile expert's table (cached) and needs no shared
-// memory or barrier.  Rows without a source get zero scale bytes and no
-// codes; rows past the device row count are not touched.  Codes and scale
-// bytes equal quant_kernel's expert modes.
+// row's token).  A work item is half a tile: the CTA tabulates the 128
+// divisors of the tile's expert scale (as quant_nv_kernel does for a tensor)
+// when the expert changes, then takes the item's 64 x nb blocks as a flat
+// range, QU per thread in flight, with the row and block of each step
+// advanced by constants (no division per block).  Rows without a source get
+// zero scale bytes and no codes; rows past the device row count are not
+// touched.
+// Codes and scale bytes equal quant_kernel's expert modes: each divisor entry
+// is nvfp4_divisor's, with the product path wherever it is proven.
 __global__ void __launch_bounds__(QT, 3) quant_expert_rows_kernel(const QuantLaunch q) {
+    __shared__ float2 dtab[128];
+    __shared__ int64_t s_x[QE_ROWS];   // element offset of the row's source, -1: zero row, -2: past the rows
+    __shared__ int64_t s_c[QE_ROWS];   // byte offset of the row's codes
+    __shared__ int64_t s_sf[QE_ROWS];  // byte offset of the row's scale bytes (block 0)
     pdl_wait();
     pdl_launch_dependents();
+    if (blockIdx.x == 0 && q.sg_mode == SG_EXPERT_AMAX && q.expert_sg_out)
+        for (int e = threadIdx.x; e < q.n_experts; e += QT) q.expert_sg_out[e] = __fdiv_rn(q.table[e], 2688.0f);
     const int nb = (int)sf_cols_padded(q.k, 16);
     const int kblocks = (int)(q.k / 16);
-    const int bpt = nb < QT ? nb : QT;  // threads per row
-    const int rpi = QT / bpt;           // rows per CTA step
-    const int ty = threadIdx.x / bpt, tx = threadIdx.x - ty * bpt;
-    if (ty >= rpi) return;
+    const int per_item = QE_ROWS * nb;
     const int64_t row_limit = q.rows_dev ? (int64_t)(*q.rows_dev) : q.rows_pad;
+    const int64_t items = (row_limit + QE_ROWS - 1) / QE_ROWS;
     const int64_t cb = q.k / 2;
-    const int64_t rstep = (int64_t)gridDim.x * rpi;
-    for (int b = tx; b < nb; b += bpt) {
-        const bool bdata = b < kblocks;
-        const int64_t sf_col = (int64_t)(b >> 2) * 512 + (b & 3);
-        for (int64_t r0 = (int64_t)blockIdx.x * rpi + ty; r0 < row_limit; r0 += QU * rstep) {
-            uint4 v[QU][2];
-            int64_t src[QU];
+    const int dq = QT / nb, dr = QT - dq * nb;  // a step of QT blocks: dq rows and dr blocks
+    const int t_row = threadIdx.x / nb, t_col = threadIdx.x - t_row * nb;
+    int cached = -1;
+    float p = 0.0f, inv_p = 0.0f;
+    uint4 v[QU][2];
+    int rj[QU], cj[QU];
+    // this thread's next QU blocks of the item: row / block indices, then the loads
+    auto load = [&](int base, int& row, int& col) {
 #pragma unroll
-            for (int j = 0; j < QU; ++j) {
-                const int64_t r = r0 + j * rstep;
-                v[j][0] = v[j][1] = make_uint4(0u, 0u, 0u, 0u);
-                src[j] = -2;
-                if (r < row_limit) {
-                    const int64_t m = r < q.rows ? (int64_t)__ldg(q.row_map + r) : -1;
-                    src[j] = m < 0 ? -1 : (q.row_map_is_mask ? r : m);
-                    if (src[j] >= 0 && bdata) {
-                        const uint4* px = reinterpret_cast<const uint4*>(q.x + src[j] * q.x_ld + (int64_t)b * 16);
-                        v[j][0] = __ldg(px);
-                        v[j][1] = __ldg(px + 1);
-                    }
-                }
+        for (int j = 0; j < QU; ++j) {
+            rj[j] = row;
+            cj[j] = col;
+            v[j][0] = v[j][1] = make_uint4(0u, 0u, 0u, 0u);
+            const int64_t xo = base + j * QT < per_item ? s_x[row] : -1;
+            if (xo >= 0 && col < kblocks) {
+                const uint4* px = reinterpret_cast<const uint4*>(q.x + xo + (int64_t)col * 16);
+                v[j][0] = __ldg(px);
+                v[j][1] = __ldg(px + 1);
             }
+            row += dq;
+            col += dr;
+            if (col >= nb) {
+                col -= nb;
+                ++row;
+            }
+        }
+    };
+    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+        const int64_t r0 = it * QE_ROWS;
+        const int e = q.tile_expert[it / (128 / QE_ROWS)];
+        const float tv = q.table[e];
+        __syncthreads();  // the previous item is done with the table and the row offsets
+        if (threadIdx.x < QE_ROWS) {
+            const int64_t r = r0 + threadIdx.x;
+            int64_t xo = -2;
+            if (r < row_limit) {
+                const int64_t m = r < q.rows ? (int64_t)q.row_map[r] : -1;
+                xo = m < 0 ? -1 : (q.row_map_is_mask ? r : m) * q.x_ld;
+            }
+            s_x[threadIdx.x] = xo;
+            s_c[threadIdx.x] = r * cb;
+            s_sf[threadIdx.x] = (r >> 7) * (int64_t)(nb >> 2) * 512 + ((r & 31) << 4) + (((r >> 5) & 3) << 2);
+        }
+        __syncthreads();
+        int row = t_row, col = t_col;  // of this thread's next block in the item
+        load(threadIdx.x, row, col);   // in flight while the divisor table is formed
+        if (e != cached) {             // the same expert for every thread
+            const float sg = q.sg_mode == SG_EXPERT_TABLE ? tv : __fdiv_rn(tv, 2688.0f);
+            if (threadIdx.x < 128) dtab[threadIdx.x] = nvfp4_divisor(threadIdx.x, sg, true);
+            p = __fmul_rn(sg, 6.0f);
+            inv_p = nvfp4_inv_p(p);
+            cached = e;
+            __syncthreads();
+        }
+        for (int base = threadIdx.x; base < per_item; base += QU * QT) {
+            if (base != (int)threadIdx.x) load(base, row, col);
 #pragma unroll
             for (int j = 0; j < QU; ++j) {
-                if (src[j] == -2) break;  // later rows are past the limit too
-                const int64_t r = r0 + j * rstep;
-                const float2* t = q.etab + (int64_t)__ldg(q.tile_expert + (r >> 7)) * kEtabStride;
-                const float2 pi = __ldg(t + 128);
+                if (base + j * QT >= per_item) break;
+                const int64_t xo = s_x[rj[j]];
+                if (xo == -2) continue;
                 const uint32_t am = absmax8(v[j][1], absmax8(v[j][0], 0u));
-                const uint32_t sbyte =
-                    nvfp4_scale_byte(__uint_as_float(max(am & 0xFFFFu, am >> 16) << 16), pi.x, pi.y);
-                if (src[j] >= 0 && bdata) {
-                    const float2 d = __ldg(t + sbyte);
+                const uint32_t sbyte = nvfp4_scale_byte(__uint_as_float(max(am & 0xFFFFu, am >> 16) << 16), p, inv_p);
+                const int c = cj[j];
+                if (xo >= 0 && c < kblocks) {
+                    const float2 d = dtab[sbyte];
                     uint2 w = make_uint2(0u, 0u);
                     if (d.y > 0.0f)
                         w = make_uint2(e2m1_word_rd(v[j][0], d.y), e2m1_word_rd(v[j][1], d.y));
                     else if (d.x != 0.0f)
                         w = nvfp4_block_slow(v[j][0], v[j][1], d);
-                    *reinterpret_cast<uint2*>(q.codes + r * cb + (int64_t)b * 8) = w;
+                    *reinterpret_cast<uint2*>(q.codes + s_c[rj[j]] + (int64_t)c * 8) = w;
                 }
-                q.scales[((r >> 7) * (int64_t)(nb >> 2)) * 512 + ((r & 31) << 4) + (((r >> 5) & 3) << 2) + sf_col] =
-                    (uint8_t)sbyte;
+                q.scales[s_sf[rj[j]] + (c >> 2) * 512 + (c & 3)] = (uint8_t)sbyte;
             }
         }
     }
@@ -623,19 +644,14 @@ cudaError_t launch_quant(const QuantLaunch& q, cudaStream_t s) {
         void* args[] = {(void*)&qq};
         return launch_ex((const void*)quant_tiles_kernel, dim3((unsigned)blocks), dim3(QT), 0, q.pdl, s, args);
     }
-    if (q.fmt == FP4_NVFP4 && !q.skip_masked_rows && q.row_map && q.tile_expert && q.etab && q.n_experts > 0 &&
+    if (q.fmt == FP4_NVFP4 && !q.skip_masked_rows && q.row_map && q.tile_expert &&
         (q.sg_mode == SG_EXPERT_TABLE || q.sg_mode == SG_EXPERT_AMAX)) {
-        QuantLaunch qq = q;
-        void* args[] = {(void*)&qq};
-        cudaError_t e = launch_ex((const void*)expert_tables_kernel, dim3((unsigned)q.n_experts), dim3(128), 0, q.pdl,
-                                  s, args);
-        if (e != cudaSuccess) return e;
-        const int64_t nb = sf_cols_padded(q.k, 16);
-        const int64_t rpi = QT / (nb < QT ? nb : QT);
-        int64_t blocks = (q.rows_pad + rpi * QU - 1) / (rpi * QU);
+        int64_t blocks = q.rows_pad / QE_ROWS;  // upper bound on the items
         if (blocks > (int64_t)sms * 3) blocks = (int64_t)sms * 3;  // one resident wave
         if (blocks < 1) blocks = 1;
-        return launch_ex((const void*)quant_expert_rows_kernel, dim3((unsigned)blocks), dim3(QT), 0, true, s, args);
+        QuantLaunch qq = q;
+        void* args[] = {(void*)&qq};
+        return launch_ex((const void*)quant_expert_rows_kernel, dim3((unsigned)blocks), dim3(QT), 0, q.pdl, s, args);
     }
     const int64_t nb16 = sf_cols_padded(q.k, 16);
     // quant_nv_kernel keeps rows, row steps and scale offsets in 32 bits
