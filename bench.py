@@ -530,7 +530,7 @@ def run_secondary(torch, fp4, L, I, dev, peaks):
         byt = wbytes + m * nk * 2 + m * 14336 * 2
         out["decode_m%d" % m] = {"us": round(ms * 1e3, 2), "GB/s": round(byt / (ms * 1e-3) / 1e9, 1),
                                  "frac_hbm": round(byt / (ms * 1e-3) / 1e9 / hbm, 4),
-                                 "note": ("one fused launch (activations quantised in the GEMM kernel)" if m <= 6
+                                 "note": ("one fused launch (activations quantised in the GEMM kernel)" if m <= 8
                                           else "quantise (amax + quantise launches) + GEMM")
                                          + ", CUDA graph, 8 rotating weight copies"}
     # weight-only (W4A16) decode on the same weights: bf16 activations, not quantised

@@ -105,7 +105,7 @@ void fp4_set_arch_override(int sm);
 
 /* Tuning and test hook (no counterpart on the pages): which kernels fp4_gemm /
  * fp4_gemm_prequant use.  0 = automatic: for m > 64 the one-CTA kernel
- * (128- or 256-wide tiles); for fp4_gemm with m <= 6, k <= 8192 and
+ * (128- or 256-wide tiles); for fp4_gemm with m <= 8, k <= 8192 and
  * n >= 64 x (SM count) the fused decode kernel (activation quantisation inside
  * the GEMM launch, one CTA per 128 weight rows); otherwise for m <= 64 the
  * quantiser and a swapped-operand GEMM, split along K (with a reduction

@@ -16,9 +16,11 @@
 //   warps 0-3, 6, 8-15  first, after the dependency wait: the activations'
 //               abs-max, then all m x K activations quantised once into a
 //               compact smem copy (codes [m][K/2], scale bytes [m][K/16 or
-//               K/32]); then warp 6 copies each K block of it into the stage's
-//               operand tile (the MMA's swizzled layout) and scale slot (the
-//               MMA scale layout);
+//               K/32]), the first ring-full of K blocks also straight into
+//               their stages' operand tiles (the MMA's swizzled layout) and
+//               scale slots (the MMA scale layout), which warp 8 then marks
+//               full; warp 6 copies each later K block from the compact copy
+//               when its stage comes free;
 //   warps 0-3   scale writers (smem -> TMEM, tcgen05.st), as in gemm_kernel;
 //   warp 5      TMEM allocation and the MMA issuer;
 //   warps 8-11  epilogue: one tcgen05.ld per lane quarter, alpha, bf16.
@@ -46,17 +48,31 @@ struct DecCfg {
     static constexpr int SF_COLS = 2 * SF_CHUNKS * 4;  // P and Q scale columns per stage
     static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM_LIMIT = 227 * 1024;
-    static constexpr int MAX_K = (int)kDecodeFusedMaxK;                   // fused path: k <= MAX_K
-    static constexpr int COMPACT_MAX = 8 * (MAX_K / 2 + MAX_K / 16);      // m <= 8 rows of codes + scales
-    static constexpr int DTAB = 128 * 8;                                  // NVFP4 divisor entry per scale byte
-    static constexpr int ST_SMEM = (SMEM_LIMIT - 2048 - BAR_BYTES - COMPACT_MAX - DTAB) / STAGE_BYTES;
+    static constexpr int MAX_K = (int)kDecodeFusedMaxK;  // fused path: k <= MAX_K
+    static constexpr int DTAB = 128 * 8;                 // NVFP4 divisor entry per scale byte
+    static constexpr int FIXED = 1024 + BAR_BYTES + DTAB;  // alignment slack, barriers, divisor table
+    // The ring holds as many stages as the shared memory left beside the
+    // compact activation copy (m rows of codes and scale bytes) takes, up to
+    // MAX_STAGES: the K blocks beyond the ring wait a full copy round trip
+    // each time the ring turns, so for K = 4096 (16 K blocks) 8 stages take
+    // two turns where 7 take three.
+    static constexpr int MAX_STAGES = 12;
     static constexpr int ST_TMEM = (512 - BN) / SF_COLS;
-    static constexpr int ST_MIN = ST_SMEM < ST_TMEM ? ST_SMEM : ST_TMEM;
-    static constexpr int STAGES = ST_MIN < 12 ? ST_MIN : 12;
-    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + DTAB + COMPACT_MAX;
-    static_assert(STAGES >= 4, "pipeline too shallow");
-    static_assert(4 * STAGES + 4 <= BAR_BYTES / 8 - 4, "barrier area too small");
-    static_assert(SMEM <= SMEM_LIMIT, "shared memory budget");
+    static constexpr int64_t compact_bytes(int m, int64_t k) {
+        return ((int64_t)m * (k / 2 + k / (MX ? 32 : 16)) + 15) / 16 * 16;
+    }
+    static constexpr int stages(int m, int64_t k) {
+        const int64_t by_smem = (SMEM_LIMIT - FIXED - compact_bytes(m, k)) / STAGE_BYTES;
+        int64_t st = by_smem < ST_TMEM ? by_smem : ST_TMEM;
+        return (int)(st < MAX_STAGES ? st : MAX_STAGES);
+    }
+    static constexpr int64_t smem_bytes(int m, int64_t k) {
+        return FIXED + (int64_t)stages(m, k) * STAGE_BYTES + compact_bytes(m, k);
+    }
+    static_assert(4 * MAX_STAGES + 4 <= BAR_BYTES / 8 - 4, "barrier area too small");
+    static_assert(ST_TMEM >= MAX_STAGES, "TMEM scale columns");
+    static_assert(stages(kDecodeFusedMaxM, MAX_K) >= 4, "pipeline too shallow at the largest m and K");
+    static_assert(smem_bytes(kDecodeFusedMaxM, MAX_K) <= SMEM_LIMIT, "shared memory budget");
 };
 
 struct DecodeArgs {
@@ -69,6 +85,7 @@ struct DecodeArgs {
     float static_scale;
     float* a_global_out;    // optional: the activation s_g (device), written by CTA 0
     uint16_t* out;          // bf16 [m][n]
+    int stages;             // ring depth, DecCfg::stages(m, k)
 };
 
 template <bool MX>
@@ -76,17 +93,18 @@ __global__ void __launch_bounds__(512, 1)
     decode_fused_kernel(const __grid_constant__ CUtensorMap tmW, const DecodeArgs a, const WaitCfg wc) {
     using C = DecCfg<MX>;
     extern __shared__ uint8_t smem_raw[];
+    const int NS = a.stages;
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t* sP = smem;
-    uint8_t* sQ = sP + C::STAGES * C::P_BYTES;
-    uint8_t* sSFP = sQ + C::STAGES * C::Q_BYTES;
-    uint8_t* sSFQ = sSFP + C::STAGES * C::SFP_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sSFQ + C::STAGES * C::SFQ_BYTES);
-    uint64_t* full = bars;                     // weight tile + activation tile + scales in TMEM
-    uint64_t* empty = bars + C::STAGES;        // the stage's MMAs are complete
-    uint64_t* sfull = bars + 2 * C::STAGES;    // weight scale atoms landed + activation scales written
-    uint64_t* sempty = bars + 3 * C::STAGES;   // the writers are done with the scale slot
-    uint64_t* accf = bars + 4 * C::STAGES;
+    uint8_t* sQ = sP + NS * C::P_BYTES;
+    uint8_t* sSFP = sQ + NS * C::Q_BYTES;
+    uint8_t* sSFQ = sSFP + NS * C::SFP_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sSFQ + NS * C::SFQ_BYTES);
+    uint64_t* full = bars;            // weight tile + activation tile + scales in TMEM
+    uint64_t* empty = bars + NS;      // the stage's MMAs are complete
+    uint64_t* sfull = bars + 2 * NS;  // weight scale atoms landed + activation scales written
+    uint64_t* sempty = bars + 3 * NS; // the writers are done with the scale slot
+    uint64_t* accf = bars + 4 * NS;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(accf + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
     float* s_sg = reinterpret_cast<float*>(tslot + 2);
@@ -98,8 +116,32 @@ __global__ void __launch_bounds__(512, 1)
     uint8_t* xs = xc + a.m * cb;                                      // compact scale bytes [m][sbpr]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t tile = blockIdx.x;  // 128 weight rows
+    const int64_t kbt = (a.k + 255) / 256;
+    const int64_t ksfc = kbt * C::SF_CHUNKS;  // scale atoms per 128-row tile
+
+    // The activation threads (warps 0-3, 6, 8-15) issue their loads first, so
+    // that the latency runs under the setup (the weight stream starts after
+    // it: issued first, its copies would queue these loads behind them, and
+    // a TMA issue stalls while the copy engine's queue is full, which would
+    // hold up the setup barrier).  A thread takes 8-element chunks
+    // i = ta + 416 j, and the first R rounds' chunks stay in registers for the
+    // abs-max and the quantisation (all of them for m k <= R x 416 x 8 =
+    // 39,936 elements, e.g. 8 rows of 4096).
+    constexpr int NT = 416;
+    constexpr int R = 12;
+    const bool act_warp = warp < 4 || warp == 6 || warp >= 8;
+    const int ta = warp < 4 ? warp * 32 + lane : warp == 6 ? 128 + lane : 160 + (warp - 8) * 32 + lane;
+    const uint32_t nvec = (uint32_t)((int64_t)a.m * a.k / 8);  // < 2^16 (m <= 8, k <= 8192)
+    const uint4* xv = reinterpret_cast<const uint4*>(a.x);
+    uint4 v0[R];
+    if (act_warp) {
+        pdl_wait();
+#pragma unroll
+        for (int u = 0; u < R; ++u) v0[u] = ta + u * NT < nvec ? __ldg(xv + ta + u * NT) : make_uint4(0u, 0u, 0u, 0u);
+    }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::STAGES; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(full + s, 6);   // weight producer + activation quantiser + 4 scale writers
             mbar_init(empty + s, 1);
             mbar_init(sfull + s, 2);  // weight-scale producer + activation quantiser
@@ -110,12 +152,12 @@ __global__ void __launch_bounds__(512, 1)
         fence_mbar_init();
         prefetch_tensormap(&tmW);
     }
-    // activation tiles and their scale atoms: rows >= m stay zero for the whole launch
-    for (int i = threadIdx.x; i < C::STAGES * (C::Q_BYTES + C::SFQ_BYTES) / 16; i += 512) {
-        uint4* p = i < C::STAGES * C::Q_BYTES / 16 ? reinterpret_cast<uint4*>(sQ) + i
-                                                    : reinterpret_cast<uint4*>(sSFQ) + (i - C::STAGES * C::Q_BYTES / 16);
-        *p = make_uint4(0u, 0u, 0u, 0u);
-    }
+    // The activation scale slots start zeroed: the scale bytes past K in a last
+    // partial K block, and those of rows >= m, are never written.  The operand
+    // tiles' rows >= m are left as they are: they only feed accumulator columns
+    // >= m, which nothing reads, and E2M1 codes are finite whatever the bits.
+    for (int i = threadIdx.x; i < NS * C::SFQ_BYTES / 16; i += 512)
+        reinterpret_cast<uint4*>(sSFQ)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async();  // the zeros are visible to the tensor core's reads
     if (warp == 5) {
         tmem_alloc(tslot, 512);
@@ -129,29 +171,12 @@ __global__ void __launch_bounds__(512, 1)
     // one's tail); it waits for this grid's completion before reading the output
     pdl_launch_dependents();
 
-    const int64_t tile = blockIdx.x;  // 128 weight rows
-    const int64_t kbt = (a.k + 255) / 256;
-    const int64_t ksfc = kbt * C::SF_CHUNKS;  // scale atoms per 128-row tile
-
     // ------------------------------------------------------------------
-    // The activations (warps 0-3, 6, 8-15; the weight producers and the MMA
-    // issuer go straight to their loops): abs-max and s_g, then the compact
-    // quantised copy.  A thread takes 8-element chunks i = ta + 416 j, so
-    // lanes 2l, 2l+1 (4l..4l+3) hold the chunks of one NVFP4 (MXFP4) block.
+    // The activations (the weight producers and the MMA issuer go straight to
+    // their loops): abs-max and s_g, then the compact quantised copy.  Lanes
+    // 2l, 2l+1 (4l..4l+3) hold the chunks of one NVFP4 (MXFP4) block.
     float sg = a.static_scale;
-    if (warp < 4 || warp == 6 || warp >= 8) {
-        constexpr int NT = 416;
-        const int ta = warp < 4 ? warp * 32 + lane : warp == 6 ? 128 + lane : 160 + (warp - 8) * 32 + lane;
-        pdl_wait();
-        const uint32_t nvec = (uint32_t)((int64_t)a.m * a.k / 8);  // < 2^16 (m <= 8, k <= 8192)
-        const uint4* xv = reinterpret_cast<const uint4*>(a.x);
-        // The first R rounds' chunks are loaded at once and stay in registers for
-        // both passes (all of them for m k <= R x 416 x 8 = 39,936 elements,
-        // e.g. 8 rows of 4096): one load latency instead of one per round.
-        constexpr int R = 12;
-        uint4 v0[R];
-#pragma unroll
-        for (int u = 0; u < R; ++u) v0[u] = ta + u * NT < nvec ? __ldg(xv + ta + u * NT) : make_uint4(0u, 0u, 0u, 0u);
+    if (act_warp) {
         if (!MX && a.dynamic) {
             uint32_t mx = 0;
 #pragma unroll
@@ -195,35 +220,57 @@ __global__ void __launch_bounds__(512, 1)
             const uint32_t j0 = jb + (uint32_t)lane;
             uint32_t r = j0 / cpr, c = j0 - r * cpr;  // row and chunk of round u, stepped below
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t i = j0 + u * NT;
-                // every lane takes part in the shuffles; nvec and the chunks per row are
-                // multiples of 4 (k % 32 == 0), so a block's lanes are all in or all out
-                uint32_t am = absmax8(vb[u], 0u);
-                am = max(am & 0xFFFFu, am >> 16);
-                am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
-                if (MX) am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
-                const float amax_b = __uint_as_float(am << 16);
-                uint32_t sbyte = 0, w = 0;
-                if constexpr (!MX) {
-                    sbyte = nvfp4_scale_byte(amax_b, p_t, inv_p);
-                    float f[8];
-                    unpack8(vb[u], f);
-                    w = nvfp4_word(f, dtab[sbyte]);
-                } else {
-                    float inv;
-                    sbyte = mxfp4_scale_byte(amax_b, inv);
-                    w = mxfp4_codes8(vb[u], inv);
+            for (int u2 = 0; u2 < 4; u2 += 2) {
+                // Rounds go in pairs whose arithmetic overlaps (its stores come
+                // after both); a pair that starts beyond the activations is empty
+                // for the whole warp (jb is its first chunk): few rows leave most
+                // rounds empty.
+                if (jb + (uint32_t)(u2 * NT) >= nvec) break;
+                uint32_t w[2], sbyte[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    // every lane takes part in the shuffles; nvec and the chunks per row are
+                    // multiples of 4 (k % 32 == 0), so a block's lanes are all in or all out
+                    const uint4 v = vb[u2 + h];
+                    uint32_t am = absmax8(v, 0u);
+                    am = max(am & 0xFFFFu, am >> 16);
+                    am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+                    if (MX) am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+                    const float amax_b = __uint_as_float(am << 16);
+                    if constexpr (!MX) {
+                        sbyte[h] = nvfp4_scale_byte(amax_b, p_t, inv_p);
+                        float f[8];
+                        unpack8(v, f);
+                        w[h] = nvfp4_word(f, dtab[sbyte[h]]);
+                    } else {
+                        float inv;
+                        sbyte[h] = mxfp4_scale_byte(amax_b, inv);
+                        w[h] = mxfp4_codes8(v, inv);
+                    }
                 }
-                if (i < nvec) {
-                    *reinterpret_cast<uint32_t*>(xc + (int64_t)r * cb + c * 4) = w;
-                    if ((lane & (LPB - 1)) == 0) xs[(int64_t)r * sbpr + c / LPB] = (uint8_t)sbyte;
-                }
-                r += dr;
-                c += dc;
-                if (c >= cpr) {
-                    c -= cpr;
-                    ++r;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (j0 + (uint32_t)((u2 + h) * NT) < nvec) {
+                        *reinterpret_cast<uint32_t*>(xc + (int64_t)r * cb + c * 4) = w[h];
+                        if ((lane & (LPB - 1)) == 0) xs[(int64_t)r * sbpr + c / LPB] = (uint8_t)sbyte[h];
+                        // the first NS K blocks (32 chunks each) also go straight into
+                        // their stage's operand tile and scale slot, in the layout warp 6
+                        // gives the later ones, so the first MMAs do not wait for its copy
+                        const uint32_t kbi = c >> 5, cc = c & 31;
+                        if (kbi < (uint32_t)NS) {
+                            *reinterpret_cast<uint32_t*>(sQ + kbi * (uint32_t)C::Q_BYTES + r * 128u +
+                                                         (((cc >> 2) ^ (r & 7u)) << 4) + ((cc & 3u) << 2)) = w[h];
+                            const uint32_t jblk = cc / LPB;  // scale block within the K block
+                            if ((lane & (LPB - 1)) == 0)
+                                sSFQ[kbi * C::SFQ_BYTES + (jblk >> 2) * 512 + r * 16 + (jblk & 3)] = (uint8_t)sbyte[h];
+                        }
+                    }
+                    r += dr;
+                    c += dc;
+                    if (c >= cpr) {
+                        c -= cpr;
+                        ++r;
+                    }
                 }
             }
         };
@@ -242,7 +289,15 @@ __global__ void __launch_bounds__(512, 1)
             for (int u = 0; u < 4; ++u) vb[u] = j0 + u * NT < nvec ? __ldg(xv + j0 + u * NT) : make_uint4(0u, 0u, 0u, 0u);
             convert4(vb, jb);
         }
-        named_bar_sync(1, NT);  // the compact copy is complete
+        fence_proxy_async();    // the stage tiles written above are read by the tensor core
+        named_bar_sync(1, NT);  // the compact copy (and the first NS stages' tiles) are complete
+        if (warp == 8 && lane < (kbt < NS ? (int)kbt : NS)) {
+            // the activation part of the first turn of the ring is in place: a
+            // warp that has nothing else to do until the epilogue says so, lane
+            // s for stage s
+            mbar_arrive(full + lane);
+            mbar_arrive(sfull + lane);
+        }
     }
 
     if (warp < 4) {
@@ -269,7 +324,7 @@ __global__ void __launch_bounds__(512, 1)
                 mbar_arrive(full + stage);
                 mbar_arrive(sempty + stage);
             }
-            if (++stage == C::STAGES) {
+            if (++stage == NS) {
                 stage = 0;
                 ph ^= 1u;
             }
@@ -298,7 +353,7 @@ __global__ void __launch_bounds__(512, 1)
                 }
                 issued |= 1u << stage;
                 issued_ph = (issued_ph & ~(1u << stage)) | (ph << stage);
-                if (++stage == C::STAGES) {
+                if (++stage == NS) {
                     stage = 0;
                     ph ^= 1u;
                 }
@@ -309,7 +364,7 @@ __global__ void __launch_bounds__(512, 1)
                 WaitCfg w2 = wc;
                 if (w2.limit_ns > 1000000ull) w2.limit_ns = 1000000ull;
                 volatile int never = 0;
-                for (int s = 0; s < C::STAGES; ++s)
+                for (int s = 0; s < NS; ++s)
                     if ((issued >> s) & 1u)
                         mbar_wait(is_sf ? sfull + s : full + s, (issued_ph >> s) & 1u, w2, &never);
             }
@@ -349,7 +404,7 @@ __global__ void __launch_bounds__(512, 1)
                 }
                 any = true;
                 mma_commit(empty + stage);
-                if (++stage == C::STAGES) {
+                if (++stage == NS) {
                     stage = 0;
                     ph ^= 1u;
                 }
@@ -371,10 +426,11 @@ __global__ void __launch_bounds__(512, 1)
             // 3. per K block: the m rows' codes into the stage's operand tile
             //    (row r, 16-byte piece c at piece c ^ (r % 8)), their scale
             //    bytes into the slot (block j at atom j / 4, row r, column j % 4)
+            //    from the second turn of the ring on (warp 8 signalled the first)
             constexpr int BPK = MX ? 8 : 16;  // scale blocks per K block
-            uint32_t ph = 0;
+            uint32_t ph = 1;
             int stage = 0;
-            for (int64_t kb = 0; kb < kbt; ++kb) {
+            for (int64_t kb = NS; kb < kbt; ++kb) {
                 // the stage's previous MMAs (and so the writers' reads of the slot) are done
                 if (!mbar_wait(empty + stage, ph ^ 1u, wc, abort_flag)) break;
                 const uint32_t qbase = smem_u32(sQ + stage * C::Q_BYTES);
@@ -408,7 +464,7 @@ __global__ void __launch_bounds__(512, 1)
                     mbar_arrive(full + stage);
                     mbar_arrive(sfull + stage);
                 }
-                if (++stage == C::STAGES) {
+                if (++stage == NS) {
                     stage = 0;
                     ph ^= 1u;
                 }
@@ -464,7 +520,7 @@ static cudaError_t launch_dec(const uint8_t* w_codes, const DecodeArgs& a, bool 
     using C = DecCfg<MX>;
     auto kern = decode_fused_kernel<MX>;
     static uint64_t attr_done = 0;  // devices on which this instantiation is opted in
-    if (cudaError_t e = set_smem_attr_once((const void*)kern, C::SMEM, attr_done)) return e;
+    if (cudaError_t e = set_smem_attr_once((const void*)kern, C::SMEM_LIMIT, attr_done)) return e;
     auto fn = dec_encode_fn();
     if (!fn) return cudaErrorNotSupported;
     CUtensorMap tm;
@@ -484,11 +540,12 @@ static cudaError_t launch_dec(const uint8_t* w_codes, const DecodeArgs& a, bool 
     wc.limit_ns = wait_limit_ns();
     wc.err = d->err_word;
     DecodeArgs aa = a;
+    aa.stages = C::stages(a.m, a.k);
     void* args[] = {(void*)&tm, (void*)&aa, (void*)&wc};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((a.n + 127) / 128));
     cfg.blockDim = dim3(512);
-    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.dynamicSmemBytes = (size_t)C::smem_bytes(a.m, a.k);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     if (pdl) {

@@ -248,9 +248,7 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
                 return mx ? launch_one<64, FK_MX4, EPI_PARTIAL_T>(g, s) : launch_one<64, FK_NV4, EPI_PARTIAL_T>(g, s);
             break;
         case EPI_SWIGLU:
-        case EPI_COMBINE:
         case EPI_SWIGLU_T:
-        case EPI_COMBINE_T:
         case EPI_DSLOT:
         case EPI_DSLOT_T:
             return launch_gemm_moe(g, s);
@@ -264,7 +262,6 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
 cudaError_t launch_gemm_moe(const GemmLaunch& g, cudaStream_t s) {
     if (g.fmt != FP4_NVFP4) return cudaErrorInvalidValue;
     if (g.epi == EPI_SWIGLU_T && g.bn == 32) return launch_one<32, FK_NV4, EPI_SWIGLU_T>(g, s);
-    if (g.epi == EPI_COMBINE_T && g.bn == 32) return launch_one<32, FK_NV4, EPI_COMBINE_T>(g, s);
     if (g.epi == EPI_DSLOT_T && g.bn == 32) return launch_one<32, FK_NV4, EPI_DSLOT_T>(g, s);
     if (g.epi == EPI_DSLOT) {
         if (g.bn == 128) return launch_one<128, FK_NV4, EPI_DSLOT>(g, s);
@@ -274,9 +271,6 @@ cudaError_t launch_gemm_moe(const GemmLaunch& g, cudaStream_t s) {
         if (g.bn == 256) return launch_one<256, FK_NV4, EPI_SWIGLU>(g, s);
         if (g.bn == 128) return launch_one<128, FK_NV4, EPI_SWIGLU>(g, s);
         if (g.bn == 64) return launch_one<64, FK_NV4, EPI_SWIGLU>(g, s);
-    } else {
-        if (g.bn == 128) return launch_one<128, FK_NV4, EPI_COMBINE>(g, s);
-        if (g.bn == 64) return launch_one<64, FK_NV4, EPI_COMBINE>(g, s);
     }
     set_error("no MoE GEMM instantiation for BN %d", g.bn);
     return cudaErrorInvalidValue;

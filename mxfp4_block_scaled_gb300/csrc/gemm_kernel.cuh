@@ -80,12 +80,12 @@ constexpr int kSwigluXBytes = 2 * 2 * 32 * 32 * 4;
 
 template <int EPI>
 constexpr bool epi_swapped_grouped() {
-    return EPI == EPI_SWIGLU_T || EPI == EPI_COMBINE_T || EPI == EPI_DSLOT_T;
+    return EPI == EPI_SWIGLU_T || EPI == EPI_DSLOT_T;
 }
 
 template <int EPI>
 constexpr bool epi_grouped() {
-    return EPI == EPI_SWIGLU || EPI == EPI_COMBINE || EPI == EPI_DSLOT || epi_swapped_grouped<EPI>();
+    return EPI == EPI_SWIGLU || EPI == EPI_DSLOT || epi_swapped_grouped<EPI>();
 }
 
 // Grouped GEMMs: a CTA's first kUnitTable units' (expert, end of real token
@@ -323,11 +323,6 @@ __device__ __forceinline__ uint4 rotate_words(uint4 v, uint32_t s) {
     if (s == 2) return make_uint4(v.z, v.w, v.x, v.y);
     if (s == 3) return make_uint4(v.w, v.x, v.y, v.z);
     return v;
-}
-
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
 }
 
 template <int BN, int FK, int EPI>
@@ -623,8 +618,7 @@ __global__ void __launch_bounds__(512, 1)
         constexpr int GRAN = EPI == EPI_SWIGLU ? 64 : epi_swapped_grouped<EPI>() ? 16 : 32;
         constexpr int CPW = BN / 2 > GRAN ? BN / 2 : GRAN;  // columns per warp
         constexpr int NLD = CPW / 32;
-        static_assert((EPI != EPI_COMBINE && EPI != EPI_DSLOT) || CPW <= 64,
-                      "fp32 combine keeps its columns in registers");
+        static_assert(EPI != EPI_DSLOT || CPW <= 64, "fp32 rows keep their columns in registers");
         const int qd = warp & 3;  // the TMEM lane quarter this warp may access
         const int c_begin = ((warp - 8) >> 2) * CPW;
         const bool has_cols = c_begin < BN;
@@ -635,31 +629,9 @@ __global__ void __launch_bounds__(512, 1)
         uint32_t aph = 0;
         uint32_t n_done = 0;  // units converted by this warp (EPI_SWIGLU_T buffer parity)
         for (int64_t u = blockIdx.x; u < sc.units; u += gridDim.x) {
-            // EPI_COMBINE_T: lane i of round q holds column 32 q + i's token and
-            // routing weight, fetched before the wait for the MMAs
-            constexpr int NPF = (CPW + 31) / 32;
-            int pf_tok[NPF];
-            float pf_w[NPF];
-#pragma unroll
-            for (int q = 0; q < NPF; ++q) {
-                pf_tok[q] = 0;
-                pf_w[q] = 0.0f;
-            }
             if constexpr (epi_swapped_grouped<EPI>()) {
                 const Unit wp = decode_unit<BN, EPI>(g, sc, u, ut);
                 if (wp.empty) continue;
-                if constexpr (EPI == EPI_COMBINE_T) {
-#pragma unroll
-                    for (int q = 0; q < NPF; ++q) {
-                        const int col = q * 32 + lane;
-                        const int64_t row = wp.q_row0 + c_begin + col;
-                        if (col < CPW && row < wp.vend) {
-                            const int slot = g.row_src[row];
-                            pf_tok[q] = slot / g.top_k;
-                            pf_w[q] = g.slot_weight[slot];
-                        }
-                    }
-                }
             }
             if (!mbar_wait(accf + acc, aph, wc, abort_flag)) break;
             tc_fence_after();
@@ -838,34 +810,6 @@ __global__ void __launch_bounds__(512, 1)
                     for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
                     if (lane == 0 && m) atomicMax(reinterpret_cast<unsigned int*>(g.amax_out) + w.e, m << 16);
                 }
-            } else if constexpr (EPI == EPI_COMBINE) {
-                uint32_t r[NLD][32];
-                if (has_cols) {
-#pragma unroll
-                    for (int j = 0; j < NLD; ++j) tmem_ld32(tb + j * 32, r[j]);
-                    tmem_ld_wait();
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(acce + acc);
-                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
-                const int64_t prow = w.p_row0 + qd * 32 + lane;
-                const float alpha = __fmul_rn(g.p_global[w.e], g.q_global[w.e]);
-                const bool valid = has_cols && prow < w.vend;
-                if (valid) {
-                    const int slot = g.row_src[prow];
-                    const float sc = __fmul_rn(g.slot_weight[slot], alpha);
-                    float* yrow = reinterpret_cast<float*>(g.out) + (int64_t)(slot / g.top_k) * g.ldo +
-                                  w.qt * BN + c_begin;
-#pragma unroll
-                    for (int j = 0; j < NLD; ++j)
-#pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            red_add_v4(yrow + j * 32 + 4 * v, __fmul_rn(sc, __uint_as_float(r[j][4 * v])),
-                                       __fmul_rn(sc, __uint_as_float(r[j][4 * v + 1])),
-                                       __fmul_rn(sc, __uint_as_float(r[j][4 * v + 2])),
-                                       __fmul_rn(sc, __uint_as_float(r[j][4 * v + 3])));
-                }
             } else if constexpr (EPI == EPI_DSLOT) {
                 // token rows (expert-sorted, padded): D[row][feature] = alpha * acc
                 // (fp32).  Per 32-column chunk the warp writes its 32 rows to its
@@ -979,39 +923,6 @@ __global__ void __launch_bounds__(512, 1)
                 for (int o2 = 16; o2 > 0; o2 >>= 1) amax_bits = max(amax_bits, __shfl_xor_sync(0xFFFFFFFFu, amax_bits, o2));
                 if (lane == 0 && amax_bits) atomicMax(reinterpret_cast<unsigned int*>(g.amax_out) + w.e, amax_bits << 16);
                 ++n_done;
-            } else if constexpr (EPI == EPI_COMBINE_T) {
-                // P rows are the expert's W2 rows (output features), columns the
-                // sub-tile's token rows (CPW per warpgroup):
-                // y[token][feature] += weight * alpha * acc.  (At T = 4096 with
-                // 128-token tiles this form ran 157 us against 129 us for the
-                // token-row combine: the L2 reduction rate follows elements,
-                // not requests, and scalar reductions cost 4x the instructions.)
-                static_assert(CPW % 16 == 0, "whole 16-column loads");
-                uint32_t r[CPW / 16][16];
-#pragma unroll
-                for (int c = 0; c < CPW / 16; ++c) tmem_ld16(tb + c * 16, r[c]);
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(acce + acc);
-                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
-                const float alpha = __fmul_rn(g.q_global[w.e], g.p_global[w.e]);
-                const int64_t hd = w.qt * 128 + qd * 32 + lane;
-                const int64_t vend = w.vend;
-                const int64_t row0 = w.q_row0 + c_begin;
-                float* y = reinterpret_cast<float*>(g.out) + hd;
-#pragma unroll
-                for (int q = 0; q < NPF; ++q) {
-                    const float wsc = __fmul_rn(pf_w[q], alpha);
-#pragma unroll
-                    for (int i = 0; i < 32 && q * 32 + i < CPW; ++i) {
-                        const int t_i = __shfl_sync(0xFFFFFFFFu, pf_tok[q], i);
-                        const float s_i = __shfl_sync(0xFFFFFFFFu, wsc, i);
-                        if (row0 + q * 32 + i < vend)
-                            atomicAdd(y + (int64_t)t_i * g.ldo,
-                                      __fmul_rn(s_i, __uint_as_float(r[(q * 32 + i) / 16][(q * 32 + i) % 16])));
-                    }
-                }
             }
             if (++acc == C::ACC) {
                 acc = 0;

@@ -83,12 +83,10 @@ enum Epi : int {
     EPI_BF16_T = 1,     // out[q][p] = bf16(alpha * acc)            (P = weights, swap-AB)
     EPI_PARTIAL_T = 2,  // part[split][q][p] = acc (fp32, alpha applied by the reduction)
     EPI_SWIGLU = 3,     // grouped: h[p][f] = bf16(SiLU(gate) * up), amax per expert
-    EPI_COMBINE = 4,    // grouped: y[token][q] += weight * alpha * acc (fp32 atomics)
     EPI_PARTIAL = 5,    // part[split][p][q] = acc (fp32, P = activations; alpha applied by the reduction)
     // grouped with the operands swapped (P = an expert's weight rows, Q = 32-row
     // tiles of its tokens), for a few tokens per expert:
     EPI_SWIGLU_T = 6,   // h[q][f] = bf16(SiLU(gate) * up), amax per expert
-    EPI_COMBINE_T = 7,  // y[token of q][p] += weight * alpha * acc (fp32 reductions)
     // grouped GEMM2 outputs per routing slot (token * top_k + j), fp32, summed
     // in slot order by a separate combine (same bits every run):
     EPI_DSLOT = 8,      // d[p][q] = alpha * acc (fp32, TMA stores; P = expert-sorted token rows)
@@ -116,14 +114,14 @@ struct GemmLaunch {
     const float* p_global = nullptr;  // NVFP4 global scale(s) of P (per expert when grouped && p_global_per_expert)
     const float* q_global = nullptr;  // NVFP4 global scale(s) of Q (per expert when grouped)
     bool p_global_per_expert = false;
-    bool q_global_per_expert = false;  // EPI_SWIGLU_T / EPI_COMBINE_T: Q (tokens) scale per expert
+    bool q_global_per_expert = false;  // EPI_SWIGLU_T / EPI_DSLOT_T: Q (tokens) scale per expert
     // output
     void* out = nullptr;
     int64_t ldo = 0;
     int64_t p_rows_valid = 0;     // rows of P that are real (dense)
     int splits = 1;
     // grouped (MoE).  The token side is the P operand, or the Q operand with
-    // the swapped epilogues (EPI_SWIGLU_T, EPI_COMBINE_T: P = weights, whose
+    // the swapped epilogues (EPI_SWIGLU_T, EPI_DSLOT_T: P = weights, whose
     // per-expert row count is p_rows_valid); the tables below always describe
     // the token rows, in 128-row tiles.
     bool grouped = false;
@@ -131,9 +129,6 @@ struct GemmLaunch {
     const int32_t* tile_expert = nullptr;   // expert of each 128-row token tile
     const int32_t* n_ptiles_dev = nullptr;  // number of token tiles (device)
     const int32_t* row_valid_end = nullptr; // per token tile: first padded row index (exclusive end of real rows)
-    const int32_t* row_src = nullptr;       // EPI_COMBINE(_T): source slot (token*k + j) of each token row
-    const float* slot_weight = nullptr;     // EPI_COMBINE: routing weight of each slot
-    int top_k = 0;
     float* amax_out = nullptr;              // EPI_SWIGLU: per-expert amax of h (as uint bits, atomicMax)
     int max_ctas = 0;                       // 0 = one per SM
     bool pdl = false;
@@ -157,10 +152,10 @@ int64_t gemm_k_blocks(int64_t k);  // K blocks of the one-CTA GEMM
 // weight rows, bf16 out [m][n].
 constexpr int kDecodeFusedMaxM = 8;
 // rows up to which the automatic policy takes the fused kernel: on the
-// 14336 x 4096 decode it is 4.3 / 2.0 us faster at m = 1 / 4 than the quantise
-// + GEMM launches, and 0.4 us slower at m = 8 (the in-kernel quantisation of
-// every row by every CTA grows with m)
-constexpr int kDecodeFusedAutoMaxM = 6;
+// 14336 x 4096 decode it is faster than the quantise + GEMM launches at every
+// m <= 8 (about 5 us at m = 1, 2 us at m = 8); the in-kernel quantisation of
+// every row by every CTA grows with m, so more rows go to the launch chain
+constexpr int kDecodeFusedAutoMaxM = 8;
 constexpr int64_t kDecodeFusedMaxK = 8192;
 cudaError_t launch_decode_fused(int fmt, const uint16_t* x, int m, int64_t n, int64_t k, const uint8_t* w_codes,
                                 const uint8_t* w_scales, const float* w_global, int dynamic, float static_scale,

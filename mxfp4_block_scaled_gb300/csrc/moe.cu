@@ -1292,9 +1292,6 @@ static fp4_status moe_run(const void* hidden, const float* logits, int64_t T, in
         g.tile_expert = tile_expert;
         g.n_ptiles_dev = n_ptiles;
         g.row_valid_end = row_valid_end;
-        g.row_src = row_src;
-        g.slot_weight = wts;
-        g.top_k = (int)k;
         g.pdl = pdl;
         MOE_CUDA(launch_gemm(g, s), "GEMM2 launch");
         const float4* d4 = reinterpret_cast<const float4*>(y);

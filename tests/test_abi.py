@@ -169,13 +169,15 @@ def test_plan_prefill_tile_width(F):
 
 def test_plan_decode_split_and_fused(F):
     p = F.plan_gemm(8, 14336, 4096, SMS)
-    assert p["small_m"] and p["bn"] == 32 and p["splits"] == 1 and not p["fused_decode"]  # 112 tiles >= 76
+    assert p["small_m"] and p["bn"] == 32 and p["splits"] == 1 and p["fused_decode"]  # 112 tiles >= 76
+    p = F.plan_gemm(9, 14336, 4096, SMS)  # the launch chain's swapped GEMM, whole K per tile
+    assert p["small_m"] and p["bn"] == 32 and p["splits"] == 1 and not p["fused_decode"]
     assert F.plan_gemm(40, 14336, 4096, SMS)["bn"] == 64
     # 32 weight tiles are split along K: ceil(3 x 152 / 32) = 15, at most half the 16 K blocks -> 8
     assert F.plan_gemm(8, 4096, 4096, SMS)["splits"] == 8
-    assert F.plan_gemm(1, 14336, 4096, SMS)["fused_decode"]          # m <= 6 and tiles for half the SMs
+    assert F.plan_gemm(1, 14336, 4096, SMS)["fused_decode"]          # m <= 8 and tiles for half the SMs
     assert not F.plan_gemm(1, 4096, 4096, SMS)["fused_decode"]       # 32 tiles < 76
-    assert not F.plan_gemm(7, 14336, 4096, SMS)["fused_decode"]      # above the automatic m limit
+    assert not F.plan_gemm(9, 14336, 4096, SMS)["fused_decode"]      # above the fused kernel's m limit
     assert not F.plan_gemm(1, 14336, 8192 + 32, SMS)["fused_decode"]  # k above the fused kernel's limit
 
 
