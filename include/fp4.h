@@ -115,10 +115,13 @@ void fp4_set_arch_override(int sm);
  * n >= 256; 3 = the fused decode kernel for every fp4_gemm with m <= 8 and
  * k <= 8192; 4 = fp4_gemm_w4a16 always on its tensor-core kernel (policy 0
  * takes it for m >= 3 when the weight's 128-row tiles fill at least half the
- * SMs, else the CUDA-core kernel).
+ * SMs, else the CUDA-core kernel); 5 = for m > 64 with 256-wide tiles, an
+ * even number of 128-row activation tiles and a pair unit for every cluster,
+ * the one-CTA kernel in clusters of two CTAs whose two activation tiles share
+ * each 256-row weight tile (each CTA multicasts one half of it into both).
  * Process-wide, host-side; results agree within the GEMM tolerance under every
  * policy (codes and scales are identical).
- * FP4_ERR_INVALID_ARG for a value outside 0..4 (the policy is unchanged). */
+ * FP4_ERR_INVALID_ARG for a value outside 0..5 (the policy is unchanged). */
 fp4_status fp4_set_gemm_tile_policy(int policy);
 
 /* Tuning and test hook (no counterpart on the pages): which implementation
@@ -137,7 +140,8 @@ fp4_status fp4_set_moe_policy(int policy);
  * `sm_count` SMs under the current tile policy.  out[0] = 1 for the
  * small-m (swapped-operand) path, out[1] = the tile width on the MMA's N side,
  * out[2] = the number of K splits, out[3] = 1 for the CTA-pair kernel,
- * out[4] = 1 when fp4_gemm takes the fused decode kernel.  max_out >= 5. */
+ * out[4] = 1 when fp4_gemm takes the fused decode kernel, and (max_out >= 6)
+ * out[5] = 1 for the weight-tile-sharing CTA pairs.  max_out >= 5. */
 fp4_status fp4_debug_plan_gemm(int64_t m, int64_t n, int64_t k, int sm_count, int64_t* out, int max_out);
 
 /* Test hook for failure detection: launches one tiny kernel whose thread waits

@@ -188,7 +188,7 @@ extern "C" size_t fp4_scales_bytes(int fmt, int64_t rows, int64_t k) {
 extern "C" void fp4_set_arch_override(int sm) { g_arch_override = sm; }
 
 extern "C" fp4_status fp4_set_gemm_tile_policy(int policy) {
-    CHECK_OR_RETURN(policy >= 0 && policy <= 4, FP4_ERR_INVALID_ARG, "tile policy %d not in 0..4", policy);
+    CHECK_OR_RETURN(policy >= 0 && policy <= 5, FP4_ERR_INVALID_ARG, "tile policy %d not in 0..5", policy);
     g_tile_policy = policy;
     return FP4_OK;
 }
@@ -307,6 +307,7 @@ static const int64_t kDecodeMaxM = 64;
 struct GemmPlan {
     bool decode;
     bool pair;  // CTA-pair kernel (256 x 256 tiles)
+    bool mc;    // one-CTA kernel in clusters of two sharing each 256-row weight tile (TMA multicast)
     int bn;
     int splits;
 };
@@ -314,6 +315,7 @@ struct GemmPlan {
 static GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int sms) {
     GemmPlan p;
     p.pair = false;
+    p.mc = false;
     const int64_t kbt = gemm_k_blocks(k);
     if (m <= kDecodeMaxM) {
         // decode, swap-AB: the weights are the MMA's M side (128-row tiles), the
@@ -343,12 +345,16 @@ static GemmPlan plan_gemm(int64_t m, int64_t n, int64_t k, int sms) {
         const int64_t w128 = (((m + 127) / 128) * ((n + 127) / 128) + sms - 1) / sms;
         p.bn = 3 * w256 <= 2 * w128 ? 256 : 128;
         p.splits = 1;
-        // The CTA-pair kernel is opt-in: on the 8192 x 14336 x 4096 prefill its
-        // copies (operand tiles and scale atoms alike) take about 8k cycles to
-        // land inside its main loop against well under 1k for the same copies
-        // streamed alone, the MMA issuer idles three quarters of the time, and
-        // it runs 2.4x slower than the one-CTA kernel.
+        // The CTA-pair kernel is opt-in: on the 8192 x 14336 x 4096 prefill it
+        // runs within a few percent of the one-CTA kernel (151-157 against
+        // 156-159 us), since each SM's tensor core still takes in the peer's
+        // half of the 256-wide operand tile, so an SM's operand stream per K
+        // block barely shrinks.
         p.pair = g_tile_policy == 2 && m >= 256 && n >= 256;
+        // weight-tile sharing pairs: 256-wide tiles, whole pairs of 128-row
+        // activation tiles, and enough pair units for every cluster
+        const int64_t mt = (m + 127) / 128;
+        p.mc = g_tile_policy == 5 && p.bn == 256 && mt % 2 == 0 && (mt / 2) * ((n + 255) / 256) >= sms / 2;
     }
     return p;
 }
@@ -372,6 +378,7 @@ extern "C" fp4_status fp4_debug_plan_gemm(int64_t m, int64_t n, int64_t k, int s
     out[2] = p.splits;
     out[3] = p.pair ? 1 : 0;
     out[4] = use_fused_decode(m, n, k, sm_count) ? 1 : 0;
+    if (max_out >= 6) out[5] = p.mc ? 1 : 0;
     return FP4_OK;
 }
 
@@ -434,6 +441,7 @@ static fp4_status enqueue_gemm(int fmt, const uint8_t* ac, const uint8_t* as, co
         g.out = out;
         g.ldo = n;
         g.early_q = true;  // weights
+        g.mc = p.mc;
         if (p.pair) return cuda_status(launch_gemm_pair(g, s), "GEMM launch");
         return cuda_status(launch_gemm(g, s), "GEMM launch");
     }

@@ -250,6 +250,19 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* ba
         : "memory");
 }
 
+// 2-D tiled load multicast to every CTA of cta_mask in the cluster: the box
+// lands at the same shared offset `dst` in each of them and its bytes are
+// counted on the mbarrier at the same offset `bar` in each (this GPU's own
+// memory only).
+__device__ __forceinline__ void tma_load_2d_mc(const CUtensorMap* map, uint64_t* bar, void* dst, int32_t c0, int32_t c1,
+                                               uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
+        "[%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(cta_mask)
+        : "memory");
+}
+
 // 2-D tiled load into this CTA's smem whose bytes are counted on an mbarrier
 // in either CTA of the CTA pair (`bar_cluster`: shared::cluster address, e.g.
 // from mapa_shared), so one CTA can wait for both CTAs' operand tiles.
@@ -452,6 +465,17 @@ __device__ __forceinline__ void mma_mxf4_pair(uint32_t d_tmem, uint64_t adesc, u
 __device__ __forceinline__ void mma_commit_pair_mc(uint64_t* bar, uint16_t cta_mask) {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+// Arrive (once each) on the mbarrier at this shared offset in every CTA of
+// cta_mask, when all previously issued tcgen05 ops of this (one-CTA) MMA
+// thread completed.
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
             smem_u32(bar)),
         "h"(cta_mask)
         : "memory");

@@ -77,16 +77,17 @@ static bool make_f32_out_map(CUtensorMap* m, void* base, int64_t rows, int64_t c
 
 int64_t gemm_k_blocks(int64_t k) { return (k + 2 * GEMM_KB_BYTES - 1) / (2 * GEMM_KB_BYTES); }
 
-template <int BN, int FK, int EPI>
+template <int BN, int FK, int EPI, bool MC = false>
 static cudaError_t launch_one(const GemmLaunch& g, cudaStream_t s) {
     using C = GemmCfg<BN, FK, epi_staging_bytes<EPI, FK>()>;
-    auto kern = gemm_kernel<BN, FK, EPI>;
+    auto kern = gemm_kernel<BN, FK, EPI, MC>;
     static uint64_t attr_done = 0;  // devices on which this instantiation is opted in
     if (cudaError_t e = set_smem_attr_once((const void*)kern, C::SMEM, attr_done)) return e;
     CUtensorMap tmP, tmQ, tmO;
     const int64_t row_bytes = g.k / fk_elems_per_byte<FK>();
+    // a CTA pair loads the Q tile in halves (one multicast each)
     if (!make_codes_map(&tmP, g.p_codes, g.p_rows, row_bytes, 128, GEMM_KB_BYTES) ||
-        !make_codes_map(&tmQ, g.q_codes, g.q_rows, row_bytes, BN, GEMM_KB_BYTES)) {
+        !make_codes_map(&tmQ, g.q_codes, g.q_rows, row_bytes, MC ? BN / 2 : BN, GEMM_KB_BYTES)) {
         set_error("cuTensorMapEncodeTiled failed (rows %lld/%lld, k %lld)", (long long)g.p_rows, (long long)g.q_rows,
                   (long long)g.k);
         return cudaErrorInvalidValue;
@@ -121,25 +122,53 @@ static cudaError_t launch_one(const GemmLaunch& g, cudaStream_t s) {
     }
     int64_t grid = d->sm_count;
     if (g.max_ctas > 0 && g.max_ctas < grid) grid = g.max_ctas;
-    if (units < grid) grid = units;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(512);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (MC) {
+        // pairs of CTAs (units are pairs of P tiles): as many clusters of two
+        // as can be resident at once
+        static int max_clusters[64];
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 2;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+        cfg.attrs = attr;
+        cfg.numAttrs = na;
+        if (max_clusters[d->device] == 0) {
+            cfg.gridDim = dim3((unsigned)(d->sm_count & ~1));
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, (const void*)kern, &cfg) != cudaSuccess || n < 1) {
+                cudaGetLastError();
+                n = d->sm_count / 2;
+            }
+            max_clusters[d->device] = n;
+        }
+        int64_t clusters = grid / 2 < max_clusters[d->device] ? grid / 2 : max_clusters[d->device];
+        const int64_t pair_units = units / 2;
+        if (pair_units < clusters) clusters = pair_units;
+        grid = 2 * clusters;
+    } else if (units < grid) {
+        grid = units;
+    }
     if (grid < 1) return cudaSuccess;
     WaitCfg wc;
     wc.limit_ns = wait_limit_ns();
     wc.err = d->err_word;
     GemmLaunch gg = g;
     void* args[] = {(void*)&tmP, (void*)&tmQ, (void*)&tmO, (void*)&gg, (void*)&wc};
-    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(512);
-    cfg.dynamicSmemBytes = C::SMEM;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
     if (g.pdl) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
     }
+    cfg.attrs = na ? attr : nullptr;
+    cfg.numAttrs = na;
     return cudaLaunchKernelExC(&cfg, (const void*)kern, args);
 }
 
@@ -224,6 +253,8 @@ cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
     const bool mx = g.fmt == FP4_MXFP4;
     switch (g.epi) {
         case EPI_BF16:
+            if (g.bn == 256 && g.mc && !g.grouped && g.splits == 1 && ((g.p_rows_valid + 127) / 128) % 2 == 0)
+                return mx ? launch_one<256, FK_MX4, EPI_BF16, true>(g, s) : launch_one<256, FK_NV4, EPI_BF16, true>(g, s);
             if (g.bn == 256)
                 return mx ? launch_one<256, FK_MX4, EPI_BF16>(g, s) : launch_one<256, FK_NV4, EPI_BF16>(g, s);
             if (g.bn == 128)

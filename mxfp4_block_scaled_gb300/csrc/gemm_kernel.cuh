@@ -178,7 +178,9 @@ struct Sched {
 // sub-tile run together and find it in L2) and sub-tile slowest: with a few
 // tokens per expert the later sub-tiles are empty, so the units with work come
 // first and the grid stride spreads them evenly over the CTAs.
-template <int BN, int EPI, int KB_ELEMS>
+// MC (CTA pairs sharing the Q tile, dense only): the P tiles go in pairs, so
+// n_ptiles counts pairs of 128-row tiles (the launch makes the count even).
+template <int BN, int EPI, int KB_ELEMS, bool MC = false>
 __device__ __forceinline__ Sched make_sched(const GemmLaunch& g) {
     Sched s;
     s.kbt = (g.k + KB_ELEMS - 1) / KB_ELEMS;
@@ -192,6 +194,7 @@ __device__ __forceinline__ Sched make_sched(const GemmLaunch& g) {
         s.units = s.n_ptiles * subs * s.n_qtiles;
     } else {
         s.n_ptiles = epi_grouped<EPI>() ? (int64_t)(*g.n_ptiles_dev) : (g.p_rows_valid + 127) / 128;
+        if (MC) s.n_ptiles /= 2;
         s.n_qtiles = (g.q_rows_valid + BN - 1) / BN;
         s.units = s.n_ptiles * s.n_qtiles * g.splits;
     }
@@ -212,9 +215,9 @@ __device__ __forceinline__ void unit_tile_info(const GemmLaunch& g, const int32_
     }
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool MC = false>
 __device__ __forceinline__ Unit decode_unit(const GemmLaunch& g, const Sched& sc, int64_t u,
-                                            const int32_t* ut = nullptr) {
+                                            const int32_t* ut = nullptr, uint32_t prank = 0) {
     Unit w;
     w.empty = false;
     w.vend = 0;
@@ -236,6 +239,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmLaunch& g, const Sched& sc
     const int64_t r = u / sc.splits;
     w.pt = r % sc.n_ptiles;
     w.qt = r / sc.n_ptiles;
+    if (MC) w.pt = 2 * w.pt + prank;  // the pair's tile of this CTA
     w.e = 0;
     if constexpr (epi_grouped<EPI>()) unit_tile_info(g, ut, u, w.pt, w.e, w.vend);
     w.p_row0 = w.pt * 128;
@@ -325,13 +329,26 @@ __device__ __forceinline__ uint4 rotate_words(uint4 v, uint32_t s) {
     return v;
 }
 
-template <int BN, int FK, int EPI>
+// MC: clusters of two CTAs that take the two 128-row P tiles of a pair with
+// the same Q tile; each CTA loads one half of the Q tile with a TMA multicast
+// into both CTAs' stage (tmQ's box is BN / 2 rows), and each CTA's MMA commit
+// frees the stage in both (`empty` counts the two), so a stage is rewritten
+// only when both CTAs are done with it.  The L2 sends each Q tile out once
+// per pair: per K block a CTA draws 16 KB of P, 16 KB of Q and its scale atoms
+// from the L2 instead of 16 + 32 KB.
+template <int BN, int FK, int EPI, bool MC = false>
 __global__ void __launch_bounds__(512, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ,
                 const __grid_constant__ CUtensorMap tmO, const GemmLaunch g, const WaitCfg wc) {
     using C = GemmCfg<BN, FK, epi_staging_bytes<EPI, FK>()>;
     constexpr bool MX = fk_ue8m0<FK>();  // no global scales
     static_assert(EPI != EPI_BF16 || BN >= 128, "the staged bf16 epilogue stores 64-column boxes");
+    static_assert(!MC || (EPI == EPI_BF16 && BN == 256), "CTA pairs: dense bf16 epilogue, 256-wide tiles");
+    // units: a CTA takes every ustep-th unit from ucta on; a pair takes the
+    // same units, each CTA its tile (prank) of the unit's pair of P tiles
+    const uint32_t prank = MC ? cluster_ctarank() : 0u;
+    const int64_t ucta = MC ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;
+    const int64_t ustep = MC ? (int64_t)(gridDim.x >> 1) : (int64_t)gridDim.x;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t* sP = smem;
@@ -354,7 +371,7 @@ __global__ void __launch_bounds__(512, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(full + s, 6);  // two operand producers + four scale writers
-            mbar_init(empty + s, 1);
+            mbar_init(empty + s, MC ? 2 : 1);  // the MMA commit (of each CTA of a pair)
         }
         for (int s = 0; s < C::SSLOTS; ++s) {
             mbar_init(sfull + s, 1);
@@ -376,7 +393,12 @@ __global__ void __launch_bounds__(512, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    // a pair's barriers are initialised before either CTA's copies or commits
+    // can reach the other
+    if (MC)
+        cluster_sync();
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
     // the next kernel may be scheduled now: it waits for this grid's completion
@@ -388,7 +410,7 @@ __global__ void __launch_bounds__(512, 1)
     // just before its first read of their outputs (the weight producer not at
     // all when early_p / early_q marks its operand).
     if (g.grouped) pdl_wait();
-    const Sched sc = make_sched<BN, EPI, C::KB_ELEMS>(g);
+    const Sched sc = make_sched<BN, EPI, C::KB_ELEMS, MC>(g);
     const int32_t* ut = nullptr;  // grouped: this CTA's unit table (expert, real-row end)
     if constexpr (epi_grouped<EPI>()) {
         int32_t* t = reinterpret_cast<int32_t*>(sStg + epi_staging_bytes<EPI, FK>() - kUnitTableBytes);
@@ -419,8 +441,8 @@ __global__ void __launch_bounds__(512, 1)
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         int stage = 0, slot = 0;  // operand stage (TMEM scale columns), scale ring slot
         uint32_t ph = 0, sph = 0;
-        for (int64_t u = blockIdx.x; u < sc.units; u += gridDim.x) {
-            const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
+        for (int64_t u = ucta; u < sc.units; u += ustep) {
+            const Unit w = decode_unit<BN, EPI, MC>(g, sc, u, ut, prank);
             if (w.empty) continue;
             // A Q tile narrower than 128 rows uses 32-row group(s) q_sub.. of each
             // scale atom; the words are rotated so those groups sit at column 0
@@ -483,8 +505,8 @@ __global__ void __launch_bounds__(512, 1)
             uint32_t ph = 0;
             uint32_t issued = 0, issued_ph = 0;  // per-stage bits: a copy was issued / its phase parity
             bool ok = true;
-            for (int64_t u = blockIdx.x; u < sc.units && ok; u += gridDim.x) {
-                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
+            for (int64_t u = ucta; u < sc.units && ok; u += ustep) {
+                const Unit w = decode_unit<BN, EPI, MC>(g, sc, u, ut, prank);
                 if (w.empty) continue;
                 const uint8_t* sfp = g.p_scales + (w.p_row0 >> 7) * ksfc * 512;
                 const int64_t qc0 = w.q_row0 >> 7;
@@ -509,6 +531,13 @@ __global__ void __launch_bounds__(512, 1)
                         mbar_arrive_expect_tx(full + stage, C::P_BYTES);
                         tma_load_2d(&tmP, full + stage, sP + stage * C::P_BYTES, (int32_t)(kb * C::KB_BYTES),
                                     (int32_t)w.p_row0);
+                    } else if (MC) {
+                        // this CTA's half of the Q tile into both CTAs' stage; the
+                        // other half comes from the other CTA
+                        mbar_arrive_expect_tx(full + stage, C::Q_BYTES);
+                        tma_load_2d_mc(&tmQ, full + stage, sQ + stage * C::Q_BYTES + prank * (C::Q_BYTES / 2),
+                                       (int32_t)(kb * C::KB_BYTES), (int32_t)(w.q_row0 + prank * (BN / 2)),
+                                       (uint16_t)3);
                     } else {
                         mbar_arrive_expect_tx(full + stage, C::Q_BYTES);
                         tma_load_2d(&tmQ, full + stage, sQ + stage * C::Q_BYTES, (int32_t)(kb * C::KB_BYTES),
@@ -532,6 +561,9 @@ __global__ void __launch_bounds__(512, 1)
                 volatile int never = 0;
                 for (int s = 0; s < nst; ++s)
                     if ((issued >> s) & 1u) mbar_wait(fb + s, (issued_ph >> s) & 1u, w2, &never);
+                // a pair: the other CTA's multicast halves may still be landing
+                // here (this CTA's barriers count them only with its own half)
+                if (MC) spin_ns(200000);
             }
         }
     } else if (warp == 5) {
@@ -544,8 +576,8 @@ __global__ void __launch_bounds__(512, 1)
             int acc = 0;
             uint32_t aph = 0;
             bool ok = true, any = false;
-            for (int64_t u = blockIdx.x; u < sc.units && ok; u += gridDim.x) {
-                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
+            for (int64_t u = ucta; u < sc.units && ok; u += ustep) {
+                const Unit w = decode_unit<BN, EPI, MC>(g, sc, u, ut, prank);
                 if (w.empty) continue;
                 if (!mbar_wait(acce + acc, aph ^ 1u, wc, abort_flag)) {
                     ok = false;
@@ -589,7 +621,10 @@ __global__ void __launch_bounds__(512, 1)
                             mma_mxf4<MX>(d_tmem, ad, bd, id, sfa, sfb, acc_in);
                     }
                     any = true;
-                    mma_commit(empty + stage);
+                    if (MC)
+                        mma_commit_mc(empty + stage, (uint16_t)3);  // frees the stage in both CTAs
+                    else
+                        mma_commit(empty + stage);
                     if (++stage == C::STAGES) {
                         stage = 0;
                         ph ^= 1u;
@@ -628,9 +663,9 @@ __global__ void __launch_bounds__(512, 1)
         int acc = 0;
         uint32_t aph = 0;
         uint32_t n_done = 0;  // units converted by this warp (EPI_SWIGLU_T buffer parity)
-        for (int64_t u = blockIdx.x; u < sc.units; u += gridDim.x) {
+        for (int64_t u = ucta; u < sc.units; u += ustep) {
             if constexpr (epi_swapped_grouped<EPI>()) {
-                const Unit wp = decode_unit<BN, EPI>(g, sc, u, ut);
+                const Unit wp = decode_unit<BN, EPI, MC>(g, sc, u, ut, prank);
                 if (wp.empty) continue;
             }
             if (!mbar_wait(accf + acc, aph, wc, abort_flag)) break;
@@ -666,7 +701,7 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce + acc);
-                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
+                const Unit w = decode_unit<BN, EPI, MC>(g, sc, u, ut, prank);
                 constexpr int BOXC = epi_box_cols<FK>();
                 epi_store_bf16<NLD, BOXC>(&tmO, smem_u32(sStg) + (uint32_t)(wg * epi_buffer_bytes<BOXC>()), pk, qd, lane,
                                     1u + (uint32_t)wg, w.qt * BN + c_begin, w.p_row0, g.q_rows_valid,
@@ -681,7 +716,7 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce + acc);
-                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
+                const Unit w = decode_unit<BN, EPI, MC>(g, sc, u, ut, prank);
                 const int64_t prow = w.p_row0 + qd * 32 + lane;
                 const float alpha = MX ? 1.0f : __fmul_rn(g.p_global[0], g.q_global[0]);
                 if (has_cols && prow < g.p_rows_valid) {
@@ -713,7 +748,7 @@ __global__ void __launch_bounds__(512, 1)
             } else if constexpr (EPI == EPI_PARTIAL) {
                 // split-K partials, row-major; only the warps holding real rows
                 // read TMEM (for decode-sized M that is one lane quarter)
-                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
+                const Unit w = decode_unit<BN, EPI, MC>(g, sc, u, ut, prank);
                 const int64_t row0 = w.p_row0 + qd * 32;
                 const bool any_rows = has_cols && row0 < g.p_rows_valid;
                 const int64_t prow = row0 + lane;
@@ -745,7 +780,7 @@ __global__ void __launch_bounds__(512, 1)
             } else if constexpr (EPI == EPI_SWIGLU) {
                 // Q rows are W13 rows interleaved in groups of 32 (gate, up, gate, up, ...):
                 // columns [c, c+32) are gate and [c+32, c+64) up for the same 32 features.
-                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
+                const Unit w = decode_unit<BN, EPI, MC>(g, sc, u, ut, prank);
                 const int64_t prow = w.p_row0 + qd * 32 + lane;
                 const float alpha =
                     __fmul_rn(g.p_global_per_expert ? g.p_global[w.e] : g.p_global[0], g.q_global[w.e]);
@@ -825,7 +860,7 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce + acc);
-                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
+                const Unit w = decode_unit<BN, EPI, MC>(g, sc, u, ut, prank);
                 const int64_t prow0 = w.p_row0 + qd * 32;
                 const float alpha = __fmul_rn(g.p_global[w.e], g.q_global[w.e]);
                 const uint32_t xs = smem_u32(sStg) + (uint32_t)(warp - 8) * 4096u;
@@ -862,7 +897,7 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce + acc);
-                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
+                const Unit w = decode_unit<BN, EPI, MC>(g, sc, u, ut, prank);
                 const float alpha = __fmul_rn(g.q_global[w.e], g.p_global[w.e]);
                 const int64_t hd = w.qt * 128 + qd * 32 + lane;
                 const int64_t vend = w.vend;
@@ -886,7 +921,7 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce + acc);
-                const Unit w = decode_unit<BN, EPI>(g, sc, u, ut);
+                const Unit w = decode_unit<BN, EPI, MC>(g, sc, u, ut, prank);
                 const float alpha = __fmul_rn(g.q_global[g.q_global_per_expert ? w.e : 0], g.p_global[w.e]);
                 const int pair = qd >> 1, half = wg;
                 const bool is_gate = (qd & 1) == 0;
@@ -938,6 +973,9 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    // a pair: neither CTA leaves while the other's copies or commits can
+    // still reach its shared memory
+    if (MC) cluster_sync();
 }
 
 }  // namespace fp4

@@ -131,6 +131,8 @@ struct GemmLaunch {
     const int32_t* row_valid_end = nullptr; // per token tile: first padded row index (exclusive end of real rows)
     float* amax_out = nullptr;              // EPI_SWIGLU: per-expert amax of h (as uint bits, atomicMax)
     int max_ctas = 0;                       // 0 = one per SM
+    bool mc = false;                        // dense EPI_BF16, bn 256, an even number of 128-row P tiles:
+                                            // clusters of two CTAs sharing each Q tile (TMA multicast)
     bool pdl = false;
     // Operand tiles that do not depend on the preceding kernel (the weights):
     // their producer starts loading before the programmatic-dependency wait,

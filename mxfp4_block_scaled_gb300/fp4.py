@@ -280,19 +280,21 @@ def gemm_w4a16(x, wq, out=None, stream=None):
     return out
 
 
-TILE_AUTO, TILE_ONE_CTA, TILE_CTA_PAIR, TILE_FUSED_DECODE, TILE_W4A16_TC = 0, 1, 2, 3, 4
+TILE_AUTO, TILE_ONE_CTA, TILE_CTA_PAIR, TILE_FUSED_DECODE, TILE_W4A16_TC, TILE_WEIGHT_PAIRS = 0, 1, 2, 3, 4, 5
 
 
 def set_gemm_tile_policy(policy):
-    """Choose the GEMM kernels (TILE_AUTO, TILE_ONE_CTA, TILE_CTA_PAIR, TILE_FUSED_DECODE, TILE_W4A16_TC)."""
+    """Choose the GEMM kernels (TILE_AUTO, TILE_ONE_CTA, TILE_CTA_PAIR, TILE_FUSED_DECODE, TILE_W4A16_TC,
+    TILE_WEIGHT_PAIRS)."""
     _check(lib().fp4_set_gemm_tile_policy(int(policy)))
 
 
 def plan_gemm(m, n, k, sm_count):
     """The GEMM plan for m x n x k on `sm_count` SMs (host-side query)."""
-    out = (ctypes.c_int64 * 5)()
-    _check(lib().fp4_debug_plan_gemm(m, n, k, sm_count, out, 5))
-    return {"small_m": bool(out[0]), "bn": out[1], "splits": out[2], "pair": bool(out[3]), "fused_decode": bool(out[4])}
+    out = (ctypes.c_int64 * 6)()
+    _check(lib().fp4_debug_plan_gemm(m, n, k, sm_count, out, 6))
+    return {"small_m": bool(out[0]), "bn": out[1], "splits": out[2], "pair": bool(out[3]), "fused_decode": bool(out[4]),
+            "weight_pairs": bool(out[5])}
 
 
 def device_status(stream=None):

@@ -143,9 +143,9 @@ def test_python_wrapper_raises(F):
 
 def test_tile_policy_validation(F):
     L = F.lib()
-    for p in (F.TILE_ONE_CTA, F.TILE_CTA_PAIR, F.TILE_FUSED_DECODE, F.TILE_W4A16_TC, F.TILE_AUTO):
+    for p in (F.TILE_ONE_CTA, F.TILE_CTA_PAIR, F.TILE_FUSED_DECODE, F.TILE_W4A16_TC, F.TILE_WEIGHT_PAIRS, F.TILE_AUTO):
         assert L.fp4_set_gemm_tile_policy(p) == 0
-    for bad in (-1, 5):
+    for bad in (-1, 6):
         assert L.fp4_set_gemm_tile_policy(bad) == F.STATUS_CODE["FP4_ERR_INVALID_ARG"]
         assert "tile policy" in L.fp4_last_error_message().decode()
     with pytest.raises(F.FP4Error):
@@ -160,7 +160,7 @@ SMS = 152  # GB300
 def test_plan_prefill_tile_width(F):
     """256-wide tiles when 1.5 x their waves do not exceed the 128-wide waves."""
     assert F.plan_gemm(8192, 14336, 4096, SMS) == {"small_m": False, "bn": 256, "splits": 1, "pair": False,
-                                                    "fused_decode": False}
+                                                    "fused_decode": False, "weight_pairs": False}
     assert F.plan_gemm(8192, 4096, 4096, SMS)["bn"] == 256    # 7 waves of 256 against 14 of 128
     assert F.plan_gemm(2048, 2048, 7168, SMS)["bn"] == 256    # one wave of 128 tiles against 1.7 waves
     assert F.plan_gemm(256, 512, 512, SMS)["bn"] == 128       # one wave either way
@@ -191,6 +191,12 @@ def test_plan_follows_the_tile_policy(F):
         assert not F.plan_gemm(128, 14336, 4096, SMS)["pair"]
         F.set_gemm_tile_policy(F.TILE_ONE_CTA)
         assert not F.plan_gemm(1, 14336, 4096, SMS)["fused_decode"]
+        assert not F.plan_gemm(8192, 14336, 4096, SMS)["weight_pairs"]
+        F.set_gemm_tile_policy(F.TILE_WEIGHT_PAIRS)
+        assert F.plan_gemm(8192, 14336, 4096, SMS)["weight_pairs"]      # 32 x 56 pair units
+        assert not F.plan_gemm(8064, 14336, 4096, SMS)["weight_pairs"]  # 63 activation tiles: no whole pairs
+        assert not F.plan_gemm(512, 512, 4096, SMS)["weight_pairs"]     # 2 x 2 pair units < 76 clusters
+        assert not F.plan_gemm(8, 14336, 4096, SMS)["weight_pairs"]     # decode
     finally:
         F.set_gemm_tile_policy(F.TILE_AUTO)
     c = F.STATUS_CODE

@@ -172,6 +172,46 @@ def test_prefill_full_size_sampled(F, O, n):
     check_close(got[:, cols], ref, mag, what="sampled columns")
 
 
+def test_prefill_full_size_weight_pairs(F, O):
+    """The prefill shape on the weight-tile-sharing CTA pairs: sampled rows and
+    columns as above, and the same bits as the one-CTA kernel (the MMAs and
+    the epilogue are the same; only the copies that feed them differ)."""
+    m, k, n = 8192, 4096, 14336
+    a = I.randn_bf16((m, k), 2)
+    w = I.weights_bf16(n, k, 102)
+    base = run_gemm(F, a, w, 0)
+    F.set_gemm_tile_policy(F.TILE_WEIGHT_PAIRS)
+    try:
+        assert F.plan_gemm(m, n, k, torch.cuda.get_device_properties(0).multi_processor_count)["weight_pairs"]
+        got = run_gemm(F, a, w, 0)
+    finally:
+        F.set_gemm_tile_policy(F.TILE_AUTO)
+    assert np.array_equal(got, base)
+    qa = O.quantize_nvfp4(I.u16(a))
+    qw = O.quantize_nvfp4(I.u16(w))
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([rng.choice(m, 24, replace=False), [0, 127, 128, 255, 256, m - 1]]))
+    cols = np.unique(np.concatenate([rng.choice(n, 12, replace=False), [0, 127, 128, 255, 256, n - 1]]))
+    ref, mag = O.gemm_rows(0, qa[0], qa[1], qa[2], qw[0], qw[1], qw[2], rows, np.arange(n))
+    check_close(got[rows], ref, mag, what="sampled rows")
+    ref, mag = O.gemm_rows(0, qa[0], qa[1], qa[2], qw[0], qw[1], qw[2], np.arange(m), cols)
+    check_close(got[:, cols], ref, mag, what="sampled columns")
+
+
+# the one-CTA kernel in clusters of two whose activation tiles share each
+# 256-row weight tile (TMA multicast of its halves), forced: whole pairs of
+# activation tiles, ragged N and K, one and several pair units per cluster
+@pytest.mark.parametrize("m,n,k", [(1024, 5120, 512), (1280, 4904, 1056), (2048, 10240, 256)])
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_weight_pair_kernel_shapes(F, O, m, n, k, fmt):
+    F.set_gemm_tile_policy(F.TILE_WEIGHT_PAIRS)
+    try:
+        assert F.plan_gemm(m, n, k, torch.cuda.get_device_properties(0).multi_processor_count)["weight_pairs"]
+        check_linear(F, O, I.randn_bf16((m, k), m + 5), I.weights_bf16(n, k, n + 11), fmt)
+    finally:
+        F.set_gemm_tile_policy(F.TILE_AUTO)
+
+
 def test_mxfp4_full_size(F, O):
     """MXFP4 W4A4 M=2048, K=7168, N=2048: every output element."""
     a = I.randn_bf16((2048, 7168), 4)
