@@ -237,8 +237,17 @@ __device__ __forceinline__ Unit decode_unit(const GemmLaunch& g, const Sched& sc
     }
     w.s = (int)(u % sc.splits);
     const int64_t r = u / sc.splits;
-    w.pt = r % sc.n_ptiles;
-    w.qt = r / sc.n_ptiles;
+    if constexpr (epi_grouped<EPI>()) {
+        // grouped: the expert's weight tiles fastest, so the units of one token
+        // tile run side by side and an expert's weight tiles serve its token
+        // tiles close together (token tiles fastest sent every expert's tile
+        // qt to the HBM at once: the MoE call at T = 4096 took 298 against 288 us)
+        w.qt = r % sc.n_qtiles;
+        w.pt = r / sc.n_qtiles;
+    } else {
+        w.pt = r % sc.n_ptiles;
+        w.qt = r / sc.n_ptiles;
+    }
     if (MC) w.pt = 2 * w.pt + prank;  // the pair's tile of this CTA
     w.e = 0;
     if constexpr (epi_grouped<EPI>()) unit_tile_info(g, ut, u, w.pt, w.e, w.vend);
@@ -422,7 +431,7 @@ __global__ void __launch_bounds__(512, 1)
                 if constexpr (epi_swapped_grouped<EPI>())
                     pt = (u / sc.n_qtiles) % sc.n_ptiles;
                 else
-                    pt = (u / sc.splits) % sc.n_ptiles;
+                    pt = (u / sc.splits) / sc.n_qtiles;
                 e = g.tile_expert[pt];
                 vend = g.row_valid_end[pt];
             }
