@@ -357,16 +357,20 @@ __device__ __noinline__ uint2 nvfp4_block_slow(uint4 v0, uint4 v1, float2 e) {
 }
 
 constexpr int QU = 4;        // row groups per thread per iteration: all their loads go out first
-constexpr int QNV_CTAS = 3;  // resident CTAs per SM (register budget of quant_nv_kernel)
+constexpr int QNV_CTAS = 3;  // resident CTAs per SM (register budget of quant_mx_rows_kernel)
+// quant_nv_kernel holds the next QU row groups' loads in flight while it
+// converts the current ones (twice the registers): two CTAs per SM
+constexpr int QNV_PIPE_CTAS = 2;
 
 // The NVFP4 quantiser for a tensor with one global scale (static, or dynamic
 // from the abs-max partials) and no row map: the dense linear's activations,
 // the MoE hidden states, weight prepack.  Same thread layout as quant_kernel
 // (a thread per 16-element block, `rpi` rows x `bpt` blocks per CTA step);
-// a CTA walks a contiguous range of row groups, QU at a time with all their
-// loads issued before any is converted, and takes the divisor of each scale
-// byte from its table.
-__global__ void __launch_bounds__(QT, QNV_CTAS) quant_nv_kernel(const QuantLaunch q) {
+// a CTA walks a contiguous range of row groups, QU at a time, issuing the next
+// QU groups' loads before it converts the current ones (the loads' latency
+// runs under the conversion: 38.6 -> 36.5 us for 8192 x 4096, same codes), and
+// takes the divisor of each scale byte from its table.
+__global__ void __launch_bounds__(QT, QNV_PIPE_CTAS) quant_nv_kernel(const QuantLaunch q) {
     __shared__ uint32_t red[QT / 32];
     __shared__ float sh_sg;
     __shared__ float2 dtab[128];
@@ -423,15 +427,28 @@ __global__ void __launch_bounds__(QT, QNV_CTAS) quant_nv_kernel(const QuantLaunc
     if (!active) return;
 
     bool first = true;
+    uint4 vn[QU][2];  // the next QU row groups, in flight during the conversion
     for (int b = tx; b < nb; b += bpt) {
         const bool bdata = b < kblocks;
         const uint32_t sf_col = (uint32_t)(b >> 2) * 512u + (uint32_t)(b & 3);
         uint32_t r = r_first;
         const uint16_t* px = q.x + (size_t)r * (size_t)q.x_ld + (size_t)b * 16;
         uint8_t* pc = q.codes + (size_t)r * (size_t)(q.k / 2) + (size_t)b * 8;
+        if (!first) load(g_begin, r, px, bdata);  // (the first block's rows went out before the table)
+        first = false;
         for (uint32_t g = g_begin; g < g_end; g += QU) {
-            if (!first) load(g, r, px, bdata);
-            first = false;
+            const bool more = g + QU < g_end;
+            if (more) {
+#pragma unroll
+                for (int j = 0; j < QU; ++j) {
+                    vn[j][0] = vn[j][1] = make_uint4(0u, 0u, 0u, 0u);
+                    if (g + QU + j < g_end && r + (QU + j) * rpi < rows && bdata) {
+                        const uint4* pv = reinterpret_cast<const uint4*>(px + (QU + j) * xstep);
+                        vn[j][0] = __ldg(pv);
+                        vn[j][1] = __ldg(pv + 1);
+                    }
+                }
+            }
 #pragma unroll
             for (int j = 0; j < QU; ++j) {
                 if (g + j >= g_end) break;
@@ -447,6 +464,13 @@ __global__ void __launch_bounds__(QT, QNV_CTAS) quant_nv_kernel(const QuantLaunc
                     w = nvfp4_block_slow(v[j][0], v[j][1], e);
                 if (rj < rows && bdata) *reinterpret_cast<uint2*>(pc + j * cstep) = w;
                 q.scales[(rj >> 7) * tile_sf + ((rj & 31u) << 4) + (((rj >> 5) & 3u) << 2) + sf_col] = (uint8_t)sbyte;
+            }
+            if (more) {
+#pragma unroll
+                for (int j = 0; j < QU; ++j) {
+                    v[j][0] = vn[j][0];
+                    v[j][1] = vn[j][1];
+                }
             }
             r += QU * rpi;
             px += QU * xstep;
@@ -675,7 +699,7 @@ cudaError_t launch_quant(const QuantLaunch& q, cudaStream_t s) {
         const int64_t bpt = nb < QT ? (nb + 31) / 32 * 32 : QT;
         const int64_t groups = q.rows_pad / (QT / bpt);
         int64_t blocks = (groups + QU - 1) / QU;
-        if (blocks > (int64_t)sms * QNV_CTAS) blocks = (int64_t)sms * QNV_CTAS;
+        if (blocks > (int64_t)sms * QNV_PIPE_CTAS) blocks = (int64_t)sms * QNV_PIPE_CTAS;
         if (blocks < 1) blocks = 1;
         QuantLaunch qq = q;
         void* args[] = {(void*)&qq};
