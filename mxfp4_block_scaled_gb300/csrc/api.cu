@@ -261,6 +261,10 @@ static fp4_status enqueue_quantize(int fmt, const void* x, int64_t rows, int64_t
         q.sg_mode = SG_PARTIALS;
         q.partials = partials;
         q.n_partials = np;
+        // the quantiser depends on the abs-max pass alone, which starts only after
+        // x is complete: it may start early and load its first rows before its wait
+        q.pdl = true;
+        q.x_before_wait = true;
     } else {
         q.sg_mode = SG_STATIC;
         q.static_scale = st;

@@ -69,6 +69,10 @@ struct QuantLaunch {
     int n_experts = 0;
     const int32_t* rows_dev = nullptr;  // optional device row count bound (grouped): rows beyond are skipped
     bool pdl = false;
+    // x was complete before the grid this launch depends on started (that grid
+    // writes only the partials): quant_nv_kernel may load its first rows before
+    // the dependency wait
+    bool x_before_wait = false;
 };
 
 int amax_partials_count(int64_t n_elems);

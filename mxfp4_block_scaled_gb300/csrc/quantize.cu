@@ -374,8 +374,10 @@ __global__ void __launch_bounds__(QT, QNV_PIPE_CTAS) quant_nv_kernel(const Quant
     __shared__ uint32_t red[QT / 32];
     __shared__ float sh_sg;
     __shared__ float2 dtab[128];
-    pdl_wait();
-    pdl_launch_dependents();
+    if (!q.x_before_wait) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
 
     const int nb = (int)sf_cols_padded(q.k, 16);  // scale blocks per row, padding included
     const int kblocks = (int)(q.k / 16);
@@ -407,8 +409,14 @@ __global__ void __launch_bounds__(QT, QNV_PIPE_CTAS) quant_nv_kernel(const Quant
     };
     // the first batch of rows is in flight while the global scale and the
     // divisor table are formed (neither is needed to load)
+    // (and, after the abs-max pass, before the wait for its partials: the
+    // loads overlap that pass's tail)
     const uint32_t r_first = g_begin * rpi + ty;
     if (active) load(g_begin, r_first, q.x + (size_t)r_first * (size_t)q.x_ld + (size_t)tx * 16, tx < kblocks);
+    if (q.x_before_wait) {
+        pdl_wait();  // the partials, and the buffers this grid writes
+        pdl_launch_dependents();
+    }
 
     float sg = q.static_scale;
     if (q.sg_mode == SG_PARTIALS) {
