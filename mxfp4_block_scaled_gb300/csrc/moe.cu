@@ -492,6 +492,22 @@ __global__ void __launch_bounds__(1024) moe_prep_small_kernel(const PrepArgs a, 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = a.E, k = a.k;
     const int T = (int)a.T;
+    // the logits of a warp's tokens are loaded first (when they fit the
+    // registers), so their latency runs under the table set-up below
+    constexpr int RT = kPrepMaxTokens / 32;     // tokens per warp at most
+    constexpr bool PRE = PER_LANE <= 8;         // all of them loaded first
+    float lg[PRE ? RT : 1][PER_LANE];
+    if constexpr (PRE) {
+#pragma unroll
+        for (int i = 0; i < RT; ++i) {
+            const int t = warp + 32 * i;
+#pragma unroll
+            for (int q = 0; q < PER_LANE; ++q) {
+                const int e = q * 32 + lane;
+                lg[i][q] = t < T && e < E ? __ldg(a.logits + (int64_t)t * E + e) : -INFINITY;
+            }
+        }
+    }
     for (int e = tid; e < E; e += 1024) {
         tokmask[e] = 0ull;
         a.amax_h[e] = 0.0f;
@@ -503,23 +519,8 @@ __global__ void __launch_bounds__(1024) moe_prep_small_kernel(const PrepArgs a, 
     if (tid == 0) cmax = 0;
     __syncthreads();
 
-    // 1. route: a warp per token (both of a warp's tokens' logits loaded first
-    // when they fit the registers)
+    // 1. route: a warp per token
     {
-        constexpr int RT = kPrepMaxTokens / 32;     // tokens per warp at most
-        constexpr bool PRE = PER_LANE <= 8;         // all of them loaded first
-        float lg[PRE ? RT : 1][PER_LANE];
-        if constexpr (PRE) {
-#pragma unroll
-            for (int i = 0; i < RT; ++i) {
-                const int t = warp + 32 * i;
-#pragma unroll
-                for (int q = 0; q < PER_LANE; ++q) {
-                    const int e = q * 32 + lane;
-                    lg[i][q] = t < T && e < E ? __ldg(a.logits + (int64_t)t * E + e) : -INFINITY;
-                }
-            }
-        }
 #pragma unroll
         for (int i = 0; i < RT; ++i) {
             const int t = warp + 32 * i;
