@@ -3,17 +3,20 @@
 // out[t][n] = bf16(alpha * sum_k deq(A)[t][k] * deq(W)[n][k]) for t < m <= 8,
 // with A = the bf16 activations quantised in this kernel (dynamic or static
 // per-tensor scale, the arithmetic of quant_math.cuh, so the codes are those
-// fp4_quantize_act gives) and W the prepacked FP4 weights.  The call is
-// bound by streaming W, so the weight tiles start loading at the first
-// instruction and everything about the activations hides under that stream:
+// fp4_quantize_act gives) and W the prepacked FP4 weights.  The call streams
+// W, so the weight tiles start loading right after the set-up barrier and the
+// activations' work runs under that stream:
 //
 //   one CTA per 128-row weight tile, the whole K (no split, no reduction);
-//   MMA: swap-AB, M = 128 weight rows, N = 32 activation rows (rows >= m are
-//   zero), K = 64 per instruction, four per 256-element K block;
+//   MMA: swap-AB, M = 128 weight rows, N = 32 activation rows (rows >= m
+//   carry zero scales and feed only accumulator columns nobody reads), K = 64
+//   per instruction, four per 256-element K block; the ring's depth is chosen
+//   per launch from the shared memory the compact copy leaves;
 //   warp 4      TMA producer of the weight tiles (128 rows x 128 B, 128-byte
-//               swizzle) -- no dependency wait, it streams from the start;
+//               swizzle) -- no dependency wait;
 //   warp 7      bulk copies of the weight scale atoms into the scale ring;
-//   warps 0-3, 6, 8-15  first, after the dependency wait: the activations'
+//   warps 0-3, 6, 8-15  first, after the dependency wait (their loads go out
+//               before the set-up barrier): the activations'
 //               abs-max, then all m x K activations quantised once into a
 //               compact smem copy (codes [m][K/2], scale bytes [m][K/16 or
 //               K/32]), the first ring-full of K blocks also straight into

@@ -23,15 +23,19 @@
 //   warps 8-15  epilogue: tcgen05.ld of the fp32 accumulator into registers,
 //               release of the TMEM stage, then alpha, bf16 (or the fused MoE
 //               epilogues) and global stores.  The bf16 output goes through a
-//               32 KB smem staging area and TMA tensor stores, so whole 128-byte
-//               lines leave the SM (row-per-thread stores from registers would
-//               scatter 16-byte pieces over 32 lines per instruction and load
-//               the L2 with several times as many write requests).
+//               small smem staging area (two boxes per epilogue warpgroup) and
+//               TMA tensor stores, so whole lines leave the SM (row-per-thread
+//               stores from registers would scatter 16-byte pieces over 32
+//               lines per instruction and load the L2 with several times as
+//               many write requests).
 // Pipelines: STAGES operand stages (full / empty; a stage is full once both
 // operand tiles landed and the four scale writers stored its scales in TMEM,
 // so the MMA thread waits once per K block), as many scale slots (scale-full /
-// scale-empty for the smem ring) and 1-2 TMEM accumulator stages (acc_full /
-// acc_empty).  Every wait is bounded.
+// scale-empty for the smem ring) and 1, 2 or 4 TMEM accumulator stages
+// (acc_full / acc_empty; one at BN = 256).  Every wait is bounded.
+// Units: tiles over a grid stride, P tiles fastest for the dense GEMM, an
+// expert's weight tiles fastest for the grouped ones; the opt-in MC variant
+// runs the dense kernel in clusters of two sharing each Q tile (see below).
 #pragma once
 
 #include "common.cuh"
