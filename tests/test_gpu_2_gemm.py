@@ -69,8 +69,10 @@ def test_pair_kernel_shapes(F, O, m, n, k, fmt):
 
 
 # the fused decode kernel (activation quantisation inside the GEMM launch),
-# forced on small and ragged shapes: n not a multiple of 128, k not of 256
-@pytest.mark.parametrize("m,n,k", [(1, 256, 512), (5, 520, 800), (8, 1000, 1056), (3, 128, 4096)])
+# forced on small and ragged shapes: n not a multiple of 128, k not of 256;
+# the ring depth follows m and k (k = 8192 at m = 8: 7 stages, 32 K blocks)
+@pytest.mark.parametrize("m,n,k", [(1, 256, 512), (5, 520, 800), (8, 1000, 1056), (3, 128, 4096), (8, 384, 8192),
+                                   (1, 256, 8192)])
 @pytest.mark.parametrize("fmt", [0, 1])
 def test_fused_decode_shapes(F, O, m, n, k, fmt):
     F.set_gemm_tile_policy(F.TILE_FUSED_DECODE)
