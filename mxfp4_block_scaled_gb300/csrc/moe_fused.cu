@@ -219,9 +219,14 @@ __global__ void __launch_bounds__(512, 1)
         prefetch_tensormap(&tm13);
         prefetch_tensormap(&tm2);
     }
-    // token operand tiles start at zero (rows past an expert's tokens are never
-    // read back; the zeros keep their scales finite)
-    for (int i = threadIdx.x; i < 2 * C::QBUF / 16; i += 512) reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0u, 0u, 0u, 0u);
+    // the token tiles' scale words start at zero: the rows past a unit's tokens
+    // (codes and scales left from set-up or an earlier unit) feed only
+    // accumulator columns nobody reads, and zero or earlier finite scales keep
+    // even those finite; the codes need no clearing (E2M1 codes are finite)
+    for (int i = threadIdx.x; i < 2 * C::MAX_KB * C::QS_BYTES / 16; i += 512) {
+        const int b = i / (C::MAX_KB * C::QS_BYTES / 16), r = i - b * (C::MAX_KB * C::QS_BYTES / 16);
+        reinterpret_cast<uint4*>(sQ + b * C::QBUF + C::MAX_KB * C::QC_BYTES)[r] = make_uint4(0u, 0u, 0u, 0u);
+    }
     if (threadIdx.x < E) {
         s_mask[threadIdx.x] = 0u;
         s_gw13[threadIdx.x] = gw;
@@ -497,8 +502,34 @@ __global__ void __launch_bounds__(512, 1)
             named_bar_sync(3, 128);
             if (s_misc[4]) break;
             const float sg = __uint_as_float((uint32_t)s_misc[3]);
+            const int K = g1 ? H : I;
+            const int bpr = K / 16;  // blocks per row
+            const int nbb = ne * bpr;
+            // the source of block bb (row r = bb / bpr of the unit's tokens, block j):
+            // the hidden row of its token, or (GEMM2) the slot's h row, written by
+            // other CTAs before the counter the decision above waited for
+            auto load_blk = [&](int bb, uint4& x0, uint4& x1) {
+                const int r = bb / bpr, j = bb - r * bpr;
+                const int slot = s_eslot[ai * kFusedMaxT + r];
+                if (g1) {
+                    const uint4* src = reinterpret_cast<const uint4*>(a.hidden + (int64_t)(slot / k) * H + j * 16);
+                    x0 = __ldg(src);
+                    x1 = __ldg(src + 1);
+                } else {
+                    const uint4* src = reinterpret_cast<const uint4*>(a.h + (int64_t)slot * I + j * 16);
+                    x0 = __ldcg(src);
+                    x1 = __ldcg(src + 1);
+                }
+            };
+            // the thread's first block is in flight while the divisors are formed
+            uint4 xn0 = make_uint4(0u, 0u, 0u, 0u), xn1 = xn0;
+            if (q < nbb) load_blk(q, xn0, xn1);
             float2* tab = dtab;  // GEMM1, dynamic scale: the prologue's table
-            if (!g1 || a.is_static) {
+            // one or two tokens (at most one block per thread): each thread takes
+            // its block's divisor itself (the table's entry for that byte, with the
+            // same refinement) instead of the table and its barrier
+            const bool direct = ne <= 2 && nbb <= 128;
+            if ((!g1 || a.is_static) && !direct) {
                 tab = dtab + (1 + qb) * 128;
                 tab[q] = nvfp4_divisor((uint32_t)q, sg, ne > 2);
                 named_bar_sync(3, 128);
@@ -510,30 +541,21 @@ __global__ void __launch_bounds__(512, 1)
             //    scale atoms (row r at r * 16)
             uint8_t* qc = sQ + qb * C::QBUF;
             uint8_t* qs = qc + C::MAX_KB * C::QC_BYTES;
-            const int K = g1 ? H : I;
-            const int bpr = K / 16;    // blocks per row
             const bool dump = t == 0;  // one unit per expert leaves the codes in the workspace
-            for (int bb = q; bb < ne * bpr; bb += 128) {
+            for (int bb = q; bb < nbb; bb += 128) {
                 const int r = bb / bpr, j = bb - r * bpr;
                 const int slot = s_eslot[ai * kFusedMaxT + r];
-                uint4 x0, x1;
-                if (g1) {
-                    const uint4* src = reinterpret_cast<const uint4*>(a.hidden + (int64_t)(slot / k) * H + j * 16);
-                    x0 = __ldg(src);
-                    x1 = __ldg(src + 1);
-                } else {
-                    const uint4* src = reinterpret_cast<const uint4*>(a.h + (int64_t)slot * I + j * 16);
-                    x0 = __ldcg(src);
-                    x1 = __ldcg(src + 1);
-                }
+                const uint4 x0 = xn0, x1 = xn1;
+                if (bb + 128 < nbb) load_blk(bb + 128, xn0, xn1);  // the next block in flight
                 uint32_t am = absmax8(x1, absmax8(x0, 0u));
                 am = max(am & 0xFFFFu, am >> 16);
                 const uint32_t sbyte = nvfp4_scale_byte(__uint_as_float(am << 16), p_t, inv_p);
+                const float2 dv = (!g1 || a.is_static) && direct ? nvfp4_divisor(sbyte, sg, ne > 2) : tab[sbyte];
                 float f[8];
                 unpack8(x0, f);
-                const uint32_t w0 = nvfp4_word(f, tab[sbyte]);
+                const uint32_t w0 = nvfp4_word(f, dv);
                 unpack8(x1, f);
-                const uint32_t w1 = nvfp4_word(f, tab[sbyte]);
+                const uint32_t w1 = nvfp4_word(f, dv);
                 const int kb = j >> 4, jj = j & 15;
                 const uint32_t qa = smem_u32(qc + kb * C::QC_BYTES) + (uint32_t)r * 128u +
                                     ((((uint32_t)jj >> 1) ^ ((uint32_t)r & 7u)) << 4) + (((uint32_t)jj & 1u) << 3);
