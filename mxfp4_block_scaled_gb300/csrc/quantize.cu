@@ -498,13 +498,15 @@ constexpr int QE_ROWS = 64;  // rows per work item (half a 128-row tile: one exp
 // row's token).  A work item is half a tile: the CTA tabulates the 128
 // divisors of the tile's expert scale (as quant_nv_kernel does for a tensor)
 // when the expert changes, then takes the item's 64 x nb blocks as a flat
-// range, QU per thread in flight, with the row and block of each step
-// advanced by constants (no division per block).  Rows without a source get
+// range, QU per thread per step with the next step's QU loads in flight
+// during the conversion (2 CTAs/SM for the registers; the requantisation of h
+// at 32768 x 768: 29.5 -> 28.1 us, same codes), with the row and block of each
+// step advanced by constants (no division per block).  Rows without a source get
 // zero scale bytes and no codes; rows past the device row count are not
 // touched.
 // Codes and scale bytes equal quant_kernel's expert modes: each divisor entry
 // is nvfp4_divisor's, with the product path wherever it is proven.
-__global__ void __launch_bounds__(QT, 3) quant_expert_rows_kernel(const QuantLaunch q) {
+__global__ void __launch_bounds__(QT, 2) quant_expert_rows_kernel(const QuantLaunch q) {
     __shared__ float2 dtab[128];
     __shared__ int64_t s_x[QE_ROWS];   // element offset of the row's source, -1: zero row, -2: past the rows
     __shared__ int64_t s_c[QE_ROWS];   // byte offset of the row's codes
@@ -523,20 +525,20 @@ __global__ void __launch_bounds__(QT, 3) quant_expert_rows_kernel(const QuantLau
     const int t_row = threadIdx.x / nb, t_col = threadIdx.x - t_row * nb;
     int cached = -1;
     float p = 0.0f, inv_p = 0.0f;
-    uint4 v[QU][2];
-    int rj[QU], cj[QU];
+    uint4 v[QU][2], vn[QU][2];
+    int rj[QU], cj[QU], rn[QU], cn[QU];
     // this thread's next QU blocks of the item: row / block indices, then the loads
     auto load = [&](int base, int& row, int& col) {
 #pragma unroll
         for (int j = 0; j < QU; ++j) {
-            rj[j] = row;
-            cj[j] = col;
-            v[j][0] = v[j][1] = make_uint4(0u, 0u, 0u, 0u);
+            rn[j] = row;
+            cn[j] = col;
+            vn[j][0] = vn[j][1] = make_uint4(0u, 0u, 0u, 0u);
             const int64_t xo = base + j * QT < per_item ? s_x[row] : -1;
             if (xo >= 0 && col < kblocks) {
                 const uint4* px = reinterpret_cast<const uint4*>(q.x + xo + (int64_t)col * 16);
-                v[j][0] = __ldg(px);
-                v[j][1] = __ldg(px + 1);
+                vn[j][0] = __ldg(px);
+                vn[j][1] = __ldg(px + 1);
             }
             row += dq;
             col += dr;
@@ -574,7 +576,14 @@ __global__ void __launch_bounds__(QT, 3) quant_expert_rows_kernel(const QuantLau
             __syncthreads();
         }
         for (int base = threadIdx.x; base < per_item; base += QU * QT) {
-            if (base != (int)threadIdx.x) load(base, row, col);
+#pragma unroll
+            for (int j = 0; j < QU; ++j) {
+                v[j][0] = vn[j][0];
+                v[j][1] = vn[j][1];
+                rj[j] = rn[j];
+                cj[j] = cn[j];
+            }
+            if (base + QU * QT < per_item) load(base + QU * QT, row, col);  // the next batch in flight
 #pragma unroll
             for (int j = 0; j < QU; ++j) {
                 if (base + j * QT >= per_item) break;
@@ -679,7 +688,7 @@ cudaError_t launch_quant(const QuantLaunch& q, cudaStream_t s) {
     if (q.fmt == FP4_NVFP4 && !q.skip_masked_rows && q.row_map && q.tile_expert &&
         (q.sg_mode == SG_EXPERT_TABLE || q.sg_mode == SG_EXPERT_AMAX)) {
         int64_t blocks = q.rows_pad / QE_ROWS;  // upper bound on the items
-        if (blocks > (int64_t)sms * 3) blocks = (int64_t)sms * 3;  // one resident wave
+        if (blocks > (int64_t)sms * 2) blocks = (int64_t)sms * 2;  // one resident wave
         if (blocks < 1) blocks = 1;
         QuantLaunch qq = q;
         void* args[] = {(void*)&qq};
